@@ -1,0 +1,102 @@
+"""The pins catch plausible mistakes: each test plants one mistake in the oracle (on
+the CPU, through monkeypatch) and checks that a pin test then fails."""
+import numpy as np
+import pytest
+
+from oracle import accept, attention, draft, tree
+from tests import test_oracle_accept as ta
+from tests import test_oracle_attention as tat
+from tests import test_oracle_draft as td
+from tests import test_oracle_tree as tt
+
+
+def test_causal_mask_instead_of_ancestor_mask_is_caught(monkeypatch):
+    monkeypatch.setattr(tree, "tree_mask", lambda p: np.tril(np.ones((len(p), len(p)), bool)))
+    with pytest.raises(AssertionError):
+        tt.test_six_node_mask_matches_printed_example()
+
+
+def test_depth_off_by_one_is_caught(monkeypatch):
+    monkeypatch.setattr(tree, "depths", lambda p: [0] + [1] * (len(p) - 1))
+    with pytest.raises(AssertionError):
+        tt.test_tree_221_diagram()
+
+
+def test_rope_sign_error_is_caught(monkeypatch):
+    orig = attention.apply_rope
+
+    def wrong(x, pos, theta):
+        return orig(x, -np.asarray(pos), theta)
+    monkeypatch.setattr(attention, "apply_rope", wrong)
+    with pytest.raises(AssertionError):
+        tat.test_rope_closed_forms()
+
+
+def test_rope_frequency_exponent_error_is_caught(monkeypatch):
+    monkeypatch.setattr(attention, "rope_inv_freq",
+                        lambda d, th: np.power(float(th), -np.arange(d // 2) / d))
+    with pytest.raises(AssertionError):
+        tat.test_rope_closed_forms()
+
+
+def test_position_without_depth_is_caught(monkeypatch):
+    monkeypatch.setattr(attention, "position_ids",
+                        lambda parents, p: np.full(len(parents), p, dtype=np.int64))
+    with pytest.raises(AssertionError):
+        tat.test_each_node_equals_causal_pass_over_its_chain([-1, 0, 0, 1, 1, 2])
+
+
+def test_unmasked_tree_part_is_caught(monkeypatch):
+    monkeypatch.setattr(attention, "tree_mask", lambda p: np.ones((len(p), len(p)), bool))
+    with pytest.raises(AssertionError):
+        tat.test_non_ancestors_do_not_matter()
+
+
+def test_score_product_instead_of_sum_is_caught(monkeypatch):
+    orig = draft.expand_level
+
+    def wrong(logits, k, parent_scores=None, parent_store=None):
+        lv = orig(logits, k, parent_scores, parent_store)
+        if parent_scores is not None:
+            r = np.asarray(logits).shape[0]
+            for s in range(r):
+                for c in range(k):
+                    lv.cu[s * k + c] = np.float32(parent_scores[s] * lv.logp[s * k + c])
+            lv.selected = draft.topk_by_score(lv.cu, k)
+        return lv
+    monkeypatch.setattr(draft, "expand_level", wrong)
+    with pytest.raises(AssertionError):
+        td.test_store_score_is_path_sum_of_logp(0)
+
+
+def test_tie_to_higher_index_is_caught(monkeypatch):
+    def wrong(row, k):
+        x = np.asarray(row, dtype=np.float64)
+        return np.lexsort((-np.arange(x.size), -x))[:k].astype(np.int32)
+    monkeypatch.setattr(draft, "row_topk", wrong)
+    with pytest.raises(AssertionError):
+        td.test_exact_ties_take_lower_indices()
+
+
+def test_walk_ignoring_tokens_is_caught(monkeypatch):
+    def wrong(tokens, parents, target):
+        path, node = [0], 0
+        kids = tree.children_of(parents)
+        while kids[node]:
+            node = kids[node][0]
+            path.append(node)
+        return path, int(target[node])
+    monkeypatch.setattr(accept, "greedy_walk", wrong)
+    with pytest.raises(AssertionError):
+        ta.test_walk_on_the_221_tree()
+
+
+def test_in_place_compaction_order_error_is_caught(monkeypatch):
+    def wrong(cache, p_len, path):
+        out = np.array(cache, copy=True)
+        for i in reversed(range(len(path))):      # decreasing order reads clobbered rows
+            out[..., p_len + i, :] = out[..., p_len + path[i], :]
+        return out
+    monkeypatch.setattr(accept, "compact", wrong)
+    with pytest.raises(AssertionError):
+        ta.test_compaction_moves_rows_and_keeps_the_rest()
