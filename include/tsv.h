@@ -1,0 +1,296 @@
+/*
+ * tsv.h — C ABI of the GB300 (sm_103a) tree speculative-decoding verification library.
+ *
+ * Hot path of EAGLE-2/3 dynamic-tree speculative decoding, one GPU:
+ *   tsv_draft_topk_expand   one level of the draft tree expansion (per-row log-softmax +
+ *                           top-k, cumulative scores, joint top-k pruning)
+ *   tsv_draft_select_final  the total_tokens best candidates laid out as a tree
+ *   tsv_tree_build_meta     ancestor bitmask, positions, retrieve_indices, child/sibling links
+ *   tsv_tree_verify_attn    RoPE + KV append + tree-masked split-KV attention of every node
+ *   tsv_accept_and_compact  greedy acceptance walk + move of the accepted KV to
+ *                           consecutive slots
+ *
+ * Pages cited (by title):
+ *   [TRT]    "TensorRT-LLM 源码完全拆解(二十二): EAGLE-3 一体式草稿——三层隐状态、草稿循环
+ *            与动态树验证"
+ *   [HB]     "推理系统手册 · 投机解码进阶：树形草稿与 EAGLE"
+ *   [EAGLE2] the EAGLE v2 dynamic-tree walkthrough (initialize_tree / topK_generate /
+ *            tree_decoding / evaluate_posterior), sections 3-5
+ *
+ * Conventions for every call:
+ *   - Every array pointer is a DEVICE pointer owned by the caller, unless stated. The
+ *     library allocates no memory and keeps no state between calls beyond a per-device
+ *     cache of device attributes.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and never synchronise the host. They can be captured into a CUDA graph.
+ *   - The return value is a tsv_status. Host-side checks (null pointers, sizes,
+ *     workspace) happen before anything is launched; on failure nothing is launched.
+ *   - Data-dependent faults (a malformed tree, a request that does not fit its cache)
+ *     are found on the device: a per-request code is written to the caller's `err`
+ *     array (where the call has one) and that request's outputs are left in the
+ *     documented safe state. Nothing traps; every device loop is bounded.
+ *   - Node 0 of every tree is the root (the last token the target model committed);
+ *     parents precede children; parents[0] == -1.
+ *   - Integer arrays are int32 unless stated; "[a, b]" is a row-major shape.
+ */
+#ifndef TSV_H
+#define TSV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tsv_stream_t; /* a cudaStream_t */
+
+/* ---- status codes (return values) ---- */
+enum tsv_status {
+  TSV_OK = 0,
+  TSV_ERR_INVALID_ARG = 1, /* null pointer, size out of range, inconsistent sizes */
+  TSV_ERR_UNSUPPORTED = 2, /* dtype / head_dim / device not supported */
+  TSV_ERR_WORKSPACE = 3,   /* workspace pointer null or too small */
+  TSV_ERR_CUDA = 4         /* a CUDA call failed; see tsv_last_cuda_error() */
+};
+
+/* ---- per-request device error codes (written to err[b]) ---- */
+enum tsv_request_error {
+  TSV_REQ_OK = 0,
+  TSV_REQ_BAD_ROOT = 1,     /* parents[b][0] != -1 */
+  TSV_REQ_BAD_PARENT = 2,   /* some parents[b][i] outside [0, i) */
+  TSV_REQ_TOO_DEEP = 3,     /* a root-to-node path longer than max_depth + 1 nodes */
+  TSV_REQ_BAD_SIZE = 4,     /* num_nodes[b] outside [1, max_nodes] or prefix_len[b] < 0 */
+  TSV_REQ_CAPACITY = 5,     /* prefix_len[b] + num_nodes[b] does not fit the KV cache */
+  TSV_REQ_BAD_BLOCK = 6,    /* a block-table entry outside [0, num_blocks) */
+  TSV_REQ_BAD_LINKS = 7     /* child/sibling links leave the tree */
+};
+
+/* ---- limits ---- */
+#define TSV_MAX_NODES 256 /* nodes per tree, root included */
+#define TSV_MAX_TOPK 16   /* top_k of the expansion */
+#define TSV_MAX_DEPTH 64  /* max_depth (edges from the root to the deepest node) */
+#define TSV_KV_BLOCK 64   /* tokens per paged KV block */
+
+/* ---- element types ---- */
+enum tsv_dtype { TSV_DTYPE_F32 = 0, TSV_DTYPE_BF16 = 1 };
+
+/* ---- KV cache description ---- */
+enum tsv_kv_layout {
+  TSV_KV_CONTIGUOUS = 0, /* k, v: [batch, num_kv_heads, capacity, head_dim] */
+  TSV_KV_PAGED = 1       /* k, v: [num_blocks, num_kv_heads, TSV_KV_BLOCK, head_dim];
+                            slot s of request b lives in block block_table[b][s / 64],
+                            row s % 64 */
+};
+
+typedef struct {
+  void* k;                     /* keys of layer 0 (keys are stored already rotated) */
+  void* v;                     /* values of layer 0 */
+  int dtype;                   /* tsv_dtype of k and v */
+  int num_kv_heads;            /* Hkv */
+  int head_dim;                /* D: 64 or 128 */
+  int layout;                  /* tsv_kv_layout */
+  int64_t capacity;            /* CONTIGUOUS: slots per (request, kv head), a multiple of 64 */
+  const int32_t* block_table;  /* PAGED: [batch, max_blocks] (device) */
+  int max_blocks;              /* PAGED: columns of block_table */
+  int num_blocks;              /* PAGED: blocks in the pool */
+  int num_layers;              /* layers reachable from k/v (>= 1) */
+  int64_t layer_stride;        /* elements from one layer's k (or v) to the next layer's */
+} tsv_kv_cache;
+
+/* Library version string and a readable name for a tsv_status. */
+const char* tsv_version(void);
+const char* tsv_status_string(int status);
+/* cudaError_t of the last failed CUDA call made by this library on this thread. */
+int tsv_last_cuda_error(void);
+
+/* --------------------------------------------------------------------------------
+ * tsv_draft_topk_expand — one level of the dynamic draft tree.
+ *
+ * [EAGLE2] section 3 (树的生长, topK_generate): every frontier row takes its top_k
+ * tokens with their log-probabilities; a candidate's cumulative score is its parent's
+ * score plus its log-probability (cu_scores = topk_p + scores[:, None]); a joint
+ * top_k over the rows * top_k candidates gives the next frontier. [TRT] section
+ * 树的三套账: candidates are laid out parent-major (flat = s * top_k + c), so the
+ * parent row of a flat index is flat / top_k.
+ *
+ * logits           fp32, row (b, s) at logits + (b * rows + s) * row_stride; the row's
+ *                  first `vocab` entries are the draft logits of frontier node s of
+ *                  request b. Level 1 has rows == 1 (the root), later levels
+ *                  rows == top_k (the previous level's frontier, best first).
+ * level            1-based expansion level: 1 for the base layer, 2 .. depth + 1 after.
+ * front_score_in   fp32 [batch, rows]: cumulative score of each frontier node
+ * front_store_in   int32 [batch, rows]: store index of each frontier node
+ *                  (both NULL at level 1: the root has score 0 and store index -1)
+ * store_*          [batch, store_cap]: the candidate store. This level writes entries
+ *                  off .. off + rows * top_k - 1, off = 0 at level 1 and
+ *                  top_k + (level - 2) * top_k^2 after: the token id, the fp32
+ *                  cumulative score and the store index of the parent (-1: root).
+ * front_*_out      [batch, top_k]: the next frontier, best first (token id, fp32
+ *                  cumulative score, store index). Must not alias the *_in arrays.
+ * workspace        device scratch of tsv_draft_topk_expand_workspace_size() bytes.
+ *
+ * Order and ties: higher values first; equal values go to the lower token id (per
+ * row) and to the lower flat index (joint). Log-probabilities are x - logsumexp(row),
+ * the log-sum-exp accumulated with compensation and finished in fp64, rounded to
+ * fp32; cumulative scores are fp32 sums. Returns TSV_ERR_INVALID_ARG for top_k
+ * outside [1, TSV_MAX_TOPK], vocab < top_k, row_stride < vocab, a store too small for
+ * this level, or rows inconsistent with level.
+ * ------------------------------------------------------------------------------ */
+size_t tsv_draft_topk_expand_workspace_size(int batch, int rows, int vocab, int top_k);
+int tsv_draft_topk_expand(const float* logits, int batch, int rows, int64_t row_stride,
+                          int vocab, int top_k, int level, const float* front_score_in,
+                          const int32_t* front_store_in, int store_cap, int32_t* store_token,
+                          float* store_score, int32_t* store_parent, int32_t* front_token_out,
+                          float* front_score_out, int32_t* front_store_out, void* workspace,
+                          size_t workspace_bytes, tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_draft_select_final — keep the total_tokens best candidates as a tree.
+ *
+ * [EAGLE2] section 3: after the last level, the total_tokens highest cumulative
+ * scores among the num_candidates = top_k + depth * top_k^2 stored candidates are
+ * kept (ties to the lower store index). The kept candidates become nodes 1 ..
+ * total_tokens in ascending store index, node 0 is the root; a node's parent is the
+ * node of its parent's store index, or 0 for first-level candidates. Because a
+ * log-probability is never positive, a kept candidate's parent is always kept.
+ *
+ * tokens, parents  [batch, max_nodes] out: entries 0 .. total_tokens hold the tree,
+ *                  the rest are set to -1.
+ * num_nodes        [batch] out (may be NULL): total_tokens + 1.
+ * root_token       [batch]: token of node 0.
+ * Returns TSV_ERR_INVALID_ARG unless 1 <= total_tokens <= num_candidates <= store_cap
+ * and total_tokens + 1 <= max_nodes <= TSV_MAX_NODES, num_candidates <= 4096.
+ * ------------------------------------------------------------------------------ */
+int tsv_draft_select_final(const int32_t* store_token, const float* store_score,
+                           const int32_t* store_parent, int batch, int num_candidates,
+                           int store_cap, int total_tokens, const int32_t* root_token,
+                           int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
+                           tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_tree_build_meta — tree metadata, one warp per tree.
+ *
+ * [HB] section 实现 (tree_mask, depths; positions = prefix length + depth) and section
+ * 为什么要用树 (every node sees the prefix, its ancestors and itself; siblings share a
+ * position); [TRT] section 树构建内核做了什么 (bit-packed mask, 32 positions per
+ * word; retrieve_next_token / retrieve_next_sibling, -1 where absent); [EAGLE2]
+ * section 3 (retrieve_indices: one root-to-leaf path per leaf).
+ *
+ * parents          [batch, max_nodes] in: parent node of each node (entries at and
+ *                  beyond num_nodes[b] are ignored).
+ * num_nodes        [batch] in: nodes of request b, root included, in [1, max_nodes].
+ * prefix_len       [batch] in: committed KV length P_b (>= 0).
+ * max_depth        deepest allowed node (edges from the root), <= TSV_MAX_DEPTH.
+ * mask             [batch, max_nodes, W] uint32 out, W = ceil(max_nodes / 32): bit j % 32
+ *                  of word j / 32 in row i is set iff node j is node i or an ancestor.
+ * position_ids     [batch, max_nodes] out: P_b + depth(i).
+ * retrieve_indices [batch, max_nodes, max_depth + 1] out: row r is the r-th leaf (in
+ *                  ascending node order), columns are the node indices from the root
+ *                  to that leaf, -1 padded; rows >= num_leaves[b] are all -1.
+ * num_leaves       [batch] out.
+ * next_token       [batch, max_nodes] out: lowest-numbered child, or -1.
+ * next_sibling     [batch, max_nodes] out: next higher-numbered child of the same
+ *                  parent, or -1.
+ * err              [batch] out: tsv_request_error. On an error the request's outputs
+ *                  hold the root-only tree (every row sees only itself, positions
+ *                  P_b, one retrieve row [0, -1, ...], no links, num_leaves 1), so a
+ *                  later verification accepts only the root.
+ * Rows and columns at and beyond num_nodes[b] are zero (mask) or -1 (the rest);
+ * position_ids there are P_b.
+ * ------------------------------------------------------------------------------ */
+int tsv_tree_build_meta(const int32_t* parents, const int32_t* num_nodes,
+                        const int32_t* prefix_len, int batch, int max_nodes, int max_depth,
+                        uint32_t* mask, int32_t* position_ids, int32_t* retrieve_indices,
+                        int32_t* num_leaves, int32_t* next_token, int32_t* next_sibling,
+                        int32_t* err, tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_tree_verify_attn — tree verification attention of one layer.
+ *
+ * [HB] section 实现 (forward_with_mask) and section 为什么要用树; [EAGLE2] section 4
+ * (tree_decoding); [TRT] section CUDA Graph 里的掩码重排 (the target attention reads
+ * the padded [N, ceil(N/32)] bit mask directly).
+ * For every request b, node i < T_b = num_nodes[b] and query head h:
+ *   q' = RoPE(q[b, i, h], position_ids[b, i]),  k' = RoPE(k_new[b, i, h / G], same)
+ *   k' and v_new[b, i, .] are written to cache slot P_b + i (P_b = prefix_len[b]);
+ *   out[b, i, h] = softmax_j(scale * q' . K_j) V_j over cache slots j < P_b + T_b,
+ *   where slot j < P_b is always visible and slot P_b + t is visible iff bit t of
+ *   mask row i is set. G = num_q_heads / num_kv_heads (grouped-query attention).
+ * RoPE is the rotate-half form with inverse frequencies rope_theta^(-2m/D).
+ *
+ * shape            batch, max_nodes (node stride of q/k_new/v_new/out), num_q_heads,
+ *                  max_prefix (an upper bound on every prefix_len[b], used to size
+ *                  the split-KV grid).
+ * q, out           [batch, max_nodes, num_q_heads, head_dim], cache->dtype.
+ * k_new, v_new     [batch, max_nodes, num_kv_heads, head_dim], cache->dtype.
+ * cache            one layer's KV cache (num_layers/layer_stride are ignored). The
+ *                  prefix keys must already be rotated. On return slots P_b ..
+ *                  P_b + T_b - 1 hold the tree's rotated keys and its values, and the
+ *                  slots after them up to the next multiple of 16 are zero.
+ * position_ids, mask  as produced by tsv_tree_build_meta for the same max_nodes.
+ * workspace        tsv_tree_verify_attn_workspace_size(shape, cache) bytes of device
+ *                  scratch, 256-byte aligned.
+ * err              [batch] out (may be NULL): TSV_REQ_BAD_SIZE, TSV_REQ_CAPACITY or
+ *                  TSV_REQ_BAD_BLOCK; such a request's outputs are zero and its cache
+ *                  is left untouched.
+ * Supported: bf16 with head_dim 128 (tcgen05/TMEM tensor-core path), bf16 or f32 with
+ * head_dim 64 or 128 (CUDA-core path). num_q_heads % num_kv_heads == 0,
+ * max_nodes * G <= 1024.
+ * ------------------------------------------------------------------------------ */
+typedef struct {
+  int batch;
+  int max_nodes;
+  int num_q_heads;
+  int max_prefix;
+} tsv_attn_shape;
+
+size_t tsv_tree_verify_attn_workspace_size(const tsv_attn_shape* shape,
+                                           const tsv_kv_cache* cache);
+int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void* k_new,
+                         const void* v_new, const tsv_kv_cache* cache,
+                         const int32_t* prefix_len, const int32_t* num_nodes,
+                         const int32_t* position_ids, const uint32_t* mask, float rope_theta,
+                         float softmax_scale, void* out, void* workspace,
+                         size_t workspace_bytes, int32_t* err, tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_accept_and_compact — greedy acceptance walk and KV compaction.
+ *
+ * [HB] section 实现 (tree_speculative_generate: from the root, step to the child whose
+ * token equals the target's argmax at the current node, the lowest-numbered one;
+ * stop when none matches; the bonus token is the argmax at the last accepted node;
+ * only the accepted nodes' KV is kept, nothing is recomputed); [TRT] section
+ * 验证:在树上走一条路径 (the walk follows next_token / next_sibling) and section
+ * 接受之后:KV 从树形搬回线性 (the accepted nodes' KV moves to consecutive slots).
+ *
+ * tokens           [batch, max_nodes] in: node tokens (node 0 = root).
+ * next_token, next_sibling  [batch, max_nodes] in: links from tsv_tree_build_meta.
+ * target_argmax    [batch, max_nodes] in: the target model's argmax at every node.
+ * cache            may be NULL (walk only). Otherwise, for every layer l <
+ *                  num_layers, kv head and i < accept_len[b]:
+ *                  slot P_b + i <- slot P_b + accept_path[b][i] (keys and values).
+ * accept_path      [batch, max_depth + 1] out: accepted node indices, root first,
+ *                  -1 padded.
+ * accept_len       [batch] out: accepted nodes including the root (>= 1).
+ * bonus_token      [batch] out: target_argmax at the last accepted node.
+ * slot_map         [batch, max_depth + 1, 2] out: (source slot, destination slot) per
+ *                  accepted node, -1 padded.
+ * new_prefix_len   [batch] out: P_b + accept_len[b].
+ * err              [batch] out (may be NULL): TSV_REQ_BAD_SIZE, TSV_REQ_BAD_LINKS,
+ *                  TSV_REQ_CAPACITY or TSV_REQ_BAD_BLOCK; on an error only the root is
+ *                  accepted and the cache is not touched.
+ * ------------------------------------------------------------------------------ */
+int tsv_accept_and_compact(const int32_t* tokens, const int32_t* next_token,
+                           const int32_t* next_sibling, const int32_t* target_argmax,
+                           const int32_t* num_nodes, const int32_t* prefix_len, int batch,
+                           int max_nodes, int max_depth, const tsv_kv_cache* cache,
+                           int32_t* accept_path, int32_t* accept_len, int32_t* bonus_token,
+                           int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,
+                           tsv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSV_H */

@@ -1,0 +1,85 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol include/tsv.h
+declares, and rejects bad arguments on the host (these calls return before any CUDA
+work, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tree_speculative_decoding_verify_gb300 import _lib, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "tsv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tsv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_hot_path_calls():
+    names = declared_functions()
+    for want in ("tsv_draft_topk_expand", "tsv_draft_select_final", "tsv_tree_build_meta",
+                 "tsv_tree_verify_attn", "tsv_accept_and_compact"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(_lib.exported_symbols())
+
+
+def test_version_and_status_strings(lib):
+    assert b"sm_103a" in lib.tsv_version()
+    assert lib.tsv_status_string(0) == b"ok"
+    assert lib.tsv_status_string(3).startswith(b"workspace")
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: the checks fail first
+    # build_meta: max_nodes out of range
+    assert lib.tsv_tree_build_meta(p, p, p, 1, 0, 4, p, p, p, p, p, p, None, None) == 1
+    assert lib.tsv_tree_build_meta(p, p, p, 1, 257, 4, p, p, p, p, p, p, None, None) == 1
+    # topk: top_k too large; rows inconsistent with level; store too small
+    assert lib.tsv_draft_topk_expand(p, 1, 1, 100, 100, 17, 1, None, None, 100,
+                                     p, p, p, p, p, p, p, 1 << 20, None) == 1
+    assert lib.tsv_draft_topk_expand(p, 1, 2, 100, 100, 4, 1, None, None, 100,
+                                     p, p, p, p, p, p, p, 1 << 20, None) == 1
+    assert lib.tsv_draft_topk_expand(p, 1, 4, 100, 100, 4, 3, p, p, 10,
+                                     p, p, p, p, p, p, p, 1 << 20, None) == 1
+    # topk: workspace too small
+    assert lib.tsv_draft_topk_expand(p, 1, 1, 100, 100, 4, 1, None, None, 100,
+                                     p, p, p, p, p, p, p, 8, None) == 3
+    # select_final: total_tokens above the candidate count
+    assert lib.tsv_draft_select_final(p, p, p, 1, 10, 10, 11, p, 64, p, p, None, None) == 1
+    # attention: unsupported head_dim, GQA mismatch, missing workspace
+    k = ctypes.c_void_p(256)
+    cache = _lib.KVCacheDesc(k, k, 1, 8, 96, 0, 128, None, 0, 0, 1, 0)
+    shape = _lib.AttnShape(1, 61, 32, 2048)
+    assert lib.tsv_tree_verify_attn_workspace_size(ctypes.byref(shape), ctypes.byref(cache)) == 0
+    cache.head_dim = 128
+    shape.num_q_heads = 30
+    assert lib.tsv_tree_verify_attn(ctypes.byref(shape), p, p, p, ctypes.byref(cache), p, p, p, p,
+                                    1e4, 0.1, p, None, 0, None, None) == 1
+    shape.num_q_heads = 32
+    assert lib.tsv_tree_verify_attn_workspace_size(ctypes.byref(shape), ctypes.byref(cache)) > 0
+    assert lib.tsv_tree_verify_attn(ctypes.byref(shape), p, p, p, ctypes.byref(cache), p, p, p, p,
+                                    1e4, 0.1, p, None, 0, None, None) == 3
+    # accept: contiguous capacity not a multiple of 64
+    cache.capacity = 100
+    assert lib.tsv_accept_and_compact(p, p, p, p, p, p, 1, 61, 7, ctypes.byref(cache),
+                                      p, p, p, p, p, None, None) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert lib.tsv_tree_build_meta(None, None, None, 0, 8, 3, None, None, None, None, None,
+                                   None, None, None) == 0

@@ -1,0 +1,96 @@
+"""One whole hot-path step (expansion -> selection -> metadata -> attention -> accept +
+compaction) through the library vs the oracle's step on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import step as ostep
+from oracle import tree
+from tests import gpu_cases as gc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from tree_speculative_decoding_verify_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("name", ["llama8b", "tiny"])
+def test_whole_step_matches_oracle(name):
+    import tree_speculative_decoding_verify_gb300 as T
+    w = W.WORKLOADS[name]
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    d = gc.dev()
+    b = 0
+    tokens, parents, _ = gc.oracle_tree(w, b)
+    target = W.plant_target(w, b, tokens, parents, mode="first" if name == "tiny" else "walk")
+    p_len = w.max_prefix
+    q, k_new, v_new = W.new_qkv(w)
+    k_pre, v_pre = W.prefix_kv(w, b, p_len)
+    rnd = gc.as_bf16_f64 if dt == torch.bfloat16 else (lambda x: np.asarray(x, np.float64))
+    max_depth = (w.depth + 1) if w.fixed_parents is None else max(tree.depths(list(parents)))
+    want = ostep.hot_path_step(
+        gc.level_logits(w, b) if w.fixed_parents is None else None, w.top_k, w.total_tokens,
+        int(tokens[0]), rnd(q[b]), rnd(k_new[b]), rnd(v_new[b]), rnd(k_pre), rnd(v_pre), target,
+        w.theta, gc.scale_of(w), max_depth + 1) if w.fixed_parents is None else None
+
+    cap = int(np.ceil((p_len + w.num_nodes + 16) / 64) * 64)
+    kc = torch.zeros(1, w.num_kv_heads, cap, w.head_dim, dtype=dt, device=d)
+    vc = torch.zeros_like(kc)
+    kc[0, :, :p_len] = gc.to_dev(k_pre, dt)
+    vc[0, :, :p_len] = gc.to_dev(v_pre, dt)
+    cache = T.KVCache(kc, vc)
+    shape = T.TreeShape(1, w.num_q_heads, w.num_kv_heads, w.head_dim, p_len, vocab=w.vocab,
+                        top_k=w.top_k, depth=w.depth, total_tokens=w.total_tokens,
+                        fixed_nodes=w.num_nodes if w.fixed_parents is not None else 0,
+                        fixed_max_depth=max_depth)
+    hp = T.HotPath(shape, cache)
+    prefix = gc.i32([p_len])
+    if w.fixed_parents is not None:
+        hp.set_tree(gc.i32([tokens]), gc.i32([parents]), gc.i32([w.num_nodes]))
+        levels = None
+    else:
+        levels = [torch.from_numpy(x[None]).to(d) for x in gc.level_logits(w, b)]
+    hp.step(levels, gc.i32(W.root_tokens(w)[:1]) if levels else None, gc.to_dev(q, dt),
+            gc.to_dev(k_new, dt), gc.to_dev(v_new, dt), prefix, gc.i32([target]), w.theta,
+            gc.scale_of(w))
+    torch.cuda.synchronize()
+
+    assert hp.tokens.cpu().numpy()[0].tolist() == tokens.tolist()
+    assert hp.parents.cpu().numpy()[0].tolist() == parents.tolist()
+    assert hp.meta_err.item() == 0 and hp.attn_err.item() == 0 and hp.acc_err.item() == 0
+    if want is None:   # fixed tree: compare the parts the oracle step covers piecewise
+        from oracle import accept, attention
+        want = {}
+        out, k_rot, v_t = attention.tree_verify_attention(
+            rnd(q[b]), rnd(k_new[b]), rnd(v_new[b]), rnd(k_pre), rnd(v_pre), list(parents),
+            w.theta, gc.scale_of(w))
+        want["out"] = out
+        want["path"], want["bonus"] = accept.greedy_walk(list(tokens), list(parents), list(target))
+        want["mask"] = tree.pack_mask(tree.tree_mask(list(parents)))
+        want["pos"] = tree.position_ids(list(parents), p_len)
+    np.testing.assert_array_equal(hp.mask.cpu().numpy()[0].view(np.uint32), want["mask"])
+    np.testing.assert_array_equal(hp.position_ids.cpu().numpy()[0], want["pos"])
+    got = hp.out.float().cpu().numpy()[0]
+    diff = np.abs(got - want["out"])
+    if dt == torch.bfloat16:
+        assert diff.max() <= gc.BF16_ATOL_MAX and diff.mean() <= gc.BF16_ATOL_MEAN
+    else:
+        assert diff.max() <= gc.F32_ATOL_MAX
+    path = want["path"]
+    assert hp.accept_len.item() == len(path)
+    assert hp.accept_path.cpu().numpy()[0][:len(path)].tolist() == path
+    assert hp.bonus.item() == want["bonus"]
+    assert hp.new_prefix_len.item() == p_len + len(path)
+    assert len(path) >= 2
+    if "k_cache" in want:
+        n = len(path)
+        kv_got = kc[0, :, :p_len + n].float().cpu().numpy()
+        np.testing.assert_allclose(kv_got, want["k_cache"][:, :p_len + n], rtol=2.0 ** -7,
+                                   atol=1e-6)
+        np.testing.assert_array_equal(vc[0, :, :p_len + n].float().cpu().numpy(),
+                                      want["v_cache"][:, :p_len + n])

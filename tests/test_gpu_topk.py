@@ -1,0 +1,155 @@
+"""tsv_draft_topk_expand / tsv_draft_select_final vs the oracle, through the C ABI.
+Token ids, parents and store indices are bit-exact; fp32 scores within 1e-5 relative."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import draft
+from tests import gpu_cases as gc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from tree_speculative_decoding_verify_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def run_levels(levels_per_req, k, store_cap=None, stride_pad=0):
+    """Run every level on the GPU; levels_per_req[b][l] is [rows, V] fp32 numpy."""
+    import tree_speculative_decoding_verify_gb300 as T
+    b = len(levels_per_req)
+    nlev = len(levels_per_req[0])
+    v = levels_per_req[0][0].shape[1]
+    cap = store_cap or draft.num_candidates(k, nlev - 1)
+    d = gc.dev()
+    st = torch.full((b, cap), -7, dtype=torch.int32, device=d)
+    ss = torch.full((b, cap), -7.0, dtype=torch.float32, device=d)
+    sp = torch.full((b, cap), -7, dtype=torch.int32, device=d)
+    fronts = [(torch.zeros(b, k, dtype=torch.int32, device=d),
+               torch.zeros(b, k, dtype=torch.float32, device=d),
+               torch.zeros(b, k, dtype=torch.int32, device=d)) for _ in range(2)]
+    ws_n = max(T.draft_topk_expand_workspace_size(b, r, v, k) for r in (1, k))
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=d)
+    history = []
+    cur = None
+    for li in range(nlev):
+        rows = levels_per_req[0][li].shape[0]
+        host = np.zeros((b, rows, v + stride_pad), dtype=np.float32)
+        for bi in range(b):
+            host[bi, :, :v] = levels_per_req[bi][li]
+        lg = torch.from_numpy(host).to(d)[:, :, :v]
+        nxt = fronts[li % 2]
+        T.draft_topk_expand(lg, k, li + 1, None if cur is None else cur[1],
+                            None if cur is None else cur[2], st, ss, sp, *nxt, ws)
+        torch.cuda.synchronize()
+        history.append(tuple(t.cpu().numpy().copy() for t in nxt))
+        cur = nxt
+    return st.cpu().numpy(), ss.cpu().numpy(), sp.cpu().numpy(), history
+
+
+def compare(levels_per_req, k, **kw):
+    st, ss, sp, hist = run_levels(levels_per_req, k, **kw)
+    for b, levels in enumerate(levels_per_req):
+        exp = draft.topk_generate(levels, k)
+        c = exp.store_token.size
+        np.testing.assert_array_equal(st[b, :c], exp.store_token)
+        np.testing.assert_array_equal(sp[b, :c], exp.store_parent)
+        np.testing.assert_allclose(ss[b, :c], exp.store_score, rtol=gc.SCORE_RTOL, atol=0)
+        for li, lv in enumerate(exp.levels):
+            off = draft.level_store_offset(li + 1, k)
+            ft, fs, fi = hist[li]
+            assert fi[b].tolist() == [off + f for f in lv.selected], f"level {li + 1}"
+            assert ft[b].tolist() == [int(lv.tokens[f]) for f in lv.selected]
+    return st, ss, sp
+
+
+@pytest.mark.parametrize("v", [64, 1000, 4001, 32000])
+def test_levels_small_and_ragged_vocab(v):
+    rng = np.random.default_rng(v)
+    k, depth = 4, 3
+    reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
+             for l in range(depth + 1)] for _ in range(3)]
+    compare(reqs, k)
+
+
+def test_strided_rows_and_max_topk():
+    rng = np.random.default_rng(5)
+    k, v = 16, 3000
+    reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
+             for l in range(3)] for _ in range(2)]
+    compare(reqs, k, stride_pad=12)
+    compare(reqs, k, stride_pad=3)        # unaligned row stride -> scalar loads
+
+
+def test_exact_ties_go_to_lower_ids():
+    rng = np.random.default_rng(9)
+    k, v = 5, 777
+    reqs = []
+    for _ in range(2):
+        l1 = rng.integers(-3, 3, size=(1, v)).astype(np.float32)
+        l2 = np.tile(rng.integers(-3, 3, size=(1, v)).astype(np.float32), (k, 1))  # equal rows
+        reqs.append([l1, l2])
+    st, ss, sp = compare(reqs, k)
+    assert st.shape[1] == k + k * k
+
+
+def test_llama8b_expansion_and_final_selection():
+    import tree_speculative_decoding_verify_gb300 as T
+    w = W.WORKLOADS["llama8b"]
+    levels = gc.level_logits(w, 0)
+    st, ss, sp = compare([levels], w.top_k)
+    tokens, parents, exp = gc.oracle_tree(w, 0)
+    assert draft.margins(exp, w.total_tokens) > 0
+    d = gc.dev()
+    tok = torch.zeros(1, w.num_nodes + 3, dtype=torch.int32, device=d)
+    par = torch.zeros_like(tok)
+    nn = torch.zeros(1, dtype=torch.int32, device=d)
+    T.draft_select_final(gc.i32(st), torch.from_numpy(ss).to(d), gc.i32(sp), w.num_candidates,
+                         w.total_tokens, gc.i32(W.root_tokens(w)), tok, par, nn)
+    torch.cuda.synchronize()
+    assert tok.cpu().numpy()[0, :w.num_nodes].tolist() == tokens.tolist()
+    assert par.cpu().numpy()[0, :w.num_nodes].tolist() == parents.tolist()
+    assert tok.cpu().numpy()[0, w.num_nodes:].tolist() == [-1] * 3
+    assert nn.item() == w.num_nodes
+
+
+@pytest.mark.parametrize("name", ["long70b", "serving"])
+def test_workload_trees(name):
+    w = W.WORKLOADS[name]
+    nreq = 4 if name == "serving" else 1
+    compare([gc.level_logits(w, b) for b in range(nreq)], w.top_k)
+
+
+def test_sweep_level_640_rows_of_128256():
+    """One level of the batch-64 sweep: logits [64 x 10, 128256]; rows checked on a
+    sample of requests against the oracle's per-row top-k and log-probabilities."""
+    import tree_speculative_decoding_verify_gb300 as T
+    w = W.WORKLOADS["sweep"]
+    k = w.top_k
+    host = np.stack([W.draft_logits(w, b, 2) for b in range(w.batch)])   # [64, 10, V]
+    d = gc.dev()
+    lg = torch.from_numpy(host).to(d)
+    cap = draft.num_candidates(k, w.depth)
+    st = torch.zeros(w.batch, cap, dtype=torch.int32, device=d)
+    ss = torch.zeros(w.batch, cap, dtype=torch.float32, device=d)
+    sp = torch.zeros(w.batch, cap, dtype=torch.int32, device=d)
+    fin_s = torch.zeros(w.batch, k, dtype=torch.float32, device=d)
+    fin_i = (torch.arange(k, dtype=torch.int32, device=d) + 100).repeat(w.batch, 1)
+    outs = [torch.zeros(w.batch, k, dtype=torch.int32, device=d),
+            torch.zeros(w.batch, k, dtype=torch.float32, device=d),
+            torch.zeros(w.batch, k, dtype=torch.int32, device=d)]
+    ws = torch.empty(T.draft_topk_expand_workspace_size(w.batch, k, w.vocab, k),
+                     dtype=torch.uint8, device=d)
+    T.draft_topk_expand(lg, k, 2, fin_s, fin_i, st, ss, sp, *outs, ws)
+    torch.cuda.synchronize()
+    st, ss, sp = st.cpu().numpy(), ss.cpu().numpy(), sp.cpu().numpy()
+    for b in (0, 17, 63):
+        lv = draft.expand_level(host[b], k, np.zeros(k, np.float32), np.arange(k) + 100)
+        np.testing.assert_array_equal(st[b, k:k + k * k], lv.tokens)
+        np.testing.assert_array_equal(sp[b, k:k + k * k], lv.parent_store)
+        np.testing.assert_allclose(ss[b, k:k + k * k], lv.cu, rtol=gc.SCORE_RTOL)
+        assert outs[2].cpu().numpy()[b].tolist() == [k + f for f in lv.selected]

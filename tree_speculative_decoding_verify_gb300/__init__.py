@@ -1,0 +1,12 @@
+"""GB300-native tree speculative-decoding verification (EAGLE-2/3 dynamic trees).
+
+The compute lives in libtsv.so (hand-written CUDA for sm_103a, C ABI in include/tsv.h);
+this package is its Python binding plus a small driver that chains the calls of one
+hot-path step over preallocated device buffers.
+"""
+from ._lib import (  # noqa: F401
+    KV_BLOCK, MAX_NODES, MAX_TOPK, REQ_CODES, KVCache, TsvError, accept_and_compact,
+    draft_select_final, draft_topk_expand, draft_topk_expand_workspace_size, exported_symbols,
+    lib, tree_build_meta, tree_verify_attn, tree_verify_attn_workspace_size,
+)
+from .pipeline import HotPath, TreeShape  # noqa: F401

@@ -1,0 +1,472 @@
+// Draft tree expansion: per-row log-softmax + top-k, cumulative scores, joint top-k,
+// and the final total_tokens selection.
+//
+// Page: the EAGLE v2 dynamic-tree walkthrough, section 3 (树的生长, topK_generate):
+// each frontier row takes its top_k tokens and log-probabilities, a candidate's score is
+// its parent's score plus its log-probability (cu_scores = topk_p + scores[:, None]), a
+// joint top_k over the top_k * top_k candidates forms the next frontier, and after the
+// last level the total_tokens best of all stored candidates are kept. Candidate layout
+// follows "TensorRT-LLM 源码完全拆解(二十二)", section 树的三套账 (flat = parent * K +
+// child, parent = flat / K).
+//
+// Stage A (streaming, HBM-bound): one CTA per (row, vocab chunk) reads the chunk once
+// with 128-bit loads, keeps a per-thread sorted top-K list in registers and a sum of
+// exp(x - ref) against the running maximum ref (fp32 sums of 16 terms flushed into an
+// fp64 accumulator; a new maximum rescales the fp64 sum exactly), then merges the 256
+// lists with a warp tournament and writes the chunk's partial result. Keeping ref at the
+// maximum makes x - ref exact for every term that matters, so the log-sum-exp is good
+// to about 1e-9 and the fp32 log-probabilities round like the fp64 ones.
+// Stage B (tiny): one CTA per request merges the chunks of every row (fp64 log-sum-exp,
+// list tournament), writes the level's candidates to the store, and runs the joint
+// top-K of the cumulative scores.
+#include <float.h>
+#include <limits.h>
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tsv {
+namespace {
+
+constexpr int KMAX = TSV_MAX_TOPK;
+constexpr int A_THREADS = 256;
+constexpr int A_WARPS = A_THREADS / 32;
+constexpr int MAX_CHUNKS = 32;
+constexpr int B_THREADS = 128;
+constexpr int B_WARPS = B_THREADS / 32;
+
+struct ChunkStat {
+  double sum;  // sum of exp(x - ref) over the chunk
+  float ref;
+  float pad;
+};
+
+struct TopkWs {
+  ChunkStat* stat;  // [rows_total, chunks]
+  float* val;       // [rows_total, chunks, K]
+  int32_t* idx;     // [rows_total, chunks, K]
+};
+
+__host__ __device__ inline TopkWs carve(void* ws, int rows_total, int chunks, int k) {
+  char* p = static_cast<char*>(ws);
+  TopkWs w;
+  const size_t n = (size_t)rows_total * chunks;
+  w.stat = reinterpret_cast<ChunkStat*>(p);
+  p += (n * sizeof(ChunkStat) + 255) & ~size_t(255);
+  w.val = reinterpret_cast<float*>(p);
+  p += (n * k * sizeof(float) + 255) & ~size_t(255);
+  w.idx = reinterpret_cast<int32_t*>(p);
+  return w;
+}
+
+// Per-thread state: sorted top-K (best first) and the exp-sum against ref.
+struct RowState {
+  float v[KMAX];
+  int i[KMAX];
+  float thr_v;
+  int thr_i;
+  float ref;  // running maximum
+  float g;    // fp32 sum of the current group of terms
+  double d;   // fp64 sum of the flushed groups
+};
+
+__device__ __forceinline__ void flush(RowState& st) {
+  st.d += (double)st.g;
+  st.g = 0.f;
+}
+
+__device__ __forceinline__ void consider(RowState& st, int k, float x, int idx) {
+  if (x > st.ref) {  // new maximum: rescale the accumulated sum in fp64 (rare)
+    flush(st);
+    st.d *= exp((double)st.ref - (double)x);
+    st.ref = x;
+  }
+  st.g += expf(x - st.ref);
+  if (better(x, idx, st.thr_v, st.thr_i)) {
+    float cv = x;
+    int ci = idx;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        const bool sw = better(cv, ci, st.v[j], st.i[j]);
+        const float tv = st.v[j];
+        const int ti = st.i[j];
+        st.v[j] = sw ? cv : tv;
+        st.i[j] = sw ? ci : ti;
+        cv = sw ? tv : cv;
+        ci = sw ? ti : ci;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j == k - 1) { st.thr_v = st.v[j]; st.thr_i = st.i[j]; }
+  }
+}
+
+// (ref, sum) pairs combine against the larger reference; exp only when they differ.
+__device__ __forceinline__ void combine(float& r, double& s, float r2, double s2) {
+  if (r2 > r) {
+    s = s * exp((double)r - (double)r2) + s2;
+    r = r2;
+  } else if (r2 < r) {
+    s += s2 * exp((double)r2 - (double)r);
+  } else {
+    s += s2;
+  }
+}
+
+__device__ __forceinline__ void warp_combine(float& r, double& s) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float r2 = __shfl_xor_sync(FULL, r, o);
+    const double s2 = __shfl_xor_sync(FULL, s, o);
+    combine(r, s, r2, s2);
+  }
+}
+
+__device__ __forceinline__ void warp_argmax(float& v, int& i, int& lane_of) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(FULL, v, o);
+    const int oi = __shfl_xor_sync(FULL, i, o);
+    const int ol = __shfl_xor_sync(FULL, lane_of, o);
+    if (better(ov, oi, v, i)) { v = ov; i = oi; lane_of = ol; }
+  }
+}
+
+__device__ __forceinline__ float4 ld_stream(const float4* p) {
+  float4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p));
+  return r;
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(A_THREADS)
+topk_chunk_kernel(const float* __restrict__ logits, int64_t row_stride, int vocab, int k,
+                  int chunks, int chunk_len, TopkWs ws) {
+  __shared__ float s_lv[A_THREADS][KMAX + 1];
+  __shared__ int s_li[A_THREADS][KMAX + 1];
+  __shared__ float s_wv[A_WARPS][KMAX];
+  __shared__ int s_wi[A_WARPS][KMAX];
+  __shared__ float s_red[A_WARPS];
+  __shared__ double s_sum[A_WARPS];
+
+  const int row = blockIdx.y, chunk = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* x = logits + (int64_t)row * row_stride;
+  const int start = chunk * chunk_len;
+  const int end = min(vocab, start + chunk_len);
+
+  RowState st;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) { st.v[j] = -INFINITY; st.i[j] = INT_MAX; }
+  st.thr_v = -INFINITY;
+  st.thr_i = INT_MAX;
+  st.g = 0.f;
+  st.d = 0.0;
+
+  // Common starting reference: the largest of the first elements every thread sees.
+  float first = -INFINITY;
+  for (int e = start + tid * 4; e < min(end, start + tid * 4 + 4); ++e) first = fmaxf(first, x[e]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
+  if (lane == 0) s_red[warp] = first;
+  __syncthreads();
+  first = s_red[0];
+#pragma unroll
+  for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, s_red[w]);
+  st.ref = fmaxf(first, -FLT_MAX);  // finite, so x = -inf gives a zero term
+
+  if (VEC) {
+    const float4* x4 = reinterpret_cast<const float4*>(x + start);
+    const int n4 = (end - start) >> 2;
+    int q = tid;
+    constexpr int U = 4;
+    for (; q + (U - 1) * A_THREADS < n4; q += U * A_THREADS) {
+      float4 r[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) r[u] = ld_stream(x4 + q + u * A_THREADS);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = start + 4 * (q + u * A_THREADS);
+        consider(st, k, r[u].x, e);
+        consider(st, k, r[u].y, e + 1);
+        consider(st, k, r[u].z, e + 2);
+        consider(st, k, r[u].w, e + 3);
+      }
+      flush(st);
+    }
+    for (; q < n4; q += A_THREADS) {
+      const float4 r = ld_stream(x4 + q);
+      const int e = start + 4 * q;
+      consider(st, k, r.x, e);
+      consider(st, k, r.y, e + 1);
+      consider(st, k, r.z, e + 2);
+      consider(st, k, r.w, e + 3);
+      flush(st);
+    }
+    for (int e = start + 4 * n4 + tid; e < end; e += A_THREADS) consider(st, k, x[e], e);
+  } else {
+    for (int e = start + tid; e < end; e += A_THREADS) {
+      consider(st, k, x[e], e);
+      if (((e - start) / A_THREADS & 15) == 15) flush(st);
+    }
+  }
+  flush(st);
+
+  // Combine the (ref, sum) pairs of the block.
+  float R = st.ref;
+  double part = st.d;
+  warp_combine(R, part);
+  __syncthreads();  // s_red was read for the starting reference
+  if (lane == 0) { s_red[warp] = R; s_sum[warp] = part; }
+
+  // Top-K: every thread's sorted list -> warp tournament -> block tournament.
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) { s_lv[tid][j] = st.v[j]; s_li[tid][j] = st.i[j]; }
+  __syncthreads();
+  {
+    int ptr = 0;
+    for (int r = 0; r < k; ++r) {
+      float v = s_lv[tid][ptr];
+      int i = s_li[tid][ptr];
+      int who = lane;
+      warp_argmax(v, i, who);
+      if (lane == who) ++ptr;
+      if (lane == 0) { s_wv[warp][r] = v; s_wi[warp][r] = i; }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int ptr = 0;
+    const size_t base = ((size_t)row * chunks + chunk) * k;
+    for (int r = 0; r < k; ++r) {
+      float v = lane < A_WARPS ? s_wv[lane][ptr] : -INFINITY;
+      int i = lane < A_WARPS ? s_wi[lane][ptr] : INT_MAX;
+      int who = lane;
+      warp_argmax(v, i, who);
+      if (lane == who) ++ptr;
+      if (lane == 0) { ws.val[base + r] = v; ws.idx[base + r] = i; }
+    }
+    if (lane == 0) {
+      float rr = s_red[0];
+      double total = s_sum[0];
+      for (int w = 1; w < A_WARPS; ++w) combine(rr, total, s_red[w], s_sum[w]);
+      ChunkStat cs;
+      cs.sum = total;
+      cs.ref = rr;
+      cs.pad = 0.f;
+      ws.stat[(size_t)row * chunks + chunk] = cs;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(B_THREADS)
+topk_level_kernel(int rows, int k, int chunks, int level, TopkWs ws,
+                  const float* __restrict__ front_score_in, const int32_t* __restrict__ front_store_in,
+                  int store_cap, int32_t* __restrict__ store_token, float* __restrict__ store_score,
+                  int32_t* __restrict__ store_parent, int32_t* __restrict__ front_token_out,
+                  float* __restrict__ front_score_out, int32_t* __restrict__ front_store_out) {
+  __shared__ float s_cv[B_WARPS][MAX_CHUNKS][KMAX];
+  __shared__ int s_ci[B_WARPS][MAX_CHUNKS][KMAX];
+  __shared__ float s_cu[KMAX * KMAX];
+  __shared__ int s_tok[KMAX * KMAX];
+  const int b = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int off = level == 1 ? 0 : k + (level - 2) * k * k;
+  const int64_t srow = (int64_t)b * store_cap;
+
+  for (int s = warp; s < rows; s += B_WARPS) {
+    const int row = b * rows + s;
+    // Row log-sum-exp in fp64 from the chunk partial sums.
+    float R = -INFINITY;
+    double sum = 0.0;
+    if (lane < chunks) {
+      const ChunkStat cs = ws.stat[(size_t)row * chunks + lane];
+      R = cs.ref;
+      sum = cs.sum;
+    }
+    warp_combine(R, sum);
+    const double lse = (double)R + log(sum);
+
+    // Stage the chunk lists, then a tournament over them.
+    for (int t = lane; t < chunks * k; t += 32) {
+      const int c = t / k, j = t % k;
+      const size_t g = ((size_t)row * chunks + c) * k + j;
+      s_cv[warp][c][j] = ws.val[g];
+      s_ci[warp][c][j] = ws.idx[g];
+    }
+    __syncwarp();
+    const float pscore = level == 1 ? 0.0f : front_score_in[row];
+    const int pstore = level == 1 ? -1 : front_store_in[row];
+    int ptr = 0;
+    for (int r = 0; r < k; ++r) {
+      float v = (lane < chunks && ptr < k) ? s_cv[warp][lane][ptr] : -INFINITY;
+      int i = (lane < chunks && ptr < k) ? s_ci[warp][lane][ptr] : INT_MAX;
+      int who = lane;
+      warp_argmax(v, i, who);
+      if (lane == who) ++ptr;
+      if (lane == 0) {
+        const float logp = (float)((double)v - lse);
+        const float cu = pscore + logp;
+        const int flat = s * k + r;
+        store_token[srow + off + flat] = i;
+        store_score[srow + off + flat] = cu;
+        store_parent[srow + off + flat] = pstore;
+        s_cu[flat] = cu;
+        s_tok[flat] = i;
+      }
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // Joint top-K over the rows * K cumulative scores (ties to the lower flat index).
+  if (warp == 0) {
+    const int n = rows * k;
+    unsigned taken = 0;  // bit j: flat lane + 32 j taken
+    for (int r = 0; r < k; ++r) {
+      float v = -INFINITY;
+      int i = INT_MAX;
+      for (int j = 0; lane + 32 * j < n; ++j) {
+        const int f = lane + 32 * j;
+        if (!(taken >> j & 1u) && better(s_cu[f], f, v, i)) { v = s_cu[f]; i = f; }
+      }
+      int who = lane;
+      warp_argmax(v, i, who);
+      if (lane == who) taken |= 1u << ((i - lane) / 32);
+      if (lane == 0) {
+        front_token_out[b * k + r] = s_tok[i];
+        front_score_out[b * k + r] = v;
+        front_store_out[b * k + r] = off + i;
+      }
+    }
+  }
+}
+
+// ---- final selection --------------------------------------------------------------
+constexpr int F_THREADS = 512;
+
+__global__ void __launch_bounds__(F_THREADS)
+select_final_kernel(const int32_t* __restrict__ store_token, const float* __restrict__ store_score,
+                    const int32_t* __restrict__ store_parent, int C, int store_cap, int total,
+                    const int32_t* __restrict__ root_token, int max_nodes,
+                    int32_t* __restrict__ tokens, int32_t* __restrict__ parents,
+                    int32_t* __restrict__ num_nodes) {
+  extern __shared__ unsigned char smem[];
+  float* s_score = reinterpret_cast<float*>(smem);
+  int* s_node = reinterpret_cast<int*>(s_score + C);
+  __shared__ int s_warp[F_THREADS / 32];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t srow = (int64_t)b * store_cap;
+  for (int c = tid; c < C; c += F_THREADS) s_score[c] = store_score[srow + c];
+  __syncthreads();
+
+  // Rank by counting; each thread owns a contiguous segment of candidates.
+  const int seg = (C + F_THREADS - 1) / F_THREADS;
+  const int c0 = min(C, tid * seg), c1 = min(C, c0 + seg);
+  int mine = 0;
+  for (int c = c0; c < c1; ++c) {
+    const float v = s_score[c];
+    int rank = 0;
+    for (int j = 0; j < C && rank < total; ++j) rank += better(s_score[j], j, v, c) ? 1 : 0;
+    const bool chosen = rank < total;
+    s_node[c] = chosen ? 1 : 0;
+    mine += chosen;
+  }
+  // Exclusive scan of the per-thread counts -> node numbers in ascending store order.
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int before = incl - mine;
+  for (int w = 0; w < warp; ++w) before += s_warp[w];
+  for (int c = c0; c < c1; ++c) {
+    if (s_node[c]) s_node[c] = 1 + before++;
+  }
+  __syncthreads();
+  const int64_t trow = (int64_t)b * max_nodes;
+  for (int n = tid; n < max_nodes; n += F_THREADS) {
+    if (n > total) { tokens[trow + n] = -1; parents[trow + n] = -1; }
+  }
+  if (tid == 0) {
+    tokens[trow] = root_token[b];
+    parents[trow] = -1;
+    if (num_nodes) num_nodes[b] = total + 1;
+  }
+  for (int c = tid; c < C; c += F_THREADS) {
+    const int node = s_node[c];
+    if (!node) continue;
+    tokens[trow + node] = store_token[srow + c];
+    const int p = store_parent[srow + c];
+    const int pn = (p >= 0 && p < C) ? s_node[p] : 0;
+    parents[trow + node] = pn;
+  }
+}
+
+}  // namespace
+
+TopkPlan plan_topk(int batch, int rows, int vocab, int top_k) {
+  TopkPlan p{};
+  const int64_t rows_total = (int64_t)batch * rows;
+  const int64_t target = 4LL * device_sm_count();
+  int chunks = (int)std::min<int64_t>(MAX_CHUNKS, std::max<int64_t>(1, ceil_div(target, rows_total)));
+  // at least 2048 entries per chunk, and chunk lengths a multiple of 4
+  chunks = (int)std::max<int64_t>(1, std::min<int64_t>(chunks, ceil_div(vocab, 2048)));
+  int chunk_len = (int)round_up(ceil_div(vocab, chunks), 4);
+  chunks = (int)ceil_div(vocab, chunk_len);
+  p.chunks = chunks;
+  p.chunk_len = chunk_len;
+  const size_t n = (size_t)rows_total * chunks;
+  p.ws_bytes = align256(n * sizeof(ChunkStat)) + align256(n * top_k * sizeof(float)) +
+               align256(n * top_k * sizeof(int32_t));
+  return p;
+}
+
+int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_stride, int vocab,
+                       int top_k, int level, const float* front_score_in,
+                       const int32_t* front_store_in, int store_cap, int32_t* store_token,
+                       float* store_score, int32_t* store_parent, int32_t* front_token_out,
+                       float* front_score_out, int32_t* front_store_out, void* ws,
+                       const TopkPlan& plan, cudaStream_t stream) {
+  const int rows_total = batch * rows;
+  TopkWs w = carve(ws, rows_total, plan.chunks, top_k);
+  dim3 grid_a(plan.chunks, rows_total);
+  const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (row_stride % 4 == 0);
+  if (vec)
+    topk_chunk_kernel<true><<<grid_a, A_THREADS, 0, stream>>>(logits, row_stride, vocab, top_k,
+                                                             plan.chunks, plan.chunk_len, w);
+  else
+    topk_chunk_kernel<false><<<grid_a, A_THREADS, 0, stream>>>(logits, row_stride, vocab, top_k,
+                                                              plan.chunks, plan.chunk_len, w);
+  int st = launch_status();
+  if (st != TSV_OK) return st;
+  topk_level_kernel<<<batch, B_THREADS, 0, stream>>>(
+      rows, top_k, plan.chunks, level, w, front_score_in, front_store_in, store_cap, store_token,
+      store_score, store_parent, front_token_out, front_score_out, front_store_out);
+  return launch_status();
+}
+
+int launch_select_final(const int32_t* store_token, const float* store_score,
+                        const int32_t* store_parent, int batch, int num_candidates,
+                        int store_cap, int total_tokens, const int32_t* root_token,
+                        int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
+                        cudaStream_t stream) {
+  const size_t smem = (size_t)num_candidates * (sizeof(float) + sizeof(int));
+  select_final_kernel<<<batch, F_THREADS, smem, stream>>>(store_token, store_score, store_parent,
+                                                          num_candidates, store_cap, total_tokens,
+                                                          root_token, max_nodes, tokens, parents,
+                                                          num_nodes);
+  return launch_status();
+}
+
+}  // namespace tsv

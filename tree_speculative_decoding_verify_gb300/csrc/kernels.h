@@ -1,0 +1,63 @@
+// Internal launchers (one per kernel family); argument checks happen in api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/tsv.h"
+
+namespace tsv {
+
+int launch_build_meta(const int32_t* parents, const int32_t* num_nodes, const int32_t* prefix_len,
+                      int batch, int max_nodes, int max_depth, uint32_t* mask,
+                      int32_t* position_ids, int32_t* retrieve, int32_t* num_leaves,
+                      int32_t* next_token, int32_t* next_sibling, int32_t* err,
+                      cudaStream_t stream);
+
+int launch_accept_compact(const int32_t* tokens, const int32_t* next_token,
+                          const int32_t* next_sibling, const int32_t* target,
+                          const int32_t* num_nodes, const int32_t* prefix_len, int batch,
+                          int max_nodes, int max_depth, const tsv_kv_cache* cache,
+                          int32_t* accept_path, int32_t* accept_len, int32_t* bonus,
+                          int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,
+                          cudaStream_t stream);
+
+// Draft expansion.
+struct TopkPlan {
+  int chunks;         // CTAs per row in the streaming stage
+  int chunk_len;      // vocab entries per chunk (multiple of 4)
+  size_t ws_bytes;
+};
+TopkPlan plan_topk(int batch, int rows, int vocab, int top_k);
+int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_stride, int vocab,
+                       int top_k, int level, const float* front_score_in,
+                       const int32_t* front_store_in, int store_cap, int32_t* store_token,
+                       float* store_score, int32_t* store_parent, int32_t* front_token_out,
+                       float* front_score_out, int32_t* front_store_out, void* ws,
+                       const TopkPlan& plan, cudaStream_t stream);
+int launch_select_final(const int32_t* store_token, const float* store_score,
+                        const int32_t* store_parent, int batch, int num_candidates,
+                        int store_cap, int total_tokens, const int32_t* root_token,
+                        int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
+                        cudaStream_t stream);
+
+// Tree-verification attention.
+struct AttnPlan {
+  int batch, max_nodes, hq, hkv, group, head_dim, dtype;
+  int rows;           // max_nodes * group (query rows per kv head)
+  int rows_pad;       // rows rounded up to the M tile
+  int tile_keys;      // keys per split unit
+  int nsplit;         // splits along the keys
+  int tiles_per_split;
+  int max_prefix;
+  bool tensor_core;   // tcgen05 path
+  size_t off_qrot, off_opart, off_ml, off_valid, ws_bytes;
+};
+AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache);
+int launch_attn(const AttnPlan& plan, const void* q, const void* k_new, const void* v_new,
+                const tsv_kv_cache* cache, const int32_t* prefix_len, const int32_t* num_nodes,
+                const int32_t* position_ids, const uint32_t* mask, float rope_theta,
+                float softmax_scale, void* out, void* ws, int32_t* err, cudaStream_t stream);
+
+}  // namespace tsv

@@ -1,0 +1,142 @@
+"""One hot-path step over preallocated device buffers.
+
+    draft expansion (depth + 1 levels) -> final selection -> tree metadata ->
+    tree-verification attention (one layer) -> greedy acceptance + KV compaction
+
+Every stage is one or two calls into libtsv.so on the current stream; no stage reads
+anything back to the host, so a whole step can be captured in a CUDA graph.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+
+
+@dataclasses.dataclass(frozen=True)
+class TreeShape:
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    max_prefix: int
+    vocab: int = 0
+    top_k: int = 0
+    depth: int = 0            # expansion loop iterations after the base layer
+    total_tokens: int = 0     # draft nodes kept; the tree has total_tokens + 1 nodes
+    fixed_nodes: int = 0      # > 0: trees are given directly (no expansion)
+    fixed_max_depth: int = 0
+
+    @property
+    def max_nodes(self) -> int:
+        return self.fixed_nodes if self.fixed_nodes else self.total_tokens + 1
+
+    @property
+    def max_depth(self) -> int:
+        """Deepest node (edges from the root): one per draft level."""
+        return self.fixed_max_depth if self.fixed_nodes else self.depth + 1
+
+    @property
+    def num_candidates(self) -> int:
+        return self.top_k + self.depth * self.top_k * self.top_k
+
+
+class HotPath:
+    def __init__(self, shape: TreeShape, cache: _lib.KVCache, device=None):
+        self.s = shape
+        self.cache = cache
+        dev = torch.device(device or cache.k.device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        b, t, w = shape.batch, shape.max_nodes, (shape.max_nodes + 31) // 32
+        if not shape.fixed_nodes:
+            c, k = shape.num_candidates, shape.top_k
+            self.store_token = torch.zeros(b, c, **i32)
+            self.store_score = torch.zeros(b, c, dtype=torch.float32, device=dev)
+            self.store_parent = torch.zeros(b, c, **i32)
+            self.front = [(torch.zeros(b, k, **i32), torch.zeros(b, k, dtype=torch.float32, device=dev),
+                           torch.zeros(b, k, **i32)) for _ in range(2)]
+            ws = max(_lib.draft_topk_expand_workspace_size(b, 1, shape.vocab, k),
+                     _lib.draft_topk_expand_workspace_size(b, k, shape.vocab, k))
+            self.topk_ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+        self.tokens = torch.full((b, t), -1, **i32)
+        self.parents = torch.full((b, t), -1, **i32)
+        self.num_nodes = torch.zeros(b, **i32)
+        self.mask = torch.zeros(b, t, w, **i32)
+        self.position_ids = torch.zeros(b, t, **i32)
+        self.retrieve = torch.zeros(b, t, shape.max_depth + 1, **i32)
+        self.num_leaves = torch.zeros(b, **i32)
+        self.next_token = torch.zeros(b, t, **i32)
+        self.next_sibling = torch.zeros(b, t, **i32)
+        self.meta_err = torch.zeros(b, **i32)
+        self.attn_err = torch.zeros(b, **i32)
+        self.acc_err = torch.zeros(b, **i32)
+        d = shape.head_dim
+        self.out = torch.zeros(b, t, shape.num_q_heads, d, dtype=cache.dtype, device=dev)
+        ws = _lib.tree_verify_attn_workspace_size((b, t, shape.num_q_heads, d), cache,
+                                                  shape.max_prefix)
+        if ws == 0:
+            raise _lib.TsvError("tree_verify_attn rejects this shape")
+        self.attn_ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.accept_path = torch.zeros(b, shape.max_depth + 1, **i32)
+        self.accept_len = torch.zeros(b, **i32)
+        self.bonus = torch.zeros(b, **i32)
+        self.slot_map = torch.zeros(b, shape.max_depth + 1, 2, **i32)
+        self.new_prefix_len = torch.zeros(b, **i32)
+
+    # -- stages ------------------------------------------------------------------------
+    def expand(self, level_logits: Sequence[torch.Tensor], root_token: torch.Tensor):
+        """level_logits[0]: [B, 1, V]; level_logits[l]: [B, K, V] fp32 (device)."""
+        s = self.s
+        if len(level_logits) != s.depth + 1:
+            raise ValueError(f"expected {s.depth + 1} levels of logits")
+        cur = None
+        for li, lg in enumerate(level_logits):
+            nxt = self.front[li % 2]
+            _lib.draft_topk_expand(lg, s.top_k, li + 1,
+                                   None if cur is None else cur[1],
+                                   None if cur is None else cur[2],
+                                   self.store_token, self.store_score, self.store_parent,
+                                   nxt[0], nxt[1], nxt[2], self.topk_ws)
+            cur = nxt
+        _lib.draft_select_final(self.store_token, self.store_score, self.store_parent,
+                                s.num_candidates, s.total_tokens, root_token, self.tokens,
+                                self.parents, self.num_nodes)
+
+    def set_tree(self, tokens: torch.Tensor, parents: torch.Tensor, num_nodes: torch.Tensor):
+        """Use given trees instead of the expansion (fixed-shape drafts)."""
+        self.tokens.copy_(tokens)
+        self.parents.copy_(parents)
+        self.num_nodes.copy_(num_nodes)
+
+    def build_meta(self, prefix_len: torch.Tensor):
+        _lib.tree_build_meta(self.parents, self.num_nodes, prefix_len, self.s.max_depth,
+                             self.mask, self.position_ids, self.retrieve, self.num_leaves,
+                             self.next_token, self.next_sibling, self.meta_err)
+
+    def verify(self, q, k_new, v_new, prefix_len, rope_theta: float, softmax_scale: float):
+        _lib.tree_verify_attn(q, k_new, v_new, self.cache, prefix_len, self.num_nodes,
+                              self.position_ids, self.mask, rope_theta, softmax_scale, self.out,
+                              self.attn_ws, self.s.max_prefix, self.attn_err)
+
+    def accept(self, target_argmax, prefix_len, compact: bool = True):
+        _lib.accept_and_compact(self.tokens, self.next_token, self.next_sibling, target_argmax,
+                                self.num_nodes, prefix_len, self.s.max_depth,
+                                self.cache if compact else None, self.accept_path,
+                                self.accept_len, self.bonus, self.slot_map, self.new_prefix_len,
+                                self.acc_err)
+
+    def step(self, level_logits, root_token, q, k_new, v_new, prefix_len, target_argmax,
+             rope_theta: float, softmax_scale: float):
+        if not self.s.fixed_nodes:
+            self.expand(level_logits, root_token)
+        self.build_meta(prefix_len)
+        self.verify(q, k_new, v_new, prefix_len, rope_theta, softmax_scale)
+        self.accept(target_argmax, prefix_len)
+
+    # launches of libtsv kernels per step (for the bench's launch count)
+    def kernels_per_step(self) -> int:
+        n = 0 if self.s.fixed_nodes else 2 * (self.s.depth + 1) + 1
+        return n + 1 + 3 + 1
