@@ -1,0 +1,437 @@
+"""Benchmark of the tree-verification hot path on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one whole pass of the hot path over one batch of synthetic input:
+depth + 1 levels of draft top-k expansion, the final total_tokens selection, the
+tree metadata, tree-verification attention of one layer (RoPE, KV append, split-KV
+attention, merge) and the greedy acceptance with KV compaction. Inputs are resident
+in HBM before the timed region; the step is replayed from a CUDA graph; L2 is flushed
+(a 256 MiB write) between timed launches. The JSON line reports steps/s (whole job),
+the per-call times, the roofline of the attention call against MEASURED_PEAKS.json,
+an end-to-end number through host buffers, and the CPU oracle as a baseline.
+
+--impl reference times the CPU oracle (the reference arm: a deliberately slow,
+obviously correct restatement of the method) on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "tree-verify attn µs/layer, achieved HBM GB/s and % roofline; top-k rows/s"
+UNIT = "layer-verify steps/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def plain(x):
+    """JSON-safe copy (numpy scalars -> Python numbers)."""
+    if isinstance(x, dict):
+        return {k: plain(v) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [plain(v) for v in x]
+    if isinstance(x, np.generic):
+        return x.item()
+    return x
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama8b", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--total-tokens", type=int, default=0)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def workload(args):
+    w = W.WORKLOADS[args.workload]
+    if args.total_tokens:
+        w = w.with_(total_tokens=args.total_tokens)
+    if w.fixed_parents is not None:
+        raise SystemExit("the bench runs dynamic-tree workloads")
+    return w
+
+
+def algorithmic(w, prefix, depths_per_req, esize=2):
+    """Algorithmic bytes and FLOPs of one tree_verify_attn call.
+
+    bytes: KV prefix read once per KV head, the tree's new k/v read and written to the
+    cache, q read and out written. FLOPs: 4 * D per visible (query head, key) pair.
+    """
+    hkv, hq, d = w.num_kv_heads, w.num_q_heads, w.head_dim
+    nbytes = 0
+    flops = 0
+    for p, deps in zip(prefix, depths_per_req):
+        t = len(deps)
+        nbytes += 2 * p * hkv * d * esize + 4 * t * hkv * d * esize + 2 * t * hq * d * esize
+        flops += 4 * d * hq * sum(p + dep + 1 for dep in deps)
+    return nbytes, flops
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return m["hbm_gbs"], m["bf16_tflops"], "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, out):
+        self.out = out
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+                 "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-i",
+                 os.environ.get("LOCAL_RANK", "0")],
+                stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        if not os.path.exists(self.out):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.out):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------------------
+def native(args):
+    import torch
+    import torch.distributed as dist
+
+    import tree_speculative_decoding_verify_gb300 as T
+    from tree_speculative_decoding_verify_gb300 import build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workload(args)
+    b, k, v = w.batch, w.top_k, w.vocab
+    prefix = W.prefix_lengths(w)
+    p_max = w.max_prefix
+    paged = w.paged
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1000 + rank)
+
+    # ---- inputs resident in HBM ------------------------------------------------------
+    levels = [torch.from_numpy(W.draft_logits_batch(w, lvl)).to(dev) for lvl in range(1, w.depth + 2)]
+    root = torch.from_numpy(W.root_tokens(w)).to(dev)
+    q, k_new, v_new = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in W.new_qkv(w))
+    t_max = w.num_nodes
+    cap = int(math.ceil((p_max + t_max + 16) / 64) * 64)
+    scale = w.scale
+    if paged:
+        table, pool = W.block_table(w, cap)
+        kc = (torch.randn(pool, w.num_kv_heads, 64, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
+        vc = (torch.randn(pool, w.num_kv_heads, 64, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
+        cache = T.KVCache(kc, vc, torch.from_numpy(table).to(dev))
+    else:
+        kc = (torch.randn(b, w.num_kv_heads, cap, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
+        vc = (torch.randn(b, w.num_kv_heads, cap, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
+        cache = T.KVCache(kc, vc)
+    shape = T.TreeShape(b, w.num_q_heads, w.num_kv_heads, w.head_dim, p_max, vocab=v, top_k=k,
+                        depth=w.depth, total_tokens=w.total_tokens)
+    hp = T.HotPath(shape, cache)
+    prefix_t = torch.from_numpy(prefix).to(dev)
+    sm_scale = 1.0 / math.sqrt(w.head_dim)
+
+    # the tree the expansion builds (deterministic) -> planted target argmax
+    hp.expand(levels, root)
+    torch.cuda.synchronize()
+    toks = hp.tokens.cpu().numpy()
+    pars = hp.parents.cpu().numpy()
+    target = np.stack([W.plant_target(w, i, toks[i], pars[i]) for i in range(b)])
+    target_t = torch.from_numpy(target).to(dev)
+    depths = []
+    for i in range(b):
+        d = []
+        for p in pars[i]:
+            d.append(0 if p < 0 else d[p] + 1)
+        depths.append(d)
+
+    def step():
+        hp.step(levels, root, q, k_new, v_new, prefix_t, target_t, w.theta, sm_scale)
+
+    def attn():
+        hp.verify(q, k_new, v_new, prefix_t, w.theta, sm_scale)
+
+    lvl_ws = hp.topk_ws
+    lvl_out = hp.front[1]
+
+    def topk_level():  # one expansion level (level 2: [B, K, V] rows)
+        T.draft_topk_expand(levels[1], k, 2, hp.front[0][1], hp.front[0][2], hp.store_token,
+                            hp.store_score, hp.store_parent, *lvl_out, lvl_ws)
+
+    flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    graphs = {}
+    with torch.cuda.stream(stream):
+        for _ in range(2):  # warm the allocator and the kernels before capture
+            step(); attn(); topk_level()
+        stream.synchronize()
+        for name, fn in (("step", step), ("attn", attn), ("topk", topk_level)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                fn()
+            graphs[name] = g
+    torch.cuda.synchronize()
+
+    def timed_loop(n, record):
+        ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(n)] for name in graphs}
+        with torch.cuda.stream(stream):
+            for i in range(n):
+                for name in ("step", "attn", "topk"):
+                    flush_buf.zero_()
+                    ev[name][i][0].record(stream)
+                    graphs[name].replay()
+                    ev[name][i][1].record(stream)
+        return ev
+
+    timed_loop(args.warmup, False)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+                    if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/tsv_clocks_{rank}.csv")
+    with clocks:
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        ev = timed_loop(args.steps, True)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    ms = {name: sum(a.elapsed_time(c) for a, c in ev[name]) / args.steps for name in ev}
+
+    # ---- end to end through host buffers --------------------------------------------
+    pin = lambda t: t.cpu().pin_memory()
+    h_levels = [pin(x) for x in levels]
+    h_q, h_k, h_v, h_tgt, h_root = pin(q), pin(k_new), pin(v_new), pin(target_t), pin(root)
+    h_out = {n: torch.empty_like(t, device="cpu").pin_memory() for n, t in
+             (("len", hp.accept_len), ("path", hp.accept_path), ("bonus", hp.bonus),
+              ("newlen", hp.new_prefix_len))}
+    h2d = sum(x.numel() * x.element_size() for x in h_levels + [h_q, h_k, h_v, h_tgt, h_root])
+    d2h = sum(x.numel() * x.element_size() for x in h_out.values())
+
+    def e2e_once():
+        for src, dst in zip(h_levels, levels):
+            dst.copy_(src, non_blocking=True)
+        for src, dst in ((h_q, q), (h_k, k_new), (h_v, v_new), (h_tgt, target_t), (h_root, root)):
+            dst.copy_(src, non_blocking=True)
+        graphs["step"].replay()
+        h_out["len"].copy_(hp.accept_len, non_blocking=True)
+        h_out["path"].copy_(hp.accept_path, non_blocking=True)
+        h_out["bonus"].copy_(hp.bonus, non_blocking=True)
+        h_out["newlen"].copy_(hp.new_prefix_len, non_blocking=True)
+
+    e2e_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush_buf.zero_()
+            a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_once()
+            c.record(stream)
+            c.synchronize()
+            if i >= args.warmup:
+                e2e_ms.append(a.elapsed_time(c))
+    e2e_step_ms = sum(e2e_ms) / len(e2e_ms)
+
+    # ---- max over ranks ---------------------------------------------------------------
+    step_ms = ms["step"]
+    if world > 1:
+        t = torch.tensor([step_ms, e2e_step_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_step_ms = t.tolist()
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    hbm, tf, src = peaks()
+    nbytes, flops = algorithmic(w, prefix, depths)
+    attn_s = ms["attn"] / 1e3
+    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tf * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = nbytes / attn_s / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = flops / attn_s / 1e12, tf, "TFLOP/s"
+    topk_rows = b * k / (ms["topk"] / 1e3)
+    topk_bytes = b * k * v * 4
+    kernels_step = hp.kernels_per_step()
+    line = {
+        "metric": METRIC, "value": world * 1e3 / step_ms, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded draft logits, q/k/v, KV cache; planted target argmax)",
+        "config": {"workload": w.name, "batch": b, "prefix": (int(prefix.min()), int(prefix.max())),
+                   "nodes": t_max, "top_k": k, "depth": w.depth, "vocab": v,
+                   "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "paged": paged, "l2": "flushed (256 MiB write) before every timed launch",
+                   "parallelism": f"replicas x{world}", "graph": "CUDA graph per step"},
+        "attn_us_per_layer": ms["attn"] * 1e3,
+        "attn_hbm_GBps": nbytes / attn_s / 1e9,
+        "attn_roofline_us": max(t_hbm, t_tc) * 1e6,
+        "topk_rows_per_s": topk_rows,
+        "topk_hbm_GBps": topk_bytes / (ms["topk"] / 1e3) / 1e9,
+        "nodes_kv_tokens_per_s": sum(len(d) * (p + len(d)) for p, d in zip(prefix, depths)) / attn_s,
+        "roofline": {"kernel": "tree_verify_attn (prep + split-KV attention + merge)",
+                     "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "peak_source": src, "traffic": None,
+                     "algorithmic_bytes": nbytes, "algorithmic_flops": flops},
+        "e2e": {"value": world * 1e3 / e2e_step_ms, "unit": UNIT, "ms_per_step": e2e_step_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (kernels_step + 3 + 2),
+        "wall_s_timed_region": t_wall,
+    }
+    ck = clocks.summary()
+    if ck:
+        line["clocks"] = ck
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(plain(line)))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# --------------------------------------------------------------------------------------
+def oracle_step_inputs(w, b):
+    levels = [W.draft_logits(w, b, lvl) for lvl in range(1, w.depth + 2)]
+    p = int(W.prefix_lengths(w)[b])
+    q, k_new, v_new = W.new_qkv(w.with_(batch=b + 1))
+    k_pre, v_pre = W.prefix_kv(w, b, p)
+    return levels, p, q[b], k_new[b], v_new[b], k_pre, v_pre
+
+
+def run_oracle_step(w, b, inputs):
+    from oracle import step
+    levels, p, q, k_new, v_new, k_pre, v_pre = inputs
+    f64 = lambda x: np.asarray(x, np.float64)
+    return step.hot_path_step(levels, w.top_k, w.total_tokens, int(W.root_tokens(w)[b]), f64(q),
+                              f64(k_new), f64(v_new), f64(k_pre), f64(v_pre),
+                              lambda t, par: W.plant_target(w, b, t, par), w.theta,
+                              1 / math.sqrt(w.head_dim), w.depth + 2)
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, seconds):
+    """The oracle timed on this host: whole oracle steps for one request at a time
+    (cycling through the batch) until `seconds` have passed; steps/s scaled to the
+    workload's batch (a step processes all B requests)."""
+    inputs = [oracle_step_inputs(w, b) for b in range(min(w.batch, 4))]
+    n = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or n == 0:
+        run_oracle_step(w, n % len(inputs), inputs[n % len(inputs)])
+        n += 1
+    dt = time.perf_counter() - t0
+    per_request = dt / n
+    return {"value": 1.0 / (per_request * w.batch), "unit": UNIT, "cores": cpu_threads(),
+            "kind": "oracle",
+            "sample": f"{n} oracle steps of single requests of the {w.name} workload "
+                      f"({dt:.1f} s), scaled to a batch of {w.batch}"}
+
+
+def reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workload(args)
+    inputs = [oracle_step_inputs(w, b) for b in range(min(w.batch, 2))]
+    for i in range(args.warmup):
+        run_oracle_step(w, i % len(inputs), inputs[i % len(inputs)])
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        run_oracle_step(w, i % len(inputs), inputs[i % len(inputs)])
+        times.append(time.perf_counter() - t0)
+    per_req = sum(times) / len(times)
+    step_s = per_req * w.batch
+    value = 1.0 / step_s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": w.name, "batch": w.batch, "nodes": w.num_nodes,
+                   "sample": "each timed step is one request's oracle step, scaled by batch"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"{args.steps} single-request oracle steps of {w.name}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(plain(line)))
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if a.impl == "reference":
+        reference(a)
+    else:
+        native(a)

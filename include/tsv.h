@@ -63,7 +63,9 @@ enum tsv_request_error {
   TSV_REQ_BAD_SIZE = 4,     /* num_nodes[b] outside [1, max_nodes] or prefix_len[b] < 0 */
   TSV_REQ_CAPACITY = 5,     /* prefix_len[b] + num_nodes[b] does not fit the KV cache */
   TSV_REQ_BAD_BLOCK = 6,    /* a block-table entry outside [0, num_blocks) */
-  TSV_REQ_BAD_LINKS = 7     /* child/sibling links leave the tree */
+  TSV_REQ_BAD_LINKS = 7,    /* child/sibling links leave the tree */
+  TSV_REQ_TIMEOUT = 8       /* a bounded device-side wait gave up (the request's outputs
+                               are not valid; the GPU context stays usable) */
 };
 
 /* ---- limits ---- */
@@ -233,7 +235,8 @@ int tsv_tree_build_meta(const int32_t* parents, const int32_t* num_nodes,
  *                  scratch, 256-byte aligned.
  * err              [batch] out (may be NULL): TSV_REQ_BAD_SIZE, TSV_REQ_CAPACITY or
  *                  TSV_REQ_BAD_BLOCK; such a request's outputs are zero and its cache
- *                  is left untouched.
+ *                  is left untouched. TSV_REQ_TIMEOUT if a bounded wait of the
+ *                  tensor-core kernel gave up (its outputs are then not valid).
  * Supported: bf16 with head_dim 128 (tcgen05/TMEM tensor-core path), bf16 or f32 with
  * head_dim 64 or 128 (CUDA-core path). num_q_heads % num_kv_heads == 0,
  * max_nodes * G <= 1024.

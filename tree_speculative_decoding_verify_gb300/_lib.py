@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libtsv.so")
 
 TSV_OK, TSV_ERR_INVALID_ARG, TSV_ERR_UNSUPPORTED, TSV_ERR_WORKSPACE, TSV_ERR_CUDA = range(5)
 REQ_CODES = {0: "ok", 1: "bad_root", 2: "bad_parent", 3: "too_deep", 4: "bad_size",
-             5: "capacity", 6: "bad_block", 7: "bad_links"}
+             5: "capacity", 6: "bad_block", 7: "bad_links", 8: "timeout"}
 DTYPE_F32, DTYPE_BF16 = 0, 1
 KV_CONTIGUOUS, KV_PAGED = 0, 1
 KV_BLOCK = 64
@@ -207,7 +207,10 @@ def draft_topk_expand(logits, top_k, level, front_score_in, front_store_in, stor
     if logits.dtype != torch.float32 or not logits.is_cuda or logits.dim() != 3:
         raise TypeError("logits must be a CUDA fp32 tensor [B, rows, V]")
     b, rows, v = logits.shape
-    if logits.stride(2) != 1 or logits.stride(0) != rows * logits.stride(1):
+    # the stride of a size-1 dimension is meaningless; take the row stride from the
+    # first dimension that has more than one entry
+    rs = logits.stride(1) if rows > 1 else (logits.stride(0) if b > 1 else v)
+    if (v > 1 and logits.stride(2) != 1) or rs < v or (b > 1 and logits.stride(0) != rows * rs):
         raise ValueError("logits rows must be evenly strided with unit element stride")
     cap = store_token.shape[1]
     for name, t, dt in (("store_token", store_token, torch.int32),
@@ -223,7 +226,7 @@ def draft_topk_expand(logits, top_k, level, front_score_in, front_store_in, stor
         _need(front_store_in, torch.int32, "front_store_in", (b, rows))
     _need(workspace, torch.uint8, "workspace")
     _check(lib().tsv_draft_topk_expand(
-        _ptr(logits), b, rows, logits.stride(1), v, top_k, level,
+        _ptr(logits), b, rows, rs, v, top_k, level,
         _ptr(front_score_in if level > 1 else None), _ptr(front_store_in if level > 1 else None),
         cap, _ptr(store_token), _ptr(store_score), _ptr(store_parent), _ptr(front_token_out),
         _ptr(front_score_out), _ptr(front_store_out), _ptr(workspace), workspace.numel(),
