@@ -229,7 +229,8 @@ int tsv_tree_build_meta(const int32_t* parents, const int32_t* num_nodes,
  * cache            one layer's KV cache (num_layers/layer_stride are ignored). The
  *                  prefix keys must already be rotated. On return slots P_b ..
  *                  P_b + T_b - 1 hold the tree's rotated keys and its values, and the
- *                  slots after them up to the next multiple of 16 are zero.
+ *                  slots from P_b + T_b up to the next slot index that is a multiple of
+ *                  16 are zero (the tensor-core path reads keys in steps of 16).
  * position_ids, mask  as produced by tsv_tree_build_meta for the same max_nodes.
  * workspace        tsv_tree_verify_attn_workspace_size(shape, cache) bytes of device
  *                  scratch, 256-byte aligned.

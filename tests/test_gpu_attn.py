@@ -56,8 +56,10 @@ def make_cache(c: Case):
     import tree_speculative_decoding_verify_gb300 as T
     dev = gc.dev()
     if not c.paged:
-        k = torch.zeros(c.b, c.hkv, c.capacity, c.d, dtype=c.dtype, device=dev)
-        v = torch.zeros_like(k)
+        # slots past the prefix hold NaN: a kernel that reads a slot it should not
+        # turns the output non-finite
+        k = torch.full((c.b, c.hkv, c.capacity, c.d), float("nan"), dtype=c.dtype, device=dev)
+        v = torch.full_like(k, float("nan"))
         for b in range(c.b):
             p = int(c.prefix[b])
             k[b, :, :p] = gc.to_dev(c.k_pre[b], c.dtype)
@@ -142,16 +144,18 @@ def check(c: Case, samples=None):
         out, k_rot, v_new = oracle_one(c, b, [kv])[kv]
         diffs.append(np.abs(got[b, :n, kv * g:(kv + 1) * g] - out).ravel())
         p = int(c.prefix[b])
-        pad = ((n + 15) // 16) * 16
-        ks, vs = logical_rows(cache, table, b, kv, list(range(p, p + pad)))
+        pad_end = ((p + n + 15) // 16) * 16        # zeros up to this slot
+        ks, vs = logical_rows(cache, table, b, kv, list(range(p, pad_end)))
         tol = 2.0 ** -7 if c.dtype == torch.bfloat16 else 1e-6
         np.testing.assert_allclose(ks[:n], k_rot, rtol=tol, atol=1e-6)
         np.testing.assert_array_equal(vs[:n], v_new)
         assert (ks[n:] == 0).all() and (vs[n:] == 0).all()
         # rows past the tree are zero
         assert (got[b, n:] == 0).all()
+    for b in range(c.b):
+        bad = [kv for kv in range(c.hkv) if not np.isfinite(got[b, :, kv * g:(kv + 1) * g]).all()]
+        assert not bad, f"non-finite output: request {b}, kv heads {bad}"
     d = np.concatenate(diffs)
-    assert np.isfinite(got).all()
     if c.dtype == torch.bfloat16:
         assert d.max() <= gc.BF16_ATOL_MAX, d.max()
         assert d.mean() <= gc.BF16_ATOL_MEAN, d.mean()
@@ -174,6 +178,14 @@ def test_ragged_batch_edges(dtype, d):
              gc.random_tree(rng, 5, 3), tree.kary_parents(40, 1)]
     prefix = [0, 1, 127, 128, 129, 300]
     check(Case(trees, prefix, 8, 2, d, dtype, t_max=64, seed=d))
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_unaligned_prefixes_never_read_past_the_tree(paged):
+    rng = np.random.default_rng(21)
+    trees = [gc.random_tree(rng, n, 7) for n in (61, 13, 1, 49, 30, 2)]
+    prefix = [1000, 777, 3, 129, 510, 4093]   # P + T at every residue mod 16
+    check(Case(trees, prefix, 16, 4, 128, torch.bfloat16, seed=22, paged=paged))
 
 
 def test_llama8b_contiguous():
@@ -211,10 +223,10 @@ def test_sweep_sampled(total):
 
 
 def test_request_that_does_not_fit_is_rejected_on_device():
-    trees = [[-1, 0, 0], [-1, 0, 1]]
+    trees = [[-1, 0, 0], [-1, 0, 1, 2, 3]]     # 60 + 5 slots (rounded to 80) > 64
     c = Case(trees, [40, 60], 4, 2, 128, torch.bfloat16, capacity=64, max_prefix=60)
     got, cache, _, err = run(c)
     assert err.tolist() == [0, 5]
     assert (got[1] == 0).all() and np.isfinite(got[0]).all()
-    # the rejected request's cache is untouched (zeros from setup)
-    assert (cache.k[1, :, 60:].float() == 0).all()
+    # the rejected request's cache is untouched (NaN from setup)
+    assert torch.isnan(cache.k[1, :, 60:].float()).all()

@@ -15,6 +15,7 @@
 //   ml     [B, Hkv, nsplit, rows_pad, 2]  f32  (running max m in log2 units, sum l)
 //   valid  [B] int32                      request passed the device checks
 #include <math.h>
+#include <stdint.h>
 
 #include <algorithm>
 
@@ -34,7 +35,8 @@ constexpr float LOG2E = 1.4426950408889634f;
 __device__ int request_code(const AttnArgs& a, int b) {
   const int T = a.num_nodes[b], P = a.prefix_len[b];
   if (T < 1 || T > a.max_nodes || P < 0 || P > a.max_prefix) return TSV_REQ_BAD_SIZE;
-  const int64_t need = (int64_t)P + ((T + 15) & ~15);
+  // slots the kernels touch: the tree, then zeros up to the next multiple of 16
+  const int64_t need = ((int64_t)P + T + 15) & ~15LL;
   if (a.layout == TSV_KV_CONTIGUOUS) return need > a.capacity ? TSV_REQ_CAPACITY : TSV_REQ_OK;
   if (need > (int64_t)a.max_blocks * TSV_KV_BLOCK) return TSV_REQ_CAPACITY;
   return TSV_REQ_OK;
@@ -60,7 +62,7 @@ prep_kernel(AttnArgs a, const T* __restrict__ q, const T* __restrict__ k_new,
   int code = request_code(a, b);
   if (code == TSV_REQ_OK && a.layout == TSV_KV_PAGED) {
     const int P = a.prefix_len[b], Tn = a.num_nodes[b];
-    const int nblk = (int)((P + ((Tn + 15) & ~15) + TSV_KV_BLOCK - 1) / TSV_KV_BLOCK);
+    const int nblk = (int)((((P + Tn + 15) & ~15) + TSV_KV_BLOCK - 1) / TSV_KV_BLOCK);
     bool bad = false;
     for (int j = tid; j < nblk; j += PREP_THREADS) {
       const int blk = a.block_table[(int64_t)b * a.max_blocks + j];
@@ -115,7 +117,7 @@ prep_kernel(AttnArgs a, const T* __restrict__ q, const T* __restrict__ k_new,
       slot_ptr(a, reinterpret_cast<T*>(a.v_cache), b, h, P + i)[d] = vi[h * D + d];
     }
     if (i == Tn - 1) {  // zero the slots after the tree up to the next multiple of 16
-      const int pad = ((Tn + 15) & ~15) - Tn;
+      const int pad = ((P + Tn + 15) & ~15) - (P + Tn);
       for (int e = tid; e < pad * a.hkv * D; e += PREP_THREADS) {
         const int j = e / (a.hkv * D), h = (e / D) % a.hkv, d = e % D;
         slot_ptr(a, reinterpret_cast<T*>(a.k_cache), b, h, P + Tn + j)[d] = from_f32<T>(0.f);
@@ -215,6 +217,7 @@ merge_kernel(AttnArgs a, T* __restrict__ out) {
   const int keys = a.prefix_len[b] + a.num_nodes[b];
   const int n_tiles = (keys + a.tile_keys - 1) / a.tile_keys;
   const int nsp = (n_tiles + a.tiles_per_split - 1) / a.tiles_per_split;
+  if (nsp == 1 && a.direct_single) return;  // already final
   const int64_t pbase = ((int64_t)b * a.hkv + kv) * a.nsplit;
   // running (M, L) over this lane's splits, then a warp-shuffle combine
   float M = -INFINITY, L = 0.f;
@@ -264,12 +267,30 @@ AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache) {
   p.tensor_core = tc_supported(p);
   p.rows_pad = (int)round_up(p.rows, p.tensor_core ? TC_M_GROUP : 8);
   p.tile_keys = 128;
-  const int64_t n_tiles = ceil_div((int64_t)p.max_prefix + p.max_nodes, p.tile_keys);
-  const int64_t ctas = (int64_t)p.batch * p.hkv *
-                       (p.tensor_core ? ceil_div(p.rows, TC_M_GROUP) : 1);
-  int64_t nsplit = std::max<int64_t>(1, ceil_div(2LL * device_sm_count(), ctas));
-  nsplit = std::min<int64_t>(nsplit, n_tiles);
-  p.tiles_per_split = (int)ceil_div(n_tiles, nsplit);
+  const int64_t keys_max = (int64_t)p.max_prefix + p.max_nodes;
+  const int64_t n_tiles = ceil_div(keys_max, p.tile_keys);
+  const int sms = device_sm_count();
+  if (p.tensor_core) {
+    // One CTA per SM. Pick the split count with the shortest estimated makespan (waves x
+    // tiles per split, plus one tile of fixed cost per CTA), keeping the fp32 partials
+    // under about half of the KV bytes.
+    const int64_t units = (int64_t)p.batch * p.hkv * ceil_div(p.rows, TC_M_GROUP);
+    const int64_t rows_g = std::min<int64_t>(p.rows, TC_M_GROUP);
+    const int64_t cap = std::max<int64_t>(1, keys_max / (2 * rows_g));
+    int64_t best = 1, best_cost = INT64_MAX;
+    for (int64_t ns = 1; ns <= std::min(cap, n_tiles); ++ns) {
+      const int64_t tps = ceil_div(n_tiles, ns);
+      const int64_t eff = ceil_div(n_tiles, tps);
+      const int64_t cost = ceil_div(units * eff, sms) * (tps + 1);
+      if (cost < best_cost) { best_cost = cost; best = ns; }
+    }
+    p.tiles_per_split = (int)ceil_div(n_tiles, best);
+  } else {
+    const int64_t ctas = (int64_t)p.batch * p.hkv;
+    int64_t nsplit = std::max<int64_t>(1, ceil_div(2LL * sms, ctas));
+    nsplit = std::min<int64_t>(nsplit, n_tiles);
+    p.tiles_per_split = (int)ceil_div(n_tiles, nsplit);
+  }
   p.nsplit = (int)ceil_div(n_tiles, p.tiles_per_split);
   const size_t qsize = p.tensor_core ? 2 : 4;
   const size_t planes = (size_t)p.batch * p.hkv;
@@ -319,6 +340,7 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
   a.tile_keys = p.tile_keys;
   a.tiles_per_split = p.tiles_per_split;
   a.nsplit = p.nsplit;
+  a.direct_single = p.tensor_core ? 1 : 0;
 
   RopeTable rope{};
   for (int m = 0; m < p.head_dim / 2; ++m)

@@ -33,6 +33,7 @@ struct AttnArgs {
   // sizes
   int max_nodes, hq, hkv, group, head_dim, rows_pad, max_prefix;
   int tile_keys, tiles_per_split, nsplit;
+  int direct_single;  // a request with one split was written by the attention kernel
 };
 
 // Query rows per tensor-core CTA (two 128-row M tiles).

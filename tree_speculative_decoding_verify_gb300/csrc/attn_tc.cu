@@ -38,15 +38,16 @@ namespace tsv {
 namespace {
 
 constexpr int KEYS = 128;                 // keys per tile
-constexpr int STAGES = 2;
+constexpr int KST = 3, VST = 2;           // K and V ring depths
 constexpr int THREADS = 320;
 constexpr int TMA_WARP = 8, MMA_WARP = 9;
 constexpr uint32_t HALF = 128 * 128;      // 128 rows x 64 bf16 (one 128-byte-swizzled panel)
 constexpr uint32_t TILE = 2 * HALF;       // 128 rows x 128 bf16
 constexpr uint32_t BOX64 = 64 * 128;      // one 64-row TMA box of a panel
 constexpr uint32_t SMEM_Q = 0;            // 2 M tiles
-constexpr uint32_t SMEM_KV = 2 * TILE;    // STAGES x (K tile, V tile)
-constexpr uint32_t SMEM_BAR = SMEM_KV + STAGES * 2 * TILE;
+constexpr uint32_t SMEM_K = 2 * TILE;     // KST K tiles
+constexpr uint32_t SMEM_V = SMEM_K + KST * TILE;  // VST V tiles
+constexpr uint32_t SMEM_BAR = SMEM_V + VST * TILE;
 constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_LOG2 = 8.f;
@@ -54,9 +55,12 @@ constexpr uint32_t WAIT_LIMIT = 1u << 22;  // try_wait polls before a wait gives
 constexpr uint64_t WAIT_NS = 1000000000ull;  // and at most one second
 
 // barrier slots (8 bytes each) after SMEM_BAR
-constexpr int BAR_Q = 0, BAR_KV_FULL = 1, BAR_KV_EMPTY = BAR_KV_FULL + STAGES,
-              BAR_S_FULL = BAR_KV_EMPTY + STAGES, BAR_P_FULL = BAR_S_FULL + 2,
+constexpr int BAR_Q = 0, BAR_K_FULL = 1, BAR_K_EMPTY = BAR_K_FULL + KST,
+              BAR_V_FULL = BAR_K_EMPTY + KST, BAR_V_EMPTY = BAR_V_FULL + VST,
+              BAR_S_FULL = BAR_V_EMPTY + VST, BAR_P_FULL = BAR_S_FULL + 2,
               BAR_O_DONE = BAR_P_FULL + 2, BAR_DRAIN = BAR_O_DONE + 1, NUM_BARS = BAR_DRAIN + 1;
+static_assert(8 * NUM_BARS + 8 <= 256, "barrier area");
+static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 
 // ---- PTX wrappers ----------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -168,6 +172,45 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 32 lanes x 128 columns in one load + wait.
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+  uint32_t r[128];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {"
+      "%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,"
+      "%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,"
+      "%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,"
+      "%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,"
+      "%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,"
+      "%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,"
+      "%126,%127}, [%128];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),
+        "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+        "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
+        "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]),
+        "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]),
+        "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]),
+        "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]),
+        "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]),
+        "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]),
+        "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]),
+        "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]),
+        "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]),
+        "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]),
+        "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -183,6 +226,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -216,6 +270,7 @@ constexpr uint32_t idesc(uint32_t b_mn_major) {
 struct TcParams {
   AttnArgs a;
   float scale_log2;
+  __nv_bfloat16* out;  // [B, max_nodes, Hq, D]: written here when a request has one split
 };
 
 __device__ __forceinline__ uint32_t pick(const uint32_t (&w)[9], int i) {
@@ -264,6 +319,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const int t1 = min(n_tiles, t0 + a.tiles_per_split);
   if (t0 >= t1) return;
   const int n = t1 - t0;
+  // this CTA covers every key of its rows: it writes the final output itself
+  const bool single = n_tiles <= a.tiles_per_split;
 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -275,9 +332,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(BAR_KV_FULL + s), 1);
-      mbar_init(bar(BAR_KV_EMPTY + s), 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(bar(BAR_K_FULL + s), 1);
+      mbar_init(bar(BAR_K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(bar(BAR_V_FULL + s), 1);
+      mbar_init(bar(BAR_V_EMPTY + s), 1);
     }
     for (int m = 0; m < 2; ++m) {
       mbar_init(bar(BAR_S_FULL + m), 1);
@@ -295,7 +356,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
 
   if (warp == TMA_WARP) {
-    // ---- producer: the whole warp walks the loop, lane 0 issues ----------------------
+    // ---- producer: the whole warp walks the loop, lane 0 issues. K runs one tile ahead
+    // of V (order K0 K1 V0 K2 V1 ...), so S = Q K^T never waits behind a V load.
     const int qrow = (b * a.hkv + h) * a.rows_pad + row0;
     if (lane == 0) {
       mbar_expect_tx(bar(BAR_Q), n_mt * TILE);
@@ -304,49 +366,56 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           tma_load_2d(base + SMEM_Q + mt * TILE + hf * HALF, &tm_q, hf * 64, qrow + mt * 128,
                       bar(BAR_Q));
     }
-    int issued = 0;
-    for (int j = 0; j < n; ++j) {
-      const int st = j % STAGES;
-      if (j >= STAGES && !warp_wait(bar(BAR_KV_EMPTY + st), ((j / STAGES) - 1) & 1, abort)) break;
-      if (lane == 0) {
-        const int k0 = (t0 + j) * KEYS;
-        const int chunks = (k0 + 64 < keys) ? 2 : 1;
-        mbar_expect_tx(bar(BAR_KV_FULL + st), chunks * 4 * BOX64);
-        const uint32_t kdst = base + SMEM_KV + st * 2 * TILE;
-        const uint32_t vdst = kdst + TILE;
-        for (int c = 0; c < chunks; ++c) {
-          const int key = k0 + 64 * c;
-          int row;
-          if (a.layout == TSV_KV_CONTIGUOUS) {
-            row = (int)(((int64_t)b * a.hkv + h) * a.capacity + key);
-          } else {
-            const int blk = a.block_table[(int64_t)b * a.max_blocks + key / TSV_KV_BLOCK];
-            row = (blk * a.hkv + h) * TSV_KV_BLOCK;
-          }
-          for (int hf = 0; hf < 2; ++hf) {
-            tma_load_2d(kdst + hf * HALF + c * BOX64, &tm_k, hf * 64, row, bar(BAR_KV_FULL + st));
-            tma_load_2d(vdst + hf * HALF + c * BOX64, &tm_v, hf * 64, row, bar(BAR_KV_FULL + st));
-          }
-        }
+    auto row_of = [&](int key) -> int {
+      if (a.layout == TSV_KV_CONTIGUOUS) return (int)(((int64_t)b * a.hkv + h) * a.capacity + key);
+      const int blk = a.block_table[(int64_t)b * a.max_blocks + key / TSV_KV_BLOCK];
+      return (blk * a.hkv + h) * TSV_KV_BLOCK;
+    };
+    // one K or V tile: 1 or 2 boxes of 64 keys (a box past the last key is not loaded)
+    auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
+      if (lane != 0) return;
+      const int k0 = (t0 + j) * KEYS;
+      const int chunks = (k0 + 64 < keys) ? 2 : 1;
+      mbar_expect_tx(full, chunks * 2 * BOX64);
+      for (int c = 0; c < chunks; ++c) {
+        const int row = row_of(k0 + 64 * c);
+        for (int hf = 0; hf < 2; ++hf) tma_load_2d(dst + hf * HALF + c * BOX64, map, hf * 64, row, full);
       }
-      issued = j + 1;
+    };
+    int issued_k = 0, issued_v = 0;
+    bool ok = true;
+    for (int j = 0; ok && j <= n; ++j) {
+      if (j < n) {
+        const int st = j % KST;
+        if (j >= KST && !(ok = warp_wait(bar(BAR_K_EMPTY + st), ((j / KST) - 1) & 1, abort))) break;
+        load(&tm_k, base + SMEM_K + st * TILE, bar(BAR_K_FULL + st), j);
+        issued_k = j + 1;
+      }
+      if (j >= 1) {
+        const int jv = j - 1, st = jv % VST;
+        if (jv >= VST && !(ok = warp_wait(bar(BAR_V_EMPTY + st), ((jv / VST) - 1) & 1, abort))) break;
+        load(&tm_v, base + SMEM_V + st * TILE, bar(BAR_V_FULL + st), jv);
+        issued_v = j;
+      }
     }
     // Before the CTA can exit, every copy it started has landed (immediate unless a
     // wait above gave up).
     if (lane == 0) {
       mbar_wait(bar(BAR_Q), 0, nullptr);
-      for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
-        mbar_wait(bar(BAR_KV_FULL + j % STAGES), (j / STAGES) & 1, nullptr);
+      for (int j = issued_k > KST ? issued_k - KST : 0; j < issued_k; ++j)
+        mbar_wait(bar(BAR_K_FULL + j % KST), (j / KST) & 1, nullptr);
+      for (int j = issued_v > VST ? issued_v - VST : 0; j < issued_v; ++j)
+        mbar_wait(bar(BAR_V_FULL + j % VST), (j / VST) & 1, nullptr);
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
     // ---- MMA issuer: the whole warp walks the loop, lane 0 issues --------------------
     constexpr uint32_t ID_QK = idesc(0), ID_PV = idesc(1);
     const bool issuer = lane == 0;
-    auto qk = [&](int mt, int st) {
+    auto qk = [&](int mt, int j) {
       if (!issuer) return;
       const uint32_t qa = base + SMEM_Q + mt * TILE;
-      const uint32_t ka = base + SMEM_KV + st * 2 * TILE;
+      const uint32_t ka = base + SMEM_K + (j % KST) * TILE;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks >> 2) * HALF + (ks & 3) * 32;
@@ -354,35 +423,35 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                ks > 0);
       }
       mma_commit(bar(BAR_S_FULL + mt));
+      if (mt == n_mt - 1) mma_commit(bar(BAR_K_EMPTY + j % KST));
     };
-    auto pv = [&](int mt, int st, int ksteps, bool acc) {
+    auto pv = [&](int mt, int j, int ksteps) {
       if (!issuer) return;
-      const uint32_t va = base + SMEM_KV + st * 2 * TILE + TILE;
+      const uint32_t va = base + SMEM_V + (j % VST) * TILE;
       for (int ks = 0; ks < ksteps; ++ks)
         mma_ts(tmem + 256 + mt * 128, tmem + mt * 128 + ks * 8,
-               sdesc(va + ks * 16 * 128, HALF, 1024), ID_PV, (acc || ks > 0) ? 1u : 0u);
+               sdesc(va + ks * 16 * 128, HALF, 1024), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
+      if (mt == n_mt - 1) mma_commit(bar(BAR_V_EMPTY + j % VST));
     };
-    bool ok = warp_wait(bar(BAR_Q), 0, abort) && warp_wait(bar(BAR_KV_FULL), 0, abort);
+    bool ok = warp_wait(bar(BAR_Q), 0, abort) && warp_wait(bar(BAR_K_FULL), 0, abort);
     if (ok) {
       tc_fence_after();
       for (int mt = 0; mt < n_mt; ++mt) qk(mt, 0);
     }
     for (int j = 0; ok && j < n; ++j) {
-      const int st = j % STAGES;
       const int valid = min(KEYS, keys - (t0 + j) * KEYS);
       const int ksteps = (valid + 15) >> 4;
       for (int mt = 0; ok && mt < n_mt; ++mt) {
         if (!(ok = warp_wait(bar(BAR_P_FULL + mt), j & 1, abort))) break;
+        if (mt == 0 && !(ok = warp_wait(bar(BAR_V_FULL + j % VST), (j / VST) & 1, abort))) break;
         tc_fence_after();
-        pv(mt, st, ksteps, j > 0);
-        if (mt == n_mt - 1 && issuer) mma_commit(bar(BAR_KV_EMPTY + st));
+        pv(mt, j, ksteps);
         if (j + 1 < n) {
-          const int st2 = (j + 1) % STAGES;
           if (mt == 0) {
-            if (!(ok = warp_wait(bar(BAR_KV_FULL + st2), ((j + 1) / STAGES) & 1, abort))) break;
+            if (!(ok = warp_wait(bar(BAR_K_FULL + (j + 1) % KST), ((j + 1) / KST) & 1, abort))) break;
             tc_fence_after();
           }
-          qk(mt, st2);
+          qk(mt, j + 1);
         }
       }
     }
@@ -418,72 +487,96 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (!(ok = warp_wait(bar(BAR_S_FULL + mt), j & 1, abort))) break;
       tc_fence_after();
       const int k0 = (t0 + j) * KEYS;
-      const bool tail = k0 + KEYS > P;
-      float v[32];
-      // pass 1: row max of the visible scores
+      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+      if (k0 + KEYS > P) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) vis[c] = visible32(k0 + 32 * c, P, T, mw);
+      }
+      float v[128];
+      tmem_ld128(s_addr, v);
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(s_addr + 32 * c, v);
-        const uint32_t vis = tail ? visible32(k0 + 32 * c, P, T, mw) : 0xffffffffu;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, ((vis >> i) & 1u) ? v[i] : -INFINITY);
-      }
+      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, ((vis[i >> 5] >> (i & 31)) & 1u) ? v[i] : -INFINITY);
       const float mxs = mx * sl2;
       const bool need = mxs > m_used + RESCALE_LOG2;  // also true on the first visible tile
       const float factor = need ? ex2(m_used - mxs) : 1.f;
-      if (__any_sync(FULL, need) && j > 0) {
-        // O is quiescent: this tile's S was committed after the previous P V finished.
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(o_addr + 32 * c, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= factor;
-          tmem_st32(o_addr + 32 * c, v);
-        }
-        tmem_wait_st();
-      }
       if (need) {
         l *= factor;
         m_used = mxs;
       }
-      // pass 2: P = exp2(s * scale_log2 - m) in bf16 over the first 64 S columns
+      // P = exp2(s * scale_log2 - m) in bf16 over the first 64 S columns
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(s_addr + 32 * c, v);
-        const uint32_t vis = tail ? visible32(k0 + 32 * c, P, T, mw) : 0xffffffffu;
-        uint32_t packed[16];
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float p0 = ((vis >> i) & 1u) ? ex2(fmaf(v[i], sl2, -m_used)) : 0.f;
-          const float p1 = ((vis >> (i + 1)) & 1u) ? ex2(fmaf(v[i + 1], sl2, -m_used)) : 0.f;
+        for (int i = 0; i < 32; ++i) {
+          const int c0 = half * 64 + 2 * i;
+          const float p0 = ((vis[c0 >> 5] >> (c0 & 31)) & 1u) ? ex2(fmaf(v[c0], sl2, -m_used)) : 0.f;
+          const float p1 =
+              ((vis[(c0 + 1) >> 5] >> ((c0 + 1) & 31)) & 1u) ? ex2(fmaf(v[c0 + 1], sl2, -m_used)) : 0.f;
           l += p0 + p1;
-          __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-          packed[i >> 1] = *reinterpret_cast<uint32_t*>(&pk);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+          pk[i] = *reinterpret_cast<uint32_t*>(&b2);
         }
-        tmem_st16(s_addr + 16 * c, packed);
+        tmem_st32u(s_addr + 32 * half, pk);
+      }
+      if (__any_sync(FULL, need) && j > 0) {
+        // O is quiescent: this tile's S was committed after the previous P V finished.
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float o[32];
+          tmem_ld32(o_addr + 32 * c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= factor;
+          tmem_st32(o_addr + 32 * c, o);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(BAR_P_FULL + mt));
     }
-    // epilogue: unnormalised O row and (m, l) of this split
+    // epilogue
     if (ok) ok = warp_wait(bar(BAR_O_DONE), 0, abort);
     tc_fence_after();
-    const int64_t prow = (((int64_t)b * a.hkv + h) * a.nsplit + split) * a.rows_pad + r;
+    if (single) {
+      // normalised bf16 output: out[b, node, h * G + g, :]
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = prm.out + (((int64_t)b * a.max_nodes + node) * a.hq + h * a.group +
+                                      r % a.group) * 128;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      float o[32];
-      tmem_ld32(o_addr + 32 * c, o);
-      if (live && ok) {
-        float4* dst = reinterpret_cast<float4*>(a.o_part + prow * 128 + 32 * c);
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(o_addr + 32 * c, o);
+        if (live && ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+          for (int i = 0; i < 4; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(o[8 * i + 2 * e] * inv, o[8 * i + 2 * e + 1] * inv);
+              w[e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            d4[i] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
       }
-    }
-    if (live && ok) {
-      a.ml[prow * 2 + 0] = m_used;
-      a.ml[prow * 2 + 1] = l;
+    } else {
+      const int64_t prow = (((int64_t)b * a.hkv + h) * a.nsplit + split) * a.rows_pad + r;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(o_addr + 32 * c, o);
+        if (live && ok) {
+          float4* dst = reinterpret_cast<float4*>(a.o_part + prow * 128 + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+        }
+      }
+      if (live && ok) {
+        a.ml[prow * 2 + 0] = m_used;
+        a.ml[prow * 2 + 1] = l;
+      }
     }
   }
 
@@ -538,7 +631,6 @@ bool tc_supported(const AttnPlan& p) {
 
 int launch_attn_tc(const AttnPlan& p, const AttnArgs& a, float scale_log2, void* out,
                    cudaStream_t stream) {
-  (void)out;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -556,7 +648,7 @@ int launch_attn_tc(const AttnPlan& p, const AttnArgs& a, float scale_log2, void*
   if (!make_map(&mq, a.q_rot, (uint64_t)p.batch * p.hkv * p.rows_pad, 128) ||
       !make_map(&mk, a.k_cache, kv_rows, 64) || !make_map(&mv, a.v_cache, kv_rows, 64))
     return TSV_ERR_UNSUPPORTED;
-  TcParams prm{a, scale_log2};
+  TcParams prm{a, scale_log2, static_cast<__nv_bfloat16*>(out)};
   dim3 grid(p.nsplit, (unsigned)ceil_div(p.rows, TC_M_GROUP), p.batch * p.hkv);
   attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, prm);
   return launch_status();

@@ -9,16 +9,16 @@
 // follows "TensorRT-LLM 源码完全拆解(二十二)", section 树的三套账 (flat = parent * K +
 // child, parent = flat / K).
 //
-// Stage A (streaming, HBM-bound): one CTA per (row, vocab chunk) reads the chunk once
-// with 128-bit loads, keeps a per-thread sorted top-K list in registers and a sum of
+// One kernel per level. Each CTA streams one (row, vocab chunk) once with 128-bit loads,
+// keeping a per-thread sorted list of its best candidates in registers and a sum of
 // exp(x - ref) against the running maximum ref (fp32 sums of 16 terms flushed into an
-// fp64 accumulator; a new maximum rescales the fp64 sum exactly), then merges the 256
-// lists with a warp tournament and writes the chunk's partial result. Keeping ref at the
+// fp64 accumulator; a new maximum rescales the fp64 sum exactly). Keeping ref at the
 // maximum makes x - ref exact for every term that matters, so the log-sum-exp is good
-// to about 1e-9 and the fp32 log-probabilities round like the fp64 ones.
-// Stage B (tiny): one CTA per request merges the chunks of every row (fp64 log-sum-exp,
-// list tournament), writes the level's candidates to the store, and runs the joint
-// top-K of the cumulative scores.
+// to about 1e-9 and the fp32 log-probabilities round like the fp64 ones. The 256 lists
+// merge by a warp tournament, then a block tournament, into the chunk's partial result.
+// The last CTA of a request to finish (an atomic ticket) merges the chunks of every
+// row (fp64 log-sum-exp; one fp64 exp per chunk), writes the level's candidates to the
+// store, and runs the joint top-K of the cumulative scores.
 #include <float.h>
 #include <limits.h>
 #include <math.h>
@@ -35,8 +35,6 @@ constexpr int KMAX = TSV_MAX_TOPK;
 constexpr int A_THREADS = 256;
 constexpr int A_WARPS = A_THREADS / 32;
 constexpr int MAX_CHUNKS = 32;
-constexpr int B_THREADS = 128;
-constexpr int B_WARPS = B_THREADS / 32;
 
 struct ChunkStat {
   double sum;  // sum of exp(x - ref) over the chunk
@@ -45,9 +43,10 @@ struct ChunkStat {
 };
 
 struct TopkWs {
-  ChunkStat* stat;  // [rows_total, chunks]
-  float* val;       // [rows_total, chunks, K]
-  int32_t* idx;     // [rows_total, chunks, K]
+  ChunkStat* stat;     // [rows_total, chunks]
+  float* val;          // [rows_total, chunks, K]
+  int32_t* idx;        // [rows_total, chunks, K]
+  unsigned* tickets;   // [batch] finished chunk CTAs of each request (zeroed per call)
 };
 
 __host__ __device__ inline TopkWs carve(void* ws, int rows_total, int chunks, int k) {
@@ -59,6 +58,8 @@ __host__ __device__ inline TopkWs carve(void* ws, int rows_total, int chunks, in
   w.val = reinterpret_cast<float*>(p);
   p += (n * k * sizeof(float) + 255) & ~size_t(255);
   w.idx = reinterpret_cast<int32_t*>(p);
+  p += (n * k * sizeof(int32_t) + 255) & ~size_t(255);
+  w.tickets = reinterpret_cast<unsigned*>(p);
   return w;
 }
 
@@ -66,8 +67,6 @@ __host__ __device__ inline TopkWs carve(void* ws, int rows_total, int chunks, in
 struct RowState {
   float v[KMAX];
   int i[KMAX];
-  float thr_v;
-  int thr_i;
   float ref;  // running maximum
   float g;    // fp32 sum of the current group of terms
   double d;   // fp64 sum of the flushed groups
@@ -78,53 +77,41 @@ __device__ __forceinline__ void flush(RowState& st) {
   st.g = 0.f;
 }
 
-__device__ __forceinline__ void consider(RowState& st, int k, float x, int idx) {
+// Every thread keeps its best KMAX candidates (a superset of its best k), so the list
+// threshold is always the last slot: no register array is ever indexed at run time.
+__device__ __forceinline__ void consider(RowState& st, float x, int idx) {
   if (x > st.ref) {  // new maximum: rescale the accumulated sum in fp64 (rare)
     flush(st);
     st.d *= exp((double)st.ref - (double)x);
     st.ref = x;
   }
   st.g += expf(x - st.ref);
-  if (better(x, idx, st.thr_v, st.thr_i)) {
+  if (better(x, idx, st.v[KMAX - 1], st.i[KMAX - 1])) {
     float cv = x;
     int ci = idx;
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      if (j < k) {
-        const bool sw = better(cv, ci, st.v[j], st.i[j]);
-        const float tv = st.v[j];
-        const int ti = st.i[j];
-        st.v[j] = sw ? cv : tv;
-        st.i[j] = sw ? ci : ti;
-        cv = sw ? tv : cv;
-        ci = sw ? ti : ci;
-      }
+      const bool sw = better(cv, ci, st.v[j], st.i[j]);
+      const float tv = st.v[j];
+      const int ti = st.i[j];
+      st.v[j] = sw ? cv : tv;
+      st.i[j] = sw ? ci : ti;
+      cv = sw ? tv : cv;
+      ci = sw ? ti : ci;
     }
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j)
-      if (j == k - 1) { st.thr_v = st.v[j]; st.thr_i = st.i[j]; }
   }
 }
 
-// (ref, sum) pairs combine against the larger reference; exp only when they differ.
-__device__ __forceinline__ void combine(float& r, double& s, float r2, double s2) {
-  if (r2 > r) {
-    s = s * exp((double)r - (double)r2) + s2;
-    r = r2;
-  } else if (r2 < r) {
-    s += s2 * exp((double)r2 - (double)r);
-  } else {
-    s += s2;
-  }
-}
-
+// Sum of (ref_i, s_i) pairs over a warp against the warp's largest reference: one fp64
+// exp per lane whose reference differs (none when they all agree), then fp64 adds.
 __device__ __forceinline__ void warp_combine(float& r, double& s) {
+  float R = r;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float r2 = __shfl_xor_sync(FULL, r, o);
-    const double s2 = __shfl_xor_sync(FULL, s, o);
-    combine(r, s, r2, s2);
-  }
+  for (int o = 16; o > 0; o >>= 1) R = fmaxf(R, __shfl_xor_sync(FULL, R, o));
+  if (r != R) s = (s == 0.0) ? 0.0 : s * exp((double)r - (double)R);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+  r = R;
 }
 
 __device__ __forceinline__ void warp_argmax(float& v, int& i, int& lane_of) {
@@ -147,14 +134,21 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) {
 
 template <bool VEC>
 __global__ void __launch_bounds__(A_THREADS)
-topk_chunk_kernel(const float* __restrict__ logits, int64_t row_stride, int vocab, int k,
-                  int chunks, int chunk_len, TopkWs ws) {
+topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int vocab, int rows, int k,
+                  int chunks, int chunk_len, int level, TopkWs ws,
+                  const float* __restrict__ front_score_in, const int32_t* __restrict__ front_store_in,
+                  int store_cap, int32_t* __restrict__ store_token, float* __restrict__ store_score,
+                  int32_t* __restrict__ store_parent, int32_t* __restrict__ front_token_out,
+                  float* __restrict__ front_score_out, int32_t* __restrict__ front_store_out) {
   __shared__ float s_lv[A_THREADS][KMAX + 1];
   __shared__ int s_li[A_THREADS][KMAX + 1];
   __shared__ float s_wv[A_WARPS][KMAX];
   __shared__ int s_wi[A_WARPS][KMAX];
   __shared__ float s_red[A_WARPS];
   __shared__ double s_sum[A_WARPS];
+  __shared__ float s_cu[KMAX * KMAX];
+  __shared__ int s_tok[KMAX * KMAX];
+  __shared__ bool s_last;
 
   const int row = blockIdx.y, chunk = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -165,8 +159,6 @@ topk_chunk_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
   RowState st;
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) { st.v[j] = -INFINITY; st.i[j] = INT_MAX; }
-  st.thr_v = -INFINITY;
-  st.thr_i = INT_MAX;
   st.g = 0.f;
   st.d = 0.0;
 
@@ -194,32 +186,32 @@ topk_chunk_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int e = start + 4 * (q + u * A_THREADS);
-        consider(st, k, r[u].x, e);
-        consider(st, k, r[u].y, e + 1);
-        consider(st, k, r[u].z, e + 2);
-        consider(st, k, r[u].w, e + 3);
+        consider(st, r[u].x, e);
+        consider(st, r[u].y, e + 1);
+        consider(st, r[u].z, e + 2);
+        consider(st, r[u].w, e + 3);
       }
       flush(st);
     }
     for (; q < n4; q += A_THREADS) {
       const float4 r = ld_stream(x4 + q);
       const int e = start + 4 * q;
-      consider(st, k, r.x, e);
-      consider(st, k, r.y, e + 1);
-      consider(st, k, r.z, e + 2);
-      consider(st, k, r.w, e + 3);
+      consider(st, r.x, e);
+      consider(st, r.y, e + 1);
+      consider(st, r.z, e + 2);
+      consider(st, r.w, e + 3);
       flush(st);
     }
-    for (int e = start + 4 * n4 + tid; e < end; e += A_THREADS) consider(st, k, x[e], e);
+    for (int e = start + 4 * n4 + tid; e < end; e += A_THREADS) consider(st, x[e], e);
   } else {
     for (int e = start + tid; e < end; e += A_THREADS) {
-      consider(st, k, x[e], e);
+      consider(st, x[e], e);
       if (((e - start) / A_THREADS & 15) == 15) flush(st);
     }
   }
   flush(st);
 
-  // Combine the (ref, sum) pairs of the block.
+  // Block sum of the (ref, sum) pairs.
   float R = st.ref;
   double part = st.d;
   warp_combine(R, part);
@@ -253,61 +245,60 @@ topk_chunk_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
       if (lane == who) ++ptr;
       if (lane == 0) { ws.val[base + r] = v; ws.idx[base + r] = i; }
     }
+    float rr = lane < A_WARPS ? s_red[lane] : -INFINITY;
+    double ss = lane < A_WARPS ? s_sum[lane] : 0.0;
+    warp_combine(rr, ss);
     if (lane == 0) {
-      float rr = s_red[0];
-      double total = s_sum[0];
-      for (int w = 1; w < A_WARPS; ++w) combine(rr, total, s_red[w], s_sum[w]);
       ChunkStat cs;
-      cs.sum = total;
+      cs.sum = ss;
       cs.ref = rr;
       cs.pad = 0.f;
       ws.stat[(size_t)row * chunks + chunk] = cs;
     }
   }
-}
 
-__global__ void __launch_bounds__(B_THREADS)
-topk_level_kernel(int rows, int k, int chunks, int level, TopkWs ws,
-                  const float* __restrict__ front_score_in, const int32_t* __restrict__ front_store_in,
-                  int store_cap, int32_t* __restrict__ store_token, float* __restrict__ store_score,
-                  int32_t* __restrict__ store_parent, int32_t* __restrict__ front_token_out,
-                  float* __restrict__ front_score_out, int32_t* __restrict__ front_store_out) {
-  __shared__ float s_cv[B_WARPS][MAX_CHUNKS][KMAX];
-  __shared__ int s_ci[B_WARPS][MAX_CHUNKS][KMAX];
-  __shared__ float s_cu[KMAX * KMAX];
-  __shared__ int s_tok[KMAX * KMAX];
-  const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // The last CTA of this request to finish merges its rows and runs the joint top-K.
+  const int b = row / rows;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned t = atomicAdd(&ws.tickets[b], 1u);
+    s_last = (t == (unsigned)(rows * chunks - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
   const int off = level == 1 ? 0 : k + (level - 2) * k * k;
   const int64_t srow = (int64_t)b * store_cap;
-
-  for (int s = warp; s < rows; s += B_WARPS) {
-    const int row = b * rows + s;
-    // Row log-sum-exp in fp64 from the chunk partial sums.
-    float R = -INFINITY;
+  float* lv = &s_lv[0][0];   // reused: per warp a [MAX_CHUNKS][KMAX] slab
+  int* li = &s_li[0][0];
+  for (int s = warp; s < rows; s += A_WARPS) {
+    const int r0 = b * rows + s;
+    float Rr = -INFINITY;
     double sum = 0.0;
-    if (lane < chunks) {
-      const ChunkStat cs = ws.stat[(size_t)row * chunks + lane];
-      R = cs.ref;
-      sum = cs.sum;
+    if (lane < chunks) {  // written by other CTAs: read through L2
+      const ChunkStat* cs = &ws.stat[(size_t)r0 * chunks + lane];
+      Rr = __ldcg(&cs->ref);
+      sum = __ldcg(&cs->sum);
     }
-    warp_combine(R, sum);
-    const double lse = (double)R + log(sum);
-
-    // Stage the chunk lists, then a tournament over them.
+    warp_combine(Rr, sum);
+    const double lse = (double)Rr + log(sum);
+    float* cv = lv + warp * MAX_CHUNKS * KMAX;
+    int* ci = li + warp * MAX_CHUNKS * KMAX;
     for (int t = lane; t < chunks * k; t += 32) {
       const int c = t / k, j = t % k;
-      const size_t g = ((size_t)row * chunks + c) * k + j;
-      s_cv[warp][c][j] = ws.val[g];
-      s_ci[warp][c][j] = ws.idx[g];
+      const size_t g = ((size_t)r0 * chunks + c) * k + j;
+      cv[c * KMAX + j] = __ldcg(ws.val + g);
+      ci[c * KMAX + j] = __ldcg(ws.idx + g);
     }
     __syncwarp();
-    const float pscore = level == 1 ? 0.0f : front_score_in[row];
-    const int pstore = level == 1 ? -1 : front_store_in[row];
+    const float pscore = level == 1 ? 0.0f : front_score_in[r0];
+    const int pstore = level == 1 ? -1 : front_store_in[r0];
     int ptr = 0;
     for (int r = 0; r < k; ++r) {
-      float v = (lane < chunks && ptr < k) ? s_cv[warp][lane][ptr] : -INFINITY;
-      int i = (lane < chunks && ptr < k) ? s_ci[warp][lane][ptr] : INT_MAX;
+      float v = (lane < chunks) ? cv[lane * KMAX + ptr] : -INFINITY;
+      int i = (lane < chunks) ? ci[lane * KMAX + ptr] : INT_MAX;
       int who = lane;
       warp_argmax(v, i, who);
       if (lane == who) ++ptr;
@@ -346,6 +337,7 @@ topk_level_kernel(int rows, int k, int chunks, int level, TopkWs ws,
         front_store_out[b * k + r] = off + i;
       }
     }
+    if (lane == 0) ws.tickets[b] = 0u;
   }
 }
 
@@ -428,7 +420,7 @@ TopkPlan plan_topk(int batch, int rows, int vocab, int top_k) {
   p.chunk_len = chunk_len;
   const size_t n = (size_t)rows_total * chunks;
   p.ws_bytes = align256(n * sizeof(ChunkStat)) + align256(n * top_k * sizeof(float)) +
-               align256(n * top_k * sizeof(int32_t));
+               align256(n * top_k * sizeof(int32_t)) + align256((size_t)batch * sizeof(unsigned));
   return p;
 }
 
@@ -440,19 +432,20 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
                        const TopkPlan& plan, cudaStream_t stream) {
   const int rows_total = batch * rows;
   TopkWs w = carve(ws, rows_total, plan.chunks, top_k);
-  dim3 grid_a(plan.chunks, rows_total);
+  if (cudaMemsetAsync(w.tickets, 0, (size_t)batch * sizeof(unsigned), stream) != cudaSuccess)
+    return launch_status();
+  dim3 grid(plan.chunks, rows_total);
   const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (row_stride % 4 == 0);
   if (vec)
-    topk_chunk_kernel<true><<<grid_a, A_THREADS, 0, stream>>>(logits, row_stride, vocab, top_k,
-                                                             plan.chunks, plan.chunk_len, w);
+    topk_level_kernel<true><<<grid, A_THREADS, 0, stream>>>(
+        logits, row_stride, vocab, rows, top_k, plan.chunks, plan.chunk_len, level, w,
+        front_score_in, front_store_in, store_cap, store_token, store_score, store_parent,
+        front_token_out, front_score_out, front_store_out);
   else
-    topk_chunk_kernel<false><<<grid_a, A_THREADS, 0, stream>>>(logits, row_stride, vocab, top_k,
-                                                              plan.chunks, plan.chunk_len, w);
-  int st = launch_status();
-  if (st != TSV_OK) return st;
-  topk_level_kernel<<<batch, B_THREADS, 0, stream>>>(
-      rows, top_k, plan.chunks, level, w, front_score_in, front_store_in, store_cap, store_token,
-      store_score, store_parent, front_token_out, front_score_out, front_store_out);
+    topk_level_kernel<false><<<grid, A_THREADS, 0, stream>>>(
+        logits, row_stride, vocab, rows, top_k, plan.chunks, plan.chunk_len, level, w,
+        front_score_in, front_store_in, store_cap, store_token, store_score, store_parent,
+        front_token_out, front_score_out, front_store_out);
   return launch_status();
 }
 

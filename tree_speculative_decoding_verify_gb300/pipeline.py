@@ -138,5 +138,8 @@ class HotPath:
 
     # launches of libtsv kernels per step (for the bench's launch count)
     def kernels_per_step(self) -> int:
-        n = 0 if self.s.fixed_nodes else 2 * (self.s.depth + 1) + 1
+        """libtsv kernels one step launches: one per expansion level, the final
+        selection, the metadata, three for the attention call (prep, attention,
+        merge) and the acceptance."""
+        n = 0 if self.s.fixed_nodes else (self.s.depth + 1) + 1
         return n + 1 + 3 + 1
