@@ -86,7 +86,7 @@ prep_kernel(AttnArgs a, const T* __restrict__ q, const T* __restrict__ k_new,
       // angle in fp64, reduced to [-pi, pi] before the fp32 sin/cos
       const double ang = (double)pos * rope.inv_freq[tid];
       const double two_pi = 6.283185307179586;
-      const double red = ang - two_pi * rint(ang / two_pi);
+      const double red = ang - two_pi * rint(ang * (1.0 / two_pi));
       float sn, cs;
       sincosf((float)red, &sn, &cs);
       s_cos[tid] = cs;
@@ -125,10 +125,13 @@ prep_kernel(AttnArgs a, const T* __restrict__ q, const T* __restrict__ k_new,
       }
     }
   } else {
+    // no node here (or the request failed its checks): zero its q rows and its output
     for (int e = tid; e < a.hkv * G * D; e += PREP_THREADS) {
       const int h = e / (G * D), g = (e / D) % G, d = e % D;
       qr[((qbase + (int64_t)h * a.rows_pad) + (int64_t)i * G + g) * D + d] = from_f32<QT>(0.f);
     }
+    T* o = reinterpret_cast<T*>(a.out) + ((int64_t)b * a.max_nodes + i) * a.hq * D;
+    for (int e = tid; e < a.hq * D; e += PREP_THREADS) o[e] = from_f32<T>(0.f);
   }
   if (i == 0) {  // rows past max_nodes * G up to rows_pad
     const int extra = a.rows_pad - a.max_nodes * G;
@@ -271,19 +274,21 @@ AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache) {
   const int64_t n_tiles = ceil_div(keys_max, p.tile_keys);
   const int sms = device_sm_count();
   if (p.tensor_core) {
-    // One CTA per SM. Pick the split count with the shortest estimated makespan (waves x
-    // tiles per split, plus one tile of fixed cost per CTA), keeping the fp32 partials
-    // under about half of the KV bytes.
+    // One CTA per SM. Splits: at least ~2 CTAs per SM (request lengths vary below
+    // max_prefix), and at least the count with the shortest estimated makespan for
+    // full-length requests (waves x (tiles per split + 1 tile of fixed cost)); partials
+    // stay under about half of the KV bytes.
     const int64_t units = (int64_t)p.batch * p.hkv * ceil_div(p.rows, TC_M_GROUP);
     const int64_t rows_g = std::min<int64_t>(p.rows, TC_M_GROUP);
-    const int64_t cap = std::max<int64_t>(1, keys_max / (2 * rows_g));
+    const int64_t cap = std::max<int64_t>(1, std::min(n_tiles, keys_max / (2 * rows_g)));
     int64_t best = 1, best_cost = INT64_MAX;
-    for (int64_t ns = 1; ns <= std::min(cap, n_tiles); ++ns) {
+    for (int64_t ns = 1; ns <= cap; ++ns) {
       const int64_t tps = ceil_div(n_tiles, ns);
       const int64_t eff = ceil_div(n_tiles, tps);
       const int64_t cost = ceil_div(units * eff, sms) * (tps + 1);
       if (cost < best_cost) { best_cost = cost; best = ns; }
     }
+    best = std::min(cap, std::max(best, ceil_div(2LL * sms, units)));
     p.tiles_per_split = (int)ceil_div(n_tiles, best);
   } else {
     const int64_t ctas = (int64_t)p.batch * p.hkv;
@@ -326,6 +331,7 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
   a.mask = mask;
   a.mask_words = (p.max_nodes + 31) / 32;
   a.err = err;
+  a.out = out;
   a.q_rot = w + p.off_qrot;
   a.o_part = reinterpret_cast<float*>(w + p.off_opart);
   a.ml = reinterpret_cast<float*>(w + p.off_ml);

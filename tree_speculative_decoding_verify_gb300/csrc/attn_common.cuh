@@ -25,6 +25,7 @@ struct AttnArgs {
   const uint32_t* mask;
   int mask_words;
   int32_t* err;
+  void* out;  // [B, max_nodes, Hq, D]
   // workspace
   void* q_rot;
   float* o_part;

@@ -228,17 +228,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
 }
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
-      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
-      "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
@@ -273,15 +262,9 @@ struct TcParams {
   __nv_bfloat16* out;  // [B, max_nodes, Hq, D]: written here when a request has one split
 };
 
-__device__ __forceinline__ uint32_t pick(const uint32_t (&w)[9], int i) {
-  uint32_t r = 0;
-#pragma unroll
-  for (int k = 0; k < 9; ++k) r = (i == k) ? w[k] : r;
-  return r;
-}
-
-// Visibility of the 32 keys k .. k+31 for a row whose node has mask words mw.
-__device__ __forceinline__ uint32_t visible32(int k, int P, int T, const uint32_t (&mw)[9]) {
+// Visibility of the 32 keys k .. k+31 for a row whose node's mask words start at mrow
+// (read from L1/L2 only on the tiles that hold tree keys).
+__device__ __forceinline__ uint32_t visible32(int k, int P, int T, const uint32_t* mrow, int words) {
   if (k + 32 <= P) return 0xffffffffu;
   const int t = k - P;  // tree index of column 0
   uint32_t pre = 0;
@@ -290,13 +273,16 @@ __device__ __forceinline__ uint32_t visible32(int k, int P, int T, const uint32_
   const int ts = t < 0 ? 0 : t;
   if (ts < T) {
     const int idx = ts >> 5, off = ts & 31;
-    uint32_t bits = __funnelshift_r(pick(mw, idx), pick(mw, idx + 1), off);
+    const uint32_t lo = mrow[idx];
+    const uint32_t hi = idx + 1 < words ? mrow[idx + 1] : 0u;
+    uint32_t bits = __funnelshift_r(lo, hi, off);
     if (T - ts < 32) bits &= (1u << (T - ts)) - 1u;
     tr = bits << (ts - t);
   }
   return pre | tr;
 }
 
+// 10 warps: the schedulers holding 3 of them cap a thread at 168 registers.
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
@@ -468,15 +454,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int r = row0 + mt * 128 + quad * 32 + lane;
     const bool live = r < rows;
     const int node = r / a.group;
-    uint32_t mw[9];
-#pragma unroll
-    for (int k = 0; k < 9; ++k) mw[k] = 0;
-    if (live) {
-      const uint32_t* mrow = a.mask + ((int64_t)b * a.max_nodes + node) * a.mask_words;
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (k < a.mask_words) mw[k] = mrow[k];
-    }
+    // rows past the tree read node 0's mask (their results are never stored)
+    const uint32_t* mrow = a.mask + ((int64_t)b * a.max_nodes + (live ? node : 0)) * a.mask_words;
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + mt * 128;
     const uint32_t o_addr = tmem + lane_base + 256 + mt * 128;
@@ -487,39 +466,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (!(ok = warp_wait(bar(BAR_S_FULL + mt), j & 1, abort))) break;
       tc_fence_after();
       const int k0 = (t0 + j) * KEYS;
-      uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
-      if (k0 + KEYS > P) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) vis[c] = visible32(k0 + 32 * c, P, T, mw);
-      }
       float v[128];
       tmem_ld128(s_addr, v);
-      float mx = -INFINITY;
+      if (k0 + KEYS > P) {  // tile holds tree keys (or keys past the end): mask to -inf
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, ((vis[i >> 5] >> (i & 31)) & 1u) ? v[i] : -INFINITY);
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t vis = visible32(k0 + 32 * c, P, T, mrow, a.mask_words);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * c + i] = ((vis >> i) & 1u) ? v[32 * c + i] : -INFINITY;
+        }
+      }
+      // row max with 8 independent chains
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = v[i];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) m8[i & 7] = fmaxf(m8[i & 7], v[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const float mxs = mx * sl2;
       const bool need = mxs > m_used + RESCALE_LOG2;  // also true on the first visible tile
       const float factor = need ? ex2(m_used - mxs) : 1.f;
-      if (need) {
-        l *= factor;
-        m_used = mxs;
-      }
+      if (need) m_used = mxs;
+      // a row with nothing visible so far has only -inf scores: any finite offset works
+      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
       // P = exp2(s * scale_log2 - m) in bf16 over the first 64 S columns
+      float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c0 = half * 64 + 2 * i;
-          const float p0 = ((vis[c0 >> 5] >> (c0 & 31)) & 1u) ? ex2(fmaf(v[c0], sl2, -m_used)) : 0.f;
-          const float p1 =
-              ((vis[(c0 + 1) >> 5] >> ((c0 + 1) & 31)) & 1u) ? ex2(fmaf(v[c0 + 1], sl2, -m_used)) : 0.f;
-          l += p0 + p1;
+        for (int i = 0; i < 16; ++i) {
+          const int c0 = q * 32 + 2 * i;
+          const float p0 = ex2(fmaf(v[c0], sl2, neg_m));
+          const float p1 = ex2(fmaf(v[c0 + 1], sl2, neg_m));
+          l8[(2 * i) & 7] += p0;
+          l8[(2 * i + 1) & 7] += p1;
           __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
           pk[i] = *reinterpret_cast<uint32_t*>(&b2);
         }
-        tmem_st32u(s_addr + 32 * half, pk);
+        tmem_st16(s_addr + 16 * q, pk);
       }
+      l = l * factor + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
       if (__any_sync(FULL, need) && j > 0) {
         // O is quiescent: this tile's S was committed after the previous P V finished.
 #pragma unroll

@@ -9,16 +9,20 @@
 // follows "TensorRT-LLM 源码完全拆解(二十二)", section 树的三套账 (flat = parent * K +
 // child, parent = flat / K).
 //
-// One kernel per level. Each CTA streams one (row, vocab chunk) once with 128-bit loads,
-// keeping a per-thread sorted list of its best candidates in registers and a sum of
-// exp(x - ref) against the running maximum ref (fp32 sums of 16 terms flushed into an
-// fp64 accumulator; a new maximum rescales the fp64 sum exactly). Keeping ref at the
-// maximum makes x - ref exact for every term that matters, so the log-sum-exp is good
-// to about 1e-9 and the fp32 log-probabilities round like the fp64 ones. The 256 lists
-// merge by a warp tournament, then a block tournament, into the chunk's partial result.
-// The last CTA of a request to finish (an atomic ticket) merges the chunks of every
-// row (fp64 log-sum-exp; one fp64 exp per chunk), writes the level's candidates to the
-// store, and runs the joint top-K of the cumulative scores.
+// One kernel per level. Each CTA streams one (row, vocab chunk) once with 128-bit loads:
+//   - top-k: a warp-cooperative select. Every warp keeps its best 16 candidates spread
+//     over lanes 0-15 and a warp-uniform threshold (its 16th best). A thread only
+//     buffers elements that beat the threshold (a handful per row after the first few
+//     hundred); when any buffer is nearly full, the whole warp merges buffers and list
+//     by a 16-round tournament, so no lane ever runs a divergent insertion.
+//   - log-sum-exp: exp(x - ref) against the thread's running maximum ref, summed in fp32
+//     groups of 16 terms flushed into an fp64 accumulator. Keeping ref at the maximum
+//     makes x - ref exact for every term that matters; when a new maximum arrives the
+//     old (ref, sum) pair is parked and combined once at the end (one fp64 exp), so the
+//     log-sum-exp is good to about 1e-9 and the fp32 log-probabilities round like fp64.
+// The warps' lists merge into the chunk's top-k; the last CTA of a request to finish
+// (an atomic ticket) merges the chunks of every row, writes the level's candidates to
+// the store and runs the joint top-K of the cumulative scores.
 #include <float.h>
 #include <limits.h>
 #include <math.h>
@@ -31,10 +35,11 @@
 namespace tsv {
 namespace {
 
-constexpr int KMAX = TSV_MAX_TOPK;
+constexpr int KMAX = TSV_MAX_TOPK;  // 16: warp list length
 constexpr int A_THREADS = 256;
 constexpr int A_WARPS = A_THREADS / 32;
 constexpr int MAX_CHUNKS = 32;
+constexpr int BUF = 8;              // per-thread candidate buffer
 
 struct ChunkStat {
   double sum;  // sum of exp(x - ref) over the chunk
@@ -63,42 +68,13 @@ __host__ __device__ inline TopkWs carve(void* ws, int rows_total, int chunks, in
   return w;
 }
 
-// Per-thread state: sorted top-K (best first) and the exp-sum against ref.
-struct RowState {
-  float v[KMAX];
-  int i[KMAX];
-  float ref;  // running maximum
-  float g;    // fp32 sum of the current group of terms
-  double d;   // fp64 sum of the flushed groups
-};
-
-__device__ __forceinline__ void flush(RowState& st) {
-  st.d += (double)st.g;
-  st.g = 0.f;
-}
-
-// Every thread keeps its best KMAX candidates (a superset of its best k), so the list
-// threshold is always the last slot: no register array is ever indexed at run time.
-__device__ __forceinline__ void consider(RowState& st, float x, int idx) {
-  if (x > st.ref) {  // new maximum: rescale the accumulated sum in fp64 (rare)
-    flush(st);
-    st.d *= exp((double)st.ref - (double)x);
-    st.ref = x;
-  }
-  st.g += expf(x - st.ref);
-  if (better(x, idx, st.v[KMAX - 1], st.i[KMAX - 1])) {
-    float cv = x;
-    int ci = idx;
+__device__ __forceinline__ void warp_argmax(float& v, int& i, int& lane_of) {
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      const bool sw = better(cv, ci, st.v[j], st.i[j]);
-      const float tv = st.v[j];
-      const int ti = st.i[j];
-      st.v[j] = sw ? cv : tv;
-      st.i[j] = sw ? ci : ti;
-      cv = sw ? tv : cv;
-      ci = sw ? ti : ci;
-    }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(FULL, v, o);
+    const int oi = __shfl_xor_sync(FULL, i, o);
+    const int ol = __shfl_xor_sync(FULL, lane_of, o);
+    if (better(ov, oi, v, i)) { v = ov; i = oi; lane_of = ol; }
   }
 }
 
@@ -114,16 +90,6 @@ __device__ __forceinline__ void warp_combine(float& r, double& s) {
   r = R;
 }
 
-__device__ __forceinline__ void warp_argmax(float& v, int& i, int& lane_of) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(FULL, v, o);
-    const int oi = __shfl_xor_sync(FULL, i, o);
-    const int ol = __shfl_xor_sync(FULL, lane_of, o);
-    if (better(ov, oi, v, i)) { v = ov; i = oi; lane_of = ol; }
-  }
-}
-
 __device__ __forceinline__ float4 ld_stream(const float4* p) {
   float4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
@@ -132,20 +98,97 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) {
   return r;
 }
 
-template <bool VEC>
+// Per-thread streaming state.
+struct Stream {
+  // exp-sum
+  float ref;    // running maximum
+  float g;      // fp32 sum of the current group
+  double d;     // fp64 sum against ref
+  float ref0;   // parked older reference (-inf: none)
+  double d0;    // parked sum against ref0
+  // top-k: warp list slot (lanes 0-15), warp threshold, own buffer
+  float lv;
+  int li;
+  float thr_v;
+  int thr_i;
+  float bv[BUF];
+  int bi[BUF];
+  int bc;
+};
+
+__device__ __forceinline__ void flush(Stream& st) {
+  st.d += (double)st.g;
+  st.g = 0.f;
+}
+
+// d0 * e^(ref0 - ref) + d: the rare merge of two parked sums, kept out of line.
+__device__ __noinline__ double merge_pair(double d0, float ref0, double d, float ref) {
+  return d0 * exp((double)ref0 - (double)ref) + d;
+}
+
+__device__ __forceinline__ void consider(Stream& st, float x, int idx) {
+  if (x > st.ref) {  // new maximum: park the old pair
+    flush(st);
+    st.d0 = st.ref0 == -INFINITY ? st.d : merge_pair(st.d0, st.ref0, st.d, st.ref);
+    st.ref0 = st.ref;
+    st.d = 0.0;
+    st.ref = x;
+  }
+  st.g += expf(x - st.ref);
+  if (better(x, idx, st.thr_v, st.thr_i)) {
+#pragma unroll
+    for (int s = 0; s < BUF; ++s) {
+      if (s == st.bc) { st.bv[s] = x; st.bi[s] = idx; }
+    }
+    ++st.bc;
+  }
+}
+
+// Warp merge: new list = best 16 of (list, all buffers); threshold = its 16th entry.
+__device__ __forceinline__ void warp_merge(Stream& st, int lane) {
+  // (inlined at three sites: the streaming loop, its tail and the final merge)
+  unsigned taken = 0;       // bit s: buffer slot s used; bit BUF: list slot used
+  float nv = -INFINITY;
+  int ni = INT_MAX;
+  for (int r = 0; r < KMAX; ++r) {
+    float v = -INFINITY;
+    int i = INT_MAX, which = -1;
+    if (lane < KMAX && !(taken >> BUF & 1u) && better(st.lv, st.li, v, i)) {
+      v = st.lv; i = st.li; which = BUF;
+    }
+#pragma unroll
+    for (int s = 0; s < BUF; ++s) {
+      if (s < st.bc && !(taken >> s & 1u) && better(st.bv[s], st.bi[s], v, i)) {
+        v = st.bv[s]; i = st.bi[s]; which = s;
+      }
+    }
+    int who = lane;
+    float wv = v;
+    int wi = i;
+    warp_argmax(wv, wi, who);
+    if (lane == who && which >= 0) taken |= 1u << which;
+    if (lane == r) { nv = wv; ni = wi; }
+  }
+  st.lv = nv;
+  st.li = ni;
+  st.thr_v = __shfl_sync(FULL, nv, KMAX - 1);
+  st.thr_i = __shfl_sync(FULL, ni, KMAX - 1);
+  st.bc = 0;
+}
+
 __global__ void __launch_bounds__(A_THREADS)
 topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int vocab, int rows, int k,
-                  int chunks, int chunk_len, int level, TopkWs ws,
+                  int chunks, int chunk_len, int level, bool vec, TopkWs ws,
                   const float* __restrict__ front_score_in, const int32_t* __restrict__ front_store_in,
                   int store_cap, int32_t* __restrict__ store_token, float* __restrict__ store_score,
                   int32_t* __restrict__ store_parent, int32_t* __restrict__ front_token_out,
                   float* __restrict__ front_score_out, int32_t* __restrict__ front_store_out) {
-  __shared__ float s_lv[A_THREADS][KMAX + 1];
-  __shared__ int s_li[A_THREADS][KMAX + 1];
   __shared__ float s_wv[A_WARPS][KMAX];
   __shared__ int s_wi[A_WARPS][KMAX];
   __shared__ float s_red[A_WARPS];
   __shared__ double s_sum[A_WARPS];
+  __shared__ float s_cv[A_WARPS][MAX_CHUNKS * KMAX];
+  __shared__ int s_ci[A_WARPS][MAX_CHUNKS * KMAX];
   __shared__ float s_cu[KMAX * KMAX];
   __shared__ int s_tok[KMAX * KMAX];
   __shared__ bool s_last;
@@ -156,11 +199,18 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
   const int start = chunk * chunk_len;
   const int end = min(vocab, start + chunk_len);
 
-  RowState st;
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) { st.v[j] = -INFINITY; st.i[j] = INT_MAX; }
+  Stream st;
   st.g = 0.f;
   st.d = 0.0;
+  st.ref0 = -INFINITY;
+  st.d0 = 0.0;
+  st.lv = -INFINITY;
+  st.li = INT_MAX;
+  st.thr_v = -INFINITY;
+  st.thr_i = INT_MAX;
+  st.bc = 0;
+#pragma unroll
+  for (int s = 0; s < BUF; ++s) { st.bv[s] = -INFINITY; st.bi[s] = INT_MAX; }
 
   // Common starting reference: the largest of the first elements every thread sees.
   float first = -INFINITY;
@@ -174,67 +224,49 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
   for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, s_red[w]);
   st.ref = fmaxf(first, -FLT_MAX);  // finite, so x = -inf gives a zero term
 
-  if (VEC) {
-    const float4* x4 = reinterpret_cast<const float4*>(x + start);
-    const int n4 = (end - start) >> 2;
-    int q = tid;
-    constexpr int U = 4;
-    for (; q + (U - 1) * A_THREADS < n4; q += U * A_THREADS) {
-      float4 r[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) r[u] = ld_stream(x4 + q + u * A_THREADS);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int e = start + 4 * (q + u * A_THREADS);
-        consider(st, r[u].x, e);
-        consider(st, r[u].y, e + 1);
-        consider(st, r[u].z, e + 2);
-        consider(st, r[u].w, e + 3);
-      }
-      flush(st);
-    }
-    for (; q < n4; q += A_THREADS) {
-      const float4 r = ld_stream(x4 + q);
-      const int e = start + 4 * q;
-      consider(st, r.x, e);
-      consider(st, r.y, e + 1);
-      consider(st, r.z, e + 2);
-      consider(st, r.w, e + 3);
-      flush(st);
-    }
-    for (int e = start + 4 * n4 + tid; e < end; e += A_THREADS) consider(st, x[e], e);
-  } else {
-    for (int e = start + tid; e < end; e += A_THREADS) {
-      consider(st, x[e], e);
-      if (((e - start) / A_THREADS & 15) == 15) flush(st);
-    }
+  // Every thread takes 4 consecutive entries per step (one 128-bit load when the row is
+  // 16-byte aligned), two steps prefetched ahead; after each step the warp merges if some
+  // buffer could overflow on the next one. All lanes run the same number of steps.
+  const int steps = (end - start + 4 * A_THREADS - 1) / (4 * A_THREADS);
+  auto load4 = [&](int it) -> float4 {
+    const int e = start + 4 * (it * A_THREADS + tid);
+    if (vec && e + 3 < end) return ld_stream(reinterpret_cast<const float4*>(x + e));
+    float4 r;
+    r.x = e < end ? x[e] : -INFINITY;
+    r.y = e + 1 < end ? x[e + 1] : -INFINITY;
+    r.z = e + 2 < end ? x[e + 2] : -INFINITY;
+    r.w = e + 3 < end ? x[e + 3] : -INFINITY;
+    return r;
+  };
+  const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  float4 a = steps > 0 ? load4(0) : none;
+  float4 bnext = steps > 1 ? load4(1) : none;
+  for (int it = 0; it < steps; ++it) {
+    const float4 c = it + 2 < steps ? load4(it + 2) : none;
+    const int e = start + 4 * (it * A_THREADS + tid);
+    if (e < end) consider(st, a.x, e);
+    if (e + 1 < end) consider(st, a.y, e + 1);
+    if (e + 2 < end) consider(st, a.z, e + 2);
+    if (e + 3 < end) consider(st, a.w, e + 3);
+    if (__any_sync(FULL, st.bc > BUF - 4)) warp_merge(st, lane);
+    if ((it & 3) == 3) flush(st);
+    a = bnext;
+    bnext = c;
   }
   flush(st);
+  warp_merge(st, lane);  // the warp's final best 16
 
-  // Block sum of the (ref, sum) pairs.
+  // exp-sum: fold the parked pair, then combine over the block.
+  if (st.ref0 != -INFINITY) st.d += st.d0 * exp((double)st.ref0 - (double)st.ref);
   float R = st.ref;
   double part = st.d;
   warp_combine(R, part);
   __syncthreads();  // s_red was read for the starting reference
   if (lane == 0) { s_red[warp] = R; s_sum[warp] = part; }
-
-  // Top-K: every thread's sorted list -> warp tournament -> block tournament.
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) { s_lv[tid][j] = st.v[j]; s_li[tid][j] = st.i[j]; }
-  __syncthreads();
-  {
-    int ptr = 0;
-    for (int r = 0; r < k; ++r) {
-      float v = s_lv[tid][ptr];
-      int i = s_li[tid][ptr];
-      int who = lane;
-      warp_argmax(v, i, who);
-      if (lane == who) ++ptr;
-      if (lane == 0) { s_wv[warp][r] = v; s_wi[warp][r] = i; }
-    }
-  }
+  if (lane < KMAX) { s_wv[warp][lane] = st.lv; s_wi[warp][lane] = st.li; }
   __syncthreads();
   if (warp == 0) {
+    // block top-k: 8 sorted warp lists, lanes 0-7 hold the list heads
     int ptr = 0;
     const size_t base = ((size_t)row * chunks + chunk) * k;
     for (int r = 0; r < k; ++r) {
@@ -271,8 +303,6 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
 
   const int off = level == 1 ? 0 : k + (level - 2) * k * k;
   const int64_t srow = (int64_t)b * store_cap;
-  float* lv = &s_lv[0][0];   // reused: per warp a [MAX_CHUNKS][KMAX] slab
-  int* li = &s_li[0][0];
   for (int s = warp; s < rows; s += A_WARPS) {
     const int r0 = b * rows + s;
     float Rr = -INFINITY;
@@ -284,8 +314,8 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
     }
     warp_combine(Rr, sum);
     const double lse = (double)Rr + log(sum);
-    float* cv = lv + warp * MAX_CHUNKS * KMAX;
-    int* ci = li + warp * MAX_CHUNKS * KMAX;
+    float* cv = s_cv[warp];
+    int* ci = s_ci[warp];
     for (int t = lane; t < chunks * k; t += 32) {
       const int c = t / k, j = t % k;
       const size_t g = ((size_t)r0 * chunks + c) * k + j;
@@ -342,36 +372,52 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
 }
 
 // ---- final selection --------------------------------------------------------------
+// Bitonic sort of 64-bit keys (descending score, then ascending store index) in shared
+// memory; the first total_tokens keys are the kept candidates, numbered in ascending
+// store index by a block prefix sum.
 constexpr int F_THREADS = 512;
+
+__device__ __forceinline__ uint64_t sel_key(float score, int idx) {
+  uint32_t u = __float_as_uint(score);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // ascending float order as unsigned
+  return ((uint64_t)(~u) << 32) | (uint32_t)idx;     // ascending key = descending score
+}
 
 __global__ void __launch_bounds__(F_THREADS)
 select_final_kernel(const int32_t* __restrict__ store_token, const float* __restrict__ store_score,
-                    const int32_t* __restrict__ store_parent, int C, int store_cap, int total,
-                    const int32_t* __restrict__ root_token, int max_nodes,
+                    const int32_t* __restrict__ store_parent, int C, int npow2, int store_cap,
+                    int total, const int32_t* __restrict__ root_token, int max_nodes,
                     int32_t* __restrict__ tokens, int32_t* __restrict__ parents,
                     int32_t* __restrict__ num_nodes) {
   extern __shared__ unsigned char smem[];
-  float* s_score = reinterpret_cast<float*>(smem);
-  int* s_node = reinterpret_cast<int*>(s_score + C);
+  uint64_t* s_key = reinterpret_cast<uint64_t*>(smem);          // [npow2]
+  int* s_node = reinterpret_cast<int*>(s_key + npow2);          // [C]
   __shared__ int s_warp[F_THREADS / 32];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t srow = (int64_t)b * store_cap;
-  for (int c = tid; c < C; c += F_THREADS) s_score[c] = store_score[srow + c];
+  for (int c = tid; c < npow2; c += F_THREADS)
+    s_key[c] = c < C ? sel_key(store_score[srow + c], c) : ~0ull;
+  for (int c = tid; c < C; c += F_THREADS) s_node[c] = 0;
   __syncthreads();
-
-  // Rank by counting; each thread owns a contiguous segment of candidates.
+  for (int size = 2; size <= npow2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = tid; t < npow2 / 2; t += F_THREADS) {
+        const int lo = 2 * t - (t & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const uint64_t a = s_key[lo], c = s_key[hi];
+        if ((a > c) == up) { s_key[lo] = c; s_key[hi] = a; }
+      }
+      __syncthreads();
+    }
+  }
+  for (int r = tid; r < total; r += F_THREADS) s_node[(int)(s_key[r] & 0xffffffffu)] = 1;
+  __syncthreads();
+  // Node numbers in ascending store index: each thread owns a contiguous segment.
   const int seg = (C + F_THREADS - 1) / F_THREADS;
   const int c0 = min(C, tid * seg), c1 = min(C, c0 + seg);
   int mine = 0;
-  for (int c = c0; c < c1; ++c) {
-    const float v = s_score[c];
-    int rank = 0;
-    for (int j = 0; j < C && rank < total; ++j) rank += better(s_score[j], j, v, c) ? 1 : 0;
-    const bool chosen = rank < total;
-    s_node[c] = chosen ? 1 : 0;
-    mine += chosen;
-  }
-  // Exclusive scan of the per-thread counts -> node numbers in ascending store order.
+  for (int c = c0; c < c1; ++c) mine += s_node[c];
   int incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -400,8 +446,7 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
     if (!node) continue;
     tokens[trow + node] = store_token[srow + c];
     const int p = store_parent[srow + c];
-    const int pn = (p >= 0 && p < C) ? s_node[p] : 0;
-    parents[trow + node] = pn;
+    parents[trow + node] = (p >= 0 && p < C) ? s_node[p] : 0;
   }
 }
 
@@ -412,8 +457,9 @@ TopkPlan plan_topk(int batch, int rows, int vocab, int top_k) {
   const int64_t rows_total = (int64_t)batch * rows;
   const int64_t target = 4LL * device_sm_count();
   int chunks = (int)std::min<int64_t>(MAX_CHUNKS, std::max<int64_t>(1, ceil_div(target, rows_total)));
-  // at least 2048 entries per chunk, and chunk lengths a multiple of 4
-  chunks = (int)std::max<int64_t>(1, std::min<int64_t>(chunks, ceil_div(vocab, 2048)));
+  // at least 8192 entries per chunk (short chunks are all fixed cost), lengths a
+  // multiple of 4
+  chunks = (int)std::max<int64_t>(1, std::min<int64_t>(chunks, ceil_div(vocab, 8192)));
   int chunk_len = (int)round_up(ceil_div(vocab, chunks), 4);
   chunks = (int)ceil_div(vocab, chunk_len);
   p.chunks = chunks;
@@ -436,16 +482,10 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
     return launch_status();
   dim3 grid(plan.chunks, rows_total);
   const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (row_stride % 4 == 0);
-  if (vec)
-    topk_level_kernel<true><<<grid, A_THREADS, 0, stream>>>(
-        logits, row_stride, vocab, rows, top_k, plan.chunks, plan.chunk_len, level, w,
-        front_score_in, front_store_in, store_cap, store_token, store_score, store_parent,
-        front_token_out, front_score_out, front_store_out);
-  else
-    topk_level_kernel<false><<<grid, A_THREADS, 0, stream>>>(
-        logits, row_stride, vocab, rows, top_k, plan.chunks, plan.chunk_len, level, w,
-        front_score_in, front_store_in, store_cap, store_token, store_score, store_parent,
-        front_token_out, front_score_out, front_store_out);
+  topk_level_kernel<<<grid, A_THREADS, 0, stream>>>(
+      logits, row_stride, vocab, rows, top_k, plan.chunks, plan.chunk_len, level, vec, w,
+      front_score_in, front_store_in, store_cap, store_token, store_score, store_parent,
+      front_token_out, front_score_out, front_store_out);
   return launch_status();
 }
 
@@ -454,11 +494,22 @@ int launch_select_final(const int32_t* store_token, const float* store_score,
                         int store_cap, int total_tokens, const int32_t* root_token,
                         int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
                         cudaStream_t stream) {
-  const size_t smem = (size_t)num_candidates * (sizeof(float) + sizeof(int));
+  int npow2 = 2;
+  while (npow2 < num_candidates) npow2 <<= 1;
+  const size_t smem = (size_t)npow2 * sizeof(uint64_t) + (size_t)num_candidates * sizeof(int);
+  if (smem > 48 * 1024) {
+    static bool attr = false;
+    if (!attr) {
+      if (cudaFuncSetAttribute(select_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               64 * 1024) != cudaSuccess)
+        return launch_status();
+      attr = true;
+    }
+  }
   select_final_kernel<<<batch, F_THREADS, smem, stream>>>(store_token, store_score, store_parent,
-                                                          num_candidates, store_cap, total_tokens,
-                                                          root_token, max_nodes, tokens, parents,
-                                                          num_nodes);
+                                                          num_candidates, npow2, store_cap,
+                                                          total_tokens, root_token, max_nodes,
+                                                          tokens, parents, num_nodes);
   return launch_status();
 }
 
