@@ -259,6 +259,35 @@ int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void*
                          size_t workspace_bytes, int32_t* err, tsv_stream_t stream);
 
 /* --------------------------------------------------------------------------------
+ * tsv_tree_verify_attn_noalloc — tsv_tree_verify_attn for callers that cannot allocate.
+ *
+ * The pages have no counterpart of this call; it exists for this library's users. Some
+ * callers cannot call cudaMalloc: their device memory is entirely owned by their own
+ * pool or arena, or they run in a latency-critical loop where an allocation (which can
+ * synchronize the device) is not acceptable, and they cannot size and keep a workspace
+ * themselves. This call computes exactly what tsv_tree_verify_attn computes, with the
+ * same arguments minus the workspace, and allocates nothing: its scratch is a fixed
+ * device array of TSV_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * - Returns TSV_ERR_WORKSPACE when the call would need more scratch than that
+ *   (tsv_tree_verify_attn_workspace_size tells how much a shape needs).
+ * - The first call on a device looks up the array's device address on that device
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ * - Every call on a device shares the one array, and a call leaves its contents behind.
+ *   Nothing in it has to start at zero. Calls whose GPU work overlaps (on different
+ *   streams, without ordering between them) race on the array and give wrong results.
+ * ------------------------------------------------------------------------------ */
+#define TSV_NOALLOC_SCRATCH_BYTES (32u << 20) /* 32 MiB per device */
+
+int tsv_tree_verify_attn_noalloc(const tsv_attn_shape* shape, const void* q, const void* k_new,
+                                 const void* v_new, const tsv_kv_cache* cache,
+                                 const int32_t* prefix_len, const int32_t* num_nodes,
+                                 const int32_t* position_ids, const uint32_t* mask,
+                                 float rope_theta, float softmax_scale, void* out, int32_t* err,
+                                 tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
  * tsv_accept_and_compact — greedy acceptance walk and KV compaction.
  *
  * [HB] section 实现 (tree_speculative_generate: from the root, step to the child whose

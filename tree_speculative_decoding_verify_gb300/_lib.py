@@ -69,7 +69,10 @@ _SIGNATURES = {
                               ctypes.c_void_p, ctypes.c_void_p]),
     "tsv_accept_and_compact": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int] * 3 +
                                [ctypes.c_void_p] * 8),
+    "tsv_tree_verify_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 9 +
+                                     [ctypes.c_float] * 2 + [ctypes.c_void_p] * 3),
 }
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def lib():
@@ -284,6 +287,33 @@ def tree_verify_attn(q, k_new, v_new, cache: KVCache, prefix_len, num_nodes, pos
                                       float(softmax_scale), _ptr(out), _ptr(workspace),
                                       workspace.numel(), _ptr(err), _stream()),
            "tsv_tree_verify_attn")
+
+
+def tree_verify_attn_noalloc(q, k_new, v_new, cache: KVCache, prefix_len, num_nodes,
+                             position_ids, mask, rope_theta, softmax_scale, out, max_prefix,
+                             err=None):
+    """tree_verify_attn without a workspace argument, for callers that cannot allocate
+    device memory: the library uses a fixed scratch array of NOALLOC_SCRATCH_BYTES per
+    device instead (calls on one device share it; see include/tsv.h)."""
+    b, t, hq, d = q.shape
+    hkv = cache.num_kv_heads
+    _need(q, cache.dtype, "q")
+    _need(k_new, cache.dtype, "k_new", (b, t, hkv, d))
+    _need(v_new, cache.dtype, "v_new", (b, t, hkv, d))
+    _need(out, cache.dtype, "out", (b, t, hq, d))
+    _need(prefix_len, torch.int32, "prefix_len", (b,))
+    _need(num_nodes, torch.int32, "num_nodes", (b,))
+    _need(position_ids, torch.int32, "position_ids", (b, t))
+    _need(mask, torch.int32, "mask", (b, t, (t + 31) // 32))
+    if err is not None:
+        _need(err, torch.int32, "err", (b,))
+    s = _attn_shape(q, max_prefix)
+    _check(lib().tsv_tree_verify_attn_noalloc(ctypes.byref(s), _ptr(q), _ptr(k_new), _ptr(v_new),
+                                              ctypes.byref(cache.desc), _ptr(prefix_len),
+                                              _ptr(num_nodes), _ptr(position_ids), _ptr(mask),
+                                              float(rope_theta), float(softmax_scale), _ptr(out),
+                                              _ptr(err), _stream()),
+           "tsv_tree_verify_attn_noalloc")
 
 
 def accept_and_compact(tokens, next_token, next_sibling, target_argmax, num_nodes, prefix_len,
