@@ -76,6 +76,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// True when the phase with this parity has completed (may wait a short, hardware-chosen
+// time before answering false).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -103,9 +105,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (abort) *abort = 1;
   return false;
 }
-// The whole warp waits; every lane gets the same answer.
+// Every lane polls the barrier (the lowest wake-up latency measured); every lane gets the
+// same answer.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
-  bool ok = mbar_wait(bar, parity, abort);
+  const bool ok = mbar_wait(bar, parity, abort);
   return __all_sync(0xffffffffu, ok);
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
@@ -328,7 +331,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     for (int m = 0; m < 2; ++m) {
       mbar_init(bar(BAR_S_FULL + m), 1);
-      mbar_init(bar(BAR_P_FULL + m), 128);
+      mbar_init(bar(BAR_P_FULL + m), 4);  // one arrival per softmax warp
     }
     mbar_init(bar(BAR_O_DONE), 1);
     mbar_init(bar(BAR_DRAIN), 1);
@@ -521,7 +524,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(BAR_P_FULL + mt));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + mt));
     }
     // epilogue
     if (ok) ok = warp_wait(bar(BAR_O_DONE), 0, abort);

@@ -68,14 +68,22 @@ __host__ __device__ inline TopkWs carve(void* ws, int rows_total, int chunks, in
   return w;
 }
 
+// Order-preserving unsigned image of a float (larger float -> larger unsigned).
+__device__ __forceinline__ unsigned ord(float v) {
+  const unsigned u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Warp-wide best (value, index) pair — larger value, then lower index — with two
+// hardware warp reductions; every lane gets the pair and the lane that holds it.
 __device__ __forceinline__ void warp_argmax(float& v, int& i, int& lane_of) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(FULL, v, o);
-    const int oi = __shfl_xor_sync(FULL, i, o);
-    const int ol = __shfl_xor_sync(FULL, lane_of, o);
-    if (better(ov, oi, v, i)) { v = ov; i = oi; lane_of = ol; }
-  }
+  const unsigned u = ord(v);
+  const unsigned umax = __reduce_max_sync(FULL, u);
+  const unsigned imin = __reduce_min_sync(FULL, u == umax ? (unsigned)i : 0xffffffffu);
+  const unsigned own = __ballot_sync(FULL, u == umax && (unsigned)i == imin);
+  lane_of = __ffs(own) - 1;
+  v = __shfl_sync(FULL, v, lane_of);
+  i = (int)imin;
 }
 
 // Sum of (ref_i, s_i) pairs over a warp against the warp's largest reference: one fp64
@@ -144,16 +152,17 @@ __device__ __forceinline__ void consider(Stream& st, float x, int idx) {
   }
 }
 
-// Warp merge: new list = best 16 of (list, all buffers); threshold = its 16th entry.
-__device__ __forceinline__ void warp_merge(Stream& st, int lane) {
+// Warp merge: new list = best k of (list, all buffers), held by lanes 0 .. k-1;
+// threshold = its k-th entry.
+__device__ __forceinline__ void warp_merge(Stream& st, int lane, int k) {
   // (inlined at three sites: the streaming loop, its tail and the final merge)
   unsigned taken = 0;       // bit s: buffer slot s used; bit BUF: list slot used
   float nv = -INFINITY;
   int ni = INT_MAX;
-  for (int r = 0; r < KMAX; ++r) {
+  for (int r = 0; r < k; ++r) {
     float v = -INFINITY;
     int i = INT_MAX, which = -1;
-    if (lane < KMAX && !(taken >> BUF & 1u) && better(st.lv, st.li, v, i)) {
+    if (lane < k && !(taken >> BUF & 1u) && better(st.lv, st.li, v, i)) {
       v = st.lv; i = st.li; which = BUF;
     }
 #pragma unroll
@@ -171,8 +180,8 @@ __device__ __forceinline__ void warp_merge(Stream& st, int lane) {
   }
   st.lv = nv;
   st.li = ni;
-  st.thr_v = __shfl_sync(FULL, nv, KMAX - 1);
-  st.thr_i = __shfl_sync(FULL, ni, KMAX - 1);
+  st.thr_v = __shfl_sync(FULL, nv, k - 1);
+  st.thr_i = __shfl_sync(FULL, ni, k - 1);
   st.bc = 0;
 }
 
@@ -248,13 +257,13 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
     if (e + 1 < end) consider(st, a.y, e + 1);
     if (e + 2 < end) consider(st, a.z, e + 2);
     if (e + 3 < end) consider(st, a.w, e + 3);
-    if (__any_sync(FULL, st.bc > BUF - 4)) warp_merge(st, lane);
+    if (__any_sync(FULL, st.bc > BUF - 4)) warp_merge(st, lane, k);
     if ((it & 3) == 3) flush(st);
     a = bnext;
     bnext = c;
   }
   flush(st);
-  warp_merge(st, lane);  // the warp's final best 16
+  warp_merge(st, lane, k);  // the warp's final best k
 
   // exp-sum: fold the parked pair, then combine over the block.
   if (st.ref0 != -INFINITY) st.d += st.d0 * exp((double)st.ref0 - (double)st.ref);
@@ -263,7 +272,7 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
   warp_combine(R, part);
   __syncthreads();  // s_red was read for the starting reference
   if (lane == 0) { s_red[warp] = R; s_sum[warp] = part; }
-  if (lane < KMAX) { s_wv[warp][lane] = st.lv; s_wi[warp][lane] = st.li; }
+  if (lane < k) { s_wv[warp][lane] = st.lv; s_wi[warp][lane] = st.li; }
   __syncthreads();
   if (warp == 0) {
     // block top-k: 8 sorted warp lists, lanes 0-7 hold the list heads
