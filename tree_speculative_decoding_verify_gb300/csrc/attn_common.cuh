@@ -37,8 +37,8 @@ struct AttnArgs {
   int direct_single;  // a request with one split was written by the attention kernel
 };
 
-// Query rows per tensor-core CTA (two 128-row M tiles).
-constexpr int TC_M_GROUP = 256;
+// Query rows per tensor-core CTA (one 128-row M tile).
+constexpr int TC_M_GROUP = 128;
 
 bool tc_supported(const AttnPlan& p);
 int launch_attn_tc(const AttnPlan& p, const AttnArgs& a, float scale_log2, void* out,

@@ -6,29 +6,33 @@
 // itself; GQA heads share a KV head) and "TensorRT-LLM 源码完全拆解(二十二)", section
 // CUDA Graph 里的掩码重排 (the Blackwell attention reads the padded bit mask directly).
 //
-// One CTA = (request b, KV head h, group of 256 query rows, split of the keys). The
-// query rows of a KV head are every (node, query head of the group) pair, so the KV
-// tiles of the split are read from HBM once for all of them.
+// One CTA = (request b, KV head h, one M tile of 128 query rows, split of the keys). The
+// query rows of a KV head are every (node, query head of the group) pair, so each K/V
+// tile serves all of them (a second M tile of the same head reads it again, mostly
+// from L2).
 //
-//   warp 8      TMA producer: Q tiles once, then K/V tiles of 128 keys (64-key boxes,
-//               128-byte swizzle) into a 2-stage shared-memory ring
-//   warp 9      TMEM allocator + MMA issuer (one elected lane):
-//                 S_mt = Q_mt K^T       A, B = shared memory, both K-major
-//                 O_mt += P_mt V        A = P in TMEM, B = V in shared memory, MN-major
-//   warps 0-7   two softmax warpgroups, one per 128-row M tile; thread = query row =
-//               TMEM lane. Pass 1 takes the row max of the masked scores, pass 2 writes
-//               P = exp2(s * scale * log2e - m) as bf16 over the S columns. The running
-//               max m is only raised when the tile max exceeds it by more than 8 (log2
-//               units); O in TMEM is rescaled then, otherwise never.
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).
-// Each CTA writes its unnormalised O rows plus (m, l) to the split workspace; the merge
-// kernel (attn.cu) combines the splits with a warp-shuffle log-sum-exp reduction.
+//   warp 4      TMA producer: Q once, then K/V tiles of 128 keys (64-key boxes, 128-byte
+//               swizzle) into 3-stage K and V rings; K runs one tile ahead of V
+//   warp 5      TMEM allocator + MMA issuer (one elected lane):
+//                 S[j%2] = Q K_j^T      A, B = shared memory, both K-major
+//                 O     += P_j V_j      A = P_j in TMEM (over S[j%2]), B = V, MN-major
+//               S is double-buffered, so S for tile j+1 is computed while the softmax
+//               works on tile j; the tensor core is the only serial resource.
+//   warps 0-3   softmax warpgroup; thread = query row = TMEM lane. One x128 TMEM load
+//               of S, the row max over 8 chains, P = exp2(s * scale * log2e - m) written
+//               as bf16 over the S buffer. The running max m is raised only when a tile's
+//               max exceeds it by more than 8 (log2 units), and O in TMEM is rescaled
+//               then (after the previous P V has finished), otherwise never.
+// TMEM (512 columns allocated): S[0] [0,128) S[1] [128,256) O [256,384).
+// A CTA that covers every key of its rows writes the normalised bf16 output itself;
+// otherwise it writes its unnormalised O rows plus (m, l) for the merge kernel (attn.cu),
+// which combines the splits with a warp-shuffle log-sum-exp reduction.
 //
-// The ancestor bitmask is applied from registers: every row keeps its node's mask words
-// and builds a 32-bit visibility word per 32-column chunk with a funnel shift.
+// The ancestor bitmask is applied from a 32-bit visibility word per 32-key chunk,
+// funnel-shifted out of the row's node mask (read only on tiles that hold tree keys).
 //
 // Every mbarrier wait is bounded; on a timeout the CTA records TSV_REQ_TIMEOUT for the
-// request, stops issuing work, drains its MMAs and frees its TMEM.
+// request, stops issuing work, drains its MMAs and copies and frees its TMEM.
 #include <cuda.h>
 
 #include "attn_common.cuh"
@@ -38,27 +42,29 @@ namespace tsv {
 namespace {
 
 constexpr int KEYS = 128;                 // keys per tile
-constexpr int KST = 3, VST = 2;           // K and V ring depths
-constexpr int THREADS = 320;
-constexpr int TMA_WARP = 8, MMA_WARP = 9;
+constexpr int KST = 3, VST = 3;           // K and V ring depths
+constexpr int THREADS = 192;
+constexpr int TMA_WARP = 4, MMA_WARP = 5;
 constexpr uint32_t HALF = 128 * 128;      // 128 rows x 64 bf16 (one 128-byte-swizzled panel)
 constexpr uint32_t TILE = 2 * HALF;       // 128 rows x 128 bf16
 constexpr uint32_t BOX64 = 64 * 128;      // one 64-row TMA box of a panel
-constexpr uint32_t SMEM_Q = 0;            // 2 M tiles
-constexpr uint32_t SMEM_K = 2 * TILE;     // KST K tiles
+constexpr uint32_t SMEM_Q = 0;            // one M tile
+constexpr uint32_t SMEM_K = TILE;         // KST K tiles
 constexpr uint32_t SMEM_V = SMEM_K + KST * TILE;  // VST V tiles
 constexpr uint32_t SMEM_BAR = SMEM_V + VST * TILE;
 constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_O = 256;
 constexpr float RESCALE_LOG2 = 8.f;
-constexpr uint32_t WAIT_LIMIT = 1u << 22;  // try_wait polls before a wait gives up
+constexpr uint32_t WAIT_LIMIT = 1u << 26;  // polls before a wait gives up
 constexpr uint64_t WAIT_NS = 1000000000ull;  // and at most one second
 
 // barrier slots (8 bytes each) after SMEM_BAR
 constexpr int BAR_Q = 0, BAR_K_FULL = 1, BAR_K_EMPTY = BAR_K_FULL + KST,
               BAR_V_FULL = BAR_K_EMPTY + KST, BAR_V_EMPTY = BAR_V_FULL + VST,
               BAR_S_FULL = BAR_V_EMPTY + VST, BAR_P_FULL = BAR_S_FULL + 2,
-              BAR_O_DONE = BAR_P_FULL + 2, BAR_DRAIN = BAR_O_DONE + 1, NUM_BARS = BAR_DRAIN + 1;
+              BAR_O_STEP = BAR_P_FULL + 2, BAR_O_DONE = BAR_O_STEP + 1,
+              BAR_DRAIN = BAR_O_DONE + 1, NUM_BARS = BAR_DRAIN + 1;
 static_assert(8 * NUM_BARS + 8 <= 256, "barrier area");
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 
@@ -76,12 +82,11 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-// True when the phase with this parity has completed (may wait a short, hardware-chosen
-// time before answering false).
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// True when the phase with this parity has completed (never blocks).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -94,11 +99,15 @@ __device__ __forceinline__ uint64_t now_ns() {
   return t;
 }
 // Bounded wait: false when the limit ran out (the CTA then aborts) or, if `abort` is
-// given, when another role of the CTA has given up already.
+// given, when another role of the CTA has given up already. Polls with a short sleep
+// between tests: a blocking try_wait was measured to wake about a microsecond after the
+// phase completed, which serialised the pipeline.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
+  if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = now_ns();
   for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    __nanosleep(32);
+    if (mbar_test(bar, parity)) return true;
     if (abort && *abort) return false;
     if ((i & 1023u) == 1023u && now_ns() - t0 > WAIT_NS) break;
   }
@@ -285,13 +294,12 @@ __device__ __forceinline__ uint32_t visible32(int k, int P, int T, const uint32_
   return pre | tr;
 }
 
-// 10 warps: the schedulers holding 3 of them cap a thread at 168 registers.
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
   extern __shared__ uint8_t smem_raw[];
   const AttnArgs& a = prm.a;
-  const int split = blockIdx.x, mg = blockIdx.y;
+  const int split = blockIdx.x, mt = blockIdx.y;
   const int b = blockIdx.z / a.hkv, h = blockIdx.z % a.hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -299,9 +307,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (!a.valid[b]) return;
   const int T = a.num_nodes[b], P = a.prefix_len[b];
   const int rows = T * a.group;
-  const int row0 = mg * 256;
+  const int row0 = mt * 128;
   if (row0 >= rows) return;
-  const int n_mt = rows - row0 > 128 ? 2 : 1;
   const int keys = P + T;
   const int n_tiles = (keys + KEYS - 1) / KEYS;
   const int t0 = split * a.tiles_per_split;
@@ -329,10 +336,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(bar(BAR_V_FULL + s), 1);
       mbar_init(bar(BAR_V_EMPTY + s), 1);
     }
-    for (int m = 0; m < 2; ++m) {
-      mbar_init(bar(BAR_S_FULL + m), 1);
-      mbar_init(bar(BAR_P_FULL + m), 4);  // one arrival per softmax warp
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(BAR_S_FULL + s), 1);
+      mbar_init(bar(BAR_P_FULL + s), 4);  // one arrival per softmax warp
     }
+    mbar_init(bar(BAR_O_STEP), 1);
     mbar_init(bar(BAR_O_DONE), 1);
     mbar_init(bar(BAR_DRAIN), 1);
     *abort = 0;
@@ -349,11 +357,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // of V (order K0 K1 V0 K2 V1 ...), so S = Q K^T never waits behind a V load.
     const int qrow = (b * a.hkv + h) * a.rows_pad + row0;
     if (lane == 0) {
-      mbar_expect_tx(bar(BAR_Q), n_mt * TILE);
-      for (int mt = 0; mt < n_mt; ++mt)
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_2d(base + SMEM_Q + mt * TILE + hf * HALF, &tm_q, hf * 64, qrow + mt * 128,
-                      bar(BAR_Q));
+      mbar_expect_tx(bar(BAR_Q), TILE);
+      for (int hf = 0; hf < 2; ++hf)
+        tma_load_2d(base + SMEM_Q + hf * HALF, &tm_q, hf * 64, qrow, bar(BAR_Q));
     }
     auto row_of = [&](int key) -> int {
       if (a.layout == TSV_KV_CONTIGUOUS) return (int)(((int64_t)b * a.hkv + h) * a.capacity + key);
@@ -401,47 +407,45 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // ---- MMA issuer: the whole warp walks the loop, lane 0 issues --------------------
     constexpr uint32_t ID_QK = idesc(0), ID_PV = idesc(1);
     const bool issuer = lane == 0;
-    auto qk = [&](int mt, int j) {
+    // S[j % 2] = Q K_j^T
+    auto qk = [&](int j) {
       if (!issuer) return;
-      const uint32_t qa = base + SMEM_Q + mt * TILE;
       const uint32_t ka = base + SMEM_K + (j % KST) * TILE;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t off = (ks >> 2) * HALF + (ks & 3) * 32;
-        mma_ss(tmem + mt * 128, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), ID_QK,
-               ks > 0);
+        mma_ss(tmem + (j & 1) * 128, sdesc(base + SMEM_Q + off, 16, 1024), sdesc(ka + off, 16, 1024),
+               ID_QK, ks > 0);
       }
-      mma_commit(bar(BAR_S_FULL + mt));
-      if (mt == n_mt - 1) mma_commit(bar(BAR_K_EMPTY + j % KST));
+      mma_commit(bar(BAR_S_FULL + (j & 1)));
+      mma_commit(bar(BAR_K_EMPTY + j % KST));
     };
-    auto pv = [&](int mt, int j, int ksteps) {
+    // O += P_j V_j
+    auto pv = [&](int j, int ksteps) {
       if (!issuer) return;
       const uint32_t va = base + SMEM_V + (j % VST) * TILE;
       for (int ks = 0; ks < ksteps; ++ks)
-        mma_ts(tmem + 256 + mt * 128, tmem + mt * 128 + ks * 8,
-               sdesc(va + ks * 16 * 128, HALF, 1024), ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
-      if (mt == n_mt - 1) mma_commit(bar(BAR_V_EMPTY + j % VST));
+        mma_ts(tmem + TMEM_O, tmem + (j & 1) * 128 + ks * 8, sdesc(va + ks * 16 * 128, HALF, 1024),
+               ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
+      mma_commit(bar(BAR_V_EMPTY + j % VST));
+      mma_commit(bar(BAR_O_STEP));
     };
-    bool ok = warp_wait(bar(BAR_Q), 0, abort) && warp_wait(bar(BAR_K_FULL), 0, abort);
-    if (ok) {
+    bool ok = warp_wait(bar(BAR_Q), 0, abort);
+    for (int j = 0; ok && j < 2 && j < n; ++j) {
+      if (!(ok = warp_wait(bar(BAR_K_FULL + j % KST), (j / KST) & 1, abort))) break;
       tc_fence_after();
-      for (int mt = 0; mt < n_mt; ++mt) qk(mt, 0);
+      qk(j);
     }
     for (int j = 0; ok && j < n; ++j) {
       const int valid = min(KEYS, keys - (t0 + j) * KEYS);
-      const int ksteps = (valid + 15) >> 4;
-      for (int mt = 0; ok && mt < n_mt; ++mt) {
-        if (!(ok = warp_wait(bar(BAR_P_FULL + mt), j & 1, abort))) break;
-        if (mt == 0 && !(ok = warp_wait(bar(BAR_V_FULL + j % VST), (j / VST) & 1, abort))) break;
+      if (!(ok = warp_wait(bar(BAR_P_FULL + (j & 1)), (j >> 1) & 1, abort))) break;
+      if (!(ok = warp_wait(bar(BAR_V_FULL + j % VST), (j / VST) & 1, abort))) break;
+      tc_fence_after();
+      pv(j, (valid + 15) >> 4);
+      if (j + 2 < n) {  // issued after P_j V_j, so it may overwrite P_j's columns
+        if (!(ok = warp_wait(bar(BAR_K_FULL + (j + 2) % KST), ((j + 2) / KST) & 1, abort))) break;
         tc_fence_after();
-        pv(mt, j, ksteps);
-        if (j + 1 < n) {
-          if (mt == 0) {
-            if (!(ok = warp_wait(bar(BAR_K_FULL + (j + 1) % KST), ((j + 1) / KST) & 1, abort))) break;
-            tc_fence_after();
-          }
-          qk(mt, j + 1);
-        }
+        qk(j + 2);
       }
     }
     if (issuer) {
@@ -451,22 +455,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_wait(bar(BAR_DRAIN), 0, nullptr);
     }
     __syncwarp();
-  } else if (warp / 4 < n_mt) {
-    // ---- softmax warpgroups ----------------------------------------------------------
-    const int mt = warp / 4, quad = warp & 3;
-    const int r = row0 + mt * 128 + quad * 32 + lane;
+  } else if (warp < 4) {
+    // ---- softmax warpgroup -----------------------------------------------------------
+    const int r = row0 + warp * 32 + lane;
     const bool live = r < rows;
     const int node = r / a.group;
     // rows past the tree read node 0's mask (their results are never stored)
     const uint32_t* mrow = a.mask + ((int64_t)b * a.max_nodes + (live ? node : 0)) * a.mask_words;
-    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t s_addr = tmem + lane_base + mt * 128;
-    const uint32_t o_addr = tmem + lane_base + 256 + mt * 128;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t o_addr = tmem + lane_base + TMEM_O;
     const float sl2 = prm.scale_log2;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      if (!(ok = warp_wait(bar(BAR_S_FULL + mt), j & 1, abort))) break;
+      const uint32_t s_addr = tmem + lane_base + (j & 1) * 128;
+      if (!(ok = warp_wait(bar(BAR_S_FULL + (j & 1)), (j >> 1) & 1, abort))) break;
       tc_fence_after();
       const int k0 = (t0 + j) * KEYS;
       float v[128];
@@ -493,7 +496,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (need) m_used = mxs;
       // a row with nothing visible so far has only -inf scores: any finite offset works
       const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-      // P = exp2(s * scale_log2 - m) in bf16 over the first 64 S columns
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -512,7 +514,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       l = l * factor + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
       if (__any_sync(FULL, need) && j > 0) {
-        // O is quiescent: this tile's S was committed after the previous P V finished.
+        // O must be quiescent: wait for P_{j-1} V_{j-1} (P_{j-2} V_{j-2} finished before
+        // this tile's S was computed, so the parity names the right phase).
+        if (!(ok = warp_wait(bar(BAR_O_STEP), (j - 1) & 1, abort))) break;
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           float o[32];
@@ -525,7 +530,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + mt));
+      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + (j & 1)));
     }
     // epilogue
     if (ok) ok = warp_wait(bar(BAR_O_DONE), 0, abort);
@@ -641,7 +646,7 @@ int launch_attn_tc(const AttnPlan& p, const AttnArgs& a, float scale_log2, void*
       !make_map(&mk, a.k_cache, kv_rows, 64) || !make_map(&mv, a.v_cache, kv_rows, 64))
     return TSV_ERR_UNSUPPORTED;
   TcParams prm{a, scale_log2, static_cast<__nv_bfloat16*>(out)};
-  dim3 grid(p.nsplit, (unsigned)ceil_div(p.rows, TC_M_GROUP), p.batch * p.hkv);
+  dim3 grid(p.nsplit, (unsigned)ceil_div(p.rows, TC_M_GROUP), p.batch * p.hkv);  // M tiles of 128 rows
   attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, prm);
   return launch_status();
 }
