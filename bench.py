@@ -80,7 +80,7 @@ def algorithmic(w, prefix, depths_per_req, esize=2):
     nbytes = 0
     flops = 0
     for p, deps in zip(prefix, depths_per_req):
-        t = len(deps)
+        p, t = int(p), len(deps)  # Python ints: the FLOP count overflows 32 bits
         nbytes += 2 * p * hkv * d * esize + 4 * t * hkv * d * esize + 2 * t * hq * d * esize
         flops += 4 * d * hq * sum(p + dep + 1 for dep in deps)
     return nbytes, flops

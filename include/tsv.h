@@ -226,6 +226,8 @@ int tsv_tree_build_meta(const int32_t* parents, const int32_t* num_nodes,
  *                  the split-KV grid).
  * q, out           [batch, max_nodes, num_q_heads, head_dim], cache->dtype.
  * k_new, v_new     [batch, max_nodes, num_kv_heads, head_dim], cache->dtype.
+ *                  q, k_new, v_new and out start on 16-byte boundaries (the kernels
+ *                  move 16 bytes per access); TSV_ERR_INVALID_ARG otherwise.
  * cache            one layer's KV cache (num_layers/layer_stride are ignored). The
  *                  prefix keys must already be rotated. On return slots P_b ..
  *                  P_b + T_b - 1 hold the tree's rotated keys and its values, and the

@@ -87,6 +87,10 @@ static bool cache_ok(const tsv_kv_cache* c, bool need_layers) {
 
 using namespace tsv;
 
+namespace {
+inline bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
+}  // namespace
+
 extern "C" {
 
 const char* tsv_version(void) { return "tsv 0.1.0 (sm_103a)"; }
@@ -194,6 +198,8 @@ int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void*
   if (!(rope_theta > 0.f) || !(softmax_scale > 0.f)) return TSV_ERR_INVALID_ARG;
   if (shape->batch == 0) return TSV_OK;
   if (!q || !k_new || !v_new || !prefix_len || !num_nodes || !position_ids || !mask || !out)
+    return TSV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
     return TSV_ERR_INVALID_ARG;
   const AttnPlan plan = plan_attn(shape, cache);
   if (!workspace || workspace_bytes < plan.ws_bytes ||

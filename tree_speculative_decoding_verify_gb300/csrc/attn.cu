@@ -14,6 +14,7 @@
 //   o_part [B, Hkv, nsplit, rows_pad, D] f32  unnormalised partial outputs
 //   ml     [B, Hkv, nsplit, rows_pad, 2]  f32  (running max m in log2 units, sum l)
 //   valid  [B] int32                      request passed the device checks
+//   tickets [B, Hkv, rows_pad / 128] int32 splits finished per M tile (tensor-core path)
 #include <math.h>
 #include <stdint.h>
 
@@ -26,7 +27,7 @@
 namespace tsv {
 namespace {
 
-constexpr int PREP_THREADS = 256;
+constexpr int PREP_THREADS = 128;
 constexpr int SIMT_WARPS = 8;
 constexpr int MERGE_WARPS = 8;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -50,8 +51,76 @@ __device__ __forceinline__ T* slot_ptr(const AttnArgs& a, T* base, int b, int h,
   return base + (((int64_t)blk * a.hkv + h) * TSV_KV_BLOCK + slot % TSV_KV_BLOCK) * a.head_dim;
 }
 
-// One CTA per (node, request): rotate q and k at position_ids, append k/v to the cache,
-// zero the padding rows of q_rot and the cache slots up to the next multiple of 16.
+// Eight consecutive elements of T as one (bf16) or two (f32) 16-byte accesses.
+template <typename T> struct Vec8;
+template <> struct Vec8<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ void store(__nv_bfloat16* p) const { *reinterpret_cast<uint4*>(p) = u; }
+  __device__ __forceinline__ void zero() { u = make_uint4(0, 0, 0, 0); }
+  __device__ __forceinline__ void get(float (&f)[8]) const {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __bfloat1622float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  __device__ __forceinline__ void set(const float (&f)[8]) {
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  }
+};
+template <> struct Vec8<float> {
+  float4 x, y;
+  __device__ __forceinline__ void load(const float* p) {
+    x = reinterpret_cast<const float4*>(p)[0];
+    y = reinterpret_cast<const float4*>(p)[1];
+  }
+  __device__ __forceinline__ void store(float* p) const {
+    reinterpret_cast<float4*>(p)[0] = x;
+    reinterpret_cast<float4*>(p)[1] = y;
+  }
+  __device__ __forceinline__ void zero() { x = y = make_float4(0.f, 0.f, 0.f, 0.f); }
+  __device__ __forceinline__ void get(float (&f)[8]) const {
+    f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w; f[4] = y.x; f[5] = y.y; f[6] = y.z; f[7] = y.w;
+  }
+  __device__ __forceinline__ void set(const float (&f)[8]) {
+    x = make_float4(f[0], f[1], f[2], f[3]);
+    y = make_float4(f[4], f[5], f[6], f[7]);
+  }
+};
+
+// Rotate-half RoPE of elements m0 .. m0 + 7 of both halves of one head vector.
+template <typename T, typename U>
+__device__ __forceinline__ void rope8(const T* src, U* dst, int m0, int half, const float* cs,
+                                      const float* sn) {
+  Vec8<T> a, b;
+  a.load(src + m0);
+  b.load(src + m0 + half);
+  float x1[8], x2[8], y1[8], y2[8];
+  a.get(x1);
+  b.get(x2);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float c = cs[m0 + e], s = sn[m0 + e];
+    y1[e] = x1[e] * c - x2[e] * s;
+    y2[e] = x2[e] * c + x1[e] * s;
+  }
+  Vec8<U> o1, o2;
+  o1.set(y1);
+  o2.set(y2);
+  o1.store(dst + m0);
+  o2.store(dst + m0 + half);
+}
+
+// One CTA per (node, request): rotate q and k at position_ids, append k/v to the cache and
+// zero the cache slots after the tree up to the next multiple of 16; for a node past the
+// tree (or a request that failed its checks) zero its output row. Every access moves 16
+// bytes. Query rows of the workspace that belong to no node are left as they are: rows
+// are independent in every kernel, and such rows are never stored.
 template <typename T, typename QT>
 __global__ void __launch_bounds__(PREP_THREADS)
 prep_kernel(AttnArgs a, const T* __restrict__ q, const T* __restrict__ k_new,
@@ -71,14 +140,19 @@ prep_kernel(AttnArgs a, const T* __restrict__ q, const T* __restrict__ k_new,
     if (__syncthreads_or(bad)) code = TSV_REQ_BAD_BLOCK;
   }
   const bool ok = code == TSV_REQ_OK;
-  if (i == 0 && tid == 0) {
-    a.valid[b] = ok ? 1 : 0;
-    if (a.err) a.err[b] = code;
+  if (i == 0) {
+    if (tid == 0) {
+      a.valid[b] = ok ? 1 : 0;
+      if (a.err) a.err[b] = code;
+    }
+    // merge tickets of this request (tensor-core path)
+    if (a.tickets)
+      for (int e = tid; e < a.hkv * (a.rows_pad / 128); e += PREP_THREADS)
+        a.tickets[(int64_t)b * a.hkv * (a.rows_pad / 128) + e] = 0;
   }
   const int Tn = ok ? a.num_nodes[b] : 0;
   const int P = ok ? a.prefix_len[b] : 0;
-  QT* qr = reinterpret_cast<QT*>(a.q_rot);
-  const int64_t qbase = (int64_t)b * a.hkv * a.rows_pad;
+  const int V8 = D / 8, H8 = H / 8;
 
   if (i < Tn) {
     const int pos = a.position_ids[(int64_t)b * a.max_nodes + i];
@@ -93,52 +167,43 @@ prep_kernel(AttnArgs a, const T* __restrict__ q, const T* __restrict__ k_new,
       s_sin[tid] = sn;
     }
     __syncthreads();
+    QT* qr = reinterpret_cast<QT*>(a.q_rot);
+    const int64_t qbase = (int64_t)b * a.hkv * a.rows_pad;
     const T* qi = q + ((int64_t)b * a.max_nodes + i) * a.hq * D;
-    for (int e = tid; e < a.hq * H; e += PREP_THREADS) {
-      const int h = e / H, m = e % H;
-      const float x1 = to_f32(qi[h * D + m]), x2 = to_f32(qi[h * D + m + H]);
-      const float c = s_cos[m], s = s_sin[m];
-      QT* dst = qr + ((qbase + (int64_t)(h / G) * a.rows_pad) + (int64_t)i * G + h % G) * D;
-      dst[m] = from_f32<QT>(x1 * c - x2 * s);
-      dst[m + H] = from_f32<QT>(x2 * c + x1 * s);
+    for (int e = tid; e < a.hq * H8; e += PREP_THREADS) {
+      const int h = e / H8, m0 = (e % H8) * 8;
+      rope8(qi + h * D, qr + ((qbase + (int64_t)(h / G) * a.rows_pad) + (int64_t)i * G + h % G) * D,
+            m0, H, s_cos, s_sin);
     }
     const T* ki = k_new + ((int64_t)b * a.max_nodes + i) * a.hkv * D;
-    const T* vi = v_new + ((int64_t)b * a.max_nodes + i) * a.hkv * D;
-    for (int e = tid; e < a.hkv * H; e += PREP_THREADS) {
-      const int h = e / H, m = e % H;
-      const float x1 = to_f32(ki[h * D + m]), x2 = to_f32(ki[h * D + m + H]);
-      const float c = s_cos[m], s = s_sin[m];
-      T* dst = slot_ptr(a, reinterpret_cast<T*>(a.k_cache), b, h, P + i);
-      dst[m] = from_f32<T>(x1 * c - x2 * s);
-      dst[m + H] = from_f32<T>(x2 * c + x1 * s);
+    for (int e = tid; e < a.hkv * H8; e += PREP_THREADS) {
+      const int h = e / H8, m0 = (e % H8) * 8;
+      rope8(ki + h * D, slot_ptr(a, reinterpret_cast<T*>(a.k_cache), b, h, P + i), m0, H, s_cos,
+            s_sin);
     }
-    for (int e = tid; e < a.hkv * D; e += PREP_THREADS) {
-      const int h = e / D, d = e % D;
-      slot_ptr(a, reinterpret_cast<T*>(a.v_cache), b, h, P + i)[d] = vi[h * D + d];
+    const T* vi = v_new + ((int64_t)b * a.max_nodes + i) * a.hkv * D;
+    for (int e = tid; e < a.hkv * V8; e += PREP_THREADS) {
+      const int h = e / V8, d0 = (e % V8) * 8;
+      Vec8<T> x;
+      x.load(vi + h * D + d0);
+      x.store(slot_ptr(a, reinterpret_cast<T*>(a.v_cache), b, h, P + i) + d0);
     }
     if (i == Tn - 1) {  // zero the slots after the tree up to the next multiple of 16
       const int pad = ((P + Tn + 15) & ~15) - (P + Tn);
-      for (int e = tid; e < pad * a.hkv * D; e += PREP_THREADS) {
-        const int j = e / (a.hkv * D), h = (e / D) % a.hkv, d = e % D;
-        slot_ptr(a, reinterpret_cast<T*>(a.k_cache), b, h, P + Tn + j)[d] = from_f32<T>(0.f);
-        slot_ptr(a, reinterpret_cast<T*>(a.v_cache), b, h, P + Tn + j)[d] = from_f32<T>(0.f);
+      Vec8<T> z;
+      z.zero();
+      for (int e = tid; e < pad * a.hkv * V8; e += PREP_THREADS) {
+        const int j = e / (a.hkv * V8), h = (e / V8) % a.hkv, d0 = (e % V8) * 8;
+        z.store(slot_ptr(a, reinterpret_cast<T*>(a.k_cache), b, h, P + Tn + j) + d0);
+        z.store(slot_ptr(a, reinterpret_cast<T*>(a.v_cache), b, h, P + Tn + j) + d0);
       }
     }
   } else {
-    // no node here (or the request failed its checks): zero its q rows and its output
-    for (int e = tid; e < a.hkv * G * D; e += PREP_THREADS) {
-      const int h = e / (G * D), g = (e / D) % G, d = e % D;
-      qr[((qbase + (int64_t)h * a.rows_pad) + (int64_t)i * G + g) * D + d] = from_f32<QT>(0.f);
-    }
+    // no node here (or the request failed its checks): its output row is zero
     T* o = reinterpret_cast<T*>(a.out) + ((int64_t)b * a.max_nodes + i) * a.hq * D;
-    for (int e = tid; e < a.hq * D; e += PREP_THREADS) o[e] = from_f32<T>(0.f);
-  }
-  if (i == 0) {  // rows past max_nodes * G up to rows_pad
-    const int extra = a.rows_pad - a.max_nodes * G;
-    for (int e = tid; e < a.hkv * extra * D; e += PREP_THREADS) {
-      const int h = e / (extra * D), r = a.max_nodes * G + (e / D) % extra, d = e % D;
-      qr[((qbase + (int64_t)h * a.rows_pad) + r) * D + d] = from_f32<QT>(0.f);
-    }
+    Vec8<T> z;
+    z.zero();
+    for (int e = tid; e < a.hq * V8; e += PREP_THREADS) z.store(o + e * 8);
   }
 }
 
@@ -220,7 +285,6 @@ merge_kernel(AttnArgs a, T* __restrict__ out) {
   const int keys = a.prefix_len[b] + a.num_nodes[b];
   const int n_tiles = (keys + a.tile_keys - 1) / a.tile_keys;
   const int nsp = (n_tiles + a.tiles_per_split - 1) / a.tiles_per_split;
-  if (nsp == 1 && a.direct_single) return;  // already final
   const int64_t pbase = ((int64_t)b * a.hkv + kv) * a.nsplit;
   // running (M, L) over this lane's splits, then a warp-shuffle combine
   float M = -INFINITY, L = 0.f;
@@ -280,7 +344,8 @@ AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache) {
     // stay under about half of the KV bytes.
     const int64_t units = (int64_t)p.batch * p.hkv * ceil_div(p.rows, TC_M_GROUP);
     const int64_t rows_g = std::min<int64_t>(p.rows, TC_M_GROUP);
-    const int64_t cap = std::max<int64_t>(1, std::min(n_tiles, keys_max / (2 * rows_g)));
+    const int64_t cap = std::max<int64_t>(
+        1, std::min<int64_t>({n_tiles, keys_max / (2 * rows_g), (int64_t)TSV_ATTN_MAX_SPLITS}));
     int64_t best = 1, best_cost = INT64_MAX;
     for (int64_t ns = 1; ns <= cap; ++ns) {
       const int64_t tps = ceil_div(n_tiles, ns);
@@ -308,6 +373,8 @@ AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache) {
   off += align256(planes * p.nsplit * p.rows_pad * 2 * sizeof(float));
   p.off_valid = off;
   off += align256((size_t)p.batch * sizeof(int32_t));
+  p.off_tickets = off;
+  if (p.tensor_core) off += align256(planes * (p.rows_pad / TC_M_GROUP) * sizeof(int32_t));
   p.ws_bytes = off;
   return p;
 }
@@ -336,6 +403,7 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
   a.o_part = reinterpret_cast<float*>(w + p.off_opart);
   a.ml = reinterpret_cast<float*>(w + p.off_ml);
   a.valid = reinterpret_cast<int32_t*>(w + p.off_valid);
+  a.tickets = p.tensor_core ? reinterpret_cast<int32_t*>(w + p.off_tickets) : nullptr;
   a.max_nodes = p.max_nodes;
   a.hq = p.hq;
   a.hkv = p.hkv;
@@ -346,7 +414,6 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
   a.tile_keys = p.tile_keys;
   a.tiles_per_split = p.tiles_per_split;
   a.nsplit = p.nsplit;
-  a.direct_single = p.tensor_core ? 1 : 0;
 
   RopeTable rope{};
   for (int m = 0; m < p.head_dim / 2; ++m)
@@ -371,8 +438,8 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
   if (st != TSV_OK) return st;
 
   if (p.tensor_core) {
-    st = launch_attn_tc(p, a, scale_log2, out, stream);
-    if (st != TSV_OK) return st;
+    // the split partials are merged inside the kernel (last split of each row block)
+    return launch_attn_tc(p, a, scale_log2, out, stream);
   } else {
     dim3 gs((unsigned)ceil_div(p.rows, SIMT_WARPS), p.nsplit, p.batch * p.hkv);
     if (bf16) {

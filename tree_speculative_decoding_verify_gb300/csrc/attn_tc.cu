@@ -11,22 +11,34 @@
 // tile serves all of them (a second M tile of the same head reads it again, mostly
 // from L2).
 //
-//   warp 4      TMA producer: Q once, then K/V tiles of 128 keys (64-key boxes, 128-byte
-//               swizzle) into 3-stage K and V rings; K runs one tile ahead of V
-//   warp 5      TMEM allocator + MMA issuer (one elected lane):
-//                 S[j%2] = Q K_j^T      A, B = shared memory, both K-major
-//                 O     += P_j V_j      A = P_j in TMEM (over S[j%2]), B = V, MN-major
-//               S is double-buffered, so S for tile j+1 is computed while the softmax
-//               works on tile j; the tensor core is the only serial resource.
-//   warps 0-3   softmax warpgroup; thread = query row = TMEM lane. One x128 TMEM load
-//               of S, the row max over 8 chains, P = exp2(s * scale * log2e - m) written
-//               as bf16 over the S buffer. The running max m is raised only when a tile's
-//               max exceeds it by more than 8 (log2 units), and O in TMEM is rescaled
-//               then (after the previous P V has finished), otherwise never.
-// TMEM (512 columns allocated): S[0] [0,128) S[1] [128,256) O [256,384).
+//   warp 4      TMA producer: K/V tiles of 128 keys (64-key boxes, 128-byte swizzle)
+//               into a 4-stage K ring and a 3-stage V ring; K runs one tile ahead of V
+//   warp 5      TMEM allocator + MMA issuer (warp-uniform descriptors, one elected lane
+//               per instruction). Step j (j = 0 .. n) issues
+//                 S      = Q K_{j+1}^T      A = Q in TMEM, B = K (shared, K-major)
+//                 O     += P_{j-1} V_{j-1}  A = P[(j-1)%2] in TMEM, B = V (shared, MN-major)
+//               as soon as the softmax has read S_j into registers, so S_{j+1} is
+//               computed while the softmax works on tile j. Q and P come from TMEM: the
+//               shared-memory port then carries only the K and V tiles (TMA writes plus
+//               one MMA read each).
+//   warp 6      relay: arrives on GO for step j once K_{j+1} and V_{j-1} have landed;
+//               the four softmax warps arrive on it once they have read S_j (which
+//               also publishes P_{j-1}). The MMA warp tests that one barrier per step:
+//               every test it makes is an issue gap in which the shallow MMA queue
+//               drains, and every mbarrier operation waits behind the operand traffic
+//               of the shared-memory port (a few hundred cycles), so the critical path
+//               softmax -> MMA crosses a single barrier.
+//   warps 0-3   softmax warpgroup; thread = query row = TMEM lane. Each thread first
+//               copies its rotated query row into TMEM. Per tile: one x128 TMEM load of
+//               S, the row max over 8 chains, P = exp2(s * scale * log2e - m) rounded to
+//               bf16 and stored into P[j%2] once P_{j-2} V_{j-2} has finished with it.
+//               The running max m is raised only when a tile's max exceeds it by more
+//               than 8 (log2 units), and O in TMEM is rescaled then, otherwise never.
+// TMEM (512 columns allocated): S [0,128) O [128,256) P[0] [256,320) P[1] [320,384)
+// Q [384,448).
 // A CTA that covers every key of its rows writes the normalised bf16 output itself;
-// otherwise it writes its unnormalised O rows plus (m, l) for the merge kernel (attn.cu),
-// which combines the splits with a warp-shuffle log-sum-exp reduction.
+// otherwise it writes its unnormalised O rows plus (m, l), and the last split of the row
+// block to finish (an atomic ticket) combines them with a warp-shuffle log-sum-exp merge.
 //
 // The ancestor bitmask is applied from a 32-bit visibility word per 32-key chunk,
 // funnel-shifted out of the row's node mask (read only on tiles that hold tree keys).
@@ -42,19 +54,26 @@ namespace tsv {
 namespace {
 
 constexpr int KEYS = 128;                 // keys per tile
-constexpr int KST = 3, VST = 3;           // K and V ring depths
-constexpr int THREADS = 192;
-constexpr int TMA_WARP = 4, MMA_WARP = 5;
+constexpr int KST = 4, VST = 3;           // K and V ring depths
+constexpr int THREADS = 224;
+constexpr int TMA_WARP = 4, MMA_WARP = 5, RELAY_WARP = 6;
 constexpr uint32_t HALF = 128 * 128;      // 128 rows x 64 bf16 (one 128-byte-swizzled panel)
 constexpr uint32_t TILE = 2 * HALF;       // 128 rows x 128 bf16
 constexpr uint32_t BOX64 = 64 * 128;      // one 64-row TMA box of a panel
-constexpr uint32_t SMEM_Q = 0;            // one M tile
-constexpr uint32_t SMEM_K = TILE;         // KST K tiles
+constexpr uint32_t SMEM_K = 0;            // KST K tiles
 constexpr uint32_t SMEM_V = SMEM_K + KST * TILE;  // VST V tiles
 constexpr uint32_t SMEM_BAR = SMEM_V + VST * TILE;
 constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + alignment slack
+// split merge (after the last MMA, over the K/V rings): three 64 KB partial tiles (128 rows
+// x 128 f32, row-major), then the per-split row weights
+constexpr uint32_t MERGE_TILE = 128 * 128 * 4;
+constexpr uint32_t MERGE_W = 3 * MERGE_TILE;
+static_assert(MERGE_W + TSV_ATTN_MAX_SPLITS * 128 * 4 <= SMEM_BAR, "merge buffers");
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_O = 256;
+constexpr uint32_t TMEM_S = 0;
+constexpr uint32_t TMEM_O = 128;
+constexpr uint32_t TMEM_P = 256;  // two buffers of 64 columns: 128 bf16 per row
+constexpr uint32_t TMEM_Q = 384;  // 64 columns: the row's 128 rotated query values
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr uint32_t WAIT_LIMIT = 1u << 26;  // polls before a wait gives up
 constexpr uint64_t WAIT_NS = 1000000000ull;  // and at most one second
@@ -62,10 +81,11 @@ constexpr uint64_t WAIT_NS = 1000000000ull;  // and at most one second
 // barrier slots (8 bytes each) after SMEM_BAR
 constexpr int BAR_Q = 0, BAR_K_FULL = 1, BAR_K_EMPTY = BAR_K_FULL + KST,
               BAR_V_FULL = BAR_K_EMPTY + KST, BAR_V_EMPTY = BAR_V_FULL + VST,
-              BAR_S_FULL = BAR_V_EMPTY + VST, BAR_P_FULL = BAR_S_FULL + 2,
-              BAR_O_STEP = BAR_P_FULL + 2, BAR_O_DONE = BAR_O_STEP + 1,
-              BAR_DRAIN = BAR_O_DONE + 1, NUM_BARS = BAR_DRAIN + 1;
-static_assert(8 * NUM_BARS + 8 <= 256, "barrier area");
+              BAR_S_FULL = BAR_V_EMPTY + VST, BAR_PV_DONE = BAR_S_FULL + 1,
+              BAR_O_DONE = BAR_PV_DONE + 2,
+              BAR_DRAIN = BAR_O_DONE + 1, BAR_GO = BAR_DRAIN + 1, BAR_MERGE = BAR_GO + 2,
+              NUM_BARS = BAR_MERGE + 1;
+static_assert(8 * NUM_BARS + 12 <= 256, "barrier area");
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 
 // ---- PTX wrappers ----------------------------------------------------------------
@@ -93,20 +113,30 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// One lane of the (converged) warp gets true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile(
+      "{\n .reg .pred P;\n elect.sync _|P, 0xffffffff;\n selp.u32 %0, 1, 0, P;\n}\n"
+      : "=r"(p));
+  return p != 0;
+}
 __device__ __forceinline__ uint64_t now_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
   return t;
 }
 // Bounded wait: false when the limit ran out (the CTA then aborts) or, if `abort` is
-// given, when another role of the CTA has given up already. Polls with a short sleep
-// between tests: a blocking try_wait was measured to wake about a microsecond after the
-// phase completed, which serialised the pipeline.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
+// given, when another role of the CTA has given up already. Polls with test_wait (a
+// blocking try_wait was measured to wake about a microsecond after the phase completed).
+// Waits on the critical path spin; the others sleep briefly between tests, which was
+// measured to add a few hundred cycles of wake-up latency.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                          bool spin = false) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = now_ns();
   for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
-    __nanosleep(32);
+    if (!spin) __nanosleep(32);
     if (mbar_test(bar, parity)) return true;
     if (abort && *abort) return false;
     if ((i & 1023u) == 1023u && now_ns() - t0 > WAIT_NS) break;
@@ -116,8 +146,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 // Every lane polls the barrier (the lowest wake-up latency measured); every lane gets the
 // same answer.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
-  const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                          bool spin = false) {
+  const bool ok = mbar_wait(bar, parity, abort, spin);
   return __all_sync(0xffffffffu, ok);
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
@@ -126,6 +157,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -143,14 +181,6 @@ __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t cols) {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
                : "memory");
-}
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
 }
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
                                        uint32_t acc) {
@@ -294,9 +324,14 @@ __device__ __forceinline__ uint32_t visible32(int k, int P, int T, const uint32_
   return pre | tr;
 }
 
+// Named barrier of the four softmax warps (barrier 0 is the CTA's __syncthreads).
+__device__ __forceinline__ void softmax_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+               const TcParams prm) {
   extern __shared__ uint8_t smem_raw[];
   const AttnArgs& a = prm.a;
   const int split = blockIdx.x, mt = blockIdx.y;
@@ -325,9 +360,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + SMEM_BAR + 8 * NUM_BARS);
   volatile uint32_t* abort = tmem_slot + 1;
+  volatile uint32_t* merge_flag = tmem_slot + 2;  // this CTA merges its row block's splits
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(BAR_Q), 1);
+    mbar_init(bar(BAR_Q), 4);  // one arrival per softmax warp (Q rows in TMEM)
     for (int s = 0; s < KST; ++s) {
       mbar_init(bar(BAR_K_FULL + s), 1);
       mbar_init(bar(BAR_K_EMPTY + s), 1);
@@ -336,13 +372,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(bar(BAR_V_FULL + s), 1);
       mbar_init(bar(BAR_V_EMPTY + s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(BAR_S_FULL + s), 1);
-      mbar_init(bar(BAR_P_FULL + s), 4);  // one arrival per softmax warp
-    }
-    mbar_init(bar(BAR_O_STEP), 1);
+    mbar_init(bar(BAR_S_FULL), 1);
+    mbar_init(bar(BAR_PV_DONE + 0), 1);
+    mbar_init(bar(BAR_PV_DONE + 1), 1);
     mbar_init(bar(BAR_O_DONE), 1);
     mbar_init(bar(BAR_DRAIN), 1);
+    // step j uses GO[j % 2]: the last step needs no MMA work after step n - 1, so with
+    // one barrier its phase could complete before the MMA warp has seen step n - 1's
+    mbar_init(bar(BAR_GO + 0), 5);  // four softmax warps + the relay
+    mbar_init(bar(BAR_GO + 1), 5);
+    mbar_init(bar(BAR_MERGE), 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -355,12 +394,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   if (warp == TMA_WARP) {
     // ---- producer: the whole warp walks the loop, lane 0 issues. K runs one tile ahead
     // of V (order K0 K1 V0 K2 V1 ...), so S = Q K^T never waits behind a V load.
-    const int qrow = (b * a.hkv + h) * a.rows_pad + row0;
-    if (lane == 0) {
-      mbar_expect_tx(bar(BAR_Q), TILE);
-      for (int hf = 0; hf < 2; ++hf)
-        tma_load_2d(base + SMEM_Q + hf * HALF, &tm_q, hf * 64, qrow, bar(BAR_Q));
-    }
     auto row_of = [&](int key) -> int {
       if (a.layout == TSV_KV_CONTIGUOUS) return (int)(((int64_t)b * a.hkv + h) * a.capacity + key);
       const int blk = a.block_table[(int64_t)b * a.max_blocks + key / TSV_KV_BLOCK];
@@ -396,7 +429,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // Before the CTA can exit, every copy it started has landed (immediate unless a
     // wait above gave up).
     if (lane == 0) {
-      mbar_wait(bar(BAR_Q), 0, nullptr);
       for (int j = issued_k > KST ? issued_k - KST : 0; j < issued_k; ++j)
         mbar_wait(bar(BAR_K_FULL + j % KST), (j / KST) & 1, nullptr);
       for (int j = issued_v > VST ? issued_v - VST : 0; j < issued_v; ++j)
@@ -404,50 +436,57 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
-    // ---- MMA issuer: the whole warp walks the loop, lane 0 issues --------------------
+    // ---- MMA issuer: the whole warp walks the loop with warp-uniform descriptors; one
+    // elected lane issues each instruction (a lane-0 branch that builds descriptors per
+    // MMA was measured to issue about 30% slower than the tensor pipe drains).
     constexpr uint32_t ID_QK = idesc(0), ID_PV = idesc(1);
-    const bool issuer = lane == 0;
-    // S[j % 2] = Q K_j^T
+    constexpr uint32_t TILE_D = TILE >> 4;  // descriptor address units are 16 bytes
+    const uint64_t dk = sdesc(base + SMEM_K, 16, 1024);
+    const uint64_t dv = sdesc(base + SMEM_V, HALF, 1024);
+    // k-step ks of a K-major operand: 16 columns = 32 bytes inside a 64-column panel
+    auto kmaj = [](int ks) -> uint64_t { return (uint64_t)((ks >> 2) * (HALF >> 4) + (ks & 3) * 2); };
+    // S = Q K_j^T; A = Q in TMEM (8 columns = 16 bf16 per k-step)
     auto qk = [&](int j) {
-      if (!issuer) return;
-      const uint32_t ka = base + SMEM_K + (j % KST) * TILE;
+      const uint64_t kd = dk + (uint64_t)((j % KST) * TILE_D);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t off = (ks >> 2) * HALF + (ks & 3) * 32;
-        mma_ss(tmem + (j & 1) * 128, sdesc(base + SMEM_Q + off, 16, 1024), sdesc(ka + off, 16, 1024),
-               ID_QK, ks > 0);
+      for (int ks = 0; ks < 8; ++ks)
+        if (elect_one()) mma_ts(tmem + TMEM_S, tmem + TMEM_Q + ks * 8, kd + kmaj(ks), ID_QK, ks > 0);
+      if (elect_one()) {
+        mma_commit(bar(BAR_S_FULL));
+        mma_commit(bar(BAR_K_EMPTY + j % KST));
       }
-      mma_commit(bar(BAR_S_FULL + (j & 1)));
-      mma_commit(bar(BAR_K_EMPTY + j % KST));
+      __syncwarp();
     };
-    // O += P_j V_j
+    // O += P_j V_j over ksteps of 16 keys (V rows 16 ks .. 16 ks + 15: MN-major, 16
+    // rows of 128 bytes per k-step)
     auto pv = [&](int j, int ksteps) {
-      if (!issuer) return;
-      const uint32_t va = base + SMEM_V + (j % VST) * TILE;
-      for (int ks = 0; ks < ksteps; ++ks)
-        mma_ts(tmem + TMEM_O, tmem + (j & 1) * 128 + ks * 8, sdesc(va + ks * 16 * 128, HALF, 1024),
-               ID_PV, (j > 0 || ks > 0) ? 1u : 0u);
-      mma_commit(bar(BAR_V_EMPTY + j % VST));
-      mma_commit(bar(BAR_O_STEP));
-    };
-    bool ok = warp_wait(bar(BAR_Q), 0, abort);
-    for (int j = 0; ok && j < 2 && j < n; ++j) {
-      if (!(ok = warp_wait(bar(BAR_K_FULL + j % KST), (j / KST) & 1, abort))) break;
-      tc_fence_after();
-      qk(j);
-    }
-    for (int j = 0; ok && j < n; ++j) {
-      const int valid = min(KEYS, keys - (t0 + j) * KEYS);
-      if (!(ok = warp_wait(bar(BAR_P_FULL + (j & 1)), (j >> 1) & 1, abort))) break;
-      if (!(ok = warp_wait(bar(BAR_V_FULL + j % VST), (j / VST) & 1, abort))) break;
-      tc_fence_after();
-      pv(j, (valid + 15) >> 4);
-      if (j + 2 < n) {  // issued after P_j V_j, so it may overwrite P_j's columns
-        if (!(ok = warp_wait(bar(BAR_K_FULL + (j + 2) % KST), ((j + 2) / KST) & 1, abort))) break;
-        tc_fence_after();
-        qk(j + 2);
+      const uint64_t vd = dv + (uint64_t)((j % VST) * TILE_D);
+      const uint32_t pa = tmem + TMEM_P + (j & 1) * 64;
+      const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        if (ks < ksteps && elect_one())
+          mma_ts(tmem + TMEM_O, pa + ks * 8, vd + (uint64_t)(ks * 128), ID_PV, ks > 0 ? 1u : acc0);
+      if (elect_one()) {
+        mma_commit(bar(BAR_V_EMPTY + j % VST));
+        mma_commit(bar(BAR_PV_DONE + (j & 1)));
       }
+      __syncwarp();
+    };
+    bool ok = warp_wait(bar(BAR_Q), 0, abort) && warp_wait(bar(BAR_K_FULL), 0, abort);
+    if (ok) {
+      tc_fence_after();
+      qk(0);
     }
+    for (int j = 0; ok && j <= n; ++j) {
+      // GO phase j: S_j read by the softmax (so P_{j-1} is written), K_{j+1} and V_{j-1}
+      // landed (phase n: the last P written, V_{n-1} landed)
+      if (!(ok = warp_wait(bar(BAR_GO + (j & 1)), (j >> 1) & 1, abort, true))) break;
+      tc_fence_after();
+      if (j + 1 < n) qk(j + 1);
+      if (j >= 1) pv(j - 1, (min(KEYS, keys - (t0 + j - 1) * KEYS) + 15) >> 4);
+    }
+    const bool issuer = lane == 0;
     if (issuer) {
       if (ok) mma_commit(bar(BAR_O_DONE));
       // drain: every MMA issued above has finished before TMEM is released
@@ -455,6 +494,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_wait(bar(BAR_DRAIN), 0, nullptr);
     }
     __syncwarp();
+  } else if (warp == RELAY_WARP) {
+    // ---- relay: its share of GO phase j once K_{j+1} and V_{j-1} have landed; it then
+    // waits for the phase to complete so its next arrival cannot count toward this one
+    bool ok = true;
+    for (int j = 0; ok && j <= n; ++j) {
+      if (j + 1 < n &&
+          !(ok = warp_wait(bar(BAR_K_FULL + (j + 1) % KST), ((j + 1) / KST) & 1, abort)))
+        break;
+      if (j >= 1 && !(ok = warp_wait(bar(BAR_V_FULL + (j - 1) % VST), ((j - 1) / VST) & 1, abort)))
+        break;
+      if (lane == 0) mbar_arrive(bar(BAR_GO + (j & 1)));
+      __syncwarp();
+      if (!(ok = warp_wait(bar(BAR_GO + (j & 1)), (j >> 1) & 1, abort))) break;
+    }
   } else if (warp < 4) {
     // ---- softmax warpgroup -----------------------------------------------------------
     const int r = row0 + warp * 32 + lane;
@@ -465,15 +518,42 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const uint32_t o_addr = tmem + lane_base + TMEM_O;
     const float sl2 = prm.scale_log2;
+    {
+      // this row's rotated query (bf16 pairs, low half first) -> TMEM columns of Q; rows
+      // past the tree copy whatever the workspace holds (their results are never stored)
+      const uint4* src = reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(a.q_rot) +
+          (((int64_t)b * a.hkv + h) * a.rows_pad + r) * 128);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 x = src[4 * c + i];
+          w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
+        }
+        tmem_st16(tmem + lane_base + TMEM_Q + 16 * c, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_Q));
+    }
+    const uint32_t s_addr = tmem + lane_base + TMEM_S;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      const uint32_t s_addr = tmem + lane_base + (j & 1) * 128;
-      if (!(ok = warp_wait(bar(BAR_S_FULL + (j & 1)), (j >> 1) & 1, abort))) break;
+      const uint32_t p_addr = tmem + lane_base + TMEM_P + (j & 1) * 64;
+      if (!(ok = warp_wait(bar(BAR_S_FULL), j & 1, abort, true))) break;
       tc_fence_after();
       const int k0 = (t0 + j) * KEYS;
       float v[128];
       tmem_ld128(s_addr, v);
+      // S is in registers: the next Q K^T may overwrite it (this arrival also publishes
+      // P_{j-1}, stored and fenced at the end of the previous iteration)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_GO + (j & 1)));
       if (k0 + KEYS > P) {  // tile holds tree keys (or keys past the end): mask to -inf
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -497,9 +577,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       // a row with nothing visible so far has only -inf scores: any finite offset works
       const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[4][16];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c0 = q * 32 + 2 * i;
@@ -508,15 +588,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           l8[(2 * i) & 7] += p0;
           l8[(2 * i + 1) & 7] += p1;
           __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-          pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+          pk[q][i] = *reinterpret_cast<uint32_t*>(&b2);
         }
-        tmem_st16(s_addr + 16 * q, pk);
       }
       l = l * factor + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+      if (j >= 2) {
+        // P[j % 2] is free once P_{j-2} V_{j-2} has finished (the next completion on that
+        // barrier, P_j V_j, needs this tile's P, so the parity is unambiguous)
+        if (!(ok = warp_wait(bar(BAR_PV_DONE + (j & 1)), ((j - 2) >> 1) & 1, abort, true))) break;
+        tc_fence_after();
+      }
       if (__any_sync(FULL, need) && j > 0) {
-        // O must be quiescent: wait for P_{j-1} V_{j-1} (P_{j-2} V_{j-2} finished before
-        // this tile's S was computed, so the parity names the right phase).
-        if (!(ok = warp_wait(bar(BAR_O_STEP), (j - 1) & 1, abort))) break;
+        // O must be quiescent: P_{j-1} V_{j-1} (and with it every earlier MMA) finished
+        if (!(ok = warp_wait(bar(BAR_PV_DONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort, true)))
+          break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -527,11 +612,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           tmem_st32(o_addr + 32 * c, o);
         }
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_st16(p_addr + 16 * q, pk[q]);
       tmem_wait_st();
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_P_FULL + (j & 1)));
     }
+    // publishes the last P (GO phase n)
+    __syncwarp();
+    if (ok && lane == 0) mbar_arrive(bar(BAR_GO + (n & 1)));
     // epilogue
     if (ok) ok = warp_wait(bar(BAR_O_DONE), 0, abort);
     tc_fence_after();
@@ -573,6 +661,121 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       if (live && ok) {
         a.ml[prow * 2 + 0] = m_used;
         a.ml[prow * 2 + 1] = l;
+      }
+      // The last split of this (request, KV head, M tile) to finish merges them all:
+      // partials are published with a device-scope fence before the ticket increment,
+      // and read back through L2 after it.
+      __threadfence();
+      softmax_sync();
+      if (threadIdx.x == 0) {
+        const int nsp = (n_tiles + a.tiles_per_split - 1) / a.tiles_per_split;
+        const int old = atomicAdd(&a.tickets[((int64_t)b * a.hkv + h) * (a.rows_pad / 128) + mt], 1);
+        *merge_flag = old == nsp - 1;
+      }
+      softmax_sync();
+      if (*merge_flag) {
+        __threadfence();
+        // Log-sum-exp weights of every split for this thread's row (m in log2 units); the
+        // (m, l) loads are issued eight at a time.
+        const int nsp = (n_tiles + a.tiles_per_split - 1) / a.tiles_per_split;
+        const int t = warp * 32 + lane;
+        const int64_t pbase = ((int64_t)b * a.hkv + h) * a.nsplit;
+        const float2* mlp = reinterpret_cast<const float2*>(a.ml) + pbase * a.rows_pad + r;
+        float* wsm = reinterpret_cast<float*>(gbase + MERGE_W);  // [nsp][128]
+        float M = -INFINITY, L = 0.f;
+        for (int s0 = 0; s0 < nsp; s0 += 8) {
+          float2 ml[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            ml[u] = s0 + u < nsp ? __ldcg(mlp + (int64_t)(s0 + u) * a.rows_pad)
+                                 : make_float2(-INFINITY, 0.f);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (s0 + u < nsp) wsm[(s0 + u) * 128 + t] = ml[u].x;
+            if (ml[u].x != -INFINITY) {
+              const float mn = fmaxf(M, ml[u].x);
+              L = L * exp2f(M - mn) + ml[u].y * exp2f(ml[u].x - mn);
+              M = mn;
+            }
+          }
+        }
+        const float inv_l = L > 0.f ? 1.f / L : 0.f;
+        for (int sp = 0; sp < nsp; ++sp) {
+          const float m = wsm[sp * 128 + t];
+          wsm[sp * 128 + t] = m == -INFINITY ? 0.f : exp2f(m - M) * inv_l;
+        }
+        softmax_sync();
+        // The partial tiles (contiguous per split) come in by bulk copy, up to three at a
+        // time; tile 0 keeps the running weighted sum. Lanes cover a row's 128 columns (one
+        // float4 each); a warp handles its 32 rows eight at a time.
+        float4* tiles = reinterpret_cast<float4*>(gbase);
+        constexpr int T4 = MERGE_TILE / 16;
+        const int live_rows = min(32, rows - (row0 + warp * 32));
+        int sp = 0;
+        uint32_t phase = 0;
+        while (ok && sp < nsp) {
+          const bool first = sp == 0;
+          const int cnt = min(nsp - sp, first ? 3 : 2);
+          if (t == 0) {
+            // other CTAs' partials (seen through the ticket) and this CTA's generic
+            // shared-memory accesses, ordered before the async-proxy copies
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_expect_tx(bar(BAR_MERGE), cnt * MERGE_TILE);
+            for (int c = 0; c < cnt; ++c)
+              bulk_load(base + (first ? c : c + 1) * MERGE_TILE,
+                        a.o_part + ((pbase + sp + c) * a.rows_pad + row0) * 128, MERGE_TILE,
+                        bar(BAR_MERGE));
+          }
+          if (!(ok = warp_wait(bar(BAR_MERGE), phase, abort))) break;
+          phase ^= 1;
+          const int c0 = first ? 1 : 0;  // tile c + 1 holds split sp + c + c0
+          for (int rr0 = 0; rr0 < live_rows; rr0 += 8) {
+            float4 acc[8], y[8][2];
+            float w[8][3];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int row = warp * 32 + rr0 + u;
+              acc[u] = tiles[row * 32 + lane];
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                y[u][c] = tiles[(c + 1) * T4 + row * 32 + lane];
+#pragma unroll
+              for (int c = 0; c < 3; ++c) w[u][c] = sp + c < nsp ? wsm[(sp + c) * 128 + row] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              float4 x = acc[u];
+              if (first) {
+                x = make_float4(x.x * w[u][0], x.y * w[u][0], x.z * w[u][0], x.w * w[u][0]);
+              }
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                if (c + c0 < cnt) {
+                  const float wc = w[u][c + c0];
+                  x.x += wc * y[u][c].x;
+                  x.y += wc * y[u][c].y;
+                  x.z += wc * y[u][c].z;
+                  x.w += wc * y[u][c].w;
+                }
+              }
+              if (rr0 + u < live_rows) tiles[(warp * 32 + rr0 + u) * 32 + lane] = x;
+            }
+          }
+          softmax_sync();
+          sp += cnt;
+        }
+        // normalised bf16 output rows
+        for (int rr = 0; ok && rr < live_rows; ++rr) {
+          const int row = warp * 32 + rr, r2 = row0 + row;
+          const float4 x = tiles[row * 32 + lane];
+          __nv_bfloat16* dst = prm.out + (((int64_t)b * a.max_nodes + r2 / a.group) * a.hq +
+                                          h * a.group + r2 % a.group) * 128;
+          __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
+          reinterpret_cast<uint2*>(dst)[lane] =
+              make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        }
       }
     }
   }
@@ -638,16 +841,15 @@ int launch_attn_tc(const AttnPlan& p, const AttnArgs& a, float scale_log2, void*
       return launch_status();
     attr_set[dev] = true;
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mk, mv;
   const uint64_t kv_rows = a.layout == TSV_KV_CONTIGUOUS
                                ? (uint64_t)p.batch * p.hkv * a.capacity
                                : (uint64_t)a.num_blocks * p.hkv * TSV_KV_BLOCK;
-  if (!make_map(&mq, a.q_rot, (uint64_t)p.batch * p.hkv * p.rows_pad, 128) ||
-      !make_map(&mk, a.k_cache, kv_rows, 64) || !make_map(&mv, a.v_cache, kv_rows, 64))
+  if (!make_map(&mk, a.k_cache, kv_rows, 64) || !make_map(&mv, a.v_cache, kv_rows, 64))
     return TSV_ERR_UNSUPPORTED;
   TcParams prm{a, scale_log2, static_cast<__nv_bfloat16*>(out)};
   dim3 grid(p.nsplit, (unsigned)ceil_div(p.rows, TC_M_GROUP), p.batch * p.hkv);  // M tiles of 128 rows
-  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, prm);
+  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mk, mv, prm);
   return launch_status();
 }
 

@@ -83,6 +83,9 @@ extern "C" int tsv_tree_verify_attn_noalloc(const tsv_attn_shape* shape, const v
   if (shape->batch == 0) return TSV_OK;
   if (!q || !k_new || !v_new || !prefix_len || !num_nodes || !position_ids || !mask || !out)
     return TSV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_new) |
+       reinterpret_cast<uintptr_t>(v_new) | reinterpret_cast<uintptr_t>(out)) % 16)
+    return TSV_ERR_INVALID_ARG;
   const AttnPlan plan = plan_attn(shape, cache);
   if (plan.ws_bytes > (size_t)TSV_NOALLOC_SCRATCH_BYTES) return TSV_ERR_WORKSPACE;
   void* ws = scratch_address();
