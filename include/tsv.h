@@ -130,12 +130,16 @@ int tsv_last_cuda_error(void);
  *                  cumulative score and the store index of the parent (-1: root).
  * front_*_out      [batch, top_k]: the next frontier, best first (token id, fp32
  *                  cumulative score, store index). Must not alias the *_in arrays.
- * workspace        device scratch of tsv_draft_topk_expand_workspace_size() bytes.
+ * workspace        device scratch of tsv_draft_topk_expand_workspace_size() bytes,
+ *                  zero-filled by the caller before its first use; every call leaves
+ *                  it fit for the next (its first bytes hold per-request counters that
+ *                  each call returns to zero). One workspace sized for rows = top_k
+ *                  serves every level of a request batch.
  *
  * Order and ties: higher values first; equal values go to the lower token id (per
  * row) and to the lower flat index (joint). Log-probabilities are x - logsumexp(row),
- * the log-sum-exp accumulated with compensation and finished in fp64, rounded to
- * fp32; cumulative scores are fp32 sums. Returns TSV_ERR_INVALID_ARG for top_k
+ * the log-sum-exp accumulated in fp32 with exact (two-sum) group additions, rounded
+ * to fp32; cumulative scores are fp32 sums. Returns TSV_ERR_INVALID_ARG for top_k
  * outside [1, TSV_MAX_TOPK], vocab < top_k, row_stride < vocab, a store too small for
  * this level, or rows inconsistent with level.
  * ------------------------------------------------------------------------------ */

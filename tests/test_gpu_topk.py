@@ -33,7 +33,7 @@ def run_levels(levels_per_req, k, store_cap=None, stride_pad=0):
                torch.zeros(b, k, dtype=torch.float32, device=d),
                torch.zeros(b, k, dtype=torch.int32, device=d)) for _ in range(2)]
     ws_n = max(T.draft_topk_expand_workspace_size(b, r, v, k) for r in (1, k))
-    ws = torch.empty(ws_n, dtype=torch.uint8, device=d)
+    ws = torch.zeros(ws_n, dtype=torch.uint8, device=d)  # zeroed once, reused by every level
     history = []
     cur = None
     for li in range(nlev):
@@ -47,6 +47,8 @@ def run_levels(levels_per_req, k, store_cap=None, stride_pad=0):
                             None if cur is None else cur[2], st, ss, sp, *nxt, ws)
         torch.cuda.synchronize()
         history.append(tuple(t.cpu().numpy().copy() for t in nxt))
+        # the per-request counters at the start of the workspace are back at zero
+        assert not ws[:4 * b].view(torch.int32).any().item()
         cur = nxt
     return st.cpu().numpy(), ss.cpu().numpy(), sp.cpu().numpy(), history
 
@@ -142,7 +144,7 @@ def test_sweep_level_640_rows_of_128256():
     outs = [torch.zeros(w.batch, k, dtype=torch.int32, device=d),
             torch.zeros(w.batch, k, dtype=torch.float32, device=d),
             torch.zeros(w.batch, k, dtype=torch.int32, device=d)]
-    ws = torch.empty(T.draft_topk_expand_workspace_size(w.batch, k, w.vocab, k),
+    ws = torch.zeros(T.draft_topk_expand_workspace_size(w.batch, k, w.vocab, k),
                      dtype=torch.uint8, device=d)
     T.draft_topk_expand(lg, k, 2, fin_s, fin_i, st, ss, sp, *outs, ws)
     torch.cuda.synchronize()

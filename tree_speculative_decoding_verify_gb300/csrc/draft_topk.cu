@@ -35,36 +35,42 @@
 namespace tsv {
 namespace {
 
-constexpr int KMAX = TSV_MAX_TOPK;  // 16: warp list length
-constexpr int A_THREADS = 256;
+constexpr int KMAX = TSV_MAX_TOPK;  // 16: longest warp list
+constexpr int A_THREADS = 512;  // 16 warps: the request's merge gives every row a warp
 constexpr int A_WARPS = A_THREADS / 32;
 constexpr int MAX_CHUNKS = 32;
-constexpr int BUF = 8;              // per-thread candidate buffer
+constexpr int MIN_CHUNK = 1024;     // vocab entries per chunk at least (4 per thread)
+constexpr int CAP = 256;            // per-warp candidate buffer (shared memory)
+constexpr int STEP_MAX = 4 * 32;    // most candidates a warp appends in one step
+constexpr int MERGE_SLOTS = 1 + CAP / 32;  // entries a lane holds in a warp merge
+constexpr float L2E = 1.4426950408889634f;
 
 struct ChunkStat {
-  double sum;  // sum of exp(x - ref) over the chunk
-  float ref;
+  float ref;     // reference (a running maximum)
+  float hi, lo;  // sum of exp(x - ref) over the chunk as an unevaluated fp32 pair
   float pad;
 };
 
 struct TopkWs {
+  unsigned* tickets;   // [batch] finished chunk CTAs of each request: zero between calls
   ChunkStat* stat;     // [rows_total, chunks]
   float* val;          // [rows_total, chunks, K]
   int32_t* idx;        // [rows_total, chunks, K]
-  unsigned* tickets;   // [batch] finished chunk CTAs of each request (zeroed per call)
 };
 
-__host__ __device__ inline TopkWs carve(void* ws, int rows_total, int chunks, int k) {
+// The tickets come first, at the same place for every level of a request batch: the
+// caller zeroes the workspace once and every call leaves them at zero.
+__host__ __device__ inline TopkWs carve(void* ws, int batch, int rows_total, int chunks, int k) {
   char* p = static_cast<char*>(ws);
   TopkWs w;
   const size_t n = (size_t)rows_total * chunks;
+  w.tickets = reinterpret_cast<unsigned*>(p);
+  p += ((size_t)batch * sizeof(unsigned) + 255) & ~size_t(255);
   w.stat = reinterpret_cast<ChunkStat*>(p);
   p += (n * sizeof(ChunkStat) + 255) & ~size_t(255);
   w.val = reinterpret_cast<float*>(p);
   p += (n * k * sizeof(float) + 255) & ~size_t(255);
   w.idx = reinterpret_cast<int32_t*>(p);
-  p += (n * k * sizeof(int32_t) + 255) & ~size_t(255);
-  w.tickets = reinterpret_cast<unsigned*>(p);
   return w;
 }
 
@@ -74,27 +80,93 @@ __device__ __forceinline__ unsigned ord(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Warp-wide best (value, index) pair — larger value, then lower index — with two
-// hardware warp reductions; every lane gets the pair and the lane that holds it.
+// Warp-wide best (value, index) pair — larger value, then lower index — with one
+// hardware warp reduction when the largest value is held by one lane (a second one
+// breaks ties); every lane gets the pair and the lane that holds it.
 __device__ __forceinline__ void warp_argmax(float& v, int& i, int& lane_of) {
   const unsigned u = ord(v);
   const unsigned umax = __reduce_max_sync(FULL, u);
-  const unsigned imin = __reduce_min_sync(FULL, u == umax ? (unsigned)i : 0xffffffffu);
-  const unsigned own = __ballot_sync(FULL, u == umax && (unsigned)i == imin);
+  unsigned own = __ballot_sync(FULL, u == umax);
+  if (own & (own - 1)) {  // several lanes hold the largest value: lowest index wins
+    const unsigned imin = __reduce_min_sync(FULL, u == umax ? (unsigned)i : 0xffffffffu);
+    own = __ballot_sync(FULL, u == umax && (unsigned)i == imin);
+  }
   lane_of = __ffs(own) - 1;
   v = __shfl_sync(FULL, v, lane_of);
-  i = (int)imin;
+  i = __shfl_sync(FULL, i, lane_of);
 }
 
-// Sum of (ref_i, s_i) pairs over a warp against the warp's largest reference: one fp64
-// exp per lane whose reference differs (none when they all agree), then fp64 adds.
-__device__ __forceinline__ void warp_combine(float& r, double& s) {
+// Compare-exchange of two (value, index) entries so that entry a is the better one.
+__device__ __forceinline__ void cx(float& va, int& ia, float& vb, int& ib) {
+  const bool sw = better(vb, ib, va, ia);
+  const float tv = sw ? vb : va;
+  const int ti = sw ? ib : ia;
+  vb = sw ? va : vb;
+  ib = sw ? ia : ib;
+  va = tv;
+  ia = ti;
+}
+// Sorts n register entries best first (odd-even transposition network, n rounds).
+template <int N>
+__device__ __forceinline__ void sort_entries(float (&v)[N], int (&ix)[N]) {
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+#pragma unroll
+    for (int t = r & 1; t + 1 < N; t += 2) cx(v[t], ix[t], v[t + 1], ix[t + 1]);
+  }
+}
+// k rounds of a warp tournament over per-lane sorted entries: each round the best lane
+// head wins and that lane shifts its entries up. Lane r receives the r-th best entry.
+template <int N>
+__device__ __forceinline__ void warp_select(float (&v)[N], int (&ix)[N], int rounds, int lane,
+                                            float& out_v, int& out_i) {
+  out_v = -INFINITY;
+  out_i = INT_MAX;
+  for (int r = 0; r < rounds; ++r) {
+    float hv = v[0];
+    int hi = ix[0], who = lane;
+    warp_argmax(hv, hi, who);
+    if (lane == r) { out_v = hv; out_i = hi; }
+    if (lane == who) {
+#pragma unroll
+      for (int t = 0; t + 1 < N; ++t) { v[t] = v[t + 1]; ix[t] = ix[t + 1]; }
+      v[N - 1] = -INFINITY;
+      ix[N - 1] = INT_MAX;
+    }
+  }
+}
+
+// Exact sum of two floats as an unevaluated pair (Knuth's TwoSum): s + e == a + b.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bp = s - a;
+  e = (a - (s - bp)) + (b - bp);
+}
+// (hi, lo) += (h2, l2), renormalised.
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float h2, float l2) {
+  float s, e;
+  two_sum(hi, h2, s, e);
+  e += lo + l2;
+  hi = s + e;
+  lo = e - (hi - s);
+}
+
+// Sum of (ref_i, hi_i + lo_i) over a warp against the warp's largest reference: one
+// fp32 exp per lane whose reference differs (none when they all agree), then pair adds.
+__device__ __forceinline__ void warp_combine(float& r, float& hi, float& lo) {
   float R = r;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) R = fmaxf(R, __shfl_xor_sync(FULL, R, o));
-  if (r != R) s = (s == 0.0) ? 0.0 : s * exp((double)r - (double)R);
+  if (r != R) {
+    const float f = hi == 0.f ? 0.f : expf(r - R);
+    hi *= f;
+    lo *= f;
+  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(FULL, s, o);
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(FULL, hi, o), l2 = __shfl_xor_sync(FULL, lo, o);
+    pair_add(hi, lo, h2, l2);
+  }
   r = R;
 }
 
@@ -106,136 +178,104 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) {
   return r;
 }
 
-// Per-thread streaming state.
-struct Stream {
-  // exp-sum
-  float ref;    // running maximum
-  float g;      // fp32 sum of the current group
-  double d;     // fp64 sum against ref
-  float ref0;   // parked older reference (-inf: none)
-  double d0;    // parked sum against ref0
-  // top-k: warp list slot (lanes 0-15), warp threshold, own buffer
-  float lv;
-  int li;
-  float thr_v;
-  int thr_i;
-  float bv[BUF];
-  int bi[BUF];
-  int bc;
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+struct TopkSmem {
+  union {
+    struct {                                   // streaming: per-warp candidates
+      float bv[A_WARPS][CAP];
+      int bi[A_WARPS][CAP];
+    } s;
+  } u;
+  float lv[A_WARPS][KMAX];                     // warp lists, best first
+  int li[A_WARPS][KMAX];
+  int cnt[A_WARPS];                            // buffered candidates per warp
+  float red[A_WARPS];
+  float shi[A_WARPS], slo[A_WARPS];
+  float cu[KMAX * KMAX];
+  int tok[KMAX * KMAX];
+  bool last;
 };
 
-__device__ __forceinline__ void flush(Stream& st) {
-  st.d += (double)st.g;
-  st.g = 0.f;
-}
-
-// d0 * e^(ref0 - ref) + d: the rare merge of two parked sums, kept out of line.
-__device__ __noinline__ double merge_pair(double d0, float ref0, double d, float ref) {
-  return d0 * exp((double)ref0 - (double)ref) + d;
-}
-
-__device__ __forceinline__ void consider(Stream& st, float x, int idx) {
-  if (x > st.ref) {  // new maximum: park the old pair
-    flush(st);
-    st.d0 = st.ref0 == -INFINITY ? st.d : merge_pair(st.d0, st.ref0, st.d, st.ref);
-    st.ref0 = st.ref;
-    st.d = 0.0;
-    st.ref = x;
-  }
-  st.g += expf(x - st.ref);
-  if (better(x, idx, st.thr_v, st.thr_i)) {
+// Warp merge: list = best k of (list, buffered candidates), best first; returns the new
+// list length (warp-uniform) and sets the warp threshold to its k-th entry.
+__device__ __forceinline__ int warp_merge(TopkSmem& sm, int warp, int lane, int k, int nl,
+                                          float& thr_v, int& thr_i) {
+  __syncwarp();
+  const int n = sm.cnt[warp];
+  float v[MERGE_SLOTS];
+  int ix[MERGE_SLOTS];
+  v[0] = lane < nl ? sm.lv[warp][lane] : -INFINITY;
+  ix[0] = lane < nl ? sm.li[warp][lane] : INT_MAX;
 #pragma unroll
-    for (int s = 0; s < BUF; ++s) {
-      if (s == st.bc) { st.bv[s] = x; st.bi[s] = idx; }
-    }
-    ++st.bc;
+  for (int t = 1; t < MERGE_SLOTS; ++t) {
+    const int j = lane + 32 * (t - 1);
+    v[t] = j < n ? sm.u.s.bv[warp][j] : -INFINITY;
+    ix[t] = j < n ? sm.u.s.bi[warp][j] : INT_MAX;
   }
+  const int total = min(k, nl + n);
+  sort_entries(v, ix);
+  float nv;
+  int ni;
+  warp_select(v, ix, total, lane, nv, ni);
+  __syncwarp();
+  if (lane < total) { sm.lv[warp][lane] = nv; sm.li[warp][lane] = ni; }
+  if (lane == 0) sm.cnt[warp] = 0;
+  if (total == k) {
+    thr_v = __shfl_sync(FULL, nv, k - 1);
+    thr_i = __shfl_sync(FULL, ni, k - 1);
+  }
+  __syncwarp();
+  return total;
 }
 
-// Warp merge: new list = best k of (list, all buffers), held by lanes 0 .. k-1;
-// threshold = its k-th entry.
-__device__ __forceinline__ void warp_merge(Stream& st, int lane, int k) {
-  // (inlined at three sites: the streaming loop, its tail and the final merge)
-  unsigned taken = 0;       // bit s: buffer slot s used; bit BUF: list slot used
-  float nv = -INFINITY;
-  int ni = INT_MAX;
-  for (int r = 0; r < k; ++r) {
-    float v = -INFINITY;
-    int i = INT_MAX, which = -1;
-    if (lane < k && !(taken >> BUF & 1u) && better(st.lv, st.li, v, i)) {
-      v = st.lv; i = st.li; which = BUF;
-    }
-#pragma unroll
-    for (int s = 0; s < BUF; ++s) {
-      if (s < st.bc && !(taken >> s & 1u) && better(st.bv[s], st.bi[s], v, i)) {
-        v = st.bv[s]; i = st.bi[s]; which = s;
-      }
-    }
-    int who = lane;
-    float wv = v;
-    int wi = i;
-    warp_argmax(wv, wi, who);
-    if (lane == who && which >= 0) taken |= 1u << which;
-    if (lane == r) { nv = wv; ni = wi; }
+// Per-thread log-sum-exp state: fp32 terms exp(x - ref) summed in groups of 16, each
+// group added exactly into an unevaluated (hi, lo) pair. The reference is raised (and
+// the pair rescaled) only when an entry exceeds it by more than RAISE, so terms stay
+// below e^RAISE and the rare rescale is the only inexact step besides the terms.
+constexpr float RAISE = 16.f;
+struct Lse {
+  float ref, g, hi, lo;
+  __device__ __forceinline__ void flush() {
+    pair_add(hi, lo, g, 0.f);
+    g = 0.f;
   }
-  st.lv = nv;
-  st.li = ni;
-  st.thr_v = __shfl_sync(FULL, nv, k - 1);
-  st.thr_i = __shfl_sync(FULL, ni, k - 1);
-  st.bc = 0;
-}
+  __device__ __noinline__ void raise(float m) {
+    flush();
+    const float f = expf(ref - m);
+    hi *= f;
+    lo *= f;
+    ref = m;
+  }
+};
 
-__global__ void __launch_bounds__(A_THREADS)
+__global__ void __launch_bounds__(A_THREADS, 2)
 topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int vocab, int rows, int k,
                   int chunks, int chunk_len, int level, bool vec, TopkWs ws,
                   const float* __restrict__ front_score_in, const int32_t* __restrict__ front_store_in,
                   int store_cap, int32_t* __restrict__ store_token, float* __restrict__ store_score,
                   int32_t* __restrict__ store_parent, int32_t* __restrict__ front_token_out,
                   float* __restrict__ front_score_out, int32_t* __restrict__ front_store_out) {
-  __shared__ float s_wv[A_WARPS][KMAX];
-  __shared__ int s_wi[A_WARPS][KMAX];
-  __shared__ float s_red[A_WARPS];
-  __shared__ double s_sum[A_WARPS];
-  __shared__ float s_cv[A_WARPS][MAX_CHUNKS * KMAX];
-  __shared__ int s_ci[A_WARPS][MAX_CHUNKS * KMAX];
-  __shared__ float s_cu[KMAX * KMAX];
-  __shared__ int s_tok[KMAX * KMAX];
-  __shared__ bool s_last;
-
+  __shared__ TopkSmem sm;
   const int row = blockIdx.y, chunk = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* x = logits + (int64_t)row * row_stride;
   const int start = chunk * chunk_len;
   const int end = min(vocab, start + chunk_len);
+  if (lane == 0) sm.cnt[warp] = 0;
 
-  Stream st;
-  st.g = 0.f;
-  st.d = 0.0;
-  st.ref0 = -INFINITY;
-  st.d0 = 0.0;
-  st.lv = -INFINITY;
-  st.li = INT_MAX;
-  st.thr_v = -INFINITY;
-  st.thr_i = INT_MAX;
-  st.bc = 0;
-#pragma unroll
-  for (int s = 0; s < BUF; ++s) { st.bv[s] = -INFINITY; st.bi[s] = INT_MAX; }
-
-  // Common starting reference: the largest of the first elements every thread sees.
-  float first = -INFINITY;
-  for (int e = start + tid * 4; e < min(end, start + tid * 4 + 4); ++e) first = fmaxf(first, x[e]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
-  if (lane == 0) s_red[warp] = first;
-  __syncthreads();
-  first = s_red[0];
-#pragma unroll
-  for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, s_red[w]);
-  st.ref = fmaxf(first, -FLT_MAX);  // finite, so x = -inf gives a zero term
+  float thr_v = -INFINITY;  // warp-uniform: the warp list's k-th entry
+  int thr_i = INT_MAX;
+  int nl = 0;               // warp list length (warp-uniform)
 
   // Every thread takes 4 consecutive entries per step (one 128-bit load when the row is
-  // 16-byte aligned), two steps prefetched ahead; after each step the warp merges if some
-  // buffer could overflow on the next one. All lanes run the same number of steps.
+  // 16-byte aligned), two steps prefetched ahead. The common path per 4 entries is their
+  // max against the running maximum and the warp threshold plus four exp2 terms; entries
+  // that beat the threshold go to the warp's buffer, merged when it could overflow.
   const int steps = (end - start + 4 * A_THREADS - 1) / (4 * A_THREADS);
   auto load4 = [&](int it) -> float4 {
     const int e = start + 4 * (it * A_THREADS + tid);
@@ -250,49 +290,80 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
   const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   float4 a = steps > 0 ? load4(0) : none;
   float4 bnext = steps > 1 ? load4(1) : none;
+
+  // Common starting reference: the largest of the first entries every thread sees.
+  float first = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
+  if (lane == 0) sm.red[warp] = first;
+  __syncthreads();
+  first = sm.red[0];
+#pragma unroll
+  for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, sm.red[w]);
+  Lse lse;
+  lse.ref = fmaxf(first, -FLT_MAX);  // finite, so x = -inf gives a zero term
+  lse.g = 0.f;
+  lse.hi = 0.f;
+  lse.lo = 0.f;
+
   for (int it = 0; it < steps; ++it) {
     const float4 c = it + 2 < steps ? load4(it + 2) : none;
     const int e = start + 4 * (it * A_THREADS + tid);
-    if (e < end) consider(st, a.x, e);
-    if (e + 1 < end) consider(st, a.y, e + 1);
-    if (e + 2 < end) consider(st, a.z, e + 2);
-    if (e + 3 < end) consider(st, a.w, e + 3);
-    if (__any_sync(FULL, st.bc > BUF - 4)) warp_merge(st, lane, k);
-    if ((it & 3) == 3) flush(st);
+    const float m4 = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
+    if (m4 > lse.ref + RAISE) lse.raise(m4);
+    const float r = lse.ref;
+    lse.g += (ex2((a.x - r) * L2E) + ex2((a.y - r) * L2E)) + (ex2((a.z - r) * L2E) + ex2((a.w - r) * L2E));
+    bool appended = false;
+    if (m4 >= thr_v) {  // some entry may beat the threshold: test each exactly
+      const float xv[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (e + q < end && better(xv[q], e + q, thr_v, thr_i)) {
+          const int pos = atomicAdd(&sm.cnt[warp], 1);
+          sm.u.s.bv[warp][pos] = xv[q];
+          sm.u.s.bi[warp][pos] = e + q;
+          appended = true;
+        }
+      }
+    }
+    if (__any_sync(FULL, appended)) {
+      __syncwarp();
+      if (sm.cnt[warp] > CAP - STEP_MAX) nl = warp_merge(sm, warp, lane, k, nl, thr_v, thr_i);
+    }
+    if ((it & 3) == 3) lse.flush();
     a = bnext;
     bnext = c;
   }
-  flush(st);
-  warp_merge(st, lane, k);  // the warp's final best k
+  lse.flush();
+  nl = warp_merge(sm, warp, lane, k, nl, thr_v, thr_i);  // the warp's final best k
+  if (lane >= nl && lane < k) { sm.lv[warp][lane] = -INFINITY; sm.li[warp][lane] = INT_MAX; }
 
-  // exp-sum: fold the parked pair, then combine over the block.
-  if (st.ref0 != -INFINITY) st.d += st.d0 * exp((double)st.ref0 - (double)st.ref);
-  float R = st.ref;
-  double part = st.d;
-  warp_combine(R, part);
-  __syncthreads();  // s_red was read for the starting reference
-  if (lane == 0) { s_red[warp] = R; s_sum[warp] = part; }
-  if (lane < k) { s_wv[warp][lane] = st.lv; s_wi[warp][lane] = st.li; }
+  // exp-sum over the block
+  float R = lse.ref, phi = lse.hi, plo = lse.lo;
+  warp_combine(R, phi, plo);
+  __syncthreads();  // sm.red was read for the starting reference
+  if (lane == 0) { sm.red[warp] = R; sm.shi[warp] = phi; sm.slo[warp] = plo; }
   __syncthreads();
   if (warp == 0) {
     // block top-k: 8 sorted warp lists, lanes 0-7 hold the list heads
     int ptr = 0;
     const size_t base = ((size_t)row * chunks + chunk) * k;
     for (int r = 0; r < k; ++r) {
-      float v = lane < A_WARPS ? s_wv[lane][ptr] : -INFINITY;
-      int i = lane < A_WARPS ? s_wi[lane][ptr] : INT_MAX;
+      float v = lane < A_WARPS && ptr < k ? sm.lv[lane][ptr] : -INFINITY;
+      int i = lane < A_WARPS && ptr < k ? sm.li[lane][ptr] : INT_MAX;
       int who = lane;
       warp_argmax(v, i, who);
       if (lane == who) ++ptr;
       if (lane == 0) { ws.val[base + r] = v; ws.idx[base + r] = i; }
     }
-    float rr = lane < A_WARPS ? s_red[lane] : -INFINITY;
-    double ss = lane < A_WARPS ? s_sum[lane] : 0.0;
-    warp_combine(rr, ss);
+    float rr = lane < A_WARPS ? sm.red[lane] : -INFINITY;
+    float hh = lane < A_WARPS ? sm.shi[lane] : 0.f, ll = lane < A_WARPS ? sm.slo[lane] : 0.f;
+    warp_combine(rr, hh, ll);
     if (lane == 0) {
       ChunkStat cs;
-      cs.sum = ss;
       cs.ref = rr;
+      cs.hi = hh;
+      cs.lo = ll;
       cs.pad = 0.f;
       ws.stat[(size_t)row * chunks + chunk] = cs;
     }
@@ -304,77 +375,72 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
   if (tid == 0) {
     __threadfence();
     const unsigned t = atomicAdd(&ws.tickets[b], 1u);
-    s_last = (t == (unsigned)(rows * chunks - 1));
+    sm.last = (t == (unsigned)(rows * chunks - 1));
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!sm.last) return;
   __threadfence();
 
   const int off = level == 1 ? 0 : k + (level - 2) * k * k;
   const int64_t srow = (int64_t)b * store_cap;
-  for (int s = warp; s < rows; s += A_WARPS) {
-    const int r0 = b * rows + s;
-    float Rr = -INFINITY;
-    double sum = 0.0;
-    if (lane < chunks) {  // written by other CTAs: read through L2
-      const ChunkStat* cs = &ws.stat[(size_t)r0 * chunks + lane];
-      Rr = __ldcg(&cs->ref);
-      sum = __ldcg(&cs->sum);
+  // Warp s merges row s (rows <= 16 = warps): lane c holds chunk c's sorted list of the
+  // row in registers.
+  static_assert(A_WARPS >= TSV_MAX_TOPK, "one warp per frontier row");
+  if (warp < rows) {
+    const int s = warp, r0 = b * rows + s;
+    const bool have = lane < chunks;
+    const size_t g = (size_t)r0 * chunks + lane;
+    float cv[KMAX];
+    int ci[KMAX];
+    float4 cs = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    if (have) cs = __ldcg(reinterpret_cast<const float4*>(&ws.stat[g]));
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      cv[j] = have && j < k ? __ldcg(ws.val + g * k + j) : -INFINITY;
+      ci[j] = have && j < k ? __ldcg(ws.idx + g * k + j) : INT_MAX;
     }
-    warp_combine(Rr, sum);
-    const double lse = (double)Rr + log(sum);
-    float* cv = s_cv[warp];
-    int* ci = s_ci[warp];
-    for (int t = lane; t < chunks * k; t += 32) {
-      const int c = t / k, j = t % k;
-      const size_t g = ((size_t)r0 * chunks + c) * k + j;
-      cv[c * KMAX + j] = __ldcg(ws.val + g);
-      ci[c * KMAX + j] = __ldcg(ws.idx + g);
-    }
-    __syncwarp();
     const float pscore = level == 1 ? 0.0f : front_score_in[r0];
     const int pstore = level == 1 ? -1 : front_store_in[r0];
-    int ptr = 0;
-    for (int r = 0; r < k; ++r) {
-      float v = (lane < chunks) ? cv[lane * KMAX + ptr] : -INFINITY;
-      int i = (lane < chunks) ? ci[lane * KMAX + ptr] : INT_MAX;
-      int who = lane;
-      warp_argmax(v, i, who);
-      if (lane == who) ++ptr;
-      if (lane == 0) {
-        const float logp = (float)((double)v - lse);
-        const float cu = pscore + logp;
-        const int flat = s * k + r;
-        store_token[srow + off + flat] = i;
-        store_score[srow + off + flat] = cu;
-        store_parent[srow + off + flat] = pstore;
-        s_cu[flat] = cu;
-        s_tok[flat] = i;
-      }
+    float Rr = cs.x, sh = cs.y, sl = cs.z;
+    warp_combine(Rr, sh, sl);
+    // log(hi + lo) = log(hi) + log1p(lo / hi); |lo / hi| is below an ulp, so the second
+    // term is lo / hi
+    const float lse_hi = Rr, lse_mid = logf(sh), lse_lo = sl / sh;
+    float v;
+    int i;
+    warp_select(cv, ci, k, lane, v, i);
+    if (lane < k) {
+      const float logp = ((v - lse_hi) - lse_mid) - lse_lo;
+      const float cu = pscore + logp;
+      const int flat = s * k + lane;
+      store_token[srow + off + flat] = i;
+      store_score[srow + off + flat] = cu;
+      store_parent[srow + off + flat] = pstore;
+      sm.cu[flat] = cu;
+      sm.tok[flat] = i;
     }
-    __syncwarp();
   }
   __syncthreads();
 
   // Joint top-K over the rows * K cumulative scores (ties to the lower flat index).
   if (warp == 0) {
     const int n = rows * k;
-    unsigned taken = 0;  // bit j: flat lane + 32 j taken
-    for (int r = 0; r < k; ++r) {
-      float v = -INFINITY;
-      int i = INT_MAX;
-      for (int j = 0; lane + 32 * j < n; ++j) {
-        const int f = lane + 32 * j;
-        if (!(taken >> j & 1u) && better(s_cu[f], f, v, i)) { v = s_cu[f]; i = f; }
-      }
-      int who = lane;
-      warp_argmax(v, i, who);
-      if (lane == who) taken |= 1u << ((i - lane) / 32);
-      if (lane == 0) {
-        front_token_out[b * k + r] = s_tok[i];
-        front_score_out[b * k + r] = v;
-        front_store_out[b * k + r] = off + i;
-      }
+    float v[KMAX * KMAX / 32];
+    int ix[KMAX * KMAX / 32];
+#pragma unroll
+    for (int j = 0; j < KMAX * KMAX / 32; ++j) {
+      const int f = lane + 32 * j;
+      v[j] = f < n ? sm.cu[f] : -INFINITY;
+      ix[j] = f < n ? f : INT_MAX;
+    }
+    sort_entries(v, ix);
+    float bv;
+    int bi;
+    warp_select(v, ix, k, lane, bv, bi);
+    if (lane < k) {
+      front_token_out[b * k + lane] = sm.tok[bi];
+      front_score_out[b * k + lane] = bv;
+      front_store_out[b * k + lane] = off + bi;
     }
     if (lane == 0) ws.tickets[b] = 0u;
   }
@@ -466,16 +532,15 @@ TopkPlan plan_topk(int batch, int rows, int vocab, int top_k) {
   const int64_t rows_total = (int64_t)batch * rows;
   const int64_t target = 4LL * device_sm_count();
   int chunks = (int)std::min<int64_t>(MAX_CHUNKS, std::max<int64_t>(1, ceil_div(target, rows_total)));
-  // at least 8192 entries per chunk (short chunks are all fixed cost), lengths a
-  // multiple of 4
-  chunks = (int)std::max<int64_t>(1, std::min<int64_t>(chunks, ceil_div(vocab, 8192)));
+  // at least MIN_CHUNK entries per chunk, lengths a multiple of 4
+  chunks = (int)std::max<int64_t>(1, std::min<int64_t>(chunks, ceil_div(vocab, MIN_CHUNK)));
   int chunk_len = (int)round_up(ceil_div(vocab, chunks), 4);
   chunks = (int)ceil_div(vocab, chunk_len);
   p.chunks = chunks;
   p.chunk_len = chunk_len;
   const size_t n = (size_t)rows_total * chunks;
-  p.ws_bytes = align256(n * sizeof(ChunkStat)) + align256(n * top_k * sizeof(float)) +
-               align256(n * top_k * sizeof(int32_t)) + align256((size_t)batch * sizeof(unsigned));
+  p.ws_bytes = align256((size_t)batch * sizeof(unsigned)) + align256(n * sizeof(ChunkStat)) +
+               align256(n * top_k * sizeof(float)) + align256(n * top_k * sizeof(int32_t));
   return p;
 }
 
@@ -486,9 +551,7 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
                        float* front_score_out, int32_t* front_store_out, void* ws,
                        const TopkPlan& plan, cudaStream_t stream) {
   const int rows_total = batch * rows;
-  TopkWs w = carve(ws, rows_total, plan.chunks, top_k);
-  if (cudaMemsetAsync(w.tickets, 0, (size_t)batch * sizeof(unsigned), stream) != cudaSuccess)
-    return launch_status();
+  TopkWs w = carve(ws, batch, rows_total, plan.chunks, top_k);
   dim3 grid(plan.chunks, rows_total);
   const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (row_stride % 4 == 0);
   topk_level_kernel<<<grid, A_THREADS, 0, stream>>>(

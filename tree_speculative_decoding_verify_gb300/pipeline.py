@@ -60,7 +60,7 @@ class HotPath:
                            torch.zeros(b, k, **i32)) for _ in range(2)]
             ws = max(_lib.draft_topk_expand_workspace_size(b, 1, shape.vocab, k),
                      _lib.draft_topk_expand_workspace_size(b, k, shape.vocab, k))
-            self.topk_ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
+            self.topk_ws = torch.zeros(max(ws, 256), dtype=torch.uint8, device=dev)
         self.tokens = torch.full((b, t), -1, **i32)
         self.parents = torch.full((b, t), -1, **i32)
         self.num_nodes = torch.zeros(b, **i32)
