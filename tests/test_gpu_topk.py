@@ -155,3 +155,15 @@ def test_sweep_level_640_rows_of_128256():
         np.testing.assert_array_equal(sp[b, k:k + k * k], lv.parent_store)
         np.testing.assert_allclose(ss[b, k:k + k * k], lv.cu, rtol=gc.SCORE_RTOL)
         assert outs[2].cpu().numpy()[b].tolist() == [k + f for f in lv.selected]
+
+
+@pytest.mark.parametrize("pad", [1, 0])
+def test_whole_row_units_ragged_vocab(pad):
+    """640 frontier rows put whole rows in one unit each (one CTA streams 40003 entries):
+    the row's last three entries fall outside the 16-byte groups; stride 40004 keeps rows
+    16-byte aligned (vector loads), stride 40003 does not (scalar loads)."""
+    rng = np.random.default_rng(40003 + pad)
+    k, v, b = 10, 40003, 64
+    reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
+             for l in range(2)] for _ in range(b)]
+    compare(reqs, k, stride_pad=pad)

@@ -41,7 +41,9 @@ constexpr int A_WARPS = A_THREADS / 32;
 constexpr int MAX_CHUNKS = 32;
 constexpr int MIN_CHUNK = 1024;     // vocab entries per chunk at least (4 per thread)
 constexpr int CAP = 256;            // per-warp candidate buffer (shared memory)
-constexpr int STEP_MAX = 4 * 32;    // most candidates a warp appends in one step
+constexpr int BATCH = 16;           // buffered candidates that trigger a list update
+                                    // (a step adds at most 4 * 32: CAP > BATCH + 128)
+constexpr int BULK = 64;            // from this many on, a tournament instead of insertions
 constexpr int MERGE_SLOTS = 1 + CAP / 32;  // entries a lane holds in a warp merge
 constexpr float L2E = 1.4426950408889634f;
 
@@ -185,53 +187,18 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 struct TopkSmem {
-  union {
-    struct {                                   // streaming: per-warp candidates
-      float bv[A_WARPS][CAP];
-      int bi[A_WARPS][CAP];
-    } s;
-  } u;
-  float lv[A_WARPS][KMAX];                     // warp lists, best first
+  float bv[A_WARPS][CAP];                      // per-warp candidates (warp-owned)
+  int bi[A_WARPS][CAP];
+  float lv[A_WARPS][KMAX];                     // warp lists at the end of a unit
   int li[A_WARPS][KMAX];
   int cnt[A_WARPS];                            // buffered candidates per warp
   float red[A_WARPS];
   float shi[A_WARPS], slo[A_WARPS];
+  unsigned gthr;                               // ord() of the best warp threshold
   float cu[KMAX * KMAX];
   int tok[KMAX * KMAX];
   bool last;
 };
-
-// Warp merge: list = best k of (list, buffered candidates), best first; returns the new
-// list length (warp-uniform) and sets the warp threshold to its k-th entry.
-__device__ __forceinline__ int warp_merge(TopkSmem& sm, int warp, int lane, int k, int nl,
-                                          float& thr_v, int& thr_i) {
-  __syncwarp();
-  const int n = sm.cnt[warp];
-  float v[MERGE_SLOTS];
-  int ix[MERGE_SLOTS];
-  v[0] = lane < nl ? sm.lv[warp][lane] : -INFINITY;
-  ix[0] = lane < nl ? sm.li[warp][lane] : INT_MAX;
-#pragma unroll
-  for (int t = 1; t < MERGE_SLOTS; ++t) {
-    const int j = lane + 32 * (t - 1);
-    v[t] = j < n ? sm.u.s.bv[warp][j] : -INFINITY;
-    ix[t] = j < n ? sm.u.s.bi[warp][j] : INT_MAX;
-  }
-  const int total = min(k, nl + n);
-  sort_entries(v, ix);
-  float nv;
-  int ni;
-  warp_select(v, ix, total, lane, nv, ni);
-  __syncwarp();
-  if (lane < total) { sm.lv[warp][lane] = nv; sm.li[warp][lane] = ni; }
-  if (lane == 0) sm.cnt[warp] = 0;
-  if (total == k) {
-    thr_v = __shfl_sync(FULL, nv, k - 1);
-    thr_i = __shfl_sync(FULL, ni, k - 1);
-  }
-  __syncwarp();
-  return total;
-}
 
 // Per-thread log-sum-exp state: fp32 terms exp(x - ref) summed in groups of 16, each
 // group added exactly into an unevaluated (hi, lo) pair. The reference is raised (and
@@ -244,7 +211,9 @@ struct Lse {
     pair_add(hi, lo, g, 0.f);
     g = 0.f;
   }
-  __device__ __noinline__ void raise(float m) {
+  // rare; inlined so the state stays in registers (an out-of-line member call would
+  // keep it in local memory on the streaming path)
+  __device__ __forceinline__ void raise(float m) {
     flush();
     const float f = expf(ref - m);
     hi *= f;
@@ -253,137 +222,167 @@ struct Lse {
   }
 };
 
-__global__ void __launch_bounds__(A_THREADS, 2)
-topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int vocab, int rows, int k,
-                  int chunks, int chunk_len, int level, bool vec, TopkWs ws,
-                  const float* __restrict__ front_score_in, const int32_t* __restrict__ front_store_in,
-                  int store_cap, int32_t* __restrict__ store_token, float* __restrict__ store_score,
-                  int32_t* __restrict__ store_parent, int32_t* __restrict__ front_token_out,
-                  float* __restrict__ front_score_out, int32_t* __restrict__ front_store_out) {
-  __shared__ TopkSmem sm;
-  const int row = blockIdx.y, chunk = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float* x = logits + (int64_t)row * row_stride;
-  const int start = chunk * chunk_len;
-  const int end = min(vocab, start + chunk_len);
-  if (lane == 0) sm.cnt[warp] = 0;
-
-  float thr_v = -INFINITY;  // warp-uniform: the warp list's k-th entry
-  int thr_i = INT_MAX;
-  int nl = 0;               // warp list length (warp-uniform)
-
-  // Every thread takes 4 consecutive entries per step (one 128-bit load when the row is
-  // 16-byte aligned), two steps prefetched ahead. The common path per 4 entries is their
-  // max against the running maximum and the warp threshold plus four exp2 terms; entries
-  // that beat the threshold go to the warp's buffer, merged when it could overflow.
-  const int steps = (end - start + 4 * A_THREADS - 1) / (4 * A_THREADS);
-  auto load4 = [&](int it) -> float4 {
-    const int e = start + 4 * (it * A_THREADS + tid);
-    if (vec && e + 3 < end) return ld_stream(reinterpret_cast<const float4*>(x + e));
-    float4 r;
-    r.x = e < end ? x[e] : -INFINITY;
-    r.y = e + 1 < end ? x[e + 1] : -INFINITY;
-    r.z = e + 2 < end ? x[e + 2] : -INFINITY;
-    r.w = e + 3 < end ? x[e + 3] : -INFINITY;
-    return r;
-  };
-  const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-  float4 a = steps > 0 ? load4(0) : none;
-  float4 bnext = steps > 1 ? load4(1) : none;
-
-  // Common starting reference: the largest of the first entries every thread sees.
-  float first = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
-  if (lane == 0) sm.red[warp] = first;
-  __syncthreads();
-  first = sm.red[0];
-#pragma unroll
-  for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, sm.red[w]);
+// Streaming state of one thread for one (row, chunk) unit. The warp's top-k list lives
+// in registers, entry r in lane r (lanes >= nl hold (-inf, INT_MAX)); the threshold is
+// its k-th entry once it has k. Candidates that beat the threshold are buffered in the
+// warp's shared-memory slice and folded into the list in batches.
+struct UnitState {
   Lse lse;
-  lse.ref = fmaxf(first, -FLT_MAX);  // finite, so x = -inf gives a zero term
-  lse.g = 0.f;
-  lse.hi = 0.f;
-  lse.lo = 0.f;
+  float lv;     // this lane's list entry
+  int li;
+  float thr_v;  // warp-uniform threshold
+  int thr_i;
+  int nl;       // warp-uniform list length
+  int cnt;      // warp-uniform number of buffered candidates
+  int groups;   // float4 groups since the last flush
+};
 
-  for (int it = 0; it < steps; ++it) {
-    const float4 c = it + 2 < steps ? load4(it + 2) : none;
-    const int e = start + 4 * (it * A_THREADS + tid);
-    const float m4 = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
-    if (m4 > lse.ref + RAISE) lse.raise(m4);
-    const float r = lse.ref;
-    lse.g += (ex2((a.x - r) * L2E) + ex2((a.y - r) * L2E)) + (ex2((a.z - r) * L2E) + ex2((a.w - r) * L2E));
-    bool appended = false;
-    if (m4 >= thr_v) {  // some entry may beat the threshold: test each exactly
-      const float xv[4] = {a.x, a.y, a.z, a.w};
+__device__ __forceinline__ void set_threshold(TopkSmem& sm, UnitState& u, int lane, int k) {
+  if (u.nl == k) {
+    u.thr_v = __shfl_sync(FULL, u.lv, k - 1);
+    u.thr_i = __shfl_sync(FULL, u.li, k - 1);
+    // k entries of the unit are >= thr_v, so nothing below it reaches the unit's top k:
+    // every warp may filter with the largest such value
+    if (lane == 0) atomicMax(&sm.gthr, ord(u.thr_v));
+  }
+}
+
+// Folds the warp's buffered candidates into its list: a tournament over list and buffer
+// when many are buffered, else one ballot insertion per candidate (position = number of
+// better list entries; the entries below shift one lane down).
+__device__ __forceinline__ void fold(TopkSmem& sm, UnitState& u, int warp, int lane, int k) {
+  __syncwarp();
+  const int n = u.cnt;
+  if (n >= BULK) {
+    float v[MERGE_SLOTS];
+    int ix[MERGE_SLOTS];
+    v[0] = lane < u.nl ? u.lv : -INFINITY;
+    ix[0] = lane < u.nl ? u.li : INT_MAX;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (e + q < end && better(xv[q], e + q, thr_v, thr_i)) {
-          const int pos = atomicAdd(&sm.cnt[warp], 1);
-          sm.u.s.bv[warp][pos] = xv[q];
-          sm.u.s.bi[warp][pos] = e + q;
-          appended = true;
-        }
+    for (int t = 1; t < MERGE_SLOTS; ++t) {
+      const int j = lane + 32 * (t - 1);
+      v[t] = j < n ? sm.bv[warp][j] : -INFINITY;
+      ix[t] = j < n ? sm.bi[warp][j] : INT_MAX;
+    }
+    const int total = min(k, u.nl + n);
+    sort_entries(v, ix);
+    warp_select(v, ix, total, lane, u.lv, u.li);
+    u.nl = total;
+  } else {
+    for (int j = 0; j < n; ++j) {
+      const float cv = sm.bv[warp][j];
+      const int ci = sm.bi[warp][j];
+      if (u.nl == k && !better(cv, ci, u.thr_v, u.thr_i)) continue;  // warp-uniform
+      const int pos = __popc(__ballot_sync(FULL, lane < u.nl && better(u.lv, u.li, cv, ci)));
+      const float up_v = __shfl_up_sync(FULL, u.lv, 1);
+      const int up_i = __shfl_up_sync(FULL, u.li, 1);
+      if (lane == pos) { u.lv = cv; u.li = ci; }
+      else if (lane > pos) { u.lv = up_v; u.li = up_i; }
+      u.nl = min(k, u.nl + 1);
+      if (lane >= u.nl) { u.lv = -INFINITY; u.li = INT_MAX; }
+      if (u.nl == k) {
+        u.thr_v = __shfl_sync(FULL, u.lv, k - 1);
+        u.thr_i = __shfl_sync(FULL, u.li, k - 1);
       }
     }
-    if (__any_sync(FULL, appended)) {
-      __syncwarp();
-      if (sm.cnt[warp] > CAP - STEP_MAX) nl = warp_merge(sm, warp, lane, k, nl, thr_v, thr_i);
-    }
-    if ((it & 3) == 3) lse.flush();
-    a = bnext;
-    bnext = c;
   }
-  lse.flush();
-  nl = warp_merge(sm, warp, lane, k, nl, thr_v, thr_i);  // the warp's final best k
-  if (lane >= nl && lane < k) { sm.lv[warp][lane] = -INFINITY; sm.li[warp][lane] = INT_MAX; }
+  u.cnt = 0;
+  __syncwarp();
+  if (lane == 0) sm.cnt[warp] = 0;
+  set_threshold(sm, u, lane, k);
+  __syncwarp();
+}
 
-  // exp-sum over the block
-  float R = lse.ref, phi = lse.hi, plo = lse.lo;
-  warp_combine(R, phi, plo);
-  __syncthreads();  // sm.red was read for the starting reference
-  if (lane == 0) { sm.red[warp] = R; sm.shi[warp] = phi; sm.slo[warp] = plo; }
-  __syncthreads();
-  if (warp == 0) {
-    // block top-k: 8 sorted warp lists, lanes 0-7 hold the list heads
-    int ptr = 0;
-    const size_t base = ((size_t)row * chunks + chunk) * k;
-    for (int r = 0; r < k; ++r) {
-      float v = lane < A_WARPS && ptr < k ? sm.lv[lane][ptr] : -INFINITY;
-      int i = lane < A_WARPS && ptr < k ? sm.li[lane][ptr] : INT_MAX;
-      int who = lane;
-      warp_argmax(v, i, who);
-      if (lane == who) ++ptr;
-      if (lane == 0) { ws.val[base + r] = v; ws.idx[base + r] = i; }
-    }
-    float rr = lane < A_WARPS ? sm.red[lane] : -INFINITY;
-    float hh = lane < A_WARPS ? sm.shi[lane] : 0.f, ll = lane < A_WARPS ? sm.slo[lane] : 0.f;
-    warp_combine(rr, hh, ll);
-    if (lane == 0) {
-      ChunkStat cs;
-      cs.ref = rr;
-      cs.hi = hh;
-      cs.lo = ll;
-      cs.pad = 0.f;
-      ws.stat[(size_t)row * chunks + chunk] = cs;
+// Four consecutive entries e .. e + 3 (those at or past `end` are -inf and skipped): their
+// max against the running maximum, four exp2 terms, and the entries that beat both the
+// warp threshold and the CTA-wide bound `g` (an ord() image) appended to the warp's
+// buffer (a shared-memory counter: usually one lane at a time gets here). Warp-uniform
+// call.
+__device__ __forceinline__ void consider4(TopkSmem& sm, UnitState& u, int warp, int lane, int k,
+                                          float4 a, int e, int end, unsigned g) {
+  const float m4 = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
+  if (m4 > u.lse.ref + RAISE) u.lse.raise(m4);
+  const float r = u.lse.ref;
+  u.lse.g += (ex2((a.x - r) * L2E) + ex2((a.y - r) * L2E)) + (ex2((a.z - r) * L2E) + ex2((a.w - r) * L2E));
+  if (++u.groups == 4) {
+    u.lse.flush();
+    u.groups = 0;
+  }
+  const bool maybe = m4 >= u.thr_v && ord(m4) >= g;
+  if (maybe) {  // divergent and rare
+    const float xv[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (e + q < end && ord(xv[q]) >= g && better(xv[q], e + q, u.thr_v, u.thr_i)) {
+        const int pos = atomicAdd(&sm.cnt[warp], 1);
+        sm.bv[warp][pos] = xv[q];
+        sm.bi[warp][pos] = e + q;
+      }
     }
   }
-
-  // The last CTA of this request to finish merges its rows and runs the joint top-K.
-  const int b = row / rows;
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const unsigned t = atomicAdd(&ws.tickets[b], 1u);
-    sm.last = (t == (unsigned)(rows * chunks - 1));
+  if (__any_sync(FULL, maybe)) {
+    __syncwarp();
+    u.cnt = sm.cnt[warp];
+    if (u.cnt >= BATCH) fold(sm, u, warp, lane, k);
   }
-  __syncthreads();
-  if (!sm.last) return;
-  __threadfence();
+}
 
-  const int off = level == 1 ? 0 : k + (level - 2) * k * k;
-  const int64_t srow = (int64_t)b * store_cap;
-  // Warp s merges row s (rows <= 16 = warps): lane c holds chunk c's sorted list of the
+// Seed of the CTA-wide bound from the warps' maxima of the unit's first entries (in
+// sm.red): the k-th largest of the A_WARPS maxima (k <= A_WARPS) has k distinct entries at
+// or above it. Run by warp 0; sm.gthr is read after the next barrier.
+__device__ __forceinline__ void seed_threshold(TopkSmem& sm, int lane, int k) {
+  const float m = lane < A_WARPS ? sm.red[lane] : -INFINITY;
+  int rank = 0;  // warps whose maximum is larger (ties: lower warp first)
+#pragma unroll
+  for (int w = 0; w < A_WARPS; ++w) {
+    const float o = __shfl_sync(FULL, m, w);
+    rank += (o > m || (o == m && w < lane)) ? 1 : 0;
+  }
+  if (lane < A_WARPS && rank == k - 1) sm.gthr = ord(m);
+}
+
+// Starts a unit's per-thread state (sm.gthr and sm.cnt were reset before the CTA's last
+// barrier).
+__device__ __forceinline__ void unit_begin(UnitState& u, float ref) {
+  u.lse.ref = fmaxf(ref, -FLT_MAX);  // finite, so x = -inf gives a zero term
+  u.lse.g = 0.f;
+  u.lse.hi = 0.f;
+  u.lse.lo = 0.f;
+  u.lv = -INFINITY;
+  u.li = INT_MAX;
+  u.thr_v = -INFINITY;
+  u.thr_i = INT_MAX;
+  u.nl = 0;
+  u.cnt = 0;
+  u.groups = 0;
+}
+
+struct LevelArgs {
+  const float* logits;
+  int64_t row_stride;
+  int vocab, rows, k, chunks, chunk_len, level;
+  TopkWs ws;
+  const float* front_score_in;
+  const int32_t* front_store_in;
+  int store_cap;
+  int32_t* store_token;
+  float* store_score;
+  int32_t* store_parent;
+  int32_t* front_token_out;
+  float* front_score_out;
+  int32_t* front_store_out;
+};
+
+// The request's merge, run by the CTA that finished its last unit: every row's chunk
+// lists and exp-sums combine into the row's top-k log-probabilities and cumulative
+// scores (written to the store), then the joint top-K over the rows. Out of line: it
+// is rare, and inlined its registers would crowd the streaming loop.
+__device__ __noinline__ void request_merge(TopkSmem& sm, const LevelArgs& p, int b) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = p.k, rows = p.rows, chunks = p.chunks;
+  const int off = p.level == 1 ? 0 : k + (p.level - 2) * k * k;
+  const int64_t srow = (int64_t)b * p.store_cap;
+  // Warp s merges row s (rows <= 16 <= warps): lane c holds chunk c's sorted list of the
   // row in registers.
   static_assert(A_WARPS >= TSV_MAX_TOPK, "one warp per frontier row");
   if (warp < rows) {
@@ -393,14 +392,14 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
     float cv[KMAX];
     int ci[KMAX];
     float4 cs = make_float4(-INFINITY, 0.f, 0.f, 0.f);
-    if (have) cs = __ldcg(reinterpret_cast<const float4*>(&ws.stat[g]));
+    if (have) cs = __ldcg(reinterpret_cast<const float4*>(&p.ws.stat[g]));
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      cv[j] = have && j < k ? __ldcg(ws.val + g * k + j) : -INFINITY;
-      ci[j] = have && j < k ? __ldcg(ws.idx + g * k + j) : INT_MAX;
+      cv[j] = have && j < k ? __ldcg(p.ws.val + g * k + j) : -INFINITY;
+      ci[j] = have && j < k ? __ldcg(p.ws.idx + g * k + j) : INT_MAX;
     }
-    const float pscore = level == 1 ? 0.0f : front_score_in[r0];
-    const int pstore = level == 1 ? -1 : front_store_in[r0];
+    const float pscore = p.level == 1 ? 0.0f : p.front_score_in[r0];
+    const int pstore = p.level == 1 ? -1 : p.front_store_in[r0];
     float Rr = cs.x, sh = cs.y, sl = cs.z;
     warp_combine(Rr, sh, sl);
     // log(hi + lo) = log(hi) + log1p(lo / hi); |lo / hi| is below an ulp, so the second
@@ -413,9 +412,9 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
       const float logp = ((v - lse_hi) - lse_mid) - lse_lo;
       const float cu = pscore + logp;
       const int flat = s * k + lane;
-      store_token[srow + off + flat] = i;
-      store_score[srow + off + flat] = cu;
-      store_parent[srow + off + flat] = pstore;
+      p.store_token[srow + off + flat] = i;
+      p.store_score[srow + off + flat] = cu;
+      p.store_parent[srow + off + flat] = pstore;
       sm.cu[flat] = cu;
       sm.tok[flat] = i;
     }
@@ -438,12 +437,122 @@ topk_level_kernel(const float* __restrict__ logits, int64_t row_stride, int voca
     int bi;
     warp_select(v, ix, k, lane, bv, bi);
     if (lane < k) {
-      front_token_out[b * k + lane] = sm.tok[bi];
-      front_score_out[b * k + lane] = bv;
-      front_store_out[b * k + lane] = off + bi;
+      p.front_token_out[b * k + lane] = sm.tok[bi];
+      p.front_score_out[b * k + lane] = bv;
+      p.front_store_out[b * k + lane] = off + bi;
     }
-    if (lane == 0) ws.tickets[b] = 0u;
+    if (lane == 0) p.ws.tickets[b] = 0u;
   }
+  __syncthreads();
+}
+
+// End of a unit: the warps' final lists and exp-sums merge into the chunk's top-k and
+// (ref, sum), written to the workspace; the last unit of a request to finish (an atomic
+// ticket) then merges every row of the request and runs the joint top-K. Called by the
+// whole CTA.
+__device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int row, int chunk) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = p.k, rows = p.rows, chunks = p.chunks;
+  u.lse.flush();
+  __syncwarp();
+  u.cnt = sm.cnt[warp];
+  if (u.cnt > 0) fold(sm, u, warp, lane, k);  // the warp's final best k
+  if (lane < k) { sm.lv[warp][lane] = u.lv; sm.li[warp][lane] = u.li; }
+
+  // exp-sum over the block
+  float R = u.lse.ref, phi = u.lse.hi, plo = u.lse.lo;
+  warp_combine(R, phi, plo);
+  if (lane == 0) { sm.red[warp] = R; sm.shi[warp] = phi; sm.slo[warp] = plo; }
+  __syncthreads();
+  if (warp == 0) {
+    // block top-k: the warps' sorted lists, lane w holds list w's head
+    int ptr = 0;
+    const size_t base = ((size_t)row * chunks + chunk) * k;
+    for (int r = 0; r < k; ++r) {
+      float v = lane < A_WARPS && ptr < k ? sm.lv[lane][ptr] : -INFINITY;
+      int i = lane < A_WARPS && ptr < k ? sm.li[lane][ptr] : INT_MAX;
+      int who = lane;
+      warp_argmax(v, i, who);
+      if (lane == who) ++ptr;
+      if (lane == 0) { p.ws.val[base + r] = v; p.ws.idx[base + r] = i; }
+    }
+    float rr = lane < A_WARPS ? sm.red[lane] : -INFINITY;
+    float hh = lane < A_WARPS ? sm.shi[lane] : 0.f, ll = lane < A_WARPS ? sm.slo[lane] : 0.f;
+    warp_combine(rr, hh, ll);
+    if (lane == 0) {
+      ChunkStat cs;
+      cs.ref = rr;
+      cs.hi = hh;
+      cs.lo = ll;
+      cs.pad = 0.f;
+      p.ws.stat[(size_t)row * chunks + chunk] = cs;
+    }
+  }
+
+  // The last unit of this request to finish merges its rows and runs the joint top-K.
+  const int b = row / rows;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned t = atomicAdd(&p.ws.tickets[b], 1u);
+    sm.last = (t == (unsigned)(rows * chunks - 1));
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();
+  request_merge(sm, p, b);
+}
+
+// ---- streaming: one (row, chunk) unit per CTA -----------------------------------------
+__global__ void __launch_bounds__(A_THREADS, 2)
+topk_level_kernel(const LevelArgs p, bool vec) {
+  __shared__ TopkSmem sm;
+  const int row = blockIdx.y, chunk = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* x = p.logits + (int64_t)row * p.row_stride;
+  const int start = chunk * p.chunk_len;
+  const int end = min(p.vocab, start + p.chunk_len);
+
+  // Every thread takes 4 consecutive entries per step (one 128-bit load when the row is
+  // 16-byte aligned), two steps prefetched ahead.
+  const int steps = (end - start + 4 * A_THREADS - 1) / (4 * A_THREADS);
+  auto load4 = [&](int it) -> float4 {
+    const int e = start + 4 * (it * A_THREADS + tid);
+    if (vec && e + 3 < end) return ld_stream(reinterpret_cast<const float4*>(x + e));
+    float4 r;
+    r.x = e < end ? x[e] : -INFINITY;
+    r.y = e + 1 < end ? x[e + 1] : -INFINITY;
+    r.z = e + 2 < end ? x[e + 2] : -INFINITY;
+    r.w = e + 3 < end ? x[e + 3] : -INFINITY;
+    return r;
+  };
+  const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  float4 a = steps > 0 ? load4(0) : none;
+  float4 bnext = steps > 1 ? load4(1) : none;
+
+  // Common starting reference: the largest of the first entries every thread sees.
+  float first = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
+  if (lane == 0) { sm.red[warp] = first; sm.cnt[warp] = 0; }
+  if (tid == 0) sm.gthr = 0u;
+  __syncthreads();
+  if (warp == 0 && steps > 1) seed_threshold(sm, lane, p.k);
+  first = sm.red[0];
+#pragma unroll
+  for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, sm.red[w]);
+  __syncthreads();  // sm.red is reused by finish_unit; sm.gthr is seeded
+  UnitState u;
+  unit_begin(u, first);
+
+  for (int it = 0; it < steps; ++it) {
+    const float4 c = it + 2 < steps ? load4(it + 2) : none;
+    consider4(sm, u, warp, lane, p.k, a, start + 4 * (it * A_THREADS + tid), end,
+              *reinterpret_cast<volatile unsigned*>(&sm.gthr));
+    a = bnext;
+    bnext = c;
+  }
+  finish_unit(sm, u, p, row, chunk);
 }
 
 // ---- final selection --------------------------------------------------------------
@@ -551,13 +660,28 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
                        float* front_score_out, int32_t* front_store_out, void* ws,
                        const TopkPlan& plan, cudaStream_t stream) {
   const int rows_total = batch * rows;
-  TopkWs w = carve(ws, batch, rows_total, plan.chunks, top_k);
-  dim3 grid(plan.chunks, rows_total);
+  LevelArgs p;
+  p.logits = logits;
+  p.row_stride = row_stride;
+  p.vocab = vocab;
+  p.rows = rows;
+  p.k = top_k;
+  p.chunks = plan.chunks;
+  p.chunk_len = plan.chunk_len;
+  p.level = level;
+  p.ws = carve(ws, batch, rows_total, plan.chunks, top_k);
+  p.front_score_in = front_score_in;
+  p.front_store_in = front_store_in;
+  p.store_cap = store_cap;
+  p.store_token = store_token;
+  p.store_score = store_score;
+  p.store_parent = store_parent;
+  p.front_token_out = front_token_out;
+  p.front_score_out = front_score_out;
+  p.front_store_out = front_store_out;
   const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (row_stride % 4 == 0);
-  topk_level_kernel<<<grid, A_THREADS, 0, stream>>>(
-      logits, row_stride, vocab, rows, top_k, plan.chunks, plan.chunk_len, level, vec, w,
-      front_score_in, front_store_in, store_cap, store_token, store_score, store_parent,
-      front_token_out, front_score_out, front_store_out);
+  dim3 grid(plan.chunks, rows_total);
+  topk_level_kernel<<<grid, A_THREADS, 0, stream>>>(p, vec);
   return launch_status();
 }
 
