@@ -313,9 +313,22 @@ def native(args):
         achieved, peak, unit = nbytes / attn_s / 1e9, hbm, "GB/s"
     else:
         achieved, peak, unit = flops / attn_s / 1e12, tf, "TFLOP/s"
+    attn_roof = {"kernel": "tree_verify_attn (prep + tcgen05 split-KV attention with in-kernel merge)",
+                 "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                 "frac": achieved / peak, "peak_source": src, "traffic": None,
+                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                 "us_per_launch": ms["attn"] * 1e3}
     topk_rows = b * k / (ms["topk"] / 1e3)
     topk_bytes = b * k * v * 4
+    topk_gbps = topk_bytes / (ms["topk"] / 1e3) / 1e9
+    topk_roof = {"kernel": "draft_topk_expand level (rows x vocab fp32 logits)", "bound": "hbm",
+                 "achieved": topk_gbps, "peak": hbm, "unit": "GB/s", "frac": topk_gbps / hbm,
+                 "peak_source": src, "traffic": None, "algorithmic_bytes": topk_bytes,
+                 "us_per_launch": ms["topk"] * 1e3}
+    # the dominant kernel of the step: the attention call or the depth + 1 top-k levels
+    dominant = "topk" if ms["topk"] * (w.depth + 1) > ms["attn"] else "attn"
     kernels_step = hp.kernels_per_step()
+    attn_kernels = hp.attn_kernels()
     line = {
         "metric": METRIC, "value": world * 1e3 / step_ms, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -332,13 +345,13 @@ def native(args):
         "topk_rows_per_s": topk_rows,
         "topk_hbm_GBps": topk_bytes / (ms["topk"] / 1e3) / 1e9,
         "nodes_kv_tokens_per_s": sum(len(d) * (p + len(d)) for p, d in zip(prefix, depths)) / attn_s,
-        "roofline": {"kernel": "tree_verify_attn (prep + split-KV attention + merge)",
-                     "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "peak_source": src, "traffic": None,
-                     "algorithmic_bytes": nbytes, "algorithmic_flops": flops},
+        "roofline": topk_roof if dominant == "topk" else attn_roof,
+        "roofline_attn": attn_roof,
+        "roofline_topk": topk_roof,
         "e2e": {"value": world * 1e3 / e2e_step_ms, "unit": UNIT, "ms_per_step": e2e_step_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * (kernels_step + 3 + 1),
+        # timed region per iteration: the step graph, the attention call, one top-k level
+        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1),
         "wall_s_timed_region": t_wall,
     }
     ck = clocks.summary()

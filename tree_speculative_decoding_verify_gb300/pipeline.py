@@ -139,10 +139,14 @@ class HotPath:
     # launches of libtsv kernels per step (for the bench's launch count)
     def kernels_per_step(self) -> int:
         """libtsv kernels one step launches: one per expansion level, the final
-        selection, the metadata, the attention call (prep and the tensor-core kernel,
-        which merges its own splits, for bf16 with head_dim 128 on sm_100 and later;
-        prep, the CUDA-core kernel and the merge otherwise) and the acceptance."""
+        selection, the metadata, the attention call and the acceptance."""
         n = 0 if self.s.fixed_nodes else (self.s.depth + 1) + 1
+        return n + 1 + self.attn_kernels() + 1
+
+    def attn_kernels(self) -> int:
+        """Kernels of one tree_verify_attn call: prep and the tensor-core kernel (which
+        merges its own splits) for bf16 with head_dim 128 on sm_100 and later; prep,
+        the CUDA-core kernel and the merge otherwise."""
         tc = (self.cache.dtype == torch.bfloat16 and self.cache.head_dim == 128
               and torch.cuda.is_available() and torch.cuda.get_device_capability()[0] >= 10)
-        return n + 1 + (2 if tc else 3) + 1
+        return 2 if tc else 3
