@@ -40,7 +40,7 @@ struct AttnArgs {
 // Query rows per tensor-core CTA (one 128-row M tile).
 constexpr int TC_M_GROUP = 128;
 // Most key splits of one row block on the tensor-core path.
-#define TSV_ATTN_MAX_SPLITS 64
+#define TSV_ATTN_MAX_SPLITS 32
 
 bool tc_supported(const AttnPlan& p);
 int launch_attn_tc(const AttnPlan& p, const AttnArgs& a, float scale_log2, void* out,

@@ -12,7 +12,7 @@
 // from L2).
 //
 //   warp 4      TMA producer: K/V tiles of 128 keys (64-key boxes, 128-byte swizzle)
-//               into a 4-stage K ring and a 3-stage V ring; K runs one tile ahead of V
+//               into a 3-stage K ring and a 4-stage V ring; K runs one tile ahead of V
 //   warp 5      TMEM allocator + MMA issuer (warp-uniform descriptors, one elected lane
 //               per instruction). Step j (j = 0 .. n) issues
 //                 S      = Q K_{j+1}^T      A = Q in TMEM, B = K (shared, K-major)
@@ -21,9 +21,10 @@
 //               computed while the softmax works on tile j. Q and P come from TMEM: the
 //               shared-memory port then carries only the K and V tiles (TMA writes plus
 //               one MMA read each).
-//   warp 6      relay: arrives on GO for step j once K_{j+1} and V_{j-1} have landed;
-//               the four softmax warps arrive on it once they have read S_j (which
-//               also publishes P_{j-1}). The MMA warp tests that one barrier per step:
+//   warp 6      relay: arrives on GO for step j once K_{j+1} and V_{j-1} have landed
+//               (a step ahead of the softmax: GO alternates between two barriers by step
+//               parity); the four softmax warps arrive on it once they have read S_j
+//               (which also publishes P_{j-1}). The MMA warp tests that one barrier per step:
 //               every test it makes is an issue gap in which the shallow MMA queue
 //               drains, and every mbarrier operation waits behind the operand traffic
 //               of the shared-memory port (a few hundred cycles), so the critical path
@@ -54,7 +55,7 @@ namespace tsv {
 namespace {
 
 constexpr int KEYS = 128;                 // keys per tile
-constexpr int KST = 4, VST = 3;           // K and V ring depths
+constexpr int KST = 3, VST = 4;           // K and V ring depths (V tiles live two steps longer)
 constexpr int THREADS = 224;
 constexpr int TMA_WARP = 4, MMA_WARP = 5, RELAY_WARP = 6;
 constexpr uint32_t HALF = 128 * 128;      // 128 rows x 64 bf16 (one 128-byte-swizzled panel)
@@ -65,10 +66,10 @@ constexpr uint32_t SMEM_V = SMEM_K + KST * TILE;  // VST V tiles
 constexpr uint32_t SMEM_BAR = SMEM_V + VST * TILE;
 constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + alignment slack
 // split merge (after the last MMA, over the K/V rings): three 64 KB partial tiles (128 rows
-// x 128 f32, row-major), then the per-split row weights
+// x 128 f32, row-major), then every split's (m, l) rows, later overwritten by weights
 constexpr uint32_t MERGE_TILE = 128 * 128 * 4;
 constexpr uint32_t MERGE_W = 3 * MERGE_TILE;
-static_assert(MERGE_W + TSV_ATTN_MAX_SPLITS * 128 * 4 <= SMEM_BAR, "merge buffers");
+static_assert(MERGE_W + TSV_ATTN_MAX_SPLITS * 128 * 8 <= SMEM_BAR, "merge buffers");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S = 0;
 constexpr uint32_t TMEM_O = 128;
@@ -165,6 +166,23 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+__device__ __forceinline__ float4 lds128(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, float4 v) {
+  asm volatile("st.shared.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ float lds32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -394,34 +412,49 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   if (warp == TMA_WARP) {
     // ---- producer: the whole warp walks the loop, lane 0 issues. K runs one tile ahead
     // of V (order K0 K1 V0 K2 V1 ...), so S = Q K^T never waits behind a V load.
-    auto row_of = [&](int key) -> int {
+    // Paged caches: the block ids of 32 consecutive 64-key boxes sit in the lanes'
+    // registers (one load round trip per 16 tiles instead of one per box).
+    const int box0 = t0 * (KEYS / TSV_KV_BLOCK);
+    int win = -1;  // first box of the loaded window
+    int blk_reg = 0;
+    auto row_of = [&](int key) -> int {  // warp-uniform call
       if (a.layout == TSV_KV_CONTIGUOUS) return (int)(((int64_t)b * a.hkv + h) * a.capacity + key);
-      const int blk = a.block_table[(int64_t)b * a.max_blocks + key / TSV_KV_BLOCK];
+      const int box = key / TSV_KV_BLOCK;
+      const int w = box0 + ((box - box0) & ~31);
+      if (w != win) {
+        win = w;
+        const int nb = (keys + TSV_KV_BLOCK - 1) / TSV_KV_BLOCK;
+        blk_reg = w + lane < nb ? a.block_table[(int64_t)b * a.max_blocks + w + lane] : 0;
+      }
+      const int blk = __shfl_sync(FULL, blk_reg, box - win);
       return (blk * a.hkv + h) * TSV_KV_BLOCK;
     };
     // one K or V tile: 1 or 2 boxes of 64 keys (a box past the last key is not loaded)
     auto load = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
-      if (lane != 0) return;
       const int k0 = (t0 + j) * KEYS;
       const int chunks = (k0 + 64 < keys) ? 2 : 1;
+      int row[2];
+      for (int c = 0; c < 2; ++c) row[c] = c < chunks ? row_of(k0 + 64 * c) : 0;
+      if (lane != 0) return;
       mbar_expect_tx(full, chunks * 2 * BOX64);
-      for (int c = 0; c < chunks; ++c) {
-        const int row = row_of(k0 + 64 * c);
-        for (int hf = 0; hf < 2; ++hf) tma_load_2d(dst + hf * HALF + c * BOX64, map, hf * 64, row, full);
-      }
+      for (int c = 0; c < chunks; ++c)
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_2d(dst + hf * HALF + c * BOX64, map, hf * 64, row[c], full);
     };
     int issued_k = 0, issued_v = 0;
     bool ok = true;
     for (int j = 0; ok && j <= n; ++j) {
       if (j < n) {
         const int st = j % KST;
-        if (j >= KST && !(ok = warp_wait(bar(BAR_K_EMPTY + st), ((j / KST) - 1) & 1, abort))) break;
+        if (j >= KST && !(ok = warp_wait(bar(BAR_K_EMPTY + st), ((j / KST) - 1) & 1, abort, true)))
+          break;
         load(&tm_k, base + SMEM_K + st * TILE, bar(BAR_K_FULL + st), j);
         issued_k = j + 1;
       }
       if (j >= 1) {
         const int jv = j - 1, st = jv % VST;
-        if (jv >= VST && !(ok = warp_wait(bar(BAR_V_EMPTY + st), ((jv / VST) - 1) & 1, abort))) break;
+        if (jv >= VST && !(ok = warp_wait(bar(BAR_V_EMPTY + st), ((jv / VST) - 1) & 1, abort, true)))
+          break;
         load(&tm_v, base + SMEM_V + st * TILE, bar(BAR_V_FULL + st), jv);
         issued_v = j;
       }
@@ -459,32 +492,42 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     };
     // O += P_j V_j over ksteps of 16 keys (V rows 16 ks .. 16 ks + 15: MN-major, 16
     // rows of 128 bytes per k-step)
-    auto pv = [&](int j, int ksteps) {
+    // Also tests (without waiting) the barrier of the next step before the last k-step
+    // is issued: the test's round trip overlaps the queued MMAs instead of leaving the
+    // tensor pipe idle after them. Returns whether that phase had completed.
+    auto pv = [&](int j, int ksteps, uint32_t next_bar, uint32_t next_parity) {
       const uint64_t vd = dv + (uint64_t)((j % VST) * TILE_D);
       const uint32_t pa = tmem + TMEM_P + (j & 1) * 64;
       const uint32_t acc0 = j > 0 ? 1u : 0u;
+      bool next_ready = false;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
+      for (int ks = 0; ks < 8; ++ks) {
+        if (ks == 7 && next_bar) next_ready = mbar_test(next_bar, next_parity);
         if (ks < ksteps && elect_one())
           mma_ts(tmem + TMEM_O, pa + ks * 8, vd + (uint64_t)(ks * 128), ID_PV, ks > 0 ? 1u : acc0);
+      }
       if (elect_one()) {
         mma_commit(bar(BAR_V_EMPTY + j % VST));
         mma_commit(bar(BAR_PV_DONE + (j & 1)));
       }
-      __syncwarp();
+      return __all_sync(FULL, next_ready);
     };
     bool ok = warp_wait(bar(BAR_Q), 0, abort) && warp_wait(bar(BAR_K_FULL), 0, abort);
     if (ok) {
       tc_fence_after();
       qk(0);
     }
+    bool ready = false;  // GO phase j already seen complete
     for (int j = 0; ok && j <= n; ++j) {
       // GO phase j: S_j read by the softmax (so P_{j-1} is written), K_{j+1} and V_{j-1}
       // landed (phase n: the last P written, V_{n-1} landed)
-      if (!(ok = warp_wait(bar(BAR_GO + (j & 1)), (j >> 1) & 1, abort, true))) break;
+      if (!ready && !(ok = warp_wait(bar(BAR_GO + (j & 1)), (j >> 1) & 1, abort, true))) break;
       tc_fence_after();
       if (j + 1 < n) qk(j + 1);
-      if (j >= 1) pv(j - 1, (min(KEYS, keys - (t0 + j - 1) * KEYS) + 15) >> 4);
+      ready = false;
+      if (j >= 1)
+        ready = pv(j - 1, (min(KEYS, keys - (t0 + j - 1) * KEYS) + 15) >> 4,
+                   j < n ? bar(BAR_GO + ((j + 1) & 1)) : 0u, ((j + 1) >> 1) & 1);
     }
     const bool issuer = lane == 0;
     if (issuer) {
@@ -495,18 +538,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     __syncwarp();
   } else if (warp == RELAY_WARP) {
-    // ---- relay: its share of GO phase j once K_{j+1} and V_{j-1} have landed; it then
-    // waits for the phase to complete so its next arrival cannot count toward this one
+    // ---- relay: its share of GO phase j once K_{j+1} and V_{j-1} have landed. GO is
+    // double-buffered by step parity, so the relay only waits for phase j - 2 (the last
+    // one on the same barrier) to have completed before arriving: it runs a step ahead
+    // of the softmax instead of after it.
     bool ok = true;
     for (int j = 0; ok && j <= n; ++j) {
+      if (j >= 2 && !(ok = warp_wait(bar(BAR_GO + (j & 1)), ((j - 2) >> 1) & 1, abort, true))) break;
       if (j + 1 < n &&
-          !(ok = warp_wait(bar(BAR_K_FULL + (j + 1) % KST), ((j + 1) / KST) & 1, abort)))
+          !(ok = warp_wait(bar(BAR_K_FULL + (j + 1) % KST), ((j + 1) / KST) & 1, abort, true)))
         break;
-      if (j >= 1 && !(ok = warp_wait(bar(BAR_V_FULL + (j - 1) % VST), ((j - 1) / VST) & 1, abort)))
+      if (j >= 1 &&
+          !(ok = warp_wait(bar(BAR_V_FULL + (j - 1) % VST), ((j - 1) / VST) & 1, abort, true)))
         break;
       if (lane == 0) mbar_arrive(bar(BAR_GO + (j & 1)));
       __syncwarp();
-      if (!(ok = warp_wait(bar(BAR_GO + (j & 1)), (j >> 1) & 1, abort))) break;
     }
   } else if (warp < 4) {
     // ---- softmax warpgroup -----------------------------------------------------------
@@ -675,41 +721,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       softmax_sync();
       if (*merge_flag) {
         __threadfence();
-        // Log-sum-exp weights of every split for this thread's row (m in log2 units); the
-        // (m, l) loads are issued eight at a time.
+        // One bulk-copy round trip brings every split's (m, l) rows of this M tile and the
+        // first partial tiles (contiguous per split: 128 rows x 128 f32); later tiles come
+        // two at a time. Tile 0 keeps the running weighted sum.
         const int nsp = (n_tiles + a.tiles_per_split - 1) / a.tiles_per_split;
         const int t = warp * 32 + lane;
         const int64_t pbase = ((int64_t)b * a.hkv + h) * a.nsplit;
-        const float2* mlp = reinterpret_cast<const float2*>(a.ml) + pbase * a.rows_pad + r;
-        float* wsm = reinterpret_cast<float*>(gbase + MERGE_W);  // [nsp][128]
-        float M = -INFINITY, L = 0.f;
-        for (int s0 = 0; s0 < nsp; s0 += 8) {
-          float2 ml[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            ml[u] = s0 + u < nsp ? __ldcg(mlp + (int64_t)(s0 + u) * a.rows_pad)
-                                 : make_float2(-INFINITY, 0.f);
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (s0 + u < nsp) wsm[(s0 + u) * 128 + t] = ml[u].x;
-            if (ml[u].x != -INFINITY) {
-              const float mn = fmaxf(M, ml[u].x);
-              L = L * exp2f(M - mn) + ml[u].y * exp2f(ml[u].x - mn);
-              M = mn;
-            }
-          }
-        }
-        const float inv_l = L > 0.f ? 1.f / L : 0.f;
-        for (int sp = 0; sp < nsp; ++sp) {
-          const float m = wsm[sp * 128 + t];
-          wsm[sp * 128 + t] = m == -INFINITY ? 0.f : exp2f(m - M) * inv_l;
-        }
-        softmax_sync();
-        // The partial tiles (contiguous per split) come in by bulk copy, up to three at a
-        // time; tile 0 keeps the running weighted sum. Lanes cover a row's 128 columns (one
-        // float4 each); a warp handles its 32 rows eight at a time.
+        float2* mls = reinterpret_cast<float2*>(gbase + MERGE_W);  // [nsp][128] (m, l)
+        float* wsm = reinterpret_cast<float*>(mls);                // weights over ml.x
         float4* tiles = reinterpret_cast<float4*>(gbase);
-        constexpr int T4 = MERGE_TILE / 16;
         const int live_rows = min(32, rows - (row0 + warp * 32));
         int sp = 0;
         uint32_t phase = 0;
@@ -721,7 +741,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
             // shared-memory accesses, ordered before the async-proxy copies
             asm volatile("fence.proxy.async.global;" ::: "memory");
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_expect_tx(bar(BAR_MERGE), cnt * MERGE_TILE);
+            mbar_expect_tx(bar(BAR_MERGE), cnt * MERGE_TILE + (first ? nsp * 1024 : 0));
+            if (first)
+              for (int c = 0; c < nsp; ++c)
+                bulk_load(smem_u32(mls + c * 128), a.ml + ((pbase + c) * a.rows_pad + row0) * 2,
+                          1024, bar(BAR_MERGE));
             for (int c = 0; c < cnt; ++c)
               bulk_load(base + (first ? c : c + 1) * MERGE_TILE,
                         a.o_part + ((pbase + sp + c) * a.rows_pad + row0) * 128, MERGE_TILE,
@@ -729,38 +753,61 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           }
           if (!(ok = warp_wait(bar(BAR_MERGE), phase, abort))) break;
           phase ^= 1;
+          if (first) {
+            // log-sum-exp weights of every split for this thread's row (m in log2 units)
+            float M = -INFINITY, L = 0.f;
+            for (int c = 0; c < nsp; ++c) {
+              const float2 ml = mls[c * 128 + t];
+              if (ml.x != -INFINITY) {
+                const float mn = fmaxf(M, ml.x);
+                L = L * exp2f(M - mn) + ml.y * exp2f(ml.x - mn);
+                M = mn;
+              }
+            }
+            const float inv_l = L > 0.f ? 1.f / L : 0.f;
+            for (int c = 0; c < nsp; ++c) {
+              const float m = mls[c * 128 + t].x;
+              wsm[c * 256 + 2 * t] = m == -INFINITY ? 0.f : exp2f(m - M) * inv_l;
+            }
+            softmax_sync();
+          }
           const int c0 = first ? 1 : 0;  // tile c + 1 holds split sp + c + c0
+          // shared-space addresses: tile t, row, this lane's float4; weight of split c, row
+          const uint32_t wbase = base + MERGE_W;
+          auto taddr = [&](int tile, int row) { return base + tile * MERGE_TILE + row * 512 + lane * 16; };
+          auto waddr = [&](int c, int row) { return wbase + (uint32_t)(c * 1024 + row * 8); };
           for (int rr0 = 0; rr0 < live_rows; rr0 += 8) {
             float4 acc[8], y[8][2];
-            float w[8][3];
+            float w0[8], wy[8][2];  // static indices only: these stay in registers
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               const int row = warp * 32 + rr0 + u;
-              acc[u] = tiles[row * 32 + lane];
+              acc[u] = lds128(taddr(0, row));
+              w0[u] = lds32(waddr(sp, row));
 #pragma unroll
-              for (int c = 0; c < 2; ++c)
-                y[u][c] = tiles[(c + 1) * T4 + row * 32 + lane];
-#pragma unroll
-              for (int c = 0; c < 3; ++c) w[u][c] = sp + c < nsp ? wsm[(sp + c) * 128 + row] : 0.f;
+              for (int c = 0; c < 2; ++c) {
+                y[u][c] = lds128(taddr(c + 1, row));
+                wy[u][c] = lds32(waddr(sp + c + c0, row));
+              }
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               float4 x = acc[u];
-              if (first) {
-                x = make_float4(x.x * w[u][0], x.y * w[u][0], x.z * w[u][0], x.w * w[u][0]);
-              }
+              if (first) x = make_float4(x.x * w0[u], x.y * w0[u], x.z * w0[u], x.w * w0[u]);
 #pragma unroll
               for (int c = 0; c < 2; ++c) {
-                if (c + c0 < cnt) {
-                  const float wc = w[u][c + c0];
-                  x.x += wc * y[u][c].x;
-                  x.y += wc * y[u][c].y;
-                  x.z += wc * y[u][c].z;
-                  x.w += wc * y[u][c].w;
+                if (c + c0 < cnt) {  // a tile past cnt holds stale bytes (maybe NaN)
+                  x.x += wy[u][c] * y[u][c].x;
+                  x.y += wy[u][c] * y[u][c].y;
+                  x.z += wy[u][c] * y[u][c].z;
+                  x.w += wy[u][c] * y[u][c].w;
                 }
               }
-              if (rr0 + u < live_rows) tiles[(warp * 32 + rr0 + u) * 32 + lane] = x;
+              acc[u] = x;
             }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (rr0 + u < live_rows) sts128(taddr(0, warp * 32 + rr0 + u), acc[u]);
           }
           softmax_sync();
           sp += cnt;
