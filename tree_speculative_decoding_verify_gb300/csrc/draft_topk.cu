@@ -40,11 +40,11 @@ constexpr int A_THREADS = 512;  // 16 warps: the request's merge gives every row
 constexpr int A_WARPS = A_THREADS / 32;
 constexpr int MAX_CHUNKS = 32;
 constexpr int MIN_CHUNK = 1024;     // vocab entries per chunk at least (4 per thread)
-constexpr int CAP = 256;            // per-warp candidate buffer (shared memory)
-constexpr int BATCH = 16;           // buffered candidates that trigger a list update
-                                    // (a step adds at most 4 * 32: CAP > BATCH + 128)
-constexpr int BULK = 64;            // from this many on, a tournament instead of insertions
-constexpr int MERGE_SLOTS = 1 + CAP / 32;  // entries a lane holds in a warp merge
+constexpr int GROUPS = 32;         // buffered groups of four entries per warp
+constexpr int CTAS_PER_SM = 2;      // resident CTAs of the level kernel (launch bounds)
+// the request merge stages rows x chunks x k (value, index) pairs in shared memory
+// (and the rows' k cumulative scores and tokens)
+constexpr int MERGE_SMEM_MAX = TSV_MAX_TOPK * (MAX_CHUNKS + 1) * TSV_MAX_TOPK * 8;
 constexpr float L2E = 1.4426950408889634f;
 
 struct ChunkStat {
@@ -187,16 +187,13 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 struct TopkSmem {
-  float bv[A_WARPS][CAP];                      // per-warp candidates (warp-owned)
-  int bi[A_WARPS][CAP];
+  float4 gv[A_WARPS][GROUPS];                  // per-warp buffered groups (warp-owned)
+  int gi[A_WARPS][GROUPS];                     // index of a group's first entry
   float lv[A_WARPS][KMAX];                     // warp lists at the end of a unit
   int li[A_WARPS][KMAX];
-  int cnt[A_WARPS];                            // buffered candidates per warp
   float red[A_WARPS];
   float shi[A_WARPS], slo[A_WARPS];
   unsigned gthr;                               // ord() of the best warp threshold
-  float cu[KMAX * KMAX];
-  int tok[KMAX * KMAX];
   bool last;
 };
 
@@ -222,84 +219,58 @@ struct Lse {
   }
 };
 
+// Inverse of ord().
+__device__ __forceinline__ float unord(unsigned o) {
+  return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
 // Streaming state of one thread for one (row, chunk) unit. The warp's top-k list lives
-// in registers, entry r in lane r (lanes >= nl hold (-inf, INT_MAX)); the threshold is
-// its k-th entry once it has k. Candidates that beat the threshold are buffered in the
-// warp's shared-memory slice and folded into the list in batches.
+// in registers, entry r in lane r for r < k; entries not yet filled are placeholders
+// (-inf, INT_MAX) that every real entry beats. A group of four entries whose largest
+// beats the filter is buffered whole in the warp's shared-memory slice (one slot per
+// lane, positions from a ballot: no atomics); the list absorbs the buffer when it is
+// full and at the end of the unit.
 struct UnitState {
   Lse lse;
   float lv;     // this lane's list entry
   int li;
-  float thr_v;  // warp-uniform threshold
-  int thr_i;
-  int nl;       // warp-uniform list length
-  int cnt;      // warp-uniform number of buffered candidates
+  float thr;    // group filter: the larger of the warp's k-th value and the CTA-wide bound
+  int cnt;      // warp-uniform number of buffered groups
   int groups;   // float4 groups since the last flush
 };
 
-__device__ __forceinline__ void set_threshold(TopkSmem& sm, UnitState& u, int lane, int k) {
-  if (u.nl == k) {
-    u.thr_v = __shfl_sync(FULL, u.lv, k - 1);
-    u.thr_i = __shfl_sync(FULL, u.li, k - 1);
-    // k entries of the unit are >= thr_v, so nothing below it reaches the unit's top k:
-    // every warp may filter with the largest such value
-    if (lane == 0) atomicMax(&sm.gthr, ord(u.thr_v));
-  }
-}
-
-// Folds the warp's buffered candidates into its list: a tournament over list and buffer
-// when many are buffered, else one ballot insertion per candidate (position = number of
-// better list entries; the entries below shift one lane down).
-__device__ __forceinline__ void fold(TopkSmem& sm, UnitState& u, int warp, int lane, int k) {
+// The list absorbs the buffered groups: lane t takes group t (four entries) beside its
+// own list entry, sorts the five, and k rounds of a warp tournament pick the new list.
+// Entries at or past `end` are placeholders. The warp's k-th value then bounds the
+// unit's top k from below (k entries are at least that large), so every warp may filter
+// with the largest such value (an atomicMax of its ord() image).
+__device__ __forceinline__ void fold(TopkSmem& sm, UnitState& u, int warp, int lane, int k,
+                                     int end) {
   __syncwarp();
-  const int n = u.cnt;
-  if (n >= BULK) {
-    float v[MERGE_SLOTS];
-    int ix[MERGE_SLOTS];
-    v[0] = lane < u.nl ? u.lv : -INFINITY;
-    ix[0] = lane < u.nl ? u.li : INT_MAX;
+  float v[5];
+  int ix[5];
+  v[0] = u.lv;
+  ix[0] = u.li;
+  const bool have = lane < u.cnt;
+  const float4 g = have ? sm.gv[warp][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+  const int e = have ? sm.gi[warp][lane] : end;
+  const float gq[4] = {g.x, g.y, g.z, g.w};
 #pragma unroll
-    for (int t = 1; t < MERGE_SLOTS; ++t) {
-      const int j = lane + 32 * (t - 1);
-      v[t] = j < n ? sm.bv[warp][j] : -INFINITY;
-      ix[t] = j < n ? sm.bi[warp][j] : INT_MAX;
-    }
-    const int total = min(k, u.nl + n);
-    sort_entries(v, ix);
-    warp_select(v, ix, total, lane, u.lv, u.li);
-    u.nl = total;
-  } else {
-    for (int j = 0; j < n; ++j) {
-      const float cv = sm.bv[warp][j];
-      const int ci = sm.bi[warp][j];
-      if (u.nl == k && !better(cv, ci, u.thr_v, u.thr_i)) continue;  // warp-uniform
-      const int pos = __popc(__ballot_sync(FULL, lane < u.nl && better(u.lv, u.li, cv, ci)));
-      const float up_v = __shfl_up_sync(FULL, u.lv, 1);
-      const int up_i = __shfl_up_sync(FULL, u.li, 1);
-      if (lane == pos) { u.lv = cv; u.li = ci; }
-      else if (lane > pos) { u.lv = up_v; u.li = up_i; }
-      u.nl = min(k, u.nl + 1);
-      if (lane >= u.nl) { u.lv = -INFINITY; u.li = INT_MAX; }
-      if (u.nl == k) {
-        u.thr_v = __shfl_sync(FULL, u.lv, k - 1);
-        u.thr_i = __shfl_sync(FULL, u.li, k - 1);
-      }
-    }
+  for (int q = 0; q < 4; ++q) {
+    v[1 + q] = e + q < end ? gq[q] : -INFINITY;
+    ix[1 + q] = e + q < end ? e + q : INT_MAX;
   }
+  sort_entries(v, ix);
+  warp_select(v, ix, k, lane, u.lv, u.li);
   u.cnt = 0;
-  __syncwarp();
-  if (lane == 0) sm.cnt[warp] = 0;
-  set_threshold(sm, u, lane, k);
-  __syncwarp();
+  const float thr_v = __shfl_sync(FULL, u.lv, k - 1);
+  if (lane == 0) atomicMax(&sm.gthr, ord(thr_v));
+  u.thr = fmaxf(thr_v, unord(*reinterpret_cast<volatile unsigned*>(&sm.gthr)));
+  __syncwarp();  // the buffer slots are free again
 }
 
-// Four consecutive entries e .. e + 3 (those at or past `end` are -inf and skipped): their
-// max against the running maximum, four exp2 terms, and the entries that beat both the
-// warp threshold and the CTA-wide bound `g` (an ord() image) appended to the warp's
-// buffer (a shared-memory counter: usually one lane at a time gets here). Warp-uniform
-// call.
-__device__ __forceinline__ void consider4(TopkSmem& sm, UnitState& u, int warp, int lane, int k,
-                                          float4 a, int e, int end, unsigned g) {
+// Log-sum-exp terms of four entries (-inf entries give zero terms).
+__device__ __forceinline__ void lse4(UnitState& u, float4 a) {
   const float m4 = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
   if (m4 > u.lse.ref + RAISE) u.lse.raise(m4);
   const float r = u.lse.ref;
@@ -308,23 +279,49 @@ __device__ __forceinline__ void consider4(TopkSmem& sm, UnitState& u, int warp, 
     u.lse.flush();
     u.groups = 0;
   }
-  const bool maybe = m4 >= u.thr_v && ord(m4) >= g;
-  if (maybe) {  // divergent and rare
-    const float xv[4] = {a.x, a.y, a.z, a.w};
+}
+
+// One streaming step: the log-sum-exp terms of entries e .. e + 3 and, when their largest
+// beats the filter, the group into the warp's buffer (the list absorbs the buffer first
+// when the new groups would not fit). Every fourth step the filter takes up the CTA-wide
+// bound. Warp-uniform call.
+__device__ __forceinline__ void step4(TopkSmem& sm, UnitState& u, int warp, int lane, int k,
+                                      float4 a, int e, int end) {
+  lse4(u, a);
+  if (u.groups == 0) u.thr = fmaxf(u.thr, unord(*reinterpret_cast<volatile unsigned*>(&sm.gthr)));
+  const float m4 = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
+  const bool q = m4 >= u.thr;
+  const unsigned bal = __ballot_sync(FULL, q);
+  if (bal) {  // warp-uniform and rare once the list holds k entries
+    const int n = __popc(bal);
+    if (u.cnt + n > GROUPS) fold(sm, u, warp, lane, k, end);
+    if (q) {
+      const int pos = u.cnt + __popc(bal & ((1u << lane) - 1u));
+      sm.gv[warp][pos] = a;
+      sm.gi[warp][pos] = e;
+    }
+    u.cnt += n;
+  }
+}
+
+// A short unit (at most 4 N entries per lane, all already in registers): the warp's list
+// comes straight from a tournament over the lanes' sorted entries; nothing is buffered.
+template <int N>
+__device__ __forceinline__ void direct_select(UnitState& u, const float4 (&g)[N / 4],
+                                              const int (&e)[N / 4], int end, int lane, int k) {
+  float v[N];
+  int ix[N];
+#pragma unroll
+  for (int s = 0; s < N / 4; ++s) {
+    const float gq[4] = {g[s].x, g[s].y, g[s].z, g[s].w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      if (e + q < end && ord(xv[q]) >= g && better(xv[q], e + q, u.thr_v, u.thr_i)) {
-        const int pos = atomicAdd(&sm.cnt[warp], 1);
-        sm.bv[warp][pos] = xv[q];
-        sm.bi[warp][pos] = e + q;
-      }
+      v[4 * s + q] = e[s] + q < end ? gq[q] : -INFINITY;
+      ix[4 * s + q] = e[s] + q < end ? e[s] + q : INT_MAX;
     }
   }
-  if (__any_sync(FULL, maybe)) {
-    __syncwarp();
-    u.cnt = sm.cnt[warp];
-    if (u.cnt >= BATCH) fold(sm, u, warp, lane, k);
-  }
+  sort_entries(v, ix);
+  warp_select(v, ix, k, lane, u.lv, u.li);
 }
 
 // Seed of the CTA-wide bound from the warps' maxima of the unit's first entries (in
@@ -341,18 +338,15 @@ __device__ __forceinline__ void seed_threshold(TopkSmem& sm, int lane, int k) {
   if (lane < A_WARPS && rank == k - 1) sm.gthr = ord(m);
 }
 
-// Starts a unit's per-thread state (sm.gthr and sm.cnt were reset before the CTA's last
-// barrier).
-__device__ __forceinline__ void unit_begin(UnitState& u, float ref) {
+// Starts a unit's per-thread state (sm.gthr was set before the CTA's last barrier).
+__device__ __forceinline__ void unit_begin(UnitState& u, float ref, unsigned gthr) {
   u.lse.ref = fmaxf(ref, -FLT_MAX);  // finite, so x = -inf gives a zero term
   u.lse.g = 0.f;
   u.lse.hi = 0.f;
   u.lse.lo = 0.f;
   u.lv = -INFINITY;
   u.li = INT_MAX;
-  u.thr_v = -INFINITY;
-  u.thr_i = INT_MAX;
-  u.nl = 0;
+  u.thr = unord(gthr);
   u.cnt = 0;
   u.groups = 0;
 }
@@ -375,29 +369,54 @@ struct LevelArgs {
 
 // The request's merge, run by the CTA that finished its last unit: every row's chunk
 // lists and exp-sums combine into the row's top-k log-probabilities and cumulative
-// scores (written to the store), then the joint top-K over the rows. Out of line: it
-// is rare, and inlined its registers would crowd the streaming loop.
-__device__ __noinline__ void request_merge(TopkSmem& sm, const LevelArgs& p, int b) {
+// scores (written to the store), then the joint top-K over the rows. The request's chunk
+// lists are staged in (dynamic) shared memory with one cooperative load; each merge is k
+// rounds of a warp tournament over list heads, the winning lane stepping its pointer, so
+// no list is held in registers. Out of line: it is rare, and inlined its registers would
+// crowd the streaming loop.
+__device__ __noinline__ void request_merge(const LevelArgs& p, int b) {
+  extern __shared__ float4 dyn_smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = p.k, rows = p.rows, chunks = p.chunks;
   const int off = p.level == 1 ? 0 : k + (p.level - 2) * k * k;
   const int64_t srow = (int64_t)b * p.store_cap;
-  // Warp s merges row s (rows <= 16 <= warps): lane c holds chunk c's sorted list of the
-  // row in registers.
-  static_assert(A_WARPS >= TSV_MAX_TOPK, "one warp per frontier row");
-  if (warp < rows) {
-    const int s = warp, r0 = b * rows + s;
-    const bool have = lane < chunks;
-    const size_t g = (size_t)r0 * chunks + lane;
-    float cv[KMAX];
-    int ci[KMAX];
-    float4 cs = make_float4(-INFINITY, 0.f, 0.f, 0.f);
-    if (have) cs = __ldcg(reinterpret_cast<const float4*>(&p.ws.stat[g]));
+  // lists of the request: entry j of (row s, chunk c) at (s * chunks + c) * k + j
+  const int n = rows * chunks * k;
+  float* mv = reinterpret_cast<float*>(dyn_smem);
+  int* mi = reinterpret_cast<int*>(mv + n);
+  // the rows' cumulative scores and tokens (flat = row * k + j); through the declared
+  // shared array the compiler emits shared-memory accesses (a generic pointer to the
+  // static struct measured several times slower per tournament round)
+  float* cu_s = reinterpret_cast<float*>(mi + n);
+  int* tok_s = reinterpret_cast<int*>(cu_s + rows * k);
+  const size_t g0 = (size_t)b * n;
+  // eight loads per thread in flight before any store: one L2 round trip per 4096 entries
+  for (int t0 = tid; t0 < n; t0 += 8 * A_THREADS) {
+    float v8[8];
+    int i8[8];
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      cv[j] = have && j < k ? __ldcg(p.ws.val + g * k + j) : -INFINITY;
-      ci[j] = have && j < k ? __ldcg(p.ws.idx + g * k + j) : INT_MAX;
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + u * A_THREADS;
+      v8[u] = t < n ? __ldcg(p.ws.val + g0 + t) : 0.f;
+      i8[u] = t < n ? __ldcg(p.ws.idx + g0 + t) : 0;
     }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int t = t0 + u * A_THREADS;
+      if (t < n) {
+        mv[t] = v8[u];
+        mi[t] = i8[u];
+      }
+    }
+  }
+  static_assert(A_WARPS >= TSV_MAX_TOPK, "one warp per frontier row");
+  const int s = warp, r0 = b * rows + s;
+  float4 cs = make_float4(-INFINITY, 0.f, 0.f, 0.f);
+  if (warp < rows && lane < chunks)
+    cs = __ldcg(reinterpret_cast<const float4*>(&p.ws.stat[(size_t)r0 * chunks + lane]));
+  __syncthreads();
+  if (warp < rows) {
+    // warp s merges row s: lane c walks chunk c's sorted list
     const float pscore = p.level == 1 ? 0.0f : p.front_score_in[r0];
     const int pstore = p.level == 1 ? -1 : p.front_store_in[r0];
     float Rr = cs.x, sh = cs.y, sl = cs.z;
@@ -405,9 +424,24 @@ __device__ __noinline__ void request_merge(TopkSmem& sm, const LevelArgs& p, int
     // log(hi + lo) = log(hi) + log1p(lo / hi); |lo / hi| is below an ulp, so the second
     // term is lo / hi
     const float lse_hi = Rr, lse_mid = logf(sh), lse_lo = sl / sh;
-    float v;
-    int i;
-    warp_select(cv, ci, k, lane, v, i);
+    const bool have = lane < chunks;
+    const int lb = (s * chunks + lane) * k;
+    int ptr = 0;
+    float hv = have ? mv[lb] : -INFINITY;
+    int hi = have ? mi[lb] : INT_MAX;
+    float v = -INFINITY;
+    int i = INT_MAX;
+    for (int r = 0; r < k; ++r) {
+      float wv = hv;
+      int wi = hi, who = lane;
+      warp_argmax(wv, wi, who);
+      if (lane == r) { v = wv; i = wi; }
+      if (lane == who) {
+        ++ptr;
+        hv = ptr < k ? mv[lb + ptr] : -INFINITY;
+        hi = ptr < k ? mi[lb + ptr] : INT_MAX;
+      }
+    }
     if (lane < k) {
       const float logp = ((v - lse_hi) - lse_mid) - lse_lo;
       const float cu = pscore + logp;
@@ -415,34 +449,31 @@ __device__ __noinline__ void request_merge(TopkSmem& sm, const LevelArgs& p, int
       p.store_token[srow + off + flat] = i;
       p.store_score[srow + off + flat] = cu;
       p.store_parent[srow + off + flat] = pstore;
-      sm.cu[flat] = cu;
-      sm.tok[flat] = i;
+      cu_s[flat] = cu;
+      tok_s[flat] = i;
     }
   }
   __syncthreads();
 
-  // Joint top-K over the rows * K cumulative scores (ties to the lower flat index).
-  if (warp == 0) {
-    const int n = rows * k;
-    float v[KMAX * KMAX / 32];
-    int ix[KMAX * KMAX / 32];
-#pragma unroll
-    for (int j = 0; j < KMAX * KMAX / 32; ++j) {
-      const int f = lane + 32 * j;
-      v[j] = f < n ? sm.cu[f] : -INFINITY;
-      ix[j] = f < n ? f : INT_MAX;
+  // Joint top-K over the rows * K cumulative scores (ties to the lower flat index): entry
+  // f's rank is the number of entries better than it; the K of rank below K are the
+  // frontier, written to their rank.
+  const int nf = rows * k;
+  if (tid < nf) {
+    const float cv = cu_s[tid];
+    int rank = 0;
+#pragma unroll 4
+    for (int u = 0; u < nf; ++u) {
+      const float o = cu_s[u];
+      rank += (o > cv || (o == cv && u < tid)) ? 1 : 0;
     }
-    sort_entries(v, ix);
-    float bv;
-    int bi;
-    warp_select(v, ix, k, lane, bv, bi);
-    if (lane < k) {
-      p.front_token_out[b * k + lane] = sm.tok[bi];
-      p.front_score_out[b * k + lane] = bv;
-      p.front_store_out[b * k + lane] = off + bi;
+    if (rank < k) {
+      p.front_token_out[b * k + rank] = tok_s[tid];
+      p.front_score_out[b * k + rank] = cv;
+      p.front_store_out[b * k + rank] = off + tid;
     }
-    if (lane == 0) p.ws.tickets[b] = 0u;
   }
+  if (tid == 0) p.ws.tickets[b] = 0u;
   __syncthreads();
 }
 
@@ -450,13 +481,12 @@ __device__ __noinline__ void request_merge(TopkSmem& sm, const LevelArgs& p, int
 // (ref, sum), written to the workspace; the last unit of a request to finish (an atomic
 // ticket) then merges every row of the request and runs the joint top-K. Called by the
 // whole CTA.
-__device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int row, int chunk) {
+__device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int row, int chunk,
+                            int end) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = p.k, rows = p.rows, chunks = p.chunks;
   u.lse.flush();
-  __syncwarp();
-  u.cnt = sm.cnt[warp];
-  if (u.cnt > 0) fold(sm, u, warp, lane, k);  // the warp's final best k
+  if (u.cnt > 0) fold(sm, u, warp, lane, k, end);  // the warp's final best k
   if (lane < k) { sm.lv[warp][lane] = u.lv; sm.li[warp][lane] = u.li; }
 
   // exp-sum over the block
@@ -500,11 +530,11 @@ __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int 
   __syncthreads();
   if (!sm.last) return;
   __threadfence();
-  request_merge(sm, p, b);
+  request_merge(p, b);
 }
 
 // ---- streaming: one (row, chunk) unit per CTA -----------------------------------------
-__global__ void __launch_bounds__(A_THREADS, 2)
+__global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
 topk_level_kernel(const LevelArgs p, bool vec) {
   __shared__ TopkSmem sm;
   const int row = blockIdx.y, chunk = blockIdx.x;
@@ -534,25 +564,40 @@ topk_level_kernel(const LevelArgs p, bool vec) {
   float first = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
-  if (lane == 0) { sm.red[warp] = first; sm.cnt[warp] = 0; }
-  if (tid == 0) sm.gthr = 0u;
+  if (lane == 0) sm.red[warp] = first;
+  if (tid == 0) sm.gthr = ord(-INFINITY);
   __syncthreads();
-  if (warp == 0 && steps > 1) seed_threshold(sm, lane, p.k);
+  if (warp == 0 && steps > 2) seed_threshold(sm, lane, p.k);
   first = sm.red[0];
 #pragma unroll
   for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, sm.red[w]);
   __syncthreads();  // sm.red is reused by finish_unit; sm.gthr is seeded
   UnitState u;
-  unit_begin(u, first);
+  unit_begin(u, first, sm.gthr);
 
-  for (int it = 0; it < steps; ++it) {
-    const float4 c = it + 2 < steps ? load4(it + 2) : none;
-    consider4(sm, u, warp, lane, p.k, a, start + 4 * (it * A_THREADS + tid), end,
-              *reinterpret_cast<volatile unsigned*>(&sm.gthr));
-    a = bnext;
-    bnext = c;
+  const int e0 = start + 4 * tid;
+  if (steps <= 2) {
+    // short unit (one or two steps): no buffering, the list straight from registers
+    lse4(u, a);
+    if (steps == 2) {
+      lse4(u, bnext);
+      const float4 g[2] = {a, bnext};
+      const int e[2] = {e0, e0 + 4 * A_THREADS};
+      direct_select<8>(u, g, e, end, lane, p.k);
+    } else {
+      const float4 g[1] = {a};
+      const int e[1] = {e0};
+      direct_select<4>(u, g, e, end, lane, p.k);
+    }
+  } else {
+    for (int it = 0; it < steps; ++it) {
+      const float4 c = it + 2 < steps ? load4(it + 2) : none;
+      step4(sm, u, warp, lane, p.k, a, e0 + 4 * it * A_THREADS, end);
+      a = bnext;
+      bnext = c;
+    }
   }
-  finish_unit(sm, u, p, row, chunk);
+  finish_unit(sm, u, p, row, chunk, end);
 }
 
 // ---- final selection --------------------------------------------------------------
@@ -639,8 +684,9 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
 TopkPlan plan_topk(int batch, int rows, int vocab, int top_k) {
   TopkPlan p{};
   const int64_t rows_total = (int64_t)batch * rows;
-  const int64_t target = 4LL * device_sm_count();
-  int chunks = (int)std::min<int64_t>(MAX_CHUNKS, std::max<int64_t>(1, ceil_div(target, rows_total)));
+  // as many chunks per row as keep every unit in one wave of resident CTAs
+  const int64_t slots = (int64_t)CTAS_PER_SM * device_sm_count();
+  int chunks = (int)std::min<int64_t>(MAX_CHUNKS, std::max<int64_t>(1, slots / std::max<int64_t>(1, rows_total)));
   // at least MIN_CHUNK entries per chunk, lengths a multiple of 4
   chunks = (int)std::max<int64_t>(1, std::min<int64_t>(chunks, ceil_div(vocab, MIN_CHUNK)));
   int chunk_len = (int)round_up(ceil_div(vocab, chunks), 4);
@@ -681,7 +727,17 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
   p.front_store_out = front_store_out;
   const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (row_stride % 4 == 0);
   dim3 grid(plan.chunks, rows_total);
-  topk_level_kernel<<<grid, A_THREADS, 0, stream>>>(p, vec);
+  const size_t smem = (size_t)rows * (plan.chunks + 1) * top_k * (sizeof(float) + sizeof(int32_t));
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (smem > 48 * 1024 && dev >= 0 && dev < 64 && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(topk_level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             MERGE_SMEM_MAX) != cudaSuccess)
+      return launch_status();
+    attr_set[dev] = true;
+  }
+  topk_level_kernel<<<grid, A_THREADS, smem, stream>>>(p, vec);
   return launch_status();
 }
 
