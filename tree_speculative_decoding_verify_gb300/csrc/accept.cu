@@ -8,7 +8,7 @@
 // 验证:在树上走一条路径 (the walk follows the next_token / next_sibling lists) and
 // section 接受之后:KV 从树形搬回线性 (the accepted KV moves to consecutive slots).
 //
-// One CTA per (request, group of 8 copy units); a copy unit is one (layer, kv head,
+// One CTA per (request, copy unit); a copy unit is one (layer, kv head,
 // keys-or-values) plane. Every CTA of a request repeats the (tiny) walk from shared
 // memory, so no CTA waits for another.
 #include "common.cuh"
@@ -18,7 +18,7 @@ namespace tsv {
 namespace {
 
 constexpr int THREADS = 128;
-constexpr int UNITS_PER_CTA = 8;
+constexpr int UNITS_PER_CTA = 1;  // copy units per CTA: each CTA pays one load round trip
 constexpr int MAX_ROW_BYTES = 128 * 4;  // head_dim 128 in f32
 
 struct CacheView {

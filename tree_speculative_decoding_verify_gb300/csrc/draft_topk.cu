@@ -601,53 +601,19 @@ topk_level_kernel(const LevelArgs p, bool vec) {
 }
 
 // ---- final selection --------------------------------------------------------------
-// Bitonic sort of 64-bit keys (descending score, then ascending store index) in shared
-// memory; the first total_tokens keys are the kept candidates, numbered in ascending
-// store index by a block prefix sum.
+// The total_tokens-th best key (ord() of the score) by a three-pass radix select over
+// shared-memory histograms (11, 11 and 10 bits); the kept candidates are the keys above
+// it plus, in ascending store index, as many of the keys equal to it as are still
+// needed. Node numbers (ascending store index) come from a block prefix sum.
 constexpr int F_THREADS = 512;
+constexpr int F_MAX = 4096;   // candidates per request
+constexpr int F_BINS = 2048;  // histogram bins of the widest pass
 
-__device__ __forceinline__ uint64_t sel_key(float score, int idx) {
-  uint32_t u = __float_as_uint(score);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // ascending float order as unsigned
-  return ((uint64_t)(~u) << 32) | (uint32_t)idx;     // ascending key = descending score
-}
-
-__global__ void __launch_bounds__(F_THREADS)
-select_final_kernel(const int32_t* __restrict__ store_token, const float* __restrict__ store_score,
-                    const int32_t* __restrict__ store_parent, int C, int npow2, int store_cap,
-                    int total, const int32_t* __restrict__ root_token, int max_nodes,
-                    int32_t* __restrict__ tokens, int32_t* __restrict__ parents,
-                    int32_t* __restrict__ num_nodes) {
-  extern __shared__ unsigned char smem[];
-  uint64_t* s_key = reinterpret_cast<uint64_t*>(smem);          // [npow2]
-  int* s_node = reinterpret_cast<int*>(s_key + npow2);          // [C]
-  __shared__ int s_warp[F_THREADS / 32];
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t srow = (int64_t)b * store_cap;
-  for (int c = tid; c < npow2; c += F_THREADS)
-    s_key[c] = c < C ? sel_key(store_score[srow + c], c) : ~0ull;
-  for (int c = tid; c < C; c += F_THREADS) s_node[c] = 0;
-  __syncthreads();
-  for (int size = 2; size <= npow2; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = tid; t < npow2 / 2; t += F_THREADS) {
-        const int lo = 2 * t - (t & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const uint64_t a = s_key[lo], c = s_key[hi];
-        if ((a > c) == up) { s_key[lo] = c; s_key[hi] = a; }
-      }
-      __syncthreads();
-    }
-  }
-  for (int r = tid; r < total; r += F_THREADS) s_node[(int)(s_key[r] & 0xffffffffu)] = 1;
-  __syncthreads();
-  // Node numbers in ascending store index: each thread owns a contiguous segment.
-  const int seg = (C + F_THREADS - 1) / F_THREADS;
-  const int c0 = min(C, tid * seg), c1 = min(C, c0 + seg);
-  int mine = 0;
-  for (int c = c0; c < c1; ++c) mine += s_node[c];
-  int incl = mine;
+// Exclusive prefix sum of x over the block (thread order); s_warp holds F_THREADS / 32
+// partials. Ends with a barrier, so s_warp may be reused at once.
+__device__ __forceinline__ int block_exclusive_scan(int x, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = x;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int n = __shfl_up_sync(FULL, incl, o);
@@ -655,11 +621,81 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
   }
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
-  int before = incl - mine;
+  int before = incl - x;
   for (int w = 0; w < warp; ++w) before += s_warp[w];
-  for (int c = c0; c < c1; ++c) {
-    if (s_node[c]) s_node[c] = 1 + before++;
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(F_THREADS)
+select_final_kernel(const int32_t* __restrict__ store_token, const float* __restrict__ store_score,
+                    const int32_t* __restrict__ store_parent, int C, int store_cap,
+                    int total, const int32_t* __restrict__ root_token, int max_nodes,
+                    int32_t* __restrict__ tokens, int32_t* __restrict__ parents,
+                    int32_t* __restrict__ num_nodes) {
+  __shared__ unsigned s_key[F_MAX];
+  __shared__ int s_node[F_MAX];
+  __shared__ unsigned s_hist[F_BINS];
+  __shared__ int s_warp[F_THREADS / 32];
+  __shared__ unsigned s_sel[2];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int64_t srow = (int64_t)b * store_cap;
+  for (int c = tid; c < C; c += F_THREADS) s_key[c] = ord(store_score[srow + c]);
+
+  // radix select: after the passes, `prefix` is the total-th largest key and `need` the
+  // number of candidates with exactly that key that are kept (the lowest store indices)
+  unsigned prefix = 0;
+  int need = total;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int bits = pass == 2 ? 10 : 11;
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int nb = 1 << bits, per = nb / F_THREADS;
+    for (int i = tid; i < nb; i += F_THREADS) s_hist[i] = 0u;
+    __syncthreads();
+    for (int c = tid; c < C; c += F_THREADS) {
+      const unsigned key = s_key[c];
+      if (pass == 0 || (key >> (shift + bits)) == prefix) atomicAdd(&s_hist[(key >> shift) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    // thread t holds `per` bins from the top: nb - 1 - t * per downwards
+    int local = 0;
+    for (int q = 0; q < per; ++q) local += (int)s_hist[nb - 1 - (tid * per + q)];
+    int acc = block_exclusive_scan(local, s_warp);  // candidates in the bins above
+    if (acc < need && need <= acc + local) {
+      for (int q = 0; q < per; ++q) {
+        const int bin = nb - 1 - (tid * per + q);
+        const int n = (int)s_hist[bin];
+        if (acc + n >= need) {
+          s_sel[0] = (unsigned)bin;
+          s_sel[1] = (unsigned)acc;
+          break;
+        }
+        acc += n;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << bits) | s_sel[0];
+    need -= (int)s_sel[1];
+    __syncthreads();  // s_sel and s_hist are rewritten by the next pass
   }
+
+  // kept flags, then node numbers, over contiguous per-thread segments (store order)
+  const int seg = (C + F_THREADS - 1) / F_THREADS;
+  const int c0 = min(C, tid * seg), c1 = min(C, c0 + seg);
+  int eq = 0;
+  for (int c = c0; c < c1; ++c) eq += s_key[c] == prefix ? 1 : 0;
+  int e = block_exclusive_scan(eq, s_warp);
+  int mine = 0;
+  for (int c = c0; c < c1; ++c) {
+    const unsigned key = s_key[c];
+    const bool kept = key > prefix || (key == prefix && e++ < need);
+    s_node[c] = kept ? 1 : 0;
+    mine += kept ? 1 : 0;
+  }
+  int before = block_exclusive_scan(mine, s_warp);
+  for (int c = c0; c < c1; ++c)
+    if (s_node[c]) s_node[c] = 1 + before++;
   __syncthreads();
   const int64_t trow = (int64_t)b * max_nodes;
   for (int n = tid; n < max_nodes; n += F_THREADS) {
@@ -746,22 +782,11 @@ int launch_select_final(const int32_t* store_token, const float* store_score,
                         int store_cap, int total_tokens, const int32_t* root_token,
                         int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
                         cudaStream_t stream) {
-  int npow2 = 2;
-  while (npow2 < num_candidates) npow2 <<= 1;
-  const size_t smem = (size_t)npow2 * sizeof(uint64_t) + (size_t)num_candidates * sizeof(int);
-  if (smem > 48 * 1024) {
-    static bool attr = false;
-    if (!attr) {
-      if (cudaFuncSetAttribute(select_final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               64 * 1024) != cudaSuccess)
-        return launch_status();
-      attr = true;
-    }
-  }
-  select_final_kernel<<<batch, F_THREADS, smem, stream>>>(store_token, store_score, store_parent,
-                                                          num_candidates, npow2, store_cap,
-                                                          total_tokens, root_token, max_nodes,
-                                                          tokens, parents, num_nodes);
+  if (num_candidates > F_MAX) return TSV_ERR_INVALID_ARG;
+  select_final_kernel<<<batch, F_THREADS, 0, stream>>>(store_token, store_score, store_parent,
+                                                       num_candidates, store_cap, total_tokens,
+                                                       root_token, max_nodes, tokens, parents,
+                                                       num_nodes);
   return launch_status();
 }
 
