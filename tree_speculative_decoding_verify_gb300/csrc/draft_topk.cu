@@ -45,6 +45,8 @@ constexpr int CTAS_PER_SM = 2;      // resident CTAs of the level kernel (launch
 // the request merge stages rows x chunks x k (value, index) pairs in shared memory
 // (and the rows' k cumulative scores and tokens)
 constexpr int MERGE_SMEM_MAX = TSV_MAX_TOPK * (MAX_CHUNKS + 1) * TSV_MAX_TOPK * 8;
+// survivors of a unit's finish (value, index): at most 8 register entries per thread
+constexpr int SURV_MAX = 8 * A_THREADS;
 constexpr float L2E = 1.4426950408889634f;
 
 struct ChunkStat {
@@ -193,9 +195,18 @@ struct TopkSmem {
   int li[A_WARPS][KMAX];
   float red[A_WARPS];
   float shi[A_WARPS], slo[A_WARPS];
-  unsigned gthr;                               // ord() of the best warp threshold
+  unsigned long long gkey[A_THREADS / 8];      // best entry of each eight-lane group
+  unsigned long long gthr;                     // key() of the best warp threshold
+  unsigned long long tau;                      // bound of the unit's top k
+  int ns;                                      // survivors collected
   bool last;
 };
+
+// Order-preserving 64-bit image of an entry: larger value first, then lower index. Real
+// entries (index < INT_MAX) beat placeholders (-inf, INT_MAX) of the same value.
+__device__ __forceinline__ unsigned long long key(float v, int i) {
+  return ((unsigned long long)ord(v) << 32) | (unsigned)(~(unsigned)i);
+}
 
 // Per-thread log-sum-exp state: fp32 terms exp(x - ref) summed in groups of 16, each
 // group added exactly into an unevaluated (hi, lo) pair. The reference is raised (and
@@ -264,8 +275,9 @@ __device__ __forceinline__ void fold(TopkSmem& sm, UnitState& u, int warp, int l
   warp_select(v, ix, k, lane, u.lv, u.li);
   u.cnt = 0;
   const float thr_v = __shfl_sync(FULL, u.lv, k - 1);
-  if (lane == 0) atomicMax(&sm.gthr, ord(thr_v));
-  u.thr = fmaxf(thr_v, unord(*reinterpret_cast<volatile unsigned*>(&sm.gthr)));
+  const int thr_i = __shfl_sync(FULL, u.li, k - 1);
+  if (lane == 0) atomicMax(&sm.gthr, key(thr_v, thr_i));
+  u.thr = fmaxf(thr_v, unord((unsigned)(*reinterpret_cast<volatile unsigned long long*>(&sm.gthr) >> 32)));
   __syncwarp();  // the buffer slots are free again
 }
 
@@ -288,7 +300,8 @@ __device__ __forceinline__ void lse4(UnitState& u, float4 a) {
 __device__ __forceinline__ void step4(TopkSmem& sm, UnitState& u, int warp, int lane, int k,
                                       float4 a, int e, int end) {
   lse4(u, a);
-  if (u.groups == 0) u.thr = fmaxf(u.thr, unord(*reinterpret_cast<volatile unsigned*>(&sm.gthr)));
+  if (u.groups == 0)
+    u.thr = fmaxf(u.thr, unord((unsigned)(*reinterpret_cast<volatile unsigned long long*>(&sm.gthr) >> 32)));
   const float m4 = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
   const bool q = m4 >= u.thr;
   const unsigned bal = __ballot_sync(FULL, q);
@@ -304,26 +317,6 @@ __device__ __forceinline__ void step4(TopkSmem& sm, UnitState& u, int warp, int 
   }
 }
 
-// A short unit (at most 4 N entries per lane, all already in registers): the warp's list
-// comes straight from a tournament over the lanes' sorted entries; nothing is buffered.
-template <int N>
-__device__ __forceinline__ void direct_select(UnitState& u, const float4 (&g)[N / 4],
-                                              const int (&e)[N / 4], int end, int lane, int k) {
-  float v[N];
-  int ix[N];
-#pragma unroll
-  for (int s = 0; s < N / 4; ++s) {
-    const float gq[4] = {g[s].x, g[s].y, g[s].z, g[s].w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      v[4 * s + q] = e[s] + q < end ? gq[q] : -INFINITY;
-      ix[4 * s + q] = e[s] + q < end ? e[s] + q : INT_MAX;
-    }
-  }
-  sort_entries(v, ix);
-  warp_select(v, ix, k, lane, u.lv, u.li);
-}
-
 // Seed of the CTA-wide bound from the warps' maxima of the unit's first entries (in
 // sm.red): the k-th largest of the A_WARPS maxima (k <= A_WARPS) has k distinct entries at
 // or above it. Run by warp 0; sm.gthr is read after the next barrier.
@@ -335,18 +328,18 @@ __device__ __forceinline__ void seed_threshold(TopkSmem& sm, int lane, int k) {
     const float o = __shfl_sync(FULL, m, w);
     rank += (o > m || (o == m && w < lane)) ? 1 : 0;
   }
-  if (lane < A_WARPS && rank == k - 1) sm.gthr = ord(m);
+  if (lane < A_WARPS && rank == k - 1) sm.gthr = key(m, INT_MAX);
 }
 
 // Starts a unit's per-thread state (sm.gthr was set before the CTA's last barrier).
-__device__ __forceinline__ void unit_begin(UnitState& u, float ref, unsigned gthr) {
+__device__ __forceinline__ void unit_begin(UnitState& u, float ref, unsigned long long gthr) {
   u.lse.ref = fmaxf(ref, -FLT_MAX);  // finite, so x = -inf gives a zero term
   u.lse.g = 0.f;
   u.lse.hi = 0.f;
   u.lse.lo = 0.f;
   u.lv = -INFINITY;
   u.li = INT_MAX;
-  u.thr = unord(gthr);
+  u.thr = unord((unsigned)(gthr >> 32));
   u.cnt = 0;
   u.groups = 0;
 }
@@ -477,35 +470,115 @@ __device__ __noinline__ void request_merge(const LevelArgs& p, int b) {
   __syncthreads();
 }
 
-// End of a unit: the warps' final lists and exp-sums merge into the chunk's top-k and
-// (ref, sum), written to the workspace; the last unit of a request to finish (an atomic
-// ticket) then merges every row of the request and runs the joint top-K. Called by the
-// whole CTA.
+// End of a unit. Every entry that can still reach the unit's top k is collected in
+// shared memory by the whole CTA and ranked there. The bound tau is an entry key with k of
+// the unit's entries at or above it: the k-th best of 64 candidates -- the eight-lane
+// group maxima of a short unit, or the first four entries of every warp list when
+// streaming (there also at least the best warp threshold) -- or 0, which every entry
+// passes, when fewer than k candidates are entries. The survivors -- the warps' exact lists after a last
+// fold (streaming) or the lanes' register entries (short unit) at or above tau -- hold the
+// unit's top k; a survivor's rank is the number of survivors better than it. The last unit
+// of the request to finish (an atomic ticket) then merges the request's rows. Called by
+// the whole CTA; ng is the number of register groups per lane of a short unit (0 when
+// streaming).
 __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int row, int chunk,
-                            int end) {
+                            int end, int ng, float4 g0, float4 g1, int e0, int e1) {
+  extern __shared__ float4 dyn_smem[];
+  float* sv = reinterpret_cast<float*>(dyn_smem);
+  int* si = reinterpret_cast<int*>(sv + SURV_MAX);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = p.k, rows = p.rows, chunks = p.chunks;
   u.lse.flush();
-  if (u.cnt > 0) fold(sm, u, warp, lane, k, end);  // the warp's final best k
-  if (lane < k) { sm.lv[warp][lane] = u.lv; sm.li[warp][lane] = u.li; }
-
-  // exp-sum over the block
   float R = u.lse.ref, phi = u.lse.hi, plo = u.lse.lo;
   warp_combine(R, phi, plo);
   if (lane == 0) { sm.red[warp] = R; sm.shi[warp] = phi; sm.slo[warp] = plo; }
+  const float gv[2][4] = {{g0.x, g0.y, g0.z, g0.w}, {g1.x, g1.y, g1.z, g1.w}};
+  const int ge[2] = {e0, e1};
+  if (ng == 0) {
+    // the warp's exact top k (its last fold also raises the CTA-wide bound)
+    if (u.cnt > 0) fold(sm, u, warp, lane, k, end);
+    if (lane < k) { sm.lv[warp][lane] = u.lv; sm.li[warp][lane] = u.li; }
+    static_assert(A_THREADS / 8 == 4 * A_WARPS, "four list heads per warp");
+    if (lane < 4) sm.gkey[warp * 4 + lane] = lane < k ? key(u.lv, u.li) : 0ull;
+  } else {
+    unsigned long long best = 0ull;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (t < ng && ge[t] + q < end) best = max(best, key(gv[t][q], ge[t] + q));
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) best = max(best, __shfl_xor_sync(FULL, best, o));
+    if ((lane & 7) == 0) sm.gkey[tid >> 3] = best;
+  }
+  if (tid == 0) sm.ns = 0;
   __syncthreads();
-  if (warp == 0) {
-    // block top-k: the warps' sorted lists, lane w holds list w's head
-    int ptr = 0;
-    const size_t base = ((size_t)row * chunks + chunk) * k;
-    for (int r = 0; r < k; ++r) {
-      float v = lane < A_WARPS && ptr < k ? sm.lv[lane][ptr] : -INFINITY;
-      int i = lane < A_WARPS && ptr < k ? sm.li[lane][ptr] : INT_MAX;
-      int who = lane;
-      warp_argmax(v, i, who);
-      if (lane == who) ++ptr;
-      if (lane == 0) { p.ws.val[base + r] = v; p.ws.idx[base + r] = i; }
+  {
+    if (warp == 0) {
+      // rank of each group maximum among the 64 (ties by position); rank k - 1 is tau
+      const unsigned long long a0 = sm.gkey[lane], a1 = sm.gkey[lane + 32];
+      int r0 = 0, r1 = 0;
+#pragma unroll 8
+      for (int t = 0; t < A_THREADS / 8; ++t) {
+        const unsigned long long o = sm.gkey[t];
+        r0 += (o > a0 || (o == a0 && t < lane)) ? 1 : 0;
+        r1 += (o > a1 || (o == a1 && t < lane + 32)) ? 1 : 0;
+      }
+      if (r0 == k - 1) sm.tau = a0;
+      if (r1 == k - 1) sm.tau = a1;
     }
+    __syncthreads();
+  }
+  const unsigned long long tau = ng > 0 ? sm.tau : max(sm.tau, sm.gthr);
+
+  // survivors, appended with one shared-memory atomic per warp and entry slot
+  auto push = [&](bool keep, float v, int i) {  // warp-uniform call
+    const unsigned bal = __ballot_sync(FULL, keep);
+    if (bal) {
+      const int leader = __ffs(bal) - 1;
+      int at = 0;
+      if (lane == leader) at = atomicAdd(&sm.ns, __popc(bal));
+      at = __shfl_sync(FULL, at, leader);
+      if (keep) {
+        const int pos = at + __popc(bal & ((1u << lane) - 1u));
+        sv[pos] = v;
+        si[pos] = i;
+      }
+    }
+  };
+  if (ng == 0) {
+    // list entries: thread t holds entry t % KMAX of warp t / KMAX
+    const int w = tid / KMAX, j = tid % KMAX;
+    const bool in = tid < A_WARPS * KMAX && j < k;
+    const float v = in ? sm.lv[w][j] : -INFINITY;
+    const int i = in ? sm.li[w][j] : INT_MAX;
+    push(in && i != INT_MAX && key(v, i) >= tau, v, i);
+  } else {
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (t < ng) push(ge[t] + q < end && key(gv[t][q], ge[t] + q) >= tau, gv[t][q], ge[t] + q);
+  }
+  __syncthreads();
+  const int S = sm.ns;
+  const size_t base = ((size_t)row * chunks + chunk) * k;
+  for (int t = tid; t < S; t += A_THREADS) {
+    const float v = sv[t];
+    const int i = si[t];
+    int rank = 0;
+#pragma unroll 4
+    for (int s2 = 0; s2 < S; ++s2) {
+      const float o = sv[s2];
+      rank += (o > v || (o == v && si[s2] < i)) ? 1 : 0;
+    }
+    if (rank < k) { p.ws.val[base + rank] = v; p.ws.idx[base + rank] = i; }
+  }
+  for (int t = S + tid; t < k; t += A_THREADS) {  // fewer than k entries in the unit
+    p.ws.val[base + t] = -INFINITY;
+    p.ws.idx[base + t] = INT_MAX;
+  }
+  if (warp == A_WARPS - 1) {  // the block's exp-sum
     float rr = lane < A_WARPS ? sm.red[lane] : -INFINITY;
     float hh = lane < A_WARPS ? sm.shi[lane] : 0.f, ll = lane < A_WARPS ? sm.slo[lane] : 0.f;
     warp_combine(rr, hh, ll);
@@ -565,7 +638,7 @@ topk_level_kernel(const LevelArgs p, bool vec) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
   if (lane == 0) sm.red[warp] = first;
-  if (tid == 0) sm.gthr = ord(-INFINITY);
+  if (tid == 0) sm.gthr = 0ull;
   __syncthreads();
   if (warp == 0 && steps > 2) seed_threshold(sm, lane, p.k);
   first = sm.red[0];
@@ -577,27 +650,19 @@ topk_level_kernel(const LevelArgs p, bool vec) {
 
   const int e0 = start + 4 * tid;
   if (steps <= 2) {
-    // short unit (one or two steps): no buffering, the list straight from registers
+    // short unit (one or two steps): every entry stays in registers for the finish
     lse4(u, a);
-    if (steps == 2) {
-      lse4(u, bnext);
-      const float4 g[2] = {a, bnext};
-      const int e[2] = {e0, e0 + 4 * A_THREADS};
-      direct_select<8>(u, g, e, end, lane, p.k);
-    } else {
-      const float4 g[1] = {a};
-      const int e[1] = {e0};
-      direct_select<4>(u, g, e, end, lane, p.k);
-    }
-  } else {
-    for (int it = 0; it < steps; ++it) {
-      const float4 c = it + 2 < steps ? load4(it + 2) : none;
-      step4(sm, u, warp, lane, p.k, a, e0 + 4 * it * A_THREADS, end);
-      a = bnext;
-      bnext = c;
-    }
+    if (steps == 2) lse4(u, bnext);
+    finish_unit(sm, u, p, row, chunk, end, steps, a, bnext, e0, e0 + 4 * A_THREADS);
+    return;
   }
-  finish_unit(sm, u, p, row, chunk, end);
+  for (int it = 0; it < steps; ++it) {
+    const float4 c = it + 2 < steps ? load4(it + 2) : none;
+    step4(sm, u, warp, lane, p.k, a, e0 + 4 * it * A_THREADS, end);
+    a = bnext;
+    bnext = c;
+  }
+  finish_unit(sm, u, p, row, chunk, end, 0, none, none, end, end);
 }
 
 // ---- final selection --------------------------------------------------------------
@@ -763,13 +828,14 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
   p.front_store_out = front_store_out;
   const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (row_stride % 4 == 0);
   dim3 grid(plan.chunks, rows_total);
-  const size_t smem = (size_t)rows * (plan.chunks + 1) * top_k * (sizeof(float) + sizeof(int32_t));
+  const size_t smem = std::max<size_t>((size_t)SURV_MAX * 8,
+                                       (size_t)rows * (plan.chunks + 1) * top_k * 8);
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (smem > 48 * 1024 && dev >= 0 && dev < 64 && !attr_set[dev]) {
     if (cudaFuncSetAttribute(topk_level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             MERGE_SMEM_MAX) != cudaSuccess)
+                             std::max(MERGE_SMEM_MAX, SURV_MAX * 8)) != cudaSuccess)
       return launch_status();
     attr_set[dev] = true;
   }
