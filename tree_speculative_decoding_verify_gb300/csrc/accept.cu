@@ -53,6 +53,8 @@ accept_compact_kernel(const int32_t* __restrict__ tokens, const int32_t* __restr
   __shared__ int s_len, s_code;
   __shared__ __align__(16) unsigned char s_rows[TSV_MAX_DEPTH * MAX_ROW_BYTES];
 
+  griddep_wait();
+  griddep_launch();
   const int b = blockIdx.x;
   const int64_t row0 = (int64_t)b * max_nodes;
   const int T = num_nodes[b];
@@ -184,10 +186,10 @@ int launch_accept_compact(const int32_t* tokens, const int32_t* next_token,
     ctas_y = (int)ceil_div((int64_t)cache->num_layers * cache->num_kv_heads * 2, UNITS_PER_CTA);
   }
   dim3 grid(batch, ctas_y);
-  accept_compact_kernel<<<grid, THREADS, 0, stream>>>(
-      tokens, next_token, next_sibling, target, num_nodes, prefix_len, max_nodes, max_depth, cv,
-      cache != nullptr, accept_path, accept_len, bonus, slot_map, new_prefix_len, err);
-  return launch_status();
+  return launch_pdl(accept_compact_kernel, grid, dim3(THREADS), 0, stream, tokens, next_token,
+                    next_sibling, target, num_nodes, prefix_len, max_nodes, max_depth, cv,
+                    cache != nullptr, accept_path, accept_len, bonus, slot_map, new_prefix_len,
+                    err);
 }
 
 }  // namespace tsv

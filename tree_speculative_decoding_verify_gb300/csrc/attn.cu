@@ -126,6 +126,8 @@ __global__ void __launch_bounds__(PREP_THREADS)
 prep_kernel(AttnArgs a, const T* __restrict__ q, const T* __restrict__ k_new,
             const T* __restrict__ v_new, RopeTable rope) {
   __shared__ float s_cos[64], s_sin[64];
+  griddep_wait();
+  griddep_launch();
   const int i = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   const int D = a.head_dim, H = D / 2, G = a.group;
   int code = request_code(a, b);
@@ -212,6 +214,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(SIMT_WARPS * 32)
 simt_attn_kernel(AttnArgs a, float scale_log2) {
   constexpr int PER = D / 32;
+  griddep_wait();
+  griddep_launch();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = blockIdx.x * SIMT_WARPS + warp;
   const int split = blockIdx.y;
@@ -270,6 +274,8 @@ simt_attn_kernel(AttnArgs a, float scale_log2) {
 template <typename T>
 __global__ void __launch_bounds__(MERGE_WARPS * 32)
 merge_kernel(AttnArgs a, T* __restrict__ out) {
+  griddep_wait();
+  griddep_launch();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int r = blockIdx.x * MERGE_WARPS + warp;
   const int b = blockIdx.y / a.hkv, kv = blockIdx.y % a.hkv;
@@ -421,20 +427,21 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
   const float scale_log2 = softmax_scale * LOG2E;
 
   dim3 gprep(p.max_nodes, p.batch);
+  const dim3 bprep(PREP_THREADS);
   const bool bf16 = p.dtype == TSV_DTYPE_BF16;
+  int st;
   if (bf16) {
     using T = __nv_bfloat16;
     if (p.tensor_core)
-      prep_kernel<T, T><<<gprep, PREP_THREADS, 0, stream>>>(a, (const T*)q, (const T*)k_new,
-                                                            (const T*)v_new, rope);
+      st = launch_pdl(prep_kernel<T, T>, gprep, bprep, 0, stream, a, (const T*)q,
+                      (const T*)k_new, (const T*)v_new, rope);
     else
-      prep_kernel<T, float><<<gprep, PREP_THREADS, 0, stream>>>(a, (const T*)q, (const T*)k_new,
-                                                                (const T*)v_new, rope);
+      st = launch_pdl(prep_kernel<T, float>, gprep, bprep, 0, stream, a, (const T*)q,
+                      (const T*)k_new, (const T*)v_new, rope);
   } else {
-    prep_kernel<float, float><<<gprep, PREP_THREADS, 0, stream>>>(
-        a, (const float*)q, (const float*)k_new, (const float*)v_new, rope);
+    st = launch_pdl(prep_kernel<float, float>, gprep, bprep, 0, stream, a, (const float*)q,
+                    (const float*)k_new, (const float*)v_new, rope);
   }
-  int st = launch_status();
   if (st != TSV_OK) return st;
 
   if (p.tensor_core) {
@@ -442,21 +449,21 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
     return launch_attn_tc(p, a, scale_log2, out, stream);
   } else {
     dim3 gs((unsigned)ceil_div(p.rows, SIMT_WARPS), p.nsplit, p.batch * p.hkv);
+    const dim3 bs(SIMT_WARPS * 32);
     if (bf16) {
-      if (p.head_dim == 128) simt_attn_kernel<__nv_bfloat16, 128><<<gs, SIMT_WARPS * 32, 0, stream>>>(a, scale_log2);
-      else simt_attn_kernel<__nv_bfloat16, 64><<<gs, SIMT_WARPS * 32, 0, stream>>>(a, scale_log2);
+      if (p.head_dim == 128) st = launch_pdl(simt_attn_kernel<__nv_bfloat16, 128>, gs, bs, 0, stream, a, scale_log2);
+      else st = launch_pdl(simt_attn_kernel<__nv_bfloat16, 64>, gs, bs, 0, stream, a, scale_log2);
     } else {
-      if (p.head_dim == 128) simt_attn_kernel<float, 128><<<gs, SIMT_WARPS * 32, 0, stream>>>(a, scale_log2);
-      else simt_attn_kernel<float, 64><<<gs, SIMT_WARPS * 32, 0, stream>>>(a, scale_log2);
+      if (p.head_dim == 128) st = launch_pdl(simt_attn_kernel<float, 128>, gs, bs, 0, stream, a, scale_log2);
+      else st = launch_pdl(simt_attn_kernel<float, 64>, gs, bs, 0, stream, a, scale_log2);
     }
-    st = launch_status();
     if (st != TSV_OK) return st;
   }
 
   dim3 gm((unsigned)ceil_div(p.rows, MERGE_WARPS), p.batch * p.hkv);
-  if (bf16) merge_kernel<__nv_bfloat16><<<gm, MERGE_WARPS * 32, 0, stream>>>(a, (__nv_bfloat16*)out);
-  else merge_kernel<float><<<gm, MERGE_WARPS * 32, 0, stream>>>(a, (float*)out);
-  return launch_status();
+  const dim3 bm(MERGE_WARPS * 32);
+  if (bf16) return launch_pdl(merge_kernel<__nv_bfloat16>, gm, bm, 0, stream, a, (__nv_bfloat16*)out);
+  return launch_pdl(merge_kernel<float>, gm, bm, 0, stream, a, (float*)out);
 }
 
 }  // namespace tsv

@@ -108,6 +108,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int split = blockIdx.x, mt = blockIdx.y;
   const int b = blockIdx.z / a.hkv, h = blockIdx.z % a.hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  griddep_wait();  // the prep kernel's rotated queries, cache appends and flags
 
   // ---- the CTA's work (uniform) ------------------------------------------------------
   if (!a.valid[b]) return;
@@ -419,7 +420,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // publishes the last P (GO phase n)
     __syncwarp();
     if (ok && lane == 0) mbar_arrive(bar(BAR_GO + (n & 1)));
-    // epilogue
+    // epilogue: the CTA's share of the key loop is done; the stream's next kernel may be
+    // scheduled (it waits for this grid to complete before touching memory)
+    griddep_launch();
     if (ok) ok = warp_wait(bar(BAR_O_DONE), 0, abort);
     tc_fence_after();
     if (single) {
@@ -616,8 +619,7 @@ int launch_attn_tc(const AttnPlan& p, const AttnArgs& a, float scale_log2, void*
     return TSV_ERR_UNSUPPORTED;
   TcParams prm{a, scale_log2, static_cast<__nv_bfloat16*>(out)};
   dim3 grid(p.nsplit, (unsigned)ceil_div(p.rows, TC_M_GROUP), p.batch * p.hkv);  // M tiles of 128 rows
-  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mk, mv, prm);
-  return launch_status();
+  return launch_pdl(attn_tc_kernel, grid, dim3(THREADS), SMEM_BYTES, stream, mk, mv, prm);
 }
 
 }  // namespace tsv

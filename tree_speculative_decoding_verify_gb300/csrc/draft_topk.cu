@@ -603,6 +603,7 @@ __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int 
   __syncthreads();
   if (!sm.last) return;
   __threadfence();
+  griddep_launch();  // the other CTAs have exited: the next kernel may be scheduled
   request_merge(p, b);
 }
 
@@ -610,6 +611,7 @@ __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int 
 __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
 topk_level_kernel(const LevelArgs p, bool vec) {
   __shared__ TopkSmem sm;
+  griddep_wait();
   const int row = blockIdx.y, chunk = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* x = p.logits + (int64_t)row * p.row_stride;
@@ -705,6 +707,8 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
   __shared__ unsigned s_sel[2];
   const int b = blockIdx.x, tid = threadIdx.x;
   const int64_t srow = (int64_t)b * store_cap;
+  griddep_wait();
+  griddep_launch();
   for (int c = tid; c < C; c += F_THREADS) s_key[c] = ord(store_score[srow + c]);
 
   // radix select: after the passes, `prefix` is the total-th largest key and `need` the
@@ -839,8 +843,7 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
       return launch_status();
     attr_set[dev] = true;
   }
-  topk_level_kernel<<<grid, A_THREADS, smem, stream>>>(p, vec);
-  return launch_status();
+  return launch_pdl(topk_level_kernel, grid, dim3(A_THREADS), smem, stream, p, vec);
 }
 
 int launch_select_final(const int32_t* store_token, const float* store_score,
@@ -849,11 +852,9 @@ int launch_select_final(const int32_t* store_token, const float* store_score,
                         int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
                         cudaStream_t stream) {
   if (num_candidates > F_MAX) return TSV_ERR_INVALID_ARG;
-  select_final_kernel<<<batch, F_THREADS, 0, stream>>>(store_token, store_score, store_parent,
-                                                       num_candidates, store_cap, total_tokens,
-                                                       root_token, max_nodes, tokens, parents,
-                                                       num_nodes);
-  return launch_status();
+  return launch_pdl(select_final_kernel, dim3(batch), dim3(F_THREADS), 0, stream, store_token,
+                    store_score, store_parent, num_candidates, store_cap, total_tokens,
+                    root_token, max_nodes, tokens, parents, num_nodes);
 }
 
 }  // namespace tsv

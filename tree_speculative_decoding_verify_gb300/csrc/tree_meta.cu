@@ -26,6 +26,8 @@ build_meta_kernel(const int32_t* __restrict__ parents, const int32_t* __restrict
   __shared__ int32_t s_depth[WARPS][TSV_MAX_NODES];
   __shared__ int32_t s_first[WARPS][TSV_MAX_NODES];  // first child of a node, -1
   __shared__ int32_t s_last[WARPS][TSV_MAX_NODES];   // last child seen so far, -1
+  griddep_wait();
+  griddep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * WARPS + warp;
   if (b >= batch) return;
@@ -174,11 +176,9 @@ int launch_build_meta(const int32_t* parents, const int32_t* num_nodes, const in
                       int32_t* next_token, int32_t* next_sibling, int32_t* err,
                       cudaStream_t stream) {
   dim3 grid((unsigned)ceil_div(batch, WARPS));
-  build_meta_kernel<<<grid, WARPS * 32, 0, stream>>>(parents, num_nodes, prefix_len, batch,
-                                                      max_nodes, max_depth, mask, position_ids,
-                                                      retrieve, num_leaves, next_token,
-                                                      next_sibling, err);
-  return launch_status();
+  return launch_pdl(build_meta_kernel, grid, dim3(WARPS * 32), 0, stream, parents, num_nodes,
+                    prefix_len, batch, max_nodes, max_depth, mask, position_ids, retrieve,
+                    num_leaves, next_token, next_sibling, err);
 }
 
 }  // namespace tsv
