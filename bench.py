@@ -119,7 +119,10 @@ class Clocks:
     def __exit__(self, *a):
         if self.proc:
             self.proc.terminate()
-            self.proc.wait()
+            try:
+                self.proc.wait(timeout=10)
+            except subprocess.TimeoutExpired:  # a sampler stuck in the driver: leave it
+                self.proc.kill()
 
     def summary(self):
         if not os.path.exists(self.out):
@@ -258,6 +261,7 @@ def native(args):
     if world > 1:
         dist.barrier()
     ms = {name: sum(a.elapsed_time(c) for a, c in ev[name]) / args.steps for name in ev}
+    print("bench: timed region done", file=sys.stderr, flush=True)
 
     # ---- end to end through host buffers --------------------------------------------
     pin = lambda t: t.cpu().pin_memory()
@@ -292,6 +296,7 @@ def native(args):
             if i >= args.warmup:
                 e2e_ms.append(a.elapsed_time(c))
     e2e_step_ms = sum(e2e_ms) / len(e2e_ms)
+    print("bench: end-to-end leg done", file=sys.stderr, flush=True)
 
     # ---- max over ranks ---------------------------------------------------------------
     step_ms = ms["step"]
