@@ -317,18 +317,21 @@ __device__ __forceinline__ void step4(TopkSmem& sm, UnitState& u, int warp, int 
   }
 }
 
-// Seed of the CTA-wide bound from the warps' maxima of the unit's first entries (in
-// sm.red): the k-th largest of the A_WARPS maxima (k <= A_WARPS) has k distinct entries at
-// or above it. Run by warp 0; sm.gthr is read after the next barrier.
+// Seed of the CTA-wide bound: the k-th best of the 64 eight-lane group maxima of the unit's
+// first step (in sm.gkey, as keys with index INT_MAX: a group maximum is an entry of the
+// unit, so k entries are at or above the seed). Run by warp 0; sm.gthr is read after the
+// next barrier.
 __device__ __forceinline__ void seed_threshold(TopkSmem& sm, int lane, int k) {
-  const float m = lane < A_WARPS ? sm.red[lane] : -INFINITY;
-  int rank = 0;  // warps whose maximum is larger (ties: lower warp first)
-#pragma unroll
-  for (int w = 0; w < A_WARPS; ++w) {
-    const float o = __shfl_sync(FULL, m, w);
-    rank += (o > m || (o == m && w < lane)) ? 1 : 0;
+  const unsigned long long a0 = sm.gkey[lane], a1 = sm.gkey[lane + 32];
+  int r0 = 0, r1 = 0;
+#pragma unroll 8
+  for (int t = 0; t < A_THREADS / 8; ++t) {
+    const unsigned long long o = sm.gkey[t];
+    r0 += (o > a0 || (o == a0 && t < lane)) ? 1 : 0;
+    r1 += (o > a1 || (o == a1 && t < lane + 32)) ? 1 : 0;
   }
-  if (lane < A_WARPS && rank == k - 1) sm.gthr = key(m, INT_MAX);
+  if (r0 == k - 1) sm.gthr = a0;
+  if (r1 == k - 1) sm.gthr = a1;
 }
 
 // Starts a unit's per-thread state (sm.gthr was set before the CTA's last barrier).
@@ -619,7 +622,7 @@ topk_level_kernel(const LevelArgs p, bool vec) {
   const int end = min(p.vocab, start + p.chunk_len);
 
   // Every thread takes 4 consecutive entries per step (one 128-bit load when the row is
-  // 16-byte aligned), two steps prefetched ahead.
+  // 16-byte aligned), up to three steps prefetched ahead.
   const int steps = (end - start + 4 * A_THREADS - 1) / (4 * A_THREADS);
   auto load4 = [&](int it) -> float4 {
     const int e = start + 4 * (it * A_THREADS + tid);
@@ -635,10 +638,15 @@ topk_level_kernel(const LevelArgs p, bool vec) {
   float4 a = steps > 0 ? load4(0) : none;
   float4 bnext = steps > 1 ? load4(1) : none;
 
-  // Common starting reference: the largest of the first entries every thread sees.
+  // Common starting reference: the largest of the first entries every thread sees. The
+  // maxima of the eight-lane groups (32 entries each) of that first step also seed the
+  // CTA-wide bound of a streaming unit.
   float first = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
+  for (int o = 1; o < 8; o <<= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
+  if ((lane & 7) == 0) sm.gkey[tid >> 3] = key(first, INT_MAX);
+#pragma unroll
+  for (int o = 8; o < 32; o <<= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
   if (lane == 0) sm.red[warp] = first;
   if (tid == 0) sm.gthr = 0ull;
   __syncthreads();
@@ -658,11 +666,14 @@ topk_level_kernel(const LevelArgs p, bool vec) {
     finish_unit(sm, u, p, row, chunk, end, steps, a, bnext, e0, e0 + 4 * A_THREADS);
     return;
   }
+  // three steps in flight: 48 KB per SM with two resident CTAs
+  float4 cnext = steps > 2 ? load4(2) : none;
   for (int it = 0; it < steps; ++it) {
-    const float4 c = it + 2 < steps ? load4(it + 2) : none;
+    const float4 d = it + 3 < steps ? load4(it + 3) : none;
     step4(sm, u, warp, lane, p.k, a, e0 + 4 * it * A_THREADS, end);
     a = bnext;
-    bnext = c;
+    bnext = cnext;
+    cnext = d;
   }
   finish_unit(sm, u, p, row, chunk, end, 0, none, none, end, end);
 }
@@ -789,11 +800,20 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
 TopkPlan plan_topk(int batch, int rows, int vocab, int top_k) {
   TopkPlan p{};
   const int64_t rows_total = (int64_t)batch * rows;
-  // as many chunks per row as keep every unit in one wave of resident CTAs
+  // Chunks per row: the count with the shortest estimated makespan, waves of resident CTAs
+  // x (chunk length + a fixed cost per unit of about FIX_ENTRIES entries' streaming time:
+  // start, finish and merge).
+  constexpr int64_t FIX_ENTRIES = 16384;
   const int64_t slots = (int64_t)CTAS_PER_SM * device_sm_count();
-  int chunks = (int)std::min<int64_t>(MAX_CHUNKS, std::max<int64_t>(1, slots / std::max<int64_t>(1, rows_total)));
-  // at least MIN_CHUNK entries per chunk, lengths a multiple of 4
-  chunks = (int)std::max<int64_t>(1, std::min<int64_t>(chunks, ceil_div(vocab, MIN_CHUNK)));
+  const int64_t cmax = std::max<int64_t>(1, std::min<int64_t>(MAX_CHUNKS, ceil_div(vocab, MIN_CHUNK)));
+  int64_t best_c = 1, best_cost = INT64_MAX;
+  for (int64_t c = 1; c <= cmax; ++c) {
+    const int64_t len = round_up(ceil_div(vocab, c), 4);
+    const int64_t waves = ceil_div(rows_total * ceil_div(vocab, len), slots);
+    const int64_t cost = waves * (len + FIX_ENTRIES);
+    if (cost < best_cost) { best_cost = cost; best_c = c; }
+  }
+  int chunks = (int)best_c;
   int chunk_len = (int)round_up(ceil_div(vocab, chunks), 4);
   chunks = (int)ceil_div(vocab, chunk_len);
   p.chunks = chunks;
