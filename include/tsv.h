@@ -257,6 +257,10 @@ typedef struct {
 
 size_t tsv_tree_verify_attn_workspace_size(const tsv_attn_shape* shape,
                                            const tsv_kv_cache* cache);
+/* Kernels one tsv_tree_verify_attn call with this shape and cache launches on its stream:
+ * the prep, the attention kernel and, when the plan splits the keys of a row block, the
+ * split merge. 0 when the shape is not supported. Host only, no device work. */
+int tsv_tree_verify_attn_launches(const tsv_attn_shape* shape, const tsv_kv_cache* cache);
 int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void* k_new,
                          const void* v_new, const tsv_kv_cache* cache,
                          const int32_t* prefix_len, const int32_t* num_nodes,

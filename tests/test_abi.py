@@ -72,6 +72,8 @@ def test_host_validation_rejects_bad_arguments(lib):
                                     1e4, 0.1, p, None, 0, None, None) == 1
     shape.num_q_heads = 32
     assert lib.tsv_tree_verify_attn_workspace_size(ctypes.byref(shape), ctypes.byref(cache)) > 0
+    # prep, attention and (when the keys are split) the merge
+    assert lib.tsv_tree_verify_attn_launches(ctypes.byref(shape), ctypes.byref(cache)) in (2, 3)
     assert lib.tsv_tree_verify_attn(ctypes.byref(shape), p, p, p, ctypes.byref(cache), p, p, p, p,
                                     1e4, 0.1, p, None, 0, None, None) == 3
     # accept: contiguous capacity not a multiple of 64

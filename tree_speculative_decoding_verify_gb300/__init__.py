@@ -9,5 +9,6 @@ from ._lib import (  # noqa: F401
     draft_select_final, draft_topk_expand, draft_topk_expand_workspace_size, exported_symbols,
     lib, tree_build_meta, tree_verify_attn, tree_verify_attn_noalloc,
     tree_verify_attn_workspace_size,
+    tree_verify_attn_launches,
 )
 from .pipeline import HotPath, TreeShape  # noqa: F401

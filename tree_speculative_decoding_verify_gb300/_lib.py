@@ -64,6 +64,7 @@ _SIGNATURES = {
     "tsv_draft_select_final": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 +
                                [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 4),
     "tsv_tree_verify_attn_workspace_size": (ctypes.c_size_t, [ctypes.c_void_p] * 2),
+    "tsv_tree_verify_attn_launches": (ctypes.c_int, [ctypes.c_void_p] * 2),
     "tsv_tree_verify_attn": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_float] * 2 +
                              [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                               ctypes.c_void_p, ctypes.c_void_p]),
@@ -263,6 +264,13 @@ def tree_verify_attn_workspace_size(q_shape, cache: KVCache, max_prefix: int) ->
     b, t, hq, _ = q_shape
     s = AttnShape(b, t, hq, max_prefix)
     return int(lib().tsv_tree_verify_attn_workspace_size(ctypes.byref(s), ctypes.byref(cache.desc)))
+
+
+def tree_verify_attn_launches(q_shape, cache: KVCache, max_prefix: int) -> int:
+    """Kernels one tree_verify_attn call of this shape launches (0: unsupported)."""
+    b, t, hq, _ = q_shape
+    s = AttnShape(b, t, hq, max_prefix)
+    return int(lib().tsv_tree_verify_attn_launches(ctypes.byref(s), ctypes.byref(cache.desc)))
 
 
 def tree_verify_attn(q, k_new, v_new, cache: KVCache, prefix_len, num_nodes, position_ids, mask,

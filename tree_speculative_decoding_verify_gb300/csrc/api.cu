@@ -188,6 +188,12 @@ size_t tsv_tree_verify_attn_workspace_size(const tsv_attn_shape* shape,
   return plan_attn(shape, cache).ws_bytes;
 }
 
+int tsv_tree_verify_attn_launches(const tsv_attn_shape* shape, const tsv_kv_cache* cache) {
+  if (!attn_shape_ok(shape, cache)) return 0;
+  const AttnPlan p = plan_attn(shape, cache);
+  return p.tensor_core ? (p.nsplit > 1 ? 3 : 2) : 3;
+}
+
 int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void* k_new,
                          const void* v_new, const tsv_kv_cache* cache,
                          const int32_t* prefix_len, const int32_t* num_nodes,

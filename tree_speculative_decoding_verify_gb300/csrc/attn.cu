@@ -14,7 +14,6 @@
 //   o_part [B, Hkv, nsplit, rows_pad, D] f32  unnormalised partial outputs
 //   ml     [B, Hkv, nsplit, rows_pad, 2]  f32  (running max m in log2 units, sum l)
 //   valid  [B] int32                      request passed the device checks
-//   tickets [B, Hkv, rows_pad / 128] int32 splits finished per M tile (tensor-core path)
 #include <math.h>
 #include <stdint.h>
 
@@ -147,10 +146,6 @@ prep_kernel(AttnArgs a, const T* __restrict__ q, const T* __restrict__ k_new,
       a.valid[b] = ok ? 1 : 0;
       if (a.err) a.err[b] = code;
     }
-    // merge tickets of this request (tensor-core path)
-    if (a.tickets)
-      for (int e = tid; e < a.hkv * (a.rows_pad / 128); e += PREP_THREADS)
-        a.tickets[(int64_t)b * a.hkv * (a.rows_pad / 128) + e] = 0;
   }
   const int Tn = ok ? a.num_nodes[b] : 0;
   const int P = ok ? a.prefix_len[b] : 0;
@@ -379,8 +374,6 @@ AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache) {
   off += align256(planes * p.nsplit * p.rows_pad * 2 * sizeof(float));
   p.off_valid = off;
   off += align256((size_t)p.batch * sizeof(int32_t));
-  p.off_tickets = off;
-  if (p.tensor_core) off += align256(planes * (p.rows_pad / TC_M_GROUP) * sizeof(int32_t));
   p.ws_bytes = off;
   return p;
 }
@@ -409,7 +402,6 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
   a.o_part = reinterpret_cast<float*>(w + p.off_opart);
   a.ml = reinterpret_cast<float*>(w + p.off_ml);
   a.valid = reinterpret_cast<int32_t*>(w + p.off_valid);
-  a.tickets = p.tensor_core ? reinterpret_cast<int32_t*>(w + p.off_tickets) : nullptr;
   a.max_nodes = p.max_nodes;
   a.hq = p.hq;
   a.hkv = p.hkv;

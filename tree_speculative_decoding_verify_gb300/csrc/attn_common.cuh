@@ -31,7 +31,6 @@ struct AttnArgs {
   float* o_part;
   float* ml;
   int32_t* valid;
-  int32_t* tickets;   // [B, Hkv, rows_pad / 128] split counters (tensor-core path), or null
   // sizes
   int max_nodes, hq, hkv, group, head_dim, rows_pad, max_prefix;
   int tile_keys, tiles_per_split, nsplit;
@@ -39,6 +38,7 @@ struct AttnArgs {
 
 // Query rows per tensor-core CTA (one 128-row M tile).
 constexpr int TC_M_GROUP = 128;
+
 // Most key splits of one row block on the tensor-core path.
 #define TSV_ATTN_MAX_SPLITS 32
 

@@ -38,8 +38,10 @@
 // TMEM (512 columns allocated): S [0,128) O [128,256) P[0] [256,320) P[1] [320,384)
 // Q [384,448).
 // A CTA that covers every key of its rows writes the normalised bf16 output itself;
-// otherwise it writes its unnormalised O rows plus (m, l), and the last split of the row
-// block to finish (an atomic ticket) combines them with a warp-shuffle log-sum-exp merge.
+// otherwise it writes its unnormalised O rows plus (m, l), and the merge kernel (one warp
+// per query row, launched after this grid) combines the splits with their log-sum-exp
+// weights. (Merging inside the last split to finish cost more: one SM then reads every
+// partial of its 128 rows while the rest of the GPU idles.)
 //
 // The ancestor bitmask is applied from a 32-bit visibility word per 32-key chunk,
 // funnel-shifted out of the row's node mask (read only on tiles that hold tree keys).
@@ -67,11 +69,6 @@ constexpr uint32_t SMEM_K = 0;            // KST K tiles
 constexpr uint32_t SMEM_V = SMEM_K + KST * TILE;  // VST V tiles
 constexpr uint32_t SMEM_BAR = SMEM_V + VST * TILE;
 constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + alignment slack
-// split merge (after the last MMA, over the K/V rings): three 64 KB partial tiles (128 rows
-// x 128 f32, row-major), then every split's (m, l) rows, later overwritten by weights
-constexpr uint32_t MERGE_TILE = 128 * 128 * 4;
-constexpr uint32_t MERGE_W = 3 * MERGE_TILE;
-static_assert(MERGE_W + TSV_ATTN_MAX_SPLITS * 128 * 8 <= SMEM_BAR, "merge buffers");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_S = 0;
 constexpr uint32_t TMEM_O = 128;
@@ -84,8 +81,7 @@ constexpr int BAR_Q = 0, BAR_K_FULL = 1, BAR_K_EMPTY = BAR_K_FULL + KST,
               BAR_V_FULL = BAR_K_EMPTY + KST, BAR_V_EMPTY = BAR_V_FULL + VST,
               BAR_S_FULL = BAR_V_EMPTY + VST, BAR_PV_DONE = BAR_S_FULL + 1,
               BAR_O_DONE = BAR_PV_DONE + 2,
-              BAR_DRAIN = BAR_O_DONE + 1, BAR_GO = BAR_DRAIN + 1, BAR_MERGE = BAR_GO + 2,
-              NUM_BARS = BAR_MERGE + 1;
+              BAR_DRAIN = BAR_O_DONE + 1, BAR_GO = BAR_DRAIN + 1, NUM_BARS = BAR_GO + 2;
 static_assert(8 * NUM_BARS + 12 <= 256, "barrier area");
 static_assert(SMEM_BYTES <= 232448, "shared memory per block");
 
@@ -95,10 +91,6 @@ struct TcParams {
   __nv_bfloat16* out;  // [B, max_nodes, Hq, D]: written here when a request has one split
 };
 
-// Named barrier of the four softmax warps (barrier 0 is the CTA's __syncthreads).
-__device__ __forceinline__ void softmax_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
 
 __global__ void __launch_bounds__(THREADS, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -132,7 +124,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   auto bar = [&](int i) { return bars + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + SMEM_BAR + 8 * NUM_BARS);
   volatile uint32_t* abort = tmem_slot + 1;
-  volatile uint32_t* merge_flag = tmem_slot + 2;  // this CTA merges its row block's splits
 
   if (threadIdx.x == 0) {
     mbar_init(bar(BAR_Q), 4);  // one arrival per softmax warp (Q rows in TMEM)
@@ -153,7 +144,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // one barrier its phase could complete before the MMA warp has seen step n - 1's
     mbar_init(bar(BAR_GO + 0), 5);  // four softmax warps + the relay
     mbar_init(bar(BAR_GO + 1), 5);
-    mbar_init(bar(BAR_MERGE), 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -464,122 +454,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         a.ml[prow * 2 + 0] = m_used;
         a.ml[prow * 2 + 1] = l;
       }
-      // The last split of this (request, KV head, M tile) to finish merges them all:
-      // partials are published with a device-scope fence before the ticket increment,
-      // and read back through L2 after it.
-      __threadfence();
-      softmax_sync();
-      if (threadIdx.x == 0) {
-        const int nsp = (n_tiles + a.tiles_per_split - 1) / a.tiles_per_split;
-        const int old = atomicAdd(&a.tickets[((int64_t)b * a.hkv + h) * (a.rows_pad / 128) + mt], 1);
-        *merge_flag = old == nsp - 1;
-      }
-      softmax_sync();
-      if (*merge_flag) {
-        __threadfence();
-        // One bulk-copy round trip brings every split's (m, l) rows of this M tile and the
-        // first partial tiles (contiguous per split: 128 rows x 128 f32); later tiles come
-        // two at a time. Tile 0 keeps the running weighted sum.
-        const int nsp = (n_tiles + a.tiles_per_split - 1) / a.tiles_per_split;
-        const int t = warp * 32 + lane;
-        const int64_t pbase = ((int64_t)b * a.hkv + h) * a.nsplit;
-        float2* mls = reinterpret_cast<float2*>(gbase + MERGE_W);  // [nsp][128] (m, l)
-        float* wsm = reinterpret_cast<float*>(mls);                // weights over ml.x
-        float4* tiles = reinterpret_cast<float4*>(gbase);
-        const int live_rows = min(32, rows - (row0 + warp * 32));
-        int sp = 0;
-        uint32_t phase = 0;
-        while (ok && sp < nsp) {
-          const bool first = sp == 0;
-          const int cnt = min(nsp - sp, first ? 3 : 2);
-          if (t == 0) {
-            // other CTAs' partials (seen through the ticket) and this CTA's generic
-            // shared-memory accesses, ordered before the async-proxy copies
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_expect_tx(bar(BAR_MERGE), cnt * MERGE_TILE + (first ? nsp * 1024 : 0));
-            if (first)
-              for (int c = 0; c < nsp; ++c)
-                bulk_load(smem_u32(mls + c * 128), a.ml + ((pbase + c) * a.rows_pad + row0) * 2,
-                          1024, bar(BAR_MERGE));
-            for (int c = 0; c < cnt; ++c)
-              bulk_load(base + (first ? c : c + 1) * MERGE_TILE,
-                        a.o_part + ((pbase + sp + c) * a.rows_pad + row0) * 128, MERGE_TILE,
-                        bar(BAR_MERGE));
-          }
-          if (!(ok = warp_wait(bar(BAR_MERGE), phase, abort))) break;
-          phase ^= 1;
-          if (first) {
-            // log-sum-exp weights of every split for this thread's row (m in log2 units)
-            float M = -INFINITY, L = 0.f;
-            for (int c = 0; c < nsp; ++c) {
-              const float2 ml = mls[c * 128 + t];
-              if (ml.x != -INFINITY) {
-                const float mn = fmaxf(M, ml.x);
-                L = L * exp2f(M - mn) + ml.y * exp2f(ml.x - mn);
-                M = mn;
-              }
-            }
-            const float inv_l = L > 0.f ? 1.f / L : 0.f;
-            for (int c = 0; c < nsp; ++c) {
-              const float m = mls[c * 128 + t].x;
-              wsm[c * 256 + 2 * t] = m == -INFINITY ? 0.f : exp2f(m - M) * inv_l;
-            }
-            softmax_sync();
-          }
-          const int c0 = first ? 1 : 0;  // tile c + 1 holds split sp + c + c0
-          // shared-space addresses: tile t, row, this lane's float4; weight of split c, row
-          const uint32_t wbase = base + MERGE_W;
-          auto taddr = [&](int tile, int row) { return base + tile * MERGE_TILE + row * 512 + lane * 16; };
-          auto waddr = [&](int c, int row) { return wbase + (uint32_t)(c * 1024 + row * 8); };
-          for (int rr0 = 0; rr0 < live_rows; rr0 += 8) {
-            float4 acc[8], y[8][2];
-            float w0[8], wy[8][2];  // static indices only: these stay in registers
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int row = warp * 32 + rr0 + u;
-              acc[u] = lds128(taddr(0, row));
-              w0[u] = lds32(waddr(sp, row));
-#pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                y[u][c] = lds128(taddr(c + 1, row));
-                wy[u][c] = lds32(waddr(sp + c + c0, row));
-              }
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              float4 x = acc[u];
-              if (first) x = make_float4(x.x * w0[u], x.y * w0[u], x.z * w0[u], x.w * w0[u]);
-#pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                if (c + c0 < cnt) {  // a tile past cnt holds stale bytes (maybe NaN)
-                  x.x += wy[u][c] * y[u][c].x;
-                  x.y += wy[u][c] * y[u][c].y;
-                  x.z += wy[u][c] * y[u][c].z;
-                  x.w += wy[u][c] * y[u][c].w;
-                }
-              }
-              acc[u] = x;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              if (rr0 + u < live_rows) sts128(taddr(0, warp * 32 + rr0 + u), acc[u]);
-          }
-          softmax_sync();
-          sp += cnt;
-        }
-        // normalised bf16 output rows
-        for (int rr = 0; ok && rr < live_rows; ++rr) {
-          const int row = warp * 32 + rr, r2 = row0 + row;
-          const float4 x = tiles[row * 32 + lane];
-          __nv_bfloat16* dst = prm.out + (((int64_t)b * a.max_nodes + r2 / a.group) * a.hq +
-                                          h * a.group + r2 % a.group) * 128;
-          __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y);
-          __nv_bfloat162 hi = __floats2bfloat162_rn(x.z, x.w);
-          reinterpret_cast<uint2*>(dst)[lane] =
-              make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-        }
-      }
     }
   }
 
@@ -590,6 +464,65 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+}
+
+// ---- split merge: one warp per query row -------------------------------------------
+// Combines the key splits of the rows whose request took more than one split: lane s
+// holds split s's (m, l) (m in log2 units), the warp forms the log-sum-exp weights
+// w_s = 2^(m_s - M) / L, and lane c accumulates output columns 4c .. 4c + 3 over the splits
+// (eight partial loads in flight), written as bf16. Rows of a single-split request were
+// written by the attention kernel itself; rows past the tree were zeroed by the prep.
+constexpr int MERGE_ROWS = 8;  // warps (query rows) per CTA
+
+__global__ void __launch_bounds__(MERGE_ROWS * 32)
+tc_merge_kernel(const AttnArgs a, __nv_bfloat16* __restrict__ out) {
+  griddep_wait();
+  griddep_launch();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = blockIdx.x * MERGE_ROWS + warp;
+  const int b = blockIdx.y / a.hkv, h = blockIdx.y % a.hkv;
+  if (!a.valid[b]) return;
+  const int T = a.num_nodes[b], P = a.prefix_len[b];
+  if (r >= T * a.group) return;
+  const int n_tiles = (P + T + 127) / 128;
+  const int nsp = (n_tiles + a.tiles_per_split - 1) / a.tiles_per_split;
+  if (nsp <= 1) return;
+  const int64_t pbase = ((int64_t)b * a.hkv + h) * a.nsplit;
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < nsp) ml = reinterpret_cast<const float2*>(a.ml)[(pbase + lane) * a.rows_pad + r];
+  float M = ml.x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+  float e = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+  float L = ml.y * e;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(FULL, L, o);
+  const float w = L > 0.f ? e / L : 0.f;  // this lane's split weight
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* src = reinterpret_cast<const float4*>(a.o_part) + (pbase * a.rows_pad + r) * 32 + lane;
+  const int64_t stride = (int64_t)a.rows_pad * 32;  // float4s between splits
+  for (int s0 = 0; s0 < nsp; s0 += 8) {
+    float4 x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      x[u] = s0 + u < nsp ? __ldcg(src + (s0 + u) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float ws = __shfl_sync(FULL, w, (s0 + u) & 31);
+      if (s0 + u < nsp && ws != 0.f) {  // a split with no visible key holds no partial
+        acc.x += ws * x[u].x;
+        acc.y += ws * x[u].y;
+        acc.z += ws * x[u].z;
+        acc.w += ws * x[u].w;
+      }
+    }
+  }
+  const int node = r / a.group;
+  __nv_bfloat16* dst = out + (((int64_t)b * a.max_nodes + node) * a.hq + h * a.group + r % a.group) * 128;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  reinterpret_cast<uint2*>(dst)[lane] =
+      make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
 }
 
 }  // namespace
@@ -619,7 +552,12 @@ int launch_attn_tc(const AttnPlan& p, const AttnArgs& a, float scale_log2, void*
     return TSV_ERR_UNSUPPORTED;
   TcParams prm{a, scale_log2, static_cast<__nv_bfloat16*>(out)};
   dim3 grid(p.nsplit, (unsigned)ceil_div(p.rows, TC_M_GROUP), p.batch * p.hkv);  // M tiles of 128 rows
-  return launch_pdl(attn_tc_kernel, grid, dim3(THREADS), SMEM_BYTES, stream, mk, mv, prm);
+  const int st = launch_pdl(attn_tc_kernel, grid, dim3(THREADS), SMEM_BYTES, stream, mk, mv, prm);
+  if (st != TSV_OK || p.nsplit == 1) return st;
+  // the split merge (its warps return at once for rows of single-split requests)
+  dim3 gm((unsigned)ceil_div(p.rows, MERGE_ROWS), p.batch * p.hkv);
+  return launch_pdl(tc_merge_kernel, gm, dim3(MERGE_ROWS * 32), 0, stream, a,
+                    static_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace tsv

@@ -52,7 +52,7 @@ struct AttnPlan {
   int tiles_per_split;
   int max_prefix;
   bool tensor_core;   // tcgen05 path
-  size_t off_qrot, off_opart, off_ml, off_valid, off_tickets, ws_bytes;
+  size_t off_qrot, off_opart, off_ml, off_valid, ws_bytes;
 };
 AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache);
 int launch_attn(const AttnPlan& plan, const void* q, const void* k_new, const void* v_new,

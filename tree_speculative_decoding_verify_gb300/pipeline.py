@@ -144,9 +144,7 @@ class HotPath:
         return n + 1 + self.attn_kernels() + 1
 
     def attn_kernels(self) -> int:
-        """Kernels of one tree_verify_attn call: prep and the tensor-core kernel (which
-        merges its own splits) for bf16 with head_dim 128 on sm_100 and later; prep,
-        the CUDA-core kernel and the merge otherwise."""
-        tc = (self.cache.dtype == torch.bfloat16 and self.cache.head_dim == 128
-              and torch.cuda.is_available() and torch.cuda.get_device_capability()[0] >= 10)
-        return 2 if tc else 3
+        """Kernels of one tree_verify_attn call: prep, the attention kernel (tensor-core
+        for bf16 with head_dim 128 on sm_100 and later, CUDA-core otherwise) and the
+        split merge when the keys are split."""
+        return _lib.tree_verify_attn_launches(tuple(self.out.shape), self.cache, self.s.max_prefix)
