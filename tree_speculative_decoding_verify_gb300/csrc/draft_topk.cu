@@ -214,7 +214,7 @@ __device__ __forceinline__ unsigned long long key(float v, int i) {
 // below e^RAISE and the rare rescale is the only inexact step besides the terms.
 constexpr float RAISE = 16.f;
 struct Lse {
-  float ref, g, hi, lo;
+  float ref, rl, g, hi, lo;  // rl = ref * log2(e): a term is 2^(x log2(e) - rl), one FFMA
   __device__ __forceinline__ void flush() {
     pair_add(hi, lo, g, 0.f);
     g = 0.f;
@@ -227,7 +227,9 @@ struct Lse {
     hi *= f;
     lo *= f;
     ref = m;
+    rl = m * L2E;
   }
+  __device__ __forceinline__ float term(float x) const { return ex2(fmaf(x, L2E, -rl)); }
 };
 
 // Inverse of ord().
@@ -247,7 +249,6 @@ struct UnitState {
   int li;
   float thr;    // group filter: the larger of the warp's k-th value and the CTA-wide bound
   int cnt;      // warp-uniform number of buffered groups
-  int groups;   // float4 groups since the last flush
 };
 
 // The list absorbs the buffered groups: lane t takes group t (four entries) beside its
@@ -282,27 +283,21 @@ __device__ __forceinline__ void fold(TopkSmem& sm, UnitState& u, int warp, int l
 }
 
 // Log-sum-exp terms of four entries (-inf entries give zero terms).
-__device__ __forceinline__ void lse4(UnitState& u, float4 a) {
-  const float m4 = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
+// The log-sum-exp terms of four entries whose largest is m4 (-inf entries give zero
+// terms); the caller flushes the group sum every four calls.
+__device__ __forceinline__ void lse4(UnitState& u, float4 a, float m4) {
   if (m4 > u.lse.ref + RAISE) u.lse.raise(m4);
-  const float r = u.lse.ref;
-  u.lse.g += (ex2((a.x - r) * L2E) + ex2((a.y - r) * L2E)) + (ex2((a.z - r) * L2E) + ex2((a.w - r) * L2E));
-  if (++u.groups == 4) {
-    u.lse.flush();
-    u.groups = 0;
-  }
+  u.lse.g += (u.lse.term(a.x) + u.lse.term(a.y)) + (u.lse.term(a.z) + u.lse.term(a.w));
 }
+__device__ __forceinline__ float max4(float4 a) { return fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)); }
 
 // One streaming step: the log-sum-exp terms of entries e .. e + 3 and, when their largest
 // beats the filter, the group into the warp's buffer (the list absorbs the buffer first
-// when the new groups would not fit). Every fourth step the filter takes up the CTA-wide
-// bound. Warp-uniform call.
+// when the new groups would not fit). Warp-uniform call.
 __device__ __forceinline__ void step4(TopkSmem& sm, UnitState& u, int warp, int lane, int k,
                                       float4 a, int e, int end) {
-  lse4(u, a);
-  if (u.groups == 0)
-    u.thr = fmaxf(u.thr, unord((unsigned)(*reinterpret_cast<volatile unsigned long long*>(&sm.gthr) >> 32)));
-  const float m4 = fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w));
+  const float m4 = max4(a);
+  lse4(u, a, m4);
   const bool q = m4 >= u.thr;
   const unsigned bal = __ballot_sync(FULL, q);
   if (bal) {  // warp-uniform and rare once the list holds k entries
@@ -336,7 +331,8 @@ __device__ __forceinline__ void seed_threshold(TopkSmem& sm, int lane, int k) {
 
 // Starts a unit's per-thread state (sm.gthr was set before the CTA's last barrier).
 __device__ __forceinline__ void unit_begin(UnitState& u, float ref, unsigned long long gthr) {
-  u.lse.ref = fmaxf(ref, -FLT_MAX);  // finite, so x = -inf gives a zero term
+  u.lse.ref = fmaxf(ref, -1e30f);  // finite (and so is ref * log2(e)): x = -inf gives a zero term
+  u.lse.rl = u.lse.ref * L2E;
   u.lse.g = 0.f;
   u.lse.hi = 0.f;
   u.lse.lo = 0.f;
@@ -344,7 +340,6 @@ __device__ __forceinline__ void unit_begin(UnitState& u, float ref, unsigned lon
   u.li = INT_MAX;
   u.thr = unord((unsigned)(gthr >> 32));
   u.cnt = 0;
-  u.groups = 0;
 }
 
 struct LevelArgs {
@@ -661,19 +656,24 @@ topk_level_kernel(const LevelArgs p, bool vec) {
   const int e0 = start + 4 * tid;
   if (steps <= 2) {
     // short unit (one or two steps): every entry stays in registers for the finish
-    lse4(u, a);
-    if (steps == 2) lse4(u, bnext);
+    lse4(u, a, max4(a));
+    if (steps == 2) lse4(u, bnext, max4(bnext));
     finish_unit(sm, u, p, row, chunk, end, steps, a, bnext, e0, e0 + 4 * A_THREADS);
     return;
   }
-  // three steps in flight: 48 KB per SM with two resident CTAs
-  float4 cnext = steps > 2 ? load4(2) : none;
+  // Two steps in flight (32 KB per SM with two resident CTAs; a third did not raise the
+  // rate: the loop is bound by instructions, not by latency). Every fourth step the
+  // exp-sum group (16 terms) is flushed and the filter takes up the CTA-wide bound.
+  const unsigned long long* gthr = &sm.gthr;
   for (int it = 0; it < steps; ++it) {
-    const float4 d = it + 3 < steps ? load4(it + 3) : none;
+    const float4 c = it + 2 < steps ? load4(it + 2) : none;
     step4(sm, u, warp, lane, p.k, a, e0 + 4 * it * A_THREADS, end);
     a = bnext;
-    bnext = cnext;
-    cnext = d;
+    bnext = c;
+    if ((it & 3) == 3) {
+      u.lse.flush();
+      u.thr = fmaxf(u.thr, unord((unsigned)(*reinterpret_cast<const volatile unsigned long long*>(gthr) >> 32)));
+    }
   }
   finish_unit(sm, u, p, row, chunk, end, 0, none, none, end, end);
 }
