@@ -86,6 +86,21 @@ def algorithmic(w, prefix, depths_per_req, esize=2):
     return nbytes, flops
 
 
+# DRAM bytes (read + write) per launch of the dominant kernels, from one ncu capture of
+# the same workload each (profiles/<kernel>_<workload>.md, which give the command). The
+# attention figure is the tcgen05 kernel alone (the call's roofline also counts the prep
+# and the split merge). Absent: no capture of the current kernel for that workload.
+TRAFFIC = {
+    ("attn", "serving"): (332769536 + 35831808, "profiles/attn_tc_kernel_serving.md"),
+    ("attn", "long70b"): (571268352 + 41051392, "profiles/attn_tc_kernel_long70b.md"),
+}
+
+
+def traffic(kernel, workload):
+    t = TRAFFIC.get((kernel, workload))
+    return (t[0], t[1]) if t else (None, None)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -320,7 +335,8 @@ def native(args):
         achieved, peak, unit = flops / attn_s / 1e12, tf, "TFLOP/s"
     attn_roof = {"kernel": "tree_verify_attn (prep + tcgen05 split-KV attention with in-kernel merge)",
                  "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                 "frac": achieved / peak, "peak_source": src, "traffic": None,
+                 "frac": achieved / peak, "peak_source": src,
+                 "traffic": traffic("attn", w.name)[0], "traffic_source": traffic("attn", w.name)[1],
                  "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
                  "us_per_launch": ms["attn"] * 1e3}
     topk_rows = b * k / (ms["topk"] / 1e3)
@@ -328,7 +344,8 @@ def native(args):
     topk_gbps = topk_bytes / (ms["topk"] / 1e3) / 1e9
     topk_roof = {"kernel": "draft_topk_expand level (rows x vocab fp32 logits)", "bound": "hbm",
                  "achieved": topk_gbps, "peak": hbm, "unit": "GB/s", "frac": topk_gbps / hbm,
-                 "peak_source": src, "traffic": None, "algorithmic_bytes": topk_bytes,
+                 "peak_source": src, "traffic": traffic("topk", w.name)[0],
+                 "traffic_source": traffic("topk", w.name)[1], "algorithmic_bytes": topk_bytes,
                  "us_per_launch": ms["topk"] * 1e3}
     # the dominant kernel of the step: the attention call or the depth + 1 top-k levels
     dominant = "topk" if ms["topk"] * (w.depth + 1) > ms["attn"] else "attn"
