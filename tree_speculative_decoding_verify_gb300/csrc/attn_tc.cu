@@ -12,31 +12,31 @@
 // from L2).
 //
 //   warp 4      TMA producer: K/V tiles of 128 keys (64-key boxes, 128-byte swizzle)
-//               into a 3-stage K ring and a 4-stage V ring; K runs one tile ahead of V
+//               into a 3-stage K ring and a 4-stage V ring; K runs two tiles ahead of V
 //   warp 5      TMEM allocator + MMA issuer (warp-uniform descriptors, one elected lane
-//               per instruction). Step j (j = 0 .. n) issues
-//                 S      = Q K_{j+1}^T      A = Q in TMEM, B = K (shared, K-major)
-//                 O     += P_{j-1} V_{j-1}  A = P[(j-1)%2] in TMEM, B = V (shared, MN-major)
-//               as soon as the softmax has read S_j into registers, so S_{j+1} is
-//               computed while the softmax works on tile j. Q and P come from TMEM: the
-//               shared-memory port then carries only the K and V tiles (TMA writes plus
-//               one MMA read each).
-//   warp 6      relay: arrives on GO for step j once K_{j+1} and V_{j-1} have landed
-//               (a step ahead of the softmax: GO alternates between two barriers by step
-//               parity); the four softmax warps arrive on it once they have read S_j
-//               (which also publishes P_{j-1}). The MMA warp tests that one barrier per step:
-//               every test it makes is an issue gap in which the shallow MMA queue
-//               drains, and every mbarrier operation waits behind the operand traffic
-//               of the shared-memory port (a few hundred cycles), so the critical path
-//               softmax -> MMA crosses a single barrier.
+//               per instruction). After S_0 and S_1, step j (j = 0 .. n - 1) issues
+//                 O     += P_j V_j          A = P_j in TMEM, B = V (shared, MN-major)
+//                 S_{j+2} = Q K_{j+2}^T     A = Q in TMEM, B = K (shared, K-major)
+//               once the softmax has written P_j. S is double-buffered and P_j is
+//               written over the first half of S_j's buffer, so the softmax always finds
+//               the next S computed while it works on the current tile, and the tensor
+//               pipe always has the next P V and Q K^T queued (its in-order execution
+//               keeps S_{j+2} from overwriting P_j before P_j V_j has read it). Q and P
+//               come from TMEM: the shared-memory port carries only the K and V tiles.
+//   warp 6      relay: arrives on GO for step j once V_j and K_{j+2} have landed (a step
+//               ahead of the softmax: GO alternates between two barriers by step
+//               parity); the four softmax warps arrive on it once P_j is written. The
+//               MMA warp tests that one barrier per step: every test it makes is an issue
+//               gap in which the shallow MMA queue drains, and every mbarrier operation
+//               waits behind the operand traffic of the shared-memory port (a few hundred
+//               cycles), so the critical path softmax -> MMA crosses a single barrier.
 //   warps 0-3   softmax warpgroup; thread = query row = TMEM lane. Each thread first
 //               copies its rotated query row into TMEM. Per tile: one x128 TMEM load of
-//               S, the row max over 8 chains, P = exp2(s * scale * log2e - m) rounded to
-//               bf16 and stored into P[j%2] once P_{j-2} V_{j-2} has finished with it.
-//               The running max m is raised only when a tile's max exceeds it by more
-//               than 8 (log2 units), and O in TMEM is rescaled then, otherwise never.
-// TMEM (512 columns allocated): S [0,128) O [128,256) P[0] [256,320) P[1] [320,384)
-// Q [384,448).
+//               S_j, the row max over 8 chains, P = exp2(s * scale * log2e - m) rounded to
+//               bf16 and stored over S_j. The running max m is raised only when a tile's
+//               max exceeds it by more than 8 (log2 units), and O in TMEM is rescaled
+//               then (after P_{j-1} V_{j-1} has finished), otherwise never.
+// TMEM (512 columns allocated): S/P[0] [0,128) S/P[1] [128,256) O [256,384) Q [384,448).
 // A CTA that covers every key of its rows writes the normalised bf16 output itself;
 // otherwise it writes its unnormalised O rows plus (m, l), and the merge kernel (one warp
 // per query row, launched after this grid) combines the splits with their log-sum-exp
@@ -70,16 +70,16 @@ constexpr uint32_t SMEM_V = SMEM_K + KST * TILE;  // VST V tiles
 constexpr uint32_t SMEM_BAR = SMEM_V + VST * TILE;
 constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_S = 0;
-constexpr uint32_t TMEM_O = 128;
-constexpr uint32_t TMEM_P = 256;  // two buffers of 64 columns: 128 bf16 per row
+constexpr uint32_t TMEM_S = 0;    // two S buffers of 128 columns; P_j is written over the
+                                  // first 64 columns of S_j's buffer (128 bf16 per row)
+constexpr uint32_t TMEM_O = 256;
 constexpr uint32_t TMEM_Q = 384;  // 64 columns: the row's 128 rotated query values
 constexpr float RESCALE_LOG2 = 8.f;
 
 // barrier slots (8 bytes each) after SMEM_BAR
 constexpr int BAR_Q = 0, BAR_K_FULL = 1, BAR_K_EMPTY = BAR_K_FULL + KST,
               BAR_V_FULL = BAR_K_EMPTY + KST, BAR_V_EMPTY = BAR_V_FULL + VST,
-              BAR_S_FULL = BAR_V_EMPTY + VST, BAR_PV_DONE = BAR_S_FULL + 1,
+              BAR_S_FULL = BAR_V_EMPTY + VST, BAR_PV_DONE = BAR_S_FULL + 2,
               BAR_O_DONE = BAR_PV_DONE + 2,
               BAR_DRAIN = BAR_O_DONE + 1, BAR_GO = BAR_DRAIN + 1, NUM_BARS = BAR_GO + 2;
 static_assert(8 * NUM_BARS + 12 <= 256, "barrier area");
@@ -135,7 +135,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       mbar_init(bar(BAR_V_FULL + s), 1);
       mbar_init(bar(BAR_V_EMPTY + s), 1);
     }
-    mbar_init(bar(BAR_S_FULL), 1);
+    mbar_init(bar(BAR_S_FULL + 0), 1);
+    mbar_init(bar(BAR_S_FULL + 1), 1);
     mbar_init(bar(BAR_PV_DONE + 0), 1);
     mbar_init(bar(BAR_PV_DONE + 1), 1);
     mbar_init(bar(BAR_O_DONE), 1);
@@ -154,8 +155,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const uint32_t tmem = *tmem_slot;
 
   if (warp == TMA_WARP) {
-    // ---- producer: the whole warp walks the loop, lane 0 issues. K runs one tile ahead
-    // of V (order K0 K1 V0 K2 V1 ...), so S = Q K^T never waits behind a V load.
+    // ---- producer: the whole warp walks the loop, lane 0 issues. K runs two tiles ahead
+    // of V (order K0 K1 K2 V0 K3 V1 ...), as Q K^T does ahead of P V.
     // Paged caches: the block ids of 32 consecutive 64-key boxes sit in the lanes'
     // registers (one load round trip per 16 tiles instead of one per box).
     const int box0 = t0 * (KEYS / TSV_KV_BLOCK);
@@ -187,7 +188,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     };
     int issued_k = 0, issued_v = 0;
     bool ok = true;
-    for (int j = 0; ok && j <= n; ++j) {
+    for (int j = 0; ok && j <= n + 1; ++j) {
       if (j < n) {
         const int st = j % KST;
         if (j >= KST && !(ok = warp_wait(bar(BAR_K_EMPTY + st), ((j / KST) - 1) & 1, abort, true)))
@@ -195,12 +196,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         load(&tm_k, base + SMEM_K + st * TILE, bar(BAR_K_FULL + st), j);
         issued_k = j + 1;
       }
-      if (j >= 1) {
-        const int jv = j - 1, st = jv % VST;
+      if (j >= 2 && j - 2 < n) {
+        const int jv = j - 2, st = jv % VST;
         if (jv >= VST && !(ok = warp_wait(bar(BAR_V_EMPTY + st), ((jv / VST) - 1) & 1, abort, true)))
           break;
         load(&tm_v, base + SMEM_V + st * TILE, bar(BAR_V_FULL + st), jv);
-        issued_v = j;
+        issued_v = jv + 1;
       }
     }
     // Before the CTA can exit, every copy it started has landed (immediate unless a
@@ -222,14 +223,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint64_t dv = sdesc(base + SMEM_V, HALF, 1024);
     // k-step ks of a K-major operand: 16 columns = 32 bytes inside a 64-column panel
     auto kmaj = [](int ks) -> uint64_t { return (uint64_t)((ks >> 2) * (HALF >> 4) + (ks & 3) * 2); };
-    // S = Q K_j^T; A = Q in TMEM (8 columns = 16 bf16 per k-step)
+    // S_j = Q K_j^T into S buffer j % 2; A = Q in TMEM (8 columns = 16 bf16 per k-step).
+    // The buffer held P_{j-2}: P_{j-2} V_{j-2} was issued before, and the tensor pipe
+    // executes in order.
     auto qk = [&](int j) {
       const uint64_t kd = dk + (uint64_t)((j % KST) * TILE_D);
+      const uint32_t sd = tmem + TMEM_S + (j & 1) * 128;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        if (elect_one()) mma_ts(tmem + TMEM_S, tmem + TMEM_Q + ks * 8, kd + kmaj(ks), ID_QK, ks > 0);
+        if (elect_one()) mma_ts(sd, tmem + TMEM_Q + ks * 8, kd + kmaj(ks), ID_QK, ks > 0);
       if (elect_one()) {
-        mma_commit(bar(BAR_S_FULL));
+        mma_commit(bar(BAR_S_FULL + (j & 1)));
         mma_commit(bar(BAR_K_EMPTY + j % KST));
       }
       __syncwarp();
@@ -241,7 +245,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // tensor pipe idle after them. Returns whether that phase had completed.
     auto pv = [&](int j, int ksteps, uint32_t next_bar, uint32_t next_parity) {
       const uint64_t vd = dv + (uint64_t)((j % VST) * TILE_D);
-      const uint32_t pa = tmem + TMEM_P + (j & 1) * 64;
+      const uint32_t pa = tmem + TMEM_S + (j & 1) * 128;  // P_j over S_j's buffer
       const uint32_t acc0 = j > 0 ? 1u : 0u;
       bool next_ready = false;
 #pragma unroll
@@ -256,22 +260,25 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       }
       return __all_sync(FULL, next_ready);
     };
+    // S_0 and S_1 first; then step j issues P_j V_j and S_{j+2} = Q K_{j+2}^T, so the
+    // softmax always finds the next S computed while it works on the current one
     bool ok = warp_wait(bar(BAR_Q), 0, abort) && warp_wait(bar(BAR_K_FULL), 0, abort);
     if (ok) {
       tc_fence_after();
       qk(0);
+      if (n > 1 && (ok = warp_wait(bar(BAR_K_FULL + 1), 0, abort, true))) {
+        tc_fence_after();
+        qk(1);
+      }
     }
     bool ready = false;  // GO phase j already seen complete
-    for (int j = 0; ok && j <= n; ++j) {
-      // GO phase j: S_j read by the softmax (so P_{j-1} is written), K_{j+1} and V_{j-1}
-      // landed (phase n: the last P written, V_{n-1} landed)
+    for (int j = 0; ok && j < n; ++j) {
+      // GO phase j: P_j written by the softmax, V_j and K_{j+2} landed
       if (!ready && !(ok = warp_wait(bar(BAR_GO + (j & 1)), (j >> 1) & 1, abort, true))) break;
       tc_fence_after();
-      if (j + 1 < n) qk(j + 1);
-      ready = false;
-      if (j >= 1)
-        ready = pv(j - 1, (min(KEYS, keys - (t0 + j - 1) * KEYS) + 15) >> 4,
-                   j < n ? bar(BAR_GO + ((j + 1) & 1)) : 0u, ((j + 1) >> 1) & 1);
+      ready = pv(j, (min(KEYS, keys - (t0 + j) * KEYS) + 15) >> 4,
+                 j + 1 < n ? bar(BAR_GO + ((j + 1) & 1)) : 0u, ((j + 1) >> 1) & 1);
+      if (j + 2 < n) qk(j + 2);
     }
     const bool issuer = lane == 0;
     if (issuer) {
@@ -282,19 +289,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     }
     __syncwarp();
   } else if (warp == RELAY_WARP) {
-    // ---- relay: its share of GO phase j once K_{j+1} and V_{j-1} have landed. GO is
+    // ---- relay: its share of GO phase j once V_j and K_{j+2} have landed. GO is
     // double-buffered by step parity, so the relay only waits for phase j - 2 (the last
     // one on the same barrier) to have completed before arriving: it runs a step ahead
     // of the softmax instead of after it.
     bool ok = true;
-    for (int j = 0; ok && j <= n; ++j) {
+    for (int j = 0; ok && j < n; ++j) {
       if (j >= 2 && !(ok = warp_wait(bar(BAR_GO + (j & 1)), ((j - 2) >> 1) & 1, abort, true))) break;
-      if (j + 1 < n &&
-          !(ok = warp_wait(bar(BAR_K_FULL + (j + 1) % KST), ((j + 1) / KST) & 1, abort, true)))
+      if (j + 2 < n &&
+          !(ok = warp_wait(bar(BAR_K_FULL + (j + 2) % KST), ((j + 2) / KST) & 1, abort, true)))
         break;
-      if (j >= 1 &&
-          !(ok = warp_wait(bar(BAR_V_FULL + (j - 1) % VST), ((j - 1) / VST) & 1, abort, true)))
-        break;
+      if (!(ok = warp_wait(bar(BAR_V_FULL + j % VST), (j / VST) & 1, abort, true))) break;
       if (lane == 0) mbar_arrive(bar(BAR_GO + (j & 1)));
       __syncwarp();
     }
@@ -329,21 +334,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_Q));
     }
-    const uint32_t s_addr = tmem + lane_base + TMEM_S;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
-      const uint32_t p_addr = tmem + lane_base + TMEM_P + (j & 1) * 64;
-      if (!(ok = warp_wait(bar(BAR_S_FULL), j & 1, abort, true))) break;
+      // S_j, and then P_j over its first 64 columns, in S buffer j % 2
+      const uint32_t s_addr = tmem + lane_base + TMEM_S + (j & 1) * 128;
+      if (!(ok = warp_wait(bar(BAR_S_FULL + (j & 1)), (j >> 1) & 1, abort, true))) break;
       tc_fence_after();
       const int k0 = (t0 + j) * KEYS;
       float v[128];
       tmem_ld128(s_addr, v);
-      // S is in registers: the next Q K^T may overwrite it (this arrival also publishes
-      // P_{j-1}, stored and fenced at the end of the previous iteration)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_GO + (j & 1)));
       if (k0 + KEYS > P) {  // tile holds tree keys (or keys past the end): mask to -inf
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -382,14 +382,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         }
       }
       l = l * factor + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
-      if (j >= 2) {
-        // P[j % 2] is free once P_{j-2} V_{j-2} has finished (the next completion on that
-        // barrier, P_j V_j, needs this tile's P, so the parity is unambiguous)
-        if (!(ok = warp_wait(bar(BAR_PV_DONE + (j & 1)), ((j - 2) >> 1) & 1, abort, true))) break;
-        tc_fence_after();
-      }
       if (__any_sync(FULL, need) && j > 0) {
         // O must be quiescent: P_{j-1} V_{j-1} (and with it every earlier MMA) finished
+        // (the next completion on that barrier, P_{j+1} V_{j+1}, needs P_{j+1}, so the
+        // parity is unambiguous)
         if (!(ok = warp_wait(bar(BAR_PV_DONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abort, true)))
           break;
         tc_fence_after();
@@ -402,14 +398,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
           tmem_st32(o_addr + 32 * c, o);
         }
       }
+      // P_j over S_j (already in registers); this warp's share of GO phase j
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_st16(p_addr + 16 * q, pk[q]);
+      for (int q = 0; q < 4; ++q) tmem_st16(s_addr + 16 * q, pk[q]);
       tmem_wait_st();
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_GO + (j & 1)));
     }
-    // publishes the last P (GO phase n)
-    __syncwarp();
-    if (ok && lane == 0) mbar_arrive(bar(BAR_GO + (n & 1)));
     // epilogue: the CTA's share of the key loop is done; the stream's next kernel may be
     // scheduled (it waits for this grid to complete before touching memory)
     griddep_launch();
