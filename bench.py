@@ -51,7 +51,8 @@ def plain(x):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 2 s of timed work, at least 50)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama8b", choices=sorted(W.WORKLOADS))
     ap.add_argument("--total-tokens", type=int, default=0)
@@ -111,25 +112,40 @@ def peaks():
 
 
 class Clocks:
-    """nvidia-smi sampling during the timed region."""
+    """nvidia-smi sampling (every 50 ms, with timestamps) around the timed region; only
+    the samples taken inside the region's wall-clock window count."""
 
     def __init__(self, out):
         self.out = out
         self.proc = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,"
+                ["nvidia-smi", "--query-gpu=timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
                  "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
                  "clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "200", "-i",
+                 "--format=csv,noheader,nounits", "-lms", "50", "-i",
                  os.environ.get("LOCAL_RANK", "0")],
                 stdout=open(self.out, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        # the sampler is running (it has written a sample) before the region starts
+        t = time.time()
+        while self.proc and time.time() - t < 5.0:
+            if os.path.exists(self.out) and os.path.getsize(self.out) > 0:
+                break
+            time.sleep(0.02)
         return self
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        time.sleep(0.1)  # the sample that covers the region's end
 
     def __exit__(self, *a):
         if self.proc:
@@ -140,20 +156,25 @@ class Clocks:
                 self.proc.kill()
 
     def summary(self):
-        if not os.path.exists(self.out):
+        if not os.path.exists(self.out) or self.t0 is None or self.t1 is None:
             return None
+        import datetime
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.out):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            if not (self.t0 - 0.05 <= ts <= self.t1 + 0.05):
+                continue
+            sm.append(clk)
+            mx.append(cmax)
+            for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
@@ -263,16 +284,29 @@ def native(args):
 
     timed_loop(args.warmup, False)
     torch.cuda.synchronize()
+    if args.steps is None:
+        # enough steps for about 2 s of timed work (so the clock samples fall inside it)
+        t = time.perf_counter()
+        timed_loop(5, False)
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t) / 5
+        args.steps = int(max(50, min(20000, 2.0 / max(per, 1e-6))))
+        if world > 1:  # every rank times the same number of steps
+            n = torch.tensor([args.steps], device=dev)
+            dist.all_reduce(n, op=dist.ReduceOp.MAX)
+            args.steps = int(n.item())
     if world > 1:
         dist.barrier()
     clocks = Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
                     if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/tsv_clocks_{rank}.csv")
     with clocks:
         torch.cuda.synchronize()
+        clocks.start()
         t_wall = time.perf_counter()
         ev = timed_loop(args.steps, True)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
+        clocks.stop()
     if world > 1:
         dist.barrier()
     ms = {name: sum(a.elapsed_time(c) for a, c in ev[name]) / args.steps for name in ev}
@@ -301,7 +335,7 @@ def native(args):
 
     e2e_ms = []
     with torch.cuda.stream(stream):
-        for i in range(args.warmup + args.steps):
+        for i in range(args.warmup + min(args.steps, 200)):  # a sample of the timed steps
             flush_buf.zero_()
             a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -437,6 +471,8 @@ def reference(args):
     if rank != 0:
         return
     w = workload(args)
+    if args.steps is None:
+        args.steps = 3  # oracle steps take seconds: a small bounded sample
     inputs = [oracle_step_inputs(w, b) for b in range(min(w.batch, 2))]
     for i in range(args.warmup):
         run_oracle_step(w, i % len(inputs), inputs[i % len(inputs)])
