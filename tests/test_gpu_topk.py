@@ -167,3 +167,16 @@ def test_whole_row_units_ragged_vocab(pad):
     reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
              for l in range(2)] for _ in range(b)]
     compare(reqs, k, stride_pad=pad)
+
+
+@pytest.mark.parametrize("v", [2048, 2049, 4001, 4096])
+def test_two_step_units_in_registers(v):
+    """320 frontier rows of at most 4096 entries give one unit per row of one or two
+    128-bit steps: every entry stays in registers and the unit's top k comes from the
+    CTA-wide bound and survivor ranking (2048: exactly one step; 2049: a second step with
+    a single entry; 4001: a ragged second step; 4096: two full steps)."""
+    rng = np.random.default_rng(v)
+    k, b = 10, 32
+    reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
+             for l in range(2)] for _ in range(b)]
+    compare(reqs, k)
