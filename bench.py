@@ -92,8 +92,10 @@ def algorithmic(w, prefix, depths_per_req, esize=2):
 # attention figure is the tcgen05 kernel alone (the call's roofline also counts the prep
 # and the split merge). Absent: no capture of the current kernel for that workload.
 TRAFFIC = {
-    ("attn", "serving"): (332769536 + 35831808, "profiles/attn_tc_kernel_serving.md"),
-    ("attn", "long70b"): (571268352 + 41051392, "profiles/attn_tc_kernel_long70b.md"),
+    ("attn", "serving"): (332767232 + 35483648, "profiles/attn_tc_kernel_serving.md"),
+    ("attn", "long70b"): (606232320 + 41901824, "profiles/attn_tc_kernel_long70b.md"),
+    ("topk", "llama8b"): (1354240 + 0, "profiles/topk_level_kernel_llama8b.md"),
+    ("topk", "sweep"): (328446464 + 2847488, "profiles/topk_level_kernel_sweep.md"),
 }
 
 
