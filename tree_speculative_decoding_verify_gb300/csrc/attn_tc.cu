@@ -102,9 +102,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   griddep_wait();  // the prep kernel's rotated queries, cache appends and flags
 
-  // ---- the CTA's work (uniform) ------------------------------------------------------
-  if (!a.valid[b]) return;
-  const int T = a.num_nodes[b], P = a.prefix_len[b];
+  // ---- the CTA's work (uniform; the three loads in one round trip) -------------------
+  const int valid = a.valid[b], T = a.num_nodes[b], P = a.prefix_len[b];
+  if (!valid) return;
   const int rows = T * a.group;
   const int row0 = mt * 128;
   if (row0 >= rows) return;
@@ -125,7 +125,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + SMEM_BAR + 8 * NUM_BARS);
   volatile uint32_t* abort = tmem_slot + 1;
 
-  if (threadIdx.x == 0) {
+  // The producer warp initialises the barriers and starts loading at once; the other
+  // warps meet at a named barrier (after the TMEM allocation, with the softmax warps'
+  // query rows already on their way into registers) that the producer only arrives at.
+  uint4 qreg[16];  // softmax warps: this row's rotated query (256 bytes)
+  if (warp < 4) {
+    const uint4* src = reinterpret_cast<const uint4*>(
+        static_cast<const __nv_bfloat16*>(a.q_rot) +
+        (((int64_t)b * a.hkv + h) * a.rows_pad + row0 + warp * 32 + lane) * 128);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) qreg[i] = src[i];
+  }
+  if (threadIdx.x == TMA_WARP * 32) {
     mbar_init(bar(BAR_Q), 4);  // one arrival per softmax warp (Q rows in TMEM)
     for (int s = 0; s < KST; ++s) {
       mbar_init(bar(BAR_K_FULL + s), 1);
@@ -148,11 +159,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == MMA_WARP) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  uint32_t tmem = 0;  // the producer does not use TMEM
+  if (warp == TMA_WARP) {
+    __syncwarp();
+    asm volatile("bar.arrive 1, %0;" ::"n"(THREADS) : "memory");
+  } else {
+    if (warp == MMA_WARP) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");
+    tc_fence_after();
+    tmem = *tmem_slot;
+  }
 
   if (warp == TMA_WARP) {
     // ---- producer: the whole warp walks the loop, lane 0 issues. K runs two tiles ahead
@@ -314,17 +331,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     const uint32_t o_addr = tmem + lane_base + TMEM_O;
     const float sl2 = prm.scale_log2;
     {
-      // this row's rotated query (bf16 pairs, low half first) -> TMEM columns of Q; rows
-      // past the tree copy whatever the workspace holds (their results are never stored)
-      const uint4* src = reinterpret_cast<const uint4*>(
-          static_cast<const __nv_bfloat16*>(a.q_rot) +
-          (((int64_t)b * a.hkv + h) * a.rows_pad + r) * 128);
+      // this row's rotated query (bf16 pairs, low half first, loaded before the setup
+      // barrier) -> TMEM columns of Q; rows past the tree copy whatever the workspace
+      // holds (their results are never stored)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t w[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint4 x = src[4 * c + i];
+          const uint4 x = qreg[4 * c + i];
           w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
         }
         tmem_st16(tmem + lane_base + TMEM_Q + 16 * c, w);
