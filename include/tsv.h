@@ -22,7 +22,10 @@
  *     library allocates no memory and keeps no state between calls beyond a per-device
  *     cache of device attributes.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream)
- *     and never synchronise the host. They can be captured into a CUDA graph.
+ *     and never synchronise the host. They can be captured into a CUDA graph. Kernels
+ *     are launched with programmatic stream serialization: a kernel may be scheduled
+ *     while the previous work of the stream finishes, but it waits for that work to
+ *     complete before its first memory access, so stream order holds as usual.
  *   - The return value is a tsv_status. Host-side checks (null pointers, sizes,
  *     workspace) happen before anything is launched; on failure nothing is launched.
  *   - Data-dependent faults (a malformed tree, a request that does not fit its cache)
