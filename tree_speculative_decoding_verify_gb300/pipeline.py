@@ -87,13 +87,19 @@ class HotPath:
         self.new_prefix_len = torch.zeros(b, **i32)
 
     # -- stages ------------------------------------------------------------------------
-    def expand(self, level_logits: Sequence[torch.Tensor], root_token: torch.Tensor):
-        """level_logits[0]: [B, 1, V]; level_logits[l]: [B, K, V] fp32 (device)."""
+    def expand(self, level_logits: Sequence[torch.Tensor], root_token: torch.Tensor,
+               level_ready: Optional[Sequence[torch.cuda.Event]] = None):
+        """level_logits[0]: [B, 1, V]; level_logits[l]: [B, K, V] fp32 (device).
+        level_ready[l] (optional): an event after which level l's logits (and, for l = 0,
+        root_token) are in place; the stream waits for it just before that level, so
+        the logits of later levels can still be arriving while earlier levels run."""
         s = self.s
         if len(level_logits) != s.depth + 1:
             raise ValueError(f"expected {s.depth + 1} levels of logits")
         cur = None
         for li, lg in enumerate(level_logits):
+            if level_ready is not None and level_ready[li] is not None:
+                torch.cuda.current_stream().wait_event(level_ready[li])
             nxt = self.front[li % 2]
             _lib.draft_topk_expand(lg, s.top_k, li + 1,
                                    None if cur is None else cur[1],
@@ -129,9 +135,16 @@ class HotPath:
                                 self.acc_err)
 
     def step(self, level_logits, root_token, q, k_new, v_new, prefix_len, target_argmax,
-             rope_theta: float, softmax_scale: float):
+             rope_theta: float, softmax_scale: float,
+             level_ready: Optional[Sequence[torch.cuda.Event]] = None,
+             inputs_ready: Optional[torch.cuda.Event] = None):
+        """One hot-path step. level_ready (see expand) and inputs_ready (q, k_new, v_new,
+        prefix_len and target_argmax in place before the tree metadata) let the inputs
+        arrive on another stream while the expansion runs."""
         if not self.s.fixed_nodes:
-            self.expand(level_logits, root_token)
+            self.expand(level_logits, root_token, level_ready)
+        if inputs_ready is not None:
+            torch.cuda.current_stream().wait_event(inputs_ready)
         self.build_meta(prefix_len)
         self.verify(q, k_new, v_new, prefix_len, rope_theta, softmax_scale)
         self.accept(target_argmax, prefix_len)
