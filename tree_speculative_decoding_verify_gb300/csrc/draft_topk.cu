@@ -9,20 +9,25 @@
 // follows "TensorRT-LLM 源码完全拆解(二十二)", section 树的三套账 (flat = parent * K +
 // child, parent = flat / K).
 //
-// One kernel per level. Each CTA streams one (row, vocab chunk) once with 128-bit loads:
-//   - top-k: a warp-cooperative select. Every warp keeps its best 16 candidates spread
-//     over lanes 0-15 and a warp-uniform threshold (its 16th best). A thread only
-//     buffers elements that beat the threshold (a handful per row after the first few
-//     hundred); when any buffer is nearly full, the whole warp merges buffers and list
-//     by a 16-round tournament, so no lane ever runs a divergent insertion.
-//   - log-sum-exp: exp(x - ref) against the thread's running maximum ref, summed in fp32
-//     groups of 16 terms flushed into an fp64 accumulator. Keeping ref at the maximum
-//     makes x - ref exact for every term that matters; when a new maximum arrives the
-//     old (ref, sum) pair is parked and combined once at the end (one fp64 exp), so the
-//     log-sum-exp is good to about 1e-9 and the fp32 log-probabilities round like fp64.
-// The warps' lists merge into the chunk's top-k; the last CTA of a request to finish
-// (an atomic ticket) merges the chunks of every row, writes the level's candidates to
-// the store and runs the joint top-K of the cumulative scores.
+// One kernel per level, one CTA per (row, vocab chunk); the chunk count per row keeps the
+// units in as few waves of resident CTAs as the makespan allows (small batches: one wave
+// of short chunks). Each unit is read once with 128-bit loads:
+//   - log-sum-exp: fp32 terms 2^(x log2 e - ref log2 e) against a running reference,
+//     summed in groups of 16 and added exactly (two-sum) into an unevaluated (hi, lo)
+//     pair; the reference is raised, and the pair rescaled, only when an entry exceeds it
+//     by more than 16 (natural log units). No fp64: it runs at a small fraction of the
+//     fp32 rate on this part.
+//   - top-k: a unit of one or two steps keeps its entries in registers. A longer unit
+//     buffers the float4 groups whose largest entry beats a filter (the warp's k-th
+//     value, or a CTA-wide bound: the best warp threshold, seeded with the k-th best of
+//     the first step's 64 eight-lane group maxima) in the warp's shared-memory slice and
+//     folds them into a register list 32 groups at a time. At the end a bound with k
+//     entries of the unit at or above it leaves a handful of survivors, ranked by
+//     counting in shared memory.
+// The last CTA of a request to finish (an atomic ticket) stages the request's chunk
+// lists in shared memory, merges each row (k rounds of a warp tournament over list
+// heads), writes the level's candidates to the store and ranks the rows' cumulative
+// scores for the joint top-K.
 #include <float.h>
 #include <limits.h>
 #include <math.h>
