@@ -312,6 +312,11 @@ int tsv_tree_verify_attn_noalloc(const tsv_attn_shape* shape, const void* q, con
  *
  * tokens           [batch, max_nodes] in: node tokens (node 0 = root).
  * next_token, next_sibling  [batch, max_nodes] in: links from tsv_tree_build_meta.
+ * tree_valid       [batch] in (may be NULL: every request has a tree): 0 = the request
+ *                  has no valid tree this step ([TRT] section 每请求一份树,按 slot 存放:
+ *                  its slot was released); it takes the single-token path: only the
+ *                  root is accepted, its bonus token is target_argmax at the root and
+ *                  the cache is not touched.
  * target_argmax    [batch, max_nodes] in: the target model's argmax at every node.
  * cache            may be NULL (walk only). Otherwise, for every layer l <
  *                  num_layers, kv head and i < accept_len[b]:
@@ -329,7 +334,8 @@ int tsv_tree_verify_attn_noalloc(const tsv_attn_shape* shape, const void* q, con
  * ------------------------------------------------------------------------------ */
 int tsv_accept_and_compact(const int32_t* tokens, const int32_t* next_token,
                            const int32_t* next_sibling, const int32_t* target_argmax,
-                           const int32_t* num_nodes, const int32_t* prefix_len, int batch,
+                           const int32_t* num_nodes, const int32_t* prefix_len,
+                           const int32_t* tree_valid, int batch,
                            int max_nodes, int max_depth, const tsv_kv_cache* cache,
                            int32_t* accept_path, int32_t* accept_len, int32_t* bonus_token,
                            int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,

@@ -4,7 +4,7 @@ from __future__ import annotations
 import numpy as np
 
 
-def greedy_walk(tokens, parents, target):
+def greedy_walk(tokens, parents, target, tree_valid=True):
     """Longest accepted root-down path, handbook form.
 
     [HB] section 实现 (tree_speculative_generate): start at the root; the target's
@@ -12,9 +12,15 @@ def greedy_walk(tokens, parents, target):
     lowest-numbered such child is taken; stop when none matches. The bonus token is
     the target's argmax at the last accepted node. Returns (path, bonus); the path
     includes the root, so len(path) is the accepted length.
+
+    [TRT] section 每请求一份树,按 slot 存放: a request whose tree is not valid (its slot
+    was released: has_tree / tree_valid is false) takes the single-token path, so only
+    the root is accepted.
     """
     n = len(tokens)
     path, node = [0], 0
+    if not tree_valid:
+        return path, int(target[0])
     for _ in range(n):
         pred = int(target[node])
         child = next((c for c in range(n) if parents[c] == node and tokens[c] == pred), None)

@@ -78,7 +78,7 @@ def test_host_validation_rejects_bad_arguments(lib):
                                     1e4, 0.1, p, None, 0, None, None) == 3
     # accept: contiguous capacity not a multiple of 64
     cache.capacity = 100
-    assert lib.tsv_accept_and_compact(p, p, p, p, p, p, 1, 61, 7, ctypes.byref(cache),
+    assert lib.tsv_accept_and_compact(p, p, p, p, p, p, None, 1, 61, 7, ctypes.byref(cache),
                                       p, p, p, p, p, None, None) == 1
 
 

@@ -37,7 +37,7 @@ def planted_target(rng, tokens, parents, p=0.75, vocab=6):
     return tgt
 
 
-def run(trees, tokens, targets, prefix, t_max, max_depth, cache=None, nn=None):
+def run(trees, tokens, targets, prefix, t_max, max_depth, cache=None, nn=None, valid=None):
     import tree_speculative_decoding_verify_gb300 as T
     b = len(trees)
     d = gc.dev()
@@ -58,14 +58,16 @@ def run(trees, tokens, targets, prefix, t_max, max_depth, cache=None, nn=None):
                new_prefix_len=torch.zeros(b, dtype=torch.int32, device=d),
                err=torch.full((b,), 9, dtype=torch.int32, device=d))
     T.accept_and_compact(gc.i32(tok), gc.i32(nxt), gc.i32(sib), gc.i32(tgt), gc.i32(nn),
-                         gc.i32(prefix), max_depth, cache, **out)
+                         gc.i32(prefix), max_depth, cache, **out,
+                         tree_valid=None if valid is None else gc.i32(valid))
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
-def check_walk(got, trees, tokens, targets, prefix, max_depth):
+def check_walk(got, trees, tokens, targets, prefix, max_depth, valid=None):
     for b, p in enumerate(trees):
-        path, bonus = accept.greedy_walk(list(tokens[b]), list(p), list(targets[b]))
+        path, bonus = accept.greedy_walk(list(tokens[b]), list(p), list(targets[b]),
+                                         True if valid is None else bool(valid[b]))
         assert got["err"][b] == 0
         assert got["accept_len"][b] == len(path)
         assert got["accept_path"][b].tolist() == path + [-1] * (max_depth + 1 - len(path))
@@ -155,3 +157,25 @@ def test_bad_links_and_sizes():
     T.accept_and_compact(tok, nxt, sib, tgt, gc.i32([0, 5, 4]), gc.i32([0, 0, -1]), 3, None, **out)
     assert out["err"].cpu().tolist() == [4, 4, 4]
     assert out["accept_len"].cpu().tolist() == [1, 1, 1]
+
+
+def test_requests_without_a_tree_take_the_single_token_path():
+    """tree_valid = 0 rows accept the root alone (bonus: the root's argmax) while the
+    other requests of the batch walk their trees; the cache is untouched for them."""
+    rng = np.random.default_rng(11)
+    b, t_max, depth = 6, 40, 7
+    trees = [gc.random_tree(rng, t_max, depth) for _ in range(b)]
+    tokens, targets = [], []
+    for p in trees:
+        tok = rng.integers(0, 50, len(p)).astype(np.int32)
+        tgt = rng.integers(0, 50, len(p)).astype(np.int32)
+        for c in range(1, len(p)):  # plant matches so trees accept more than the root
+            if rng.random() < 0.6:
+                tgt[p[c]] = tok[c]
+        tokens.append(tok)
+        targets.append(tgt)
+    valid = [1, 0, 1, 0, 0, 1]
+    prefix = np.full(b, 100, np.int32)
+    got = run(trees, tokens, targets, prefix, t_max, depth, valid=valid)
+    check_walk(got, trees, tokens, targets, prefix, depth, valid=valid)
+    assert all(got["accept_len"][i] == 1 for i in range(b) if not valid[i])

@@ -95,3 +95,13 @@ def test_every_valid_path_is_reachable_by_some_target():
         for a, b in zip(chain, chain[1:]):
             target[a] = tokens[b]
         assert accept.greedy_walk(tokens, parents, target)[0] == chain
+
+
+def test_request_without_a_tree_accepts_the_root_only():
+    """A released slot (tree_valid false) takes the single-token path even where the
+    target would accept a child: path [0], bonus = the target's argmax at the root."""
+    parents = [-1, 0, 0, 1]
+    tokens = [5, 7, 8, 9]
+    target = [7, 9, 3, 4]  # with a tree: 0 -> 1 -> 3
+    assert accept.greedy_walk(tokens, parents, target) == ([0, 1, 3], 4)
+    assert accept.greedy_walk(tokens, parents, target, tree_valid=False) == ([0], 7)

@@ -68,7 +68,7 @@ _SIGNATURES = {
     "tsv_tree_verify_attn": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_float] * 2 +
                              [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                               ctypes.c_void_p, ctypes.c_void_p]),
-    "tsv_accept_and_compact": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int] * 3 +
+    "tsv_accept_and_compact": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 3 +
                                [ctypes.c_void_p] * 8),
     "tsv_tree_verify_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 9 +
                                      [ctypes.c_float] * 2 + [ctypes.c_void_p] * 3),
@@ -326,7 +326,7 @@ def tree_verify_attn_noalloc(q, k_new, v_new, cache: KVCache, prefix_len, num_no
 
 def accept_and_compact(tokens, next_token, next_sibling, target_argmax, num_nodes, prefix_len,
                        max_depth, cache: Optional[KVCache], accept_path, accept_len, bonus_token,
-                       slot_map, new_prefix_len, err=None):
+                       slot_map, new_prefix_len, err=None, tree_valid=None):
     b, t = tokens.shape
     for name, x in (("tokens", tokens), ("next_token", next_token),
                     ("next_sibling", next_sibling), ("target_argmax", target_argmax)):
@@ -340,9 +340,12 @@ def accept_and_compact(tokens, next_token, next_sibling, target_argmax, num_node
     _need(new_prefix_len, torch.int32, "new_prefix_len", (b,))
     if err is not None:
         _need(err, torch.int32, "err", (b,))
+    if tree_valid is not None:
+        _need(tree_valid, torch.int32, "tree_valid", (b,))
     desc = ctypes.byref(cache.desc) if cache is not None else None
     _check(lib().tsv_accept_and_compact(_ptr(tokens), _ptr(next_token), _ptr(next_sibling),
-                                        _ptr(target_argmax), _ptr(num_nodes), _ptr(prefix_len), b,
+                                        _ptr(target_argmax), _ptr(num_nodes), _ptr(prefix_len),
+                                        _ptr(tree_valid), b,
                                         t, max_depth, desc, _ptr(accept_path), _ptr(accept_len),
                                         _ptr(bonus_token), _ptr(slot_map), _ptr(new_prefix_len),
                                         _ptr(err), _stream()),

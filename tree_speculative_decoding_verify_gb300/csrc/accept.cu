@@ -43,7 +43,8 @@ __global__ void __launch_bounds__(THREADS)
 accept_compact_kernel(const int32_t* __restrict__ tokens, const int32_t* __restrict__ next_token,
                       const int32_t* __restrict__ next_sibling, const int32_t* __restrict__ target,
                       const int32_t* __restrict__ num_nodes, const int32_t* __restrict__ prefix_len,
-                      int max_nodes, int max_depth, CacheView cache, bool has_cache,
+                      const int32_t* __restrict__ tree_valid, int max_nodes, int max_depth,
+                      CacheView cache, bool has_cache,
                       int32_t* __restrict__ accept_path, int32_t* __restrict__ accept_len,
                       int32_t* __restrict__ bonus, int32_t* __restrict__ slot_map,
                       int32_t* __restrict__ new_prefix_len, int32_t* __restrict__ err) {
@@ -73,7 +74,9 @@ accept_compact_kernel(const int32_t* __restrict__ tokens, const int32_t* __restr
     int code = size_ok ? TSV_REQ_OK : TSV_REQ_BAD_SIZE;
     int len = 1, node = 0;
     s_path[0] = 0;
-    if (code == TSV_REQ_OK) {
+    // a request without a valid tree takes the single-token path: the root alone
+    const bool has_tree = !tree_valid || tree_valid[b] != 0;
+    if (code == TSV_REQ_OK && has_tree) {
       // Every step goes one level down; a valid tree has at most max_depth levels.
       for (int step = 0; step <= max_depth; ++step) {
         const int pred = s_tgt[node];
@@ -163,7 +166,8 @@ accept_compact_kernel(const int32_t* __restrict__ tokens, const int32_t* __restr
 
 int launch_accept_compact(const int32_t* tokens, const int32_t* next_token,
                           const int32_t* next_sibling, const int32_t* target,
-                          const int32_t* num_nodes, const int32_t* prefix_len, int batch,
+                          const int32_t* num_nodes, const int32_t* prefix_len,
+                          const int32_t* tree_valid, int batch,
                           int max_nodes, int max_depth, const tsv_kv_cache* cache,
                           int32_t* accept_path, int32_t* accept_len, int32_t* bonus,
                           int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,
@@ -187,7 +191,8 @@ int launch_accept_compact(const int32_t* tokens, const int32_t* next_token,
   }
   dim3 grid(batch, ctas_y);
   return launch_pdl(accept_compact_kernel, grid, dim3(THREADS), 0, stream, tokens, next_token,
-                    next_sibling, target, num_nodes, prefix_len, max_nodes, max_depth, cv,
+                    next_sibling, target, num_nodes, prefix_len, tree_valid, max_nodes,
+                    max_depth, cv,
                     cache != nullptr, accept_path, accept_len, bonus, slot_map, new_prefix_len,
                     err);
 }

@@ -217,7 +217,8 @@ int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void*
 
 int tsv_accept_and_compact(const int32_t* tokens, const int32_t* next_token,
                            const int32_t* next_sibling, const int32_t* target_argmax,
-                           const int32_t* num_nodes, const int32_t* prefix_len, int batch,
+                           const int32_t* num_nodes, const int32_t* prefix_len,
+                           const int32_t* tree_valid, int batch,
                            int max_nodes, int max_depth, const tsv_kv_cache* cache,
                            int32_t* accept_path, int32_t* accept_len, int32_t* bonus_token,
                            int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,
@@ -231,7 +232,8 @@ int tsv_accept_and_compact(const int32_t* tokens, const int32_t* next_token,
       !accept_path || !accept_len || !bonus_token || !slot_map || !new_prefix_len)
     return TSV_ERR_INVALID_ARG;
   return launch_accept_compact(tokens, next_token, next_sibling, target_argmax, num_nodes,
-                               prefix_len, batch, max_nodes, max_depth, cache, accept_path,
+                               prefix_len, tree_valid, batch, max_nodes, max_depth, cache,
+                               accept_path,
                                accept_len, bonus_token, slot_map, new_prefix_len, err,
                                (cudaStream_t)stream);
 }

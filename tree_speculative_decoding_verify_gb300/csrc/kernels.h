@@ -17,7 +17,8 @@ int launch_build_meta(const int32_t* parents, const int32_t* num_nodes, const in
 
 int launch_accept_compact(const int32_t* tokens, const int32_t* next_token,
                           const int32_t* next_sibling, const int32_t* target,
-                          const int32_t* num_nodes, const int32_t* prefix_len, int batch,
+                          const int32_t* num_nodes, const int32_t* prefix_len,
+                          const int32_t* tree_valid, int batch,
                           int max_nodes, int max_depth, const tsv_kv_cache* cache,
                           int32_t* accept_path, int32_t* accept_len, int32_t* bonus,
                           int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,

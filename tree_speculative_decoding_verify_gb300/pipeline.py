@@ -127,12 +127,12 @@ class HotPath:
                               self.position_ids, self.mask, rope_theta, softmax_scale, self.out,
                               self.attn_ws, self.s.max_prefix, self.attn_err)
 
-    def accept(self, target_argmax, prefix_len, compact: bool = True):
+    def accept(self, target_argmax, prefix_len, compact: bool = True, tree_valid=None):
         _lib.accept_and_compact(self.tokens, self.next_token, self.next_sibling, target_argmax,
                                 self.num_nodes, prefix_len, self.s.max_depth,
                                 self.cache if compact else None, self.accept_path,
                                 self.accept_len, self.bonus, self.slot_map, self.new_prefix_len,
-                                self.acc_err)
+                                self.acc_err, tree_valid)
 
     def step(self, level_logits, root_token, q, k_new, v_new, prefix_len, target_argmax,
              rope_theta: float, softmax_scale: float,
