@@ -23,6 +23,7 @@ Modules:
   draft      per-row log-softmax + top-k, joint pruning, final total_tokens selection
   attention  RoPE and tree-masked attention over the materialised T x (P+T) mask
   accept     greedy walk (handbook form), evaluate_posterior (EAGLE-2 form), KV compaction
+  lm_head    the target's greedy token at every node (argmax of the lm_head logits)
   step       one whole hot-path pass for one request (used for the CPU baseline)
 """
-from . import tree, draft, attention, accept, step  # noqa: F401
+from . import tree, draft, attention, accept, lm_head, step  # noqa: F401
