@@ -254,6 +254,20 @@ def native(args):
     lvl_ws = hp.topk_ws
     lvl_out = hp.front[1]
 
+    # the target's lm_head over every node of the batch (the greedy token per node)
+    lm_h, lm_v = W.TARGET_LM_HEAD[w.name]
+    lm_rows = b * t_max
+    lm_hidden = torch.from_numpy(W.lm_head_hidden(w, lm_rows, lm_h)).to(torch.bfloat16).to(dev)
+    lm_weight = torch.empty(lm_v, lm_h, dtype=torch.bfloat16, device=dev)
+    for v0, blk in W.lm_head_weight_blocks(w, lm_v, lm_h):
+        lm_weight[v0:v0 + blk.shape[0]] = torch.from_numpy(blk).to(torch.bfloat16).to(dev)
+    lm_argmax = torch.zeros(lm_rows, dtype=torch.int32, device=dev)
+    lm_ws = torch.empty(max(T.lm_head_argmax_workspace_size(lm_rows, lm_v), 256),
+                        dtype=torch.uint8, device=dev)
+
+    def lm_head():
+        T.lm_head_argmax(lm_hidden, lm_weight, lm_argmax, lm_ws)
+
     def topk_level():  # one expansion level (level 2: [B, K, V] rows)
         T.draft_topk_expand(levels[1], k, 2, hp.front[0][1], hp.front[0][2], hp.store_token,
                             hp.store_score, hp.store_parent, *lvl_out, lvl_ws)
@@ -263,9 +277,10 @@ def native(args):
     graphs = {}
     with torch.cuda.stream(stream):
         for _ in range(2):  # warm the allocator and the kernels before capture
-            step(); attn(); topk_level()
+            step(); attn(); topk_level(); lm_head()
         stream.synchronize()
-        for name, fn in (("step", step), ("attn", attn), ("topk", topk_level)):
+        for name, fn in (("step", step), ("attn", attn), ("topk", topk_level),
+                         ("lm_head", lm_head)):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 fn()
@@ -277,7 +292,7 @@ def native(args):
                      for _ in range(n)] for name in graphs}
         with torch.cuda.stream(stream):
             for i in range(n):
-                for name in ("step", "attn", "topk"):
+                for name in ("step", "attn", "topk", "lm_head"):
                     flush_buf.zero_()
                     ev[name][i][0].record(stream)
                     graphs[name].replay()
@@ -409,6 +424,22 @@ def native(args):
                  "peak_source": src, "traffic": traffic("topk", w.name)[0],
                  "traffic_source": traffic("topk", w.name)[1], "algorithmic_bytes": topk_bytes,
                  "us_per_launch": ms["topk"] * 1e3}
+    lm_s = ms["lm_head"] / 1e3
+    lm_bytes = lm_v * lm_h * 2 + lm_rows * lm_h * 2 + lm_rows * 4
+    lm_flops = 2 * lm_rows * lm_v * lm_h
+    lm_bound = "hbm" if lm_bytes / (hbm * 1e9) >= lm_flops / (tf * 1e12) else "tensor"
+    if lm_bound == "hbm":
+        lm_ach, lm_peak, lm_unit = lm_bytes / lm_s / 1e9, hbm, "GB/s"
+    else:
+        lm_ach, lm_peak, lm_unit = lm_flops / lm_s / 1e12, tf, "TFLOP/s"
+    lm_roof = {"kernel": f"lm_head_argmax (tcgen05 GEMM + argmax epilogue, {lm_rows} rows x "
+                         f"{lm_v} vocab x {lm_h} hidden, bf16)",
+               "bound": lm_bound, "achieved": lm_ach, "peak": lm_peak, "unit": lm_unit,
+               "frac": lm_ach / lm_peak, "peak_source": src,
+               "traffic": traffic("lm_head", w.name)[0],
+               "traffic_source": traffic("lm_head", w.name)[1],
+               "algorithmic_bytes": lm_bytes, "algorithmic_flops": lm_flops,
+               "us_per_launch": ms["lm_head"] * 1e3}
     # the dominant kernel of the step: the attention call or the depth + 1 top-k levels
     dominant = "topk" if ms["topk"] * (w.depth + 1) > ms["attn"] else "attn"
     kernels_step = hp.kernels_per_step()
@@ -432,10 +463,13 @@ def native(args):
         "roofline": topk_roof if dominant == "topk" else attn_roof,
         "roofline_attn": attn_roof,
         "roofline_topk": topk_roof,
+        "lm_head_us": ms["lm_head"] * 1e3,
+        "roofline_lm_head": lm_roof,
         "e2e": {"value": world * 1e3 / e2e_step_ms, "unit": UNIT, "ms_per_step": e2e_step_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        # timed region per iteration: the step graph, the attention call, one top-k level
-        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1),
+        # timed region per iteration: the step graph, the attention call, one top-k level,
+        # the lm-head argmax (GEMM + finalize)
+        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1 + 2),
         "wall_s_timed_region": t_wall,
     }
     ck = clocks.summary()

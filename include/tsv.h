@@ -7,6 +7,8 @@
  *   tsv_draft_select_final  the total_tokens best candidates laid out as a tree
  *   tsv_tree_build_meta     ancestor bitmask, positions, retrieve_indices, child/sibling links
  *   tsv_tree_verify_attn    RoPE + KV append + tree-masked split-KV attention of every node
+ *   tsv_lm_head_argmax      the target's greedy token at every node (lm_head GEMM with an
+ *                           argmax epilogue; the logits are never written)
  *   tsv_accept_and_compact  greedy acceptance walk + move of the accepted KV to
  *                           consecutive slots
  *
@@ -299,6 +301,40 @@ int tsv_tree_verify_attn_noalloc(const tsv_attn_shape* shape, const void* q, con
                                  const int32_t* position_ids, const uint32_t* mask,
                                  float rope_theta, float softmax_scale, void* out, int32_t* err,
                                  tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_lm_head_argmax — the target model's greedy token at every tree node.
+ *
+ * [HB] section 实现 (the verifier's forward returns lm_head(norm(x)) for every node; the
+ * walk takes pred = logits[node].argmax()); [EAGLE2] section 5 (evaluate_posterior
+ * compares each candidate with the target's argmax at its parent); [TRT] section
+ * 验证:在树上走一条路径 (target_predict, the argmax at every node, feeds the walk).
+ *
+ * For every row m: argmax[m] = argmax_v sum_k hidden[m, k] * weight[v, k], the LOWEST v
+ * among equal maxima; max_logit[m] = that maximum. bf16 inputs, products accumulated in
+ * fp32 on the tensor cores; the maximum is taken over the fp32 logits, so two logits
+ * closer than the fp32 accumulation error may order differently from an exact sum.
+ *
+ * hidden           [rows, hidden_size] bf16 in: final-normed hidden state of every node
+ *                  (a batch of trees flattened to rows, e.g. batch * max_nodes).
+ * weight           [vocab, hidden_size] bf16 in: the lm_head matrix, row-major.
+ * rows             >= 0 (0 launches nothing).
+ * hidden_size      a positive multiple of 64.
+ * vocab            >= 1, < 2^31.
+ * argmax           [rows] out: the greedy token per row (-1 if a bounded device-side
+ *                  wait gave up; never on a healthy GPU).
+ * max_logit        [rows] fp32 out (may be NULL): the logit of argmax[m] (NaN with -1).
+ * workspace        device scratch of tsv_lm_head_argmax_workspace_size(rows, vocab)
+ *                  bytes (depends on the device's SM count), 256-byte aligned.
+ * hidden and weight must be 16-byte aligned (they are read with the tensor-memory
+ * accelerator). Returns TSV_ERR_UNSUPPORTED on a device without tcgen05 (sm_100 and
+ * later), TSV_ERR_INVALID_ARG for a null pointer, a misaligned input or a size out of
+ * range, TSV_ERR_WORKSPACE for a missing or small workspace.
+ * ------------------------------------------------------------------------------ */
+size_t tsv_lm_head_argmax_workspace_size(int rows, int vocab);
+int tsv_lm_head_argmax(const void* hidden, const void* weight, int rows, int hidden_size,
+                       int vocab, int32_t* argmax, float* max_logit, void* workspace,
+                       size_t workspace_bytes, tsv_stream_t stream);
 
 /* --------------------------------------------------------------------------------
  * tsv_accept_and_compact — greedy acceptance walk and KV compaction.

@@ -70,6 +70,9 @@ _SIGNATURES = {
                               ctypes.c_void_p, ctypes.c_void_p]),
     "tsv_accept_and_compact": (ctypes.c_int, [ctypes.c_void_p] * 7 + [ctypes.c_int] * 3 +
                                [ctypes.c_void_p] * 8),
+    "tsv_lm_head_argmax_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 2),
+    "tsv_lm_head_argmax": (ctypes.c_int, [ctypes.c_void_p] * 2 + [ctypes.c_int] * 3 +
+                           [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]),
     "tsv_tree_verify_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 9 +
                                      [ctypes.c_float] * 2 + [ctypes.c_void_p] * 3),
 }
@@ -322,6 +325,28 @@ def tree_verify_attn_noalloc(q, k_new, v_new, cache: KVCache, prefix_len, num_no
                                               float(rope_theta), float(softmax_scale), _ptr(out),
                                               _ptr(err), _stream()),
            "tsv_tree_verify_attn_noalloc")
+
+
+def lm_head_argmax_workspace_size(rows: int, vocab: int) -> int:
+    return int(lib().tsv_lm_head_argmax_workspace_size(rows, vocab))
+
+
+def lm_head_argmax(hidden, weight, argmax, workspace, max_logit=None):
+    """argmax[m] = the lowest v maximising hidden[m] . weight[v] (bf16 in, fp32 logits).
+    hidden [rows, H] and weight [V, H] bf16; argmax [rows] int32; max_logit [rows] fp32
+    or None; workspace uint8 of lm_head_argmax_workspace_size(rows, V) bytes."""
+    rows, h = hidden.shape
+    v = weight.shape[0]
+    _need(hidden, torch.bfloat16, "hidden")
+    _need(weight, torch.bfloat16, "weight", (v, h))
+    _need(argmax, torch.int32, "argmax", (rows,))
+    if max_logit is not None:
+        _need(max_logit, torch.float32, "max_logit", (rows,))
+    _need(workspace, torch.uint8, "workspace")
+    _check(lib().tsv_lm_head_argmax(_ptr(hidden), _ptr(weight), rows, h, v, _ptr(argmax),
+                                    _ptr(max_logit), _ptr(workspace), workspace.numel(),
+                                    _stream()),
+           "tsv_lm_head_argmax")
 
 
 def accept_and_compact(tokens, next_token, next_sibling, target_argmax, num_nodes, prefix_len,

@@ -215,6 +215,26 @@ int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void*
                      rope_theta, softmax_scale, out, workspace, err, (cudaStream_t)stream);
 }
 
+size_t tsv_lm_head_argmax_workspace_size(int rows, int vocab) {
+  if (rows < 0 || vocab < 1) return 0;
+  return plan_lm_head(rows, vocab).ws_bytes;
+}
+
+int tsv_lm_head_argmax(const void* hidden, const void* weight, int rows, int hidden_size,
+                       int vocab, int32_t* argmax, float* max_logit, void* workspace,
+                       size_t workspace_bytes, tsv_stream_t stream) {
+  if (rows < 0 || vocab < 1 || hidden_size < 64 || hidden_size % 64) return TSV_ERR_INVALID_ARG;
+  if (rows == 0) return TSV_OK;
+  if (!hidden || !weight || !argmax) return TSV_ERR_INVALID_ARG;
+  if (((uintptr_t)hidden | (uintptr_t)weight) & 15u) return TSV_ERR_INVALID_ARG;
+  if (!lm_head_supported()) return TSV_ERR_UNSUPPORTED;
+  const LmPlan plan = plan_lm_head(rows, vocab);
+  if (!workspace || workspace_bytes < plan.ws_bytes || ((uintptr_t)workspace & 255u))
+    return TSV_ERR_WORKSPACE;
+  return launch_lm_head_argmax(plan, hidden, weight, rows, hidden_size, vocab, argmax, max_logit,
+                               workspace, (cudaStream_t)stream);
+}
+
 int tsv_accept_and_compact(const int32_t* tokens, const int32_t* next_token,
                            const int32_t* next_sibling, const int32_t* target_argmax,
                            const int32_t* num_nodes, const int32_t* prefix_len,

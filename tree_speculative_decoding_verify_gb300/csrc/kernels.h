@@ -61,4 +61,17 @@ int launch_attn(const AttnPlan& plan, const void* q, const void* k_new, const vo
                 const int32_t* position_ids, const uint32_t* mask, float rope_theta,
                 float softmax_scale, void* out, void* ws, int32_t* err, cudaStream_t stream);
 
+// Target lm-head argmax (the greedy token at every node).
+struct LmPlan {
+  int m_tiles;        // 128-row tiles of the node rows
+  int chunks;         // 32-entry pieces of the vocabulary
+  int splits;         // vocabulary ranges (CTAs per row tile), whole chunks each
+  size_t ws_bytes;    // one 64-bit key per (split, row)
+};
+LmPlan plan_lm_head(int rows, int vocab);
+bool lm_head_supported();
+int launch_lm_head_argmax(const LmPlan& plan, const void* hidden, const void* weight, int rows,
+                          int hidden_size, int vocab, int32_t* argmax, float* max_logit,
+                          void* ws, cudaStream_t stream);
+
 }  // namespace tsv

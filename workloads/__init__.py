@@ -45,7 +45,15 @@ KV_BLOCK = 64  # tokens per paged KV block
 _STREAMS = {
     "logits": 1, "q": 2, "k_new": 3, "v_new": 4, "k_cache": 5, "v_cache": 6,
     "prefix": 7, "blocks": 8, "root": 9, "target": 10, "tokens": 11, "pad": 12,
+    "lm_hidden": 13, "lm_weight": 14,
 }
+
+# (hidden size, vocabulary) of the target model whose lm_head gives the greedy token at
+# every node: Llama-3-8B (4096 x 128256) for the 8B-shaped workloads, Llama-3-70B
+# (8192 x 128256) for the 70B-shaped one; a small head for the tiny tree.
+TARGET_LM_HEAD = {"tiny": (64, 1000), "llama8b": (4096, 128256), "serving": (4096, 128256),
+                  "long70b": (8192, 128256), "sweep": (4096, 128256)}
+LM_WEIGHT_BLOCK = 8192  # vocabulary rows per weight draw
 
 
 @dataclasses.dataclass(frozen=True)
@@ -218,3 +226,19 @@ def block_table(w: Workload, capacity_slots: int, pool_blocks: Optional[int] = N
     pool = pool_blocks or need
     perm = rng(w, "blocks").permutation(pool).astype(np.int32)
     return perm[:need].reshape(w.batch, per_req), pool
+
+
+def lm_head_hidden(w: Workload, rows: int, hidden: int, key: int = 0) -> np.ndarray:
+    """[rows, hidden] fp32 draws ~ N(0, 1): the final-normed hidden state of every node
+    (to be cast to bf16)."""
+    return rng(w, "lm_hidden", key).standard_normal((rows, hidden), dtype=np.float32)
+
+
+def lm_head_weight_blocks(w: Workload, vocab: int, hidden: int, key: int = 0):
+    """The lm_head weight [vocab, hidden] ~ N(0, 1/sqrt(hidden)) as (v0, fp32 block) pairs
+    of LM_WEIGHT_BLOCK rows, each from its own stream (to be cast to bf16)."""
+    scale = np.float32(1.0 / math.sqrt(hidden))
+    for j, v0 in enumerate(range(0, vocab, LM_WEIGHT_BLOCK)):
+        n = min(LM_WEIGHT_BLOCK, vocab - v0)
+        g = rng(w, "lm_weight", key, j)
+        yield v0, (g.standard_normal((n, hidden), dtype=np.float32) * scale).astype(np.float32)
