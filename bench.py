@@ -96,6 +96,7 @@ TRAFFIC = {
     ("attn", "long70b"): (606232320 + 41901824, "profiles/attn_tc_kernel_long70b.md"),
     ("topk", "llama8b"): (1354240 + 0, "profiles/topk_level_kernel_llama8b.md"),
     ("topk", "sweep"): (328446464 + 2847488, "profiles/topk_level_kernel_sweep.md"),
+    ("lm_head", "llama8b"): (1052517376 + 3688704, "profiles/lm_head_argmax_kernel_llama8b.md"),
 }
 
 

@@ -318,7 +318,7 @@ int tsv_tree_verify_attn_noalloc(const tsv_attn_shape* shape, const void* q, con
  * hidden           [rows, hidden_size] bf16 in: final-normed hidden state of every node
  *                  (a batch of trees flattened to rows, e.g. batch * max_nodes).
  * weight           [vocab, hidden_size] bf16 in: the lm_head matrix, row-major.
- * rows             >= 0 (0 launches nothing).
+ * rows             0 .. 2^24 (0 launches nothing).
  * hidden_size      a positive multiple of 64.
  * vocab            >= 1, < 2^31.
  * argmax           [rows] out: the greedy token per row (-1 if a bounded device-side

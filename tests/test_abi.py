@@ -80,8 +80,19 @@ def test_host_validation_rejects_bad_arguments(lib):
     cache.capacity = 100
     assert lib.tsv_accept_and_compact(p, p, p, p, p, p, None, 1, 61, 7, ctypes.byref(cache),
                                       p, p, p, p, p, None, None) == 1
+    # lm_head argmax: hidden size not a multiple of 64, negative rows, misaligned input,
+    # workspace sizing (one 64-bit key per vocabulary range and row)
+    assert lib.tsv_lm_head_argmax(p, p, 61, 96, 128256, p, None, p, 1 << 20, None) == 1
+    assert lib.tsv_lm_head_argmax(p, p, -1, 4096, 128256, p, None, p, 1 << 20, None) == 1
+    assert lib.tsv_lm_head_argmax(ctypes.c_void_p(24), p, 61, 4096, 128256, p, None, p,
+                                  1 << 20, None) == 1
+    assert lib.tsv_lm_head_argmax_workspace_size(-1, 100) == 0
+    assert lib.tsv_lm_head_argmax_workspace_size(61, 0) == 0
+    ws = lib.tsv_lm_head_argmax_workspace_size(61, 128256)
+    assert ws > 0 and ws % 256 == 0 and ws >= 61 * 8
 
 
 def test_empty_batch_is_a_no_op(lib):
+    assert lib.tsv_lm_head_argmax(None, None, 0, 64, 10, None, None, None, 0, None) == 0
     assert lib.tsv_tree_build_meta(None, None, None, 0, 8, 3, None, None, None, None, None,
                                    None, None, None) == 0

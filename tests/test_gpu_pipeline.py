@@ -94,3 +94,48 @@ def test_whole_step_matches_oracle(name):
                                    atol=1e-6)
         np.testing.assert_array_equal(vc[0, :, :p_len + n].float().cpu().numpy(),
                                       want["v_cache"][:, :p_len + n])
+
+
+def test_step_with_the_lm_head_stage():
+    """The step with the target's lm_head in it: the greedy token of every node comes from
+    tsv_lm_head_argmax over the nodes' hidden states, and the walk follows it. Hidden
+    states are planted (a scaled copy of the wanted token's weight row plus noise) so the
+    oracle's argmax walks a chosen path; the oracle's argmax feeds the oracle's walk."""
+    import math
+
+    import tree_speculative_decoding_verify_gb300 as T
+    from oracle import accept, lm_head
+
+    w = W.WORKLOADS["llama8b"].with_(vocab=2048, top_k=4, depth=2, total_tokens=8,
+                                     prefix=("fixed", 200), num_q_heads=8, num_kv_heads=2)
+    d = gc.dev()
+    hdim, p_len = 256, 200
+    tokens, parents, _ = gc.oracle_tree(w, 0)
+    planted = W.plant_target(w, 0, tokens, parents)
+    t_max = w.num_nodes
+    weight = gc.as_bf16_f64(next(W.lm_head_weight_blocks(w, w.vocab, hdim))[1])
+    noise = W.lm_head_hidden(w, t_max, hdim) * 0.05
+    hidden = gc.as_bf16_f64(4.0 * weight[planted] + noise)
+    target, _ = lm_head.lm_head_argmax(hidden, weight)
+    assert target.tolist() == planted.tolist()  # the planted margins hold in fp64
+    path, bonus = accept.greedy_walk(list(tokens), list(parents), list(target))
+
+    q, k_new, v_new = W.new_qkv(w)
+    cap = 256
+    kc = torch.zeros(1, 2, cap, 128, dtype=torch.bfloat16, device=d)
+    vc = torch.zeros_like(kc)
+    shape = T.TreeShape(1, 8, 2, 128, p_len, vocab=w.vocab, top_k=w.top_k, depth=w.depth,
+                        total_tokens=w.total_tokens, target_vocab=w.vocab)
+    hp = T.HotPath(shape, T.KVCache(kc, vc))
+    levels = [torch.from_numpy(x[None]).to(d) for x in gc.level_logits(w, 0)]
+    bf = lambda x: gc.to_dev(x, torch.bfloat16)
+    hp.step(levels, gc.i32(W.root_tokens(w)[:1]), bf(q), bf(k_new), bf(v_new), gc.i32([p_len]),
+            None, w.theta, 1 / math.sqrt(128), hidden=bf(hidden[None]), lm_weight=bf(weight))
+    torch.cuda.synchronize()
+    assert hp.tokens.cpu().numpy()[0].tolist() == tokens.tolist()
+    assert hp.target.cpu().numpy()[0, :t_max].tolist() == target.tolist()
+    n = hp.accept_len.item()
+    assert n == len(path) and n >= 1
+    assert hp.accept_path.cpu().numpy()[0, :n].tolist() == list(path)
+    assert hp.bonus.item() == bonus
+    assert hp.kernels_per_step(lm_head=True) == hp.kernels_per_step() + 2

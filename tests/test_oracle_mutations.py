@@ -100,3 +100,40 @@ def test_in_place_compaction_order_error_is_caught(monkeypatch):
     monkeypatch.setattr(accept, "compact", wrong)
     with pytest.raises(AssertionError):
         ta.test_compaction_moves_rows_and_keeps_the_rest()
+
+
+def _lm_head_variant(later_tie_wins=False, drop_chunk_offset=False, smallest=False):
+    """lm_head_argmax with one planted mistake (written out here, not shared)."""
+    def f(hidden, weight, chunk=8192):
+        h = np.asarray(hidden, np.float64)
+        rows, v = h.shape[0], weight.shape[0]
+        best = np.full(rows, np.inf if smallest else -np.inf)
+        idx = np.zeros(rows, np.int64)
+        for v0 in range(0, v, chunk):
+            lg = h @ np.asarray(weight[v0:v0 + chunk], np.float64).T
+            j = lg.argmin(axis=1) if smallest else lg.argmax(axis=1)
+            m = lg[np.arange(rows), j]
+            if smallest:
+                better = m < best
+            else:
+                better = m >= best if later_tie_wins else m > best
+            best[better] = m[better]
+            idx[better] = (0 if drop_chunk_offset else v0) + j[better]
+        return idx, best
+    return f
+
+
+@pytest.mark.parametrize("mistake", ["later_tie_wins", "drop_chunk_offset", "smallest"])
+def test_lm_head_mistakes_are_caught(monkeypatch, mistake):
+    from oracle import lm_head
+    from tests import test_oracle_lm_head as tl
+    monkeypatch.setattr(lm_head, "lm_head_argmax", _lm_head_variant(**{mistake: True}))
+    pins = (tl.test_planted_rows_win_by_a_margin, tl.test_ties_go_to_the_lower_index_across_chunks,
+            tl.test_negative_logits_and_a_single_entry)
+    failed = 0
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed >= 1

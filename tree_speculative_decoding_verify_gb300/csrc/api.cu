@@ -216,14 +216,15 @@ int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void*
 }
 
 size_t tsv_lm_head_argmax_workspace_size(int rows, int vocab) {
-  if (rows < 0 || vocab < 1) return 0;
+  if (rows < 0 || rows > (1 << 24) || vocab < 1) return 0;
   return plan_lm_head(rows, vocab).ws_bytes;
 }
 
 int tsv_lm_head_argmax(const void* hidden, const void* weight, int rows, int hidden_size,
                        int vocab, int32_t* argmax, float* max_logit, void* workspace,
                        size_t workspace_bytes, tsv_stream_t stream) {
-  if (rows < 0 || vocab < 1 || hidden_size < 64 || hidden_size % 64) return TSV_ERR_INVALID_ARG;
+  if (rows < 0 || rows > (1 << 24) || vocab < 1 || hidden_size < 64 || hidden_size % 64)
+    return TSV_ERR_INVALID_ARG;
   if (rows == 0) return TSV_OK;
   if (!hidden || !weight || !argmax) return TSV_ERR_INVALID_ARG;
   if (((uintptr_t)hidden | (uintptr_t)weight) & 15u) return TSV_ERR_INVALID_ARG;

@@ -10,20 +10,23 @@
 //
 // logits[m, v] = sum_k hidden[m, k] * weight[v, k]: a GEMM of the node rows (M) against
 // the vocabulary (N) over the hidden size (K) on the 5th-generation tensor cores, bf16 in,
-// fp32 accumulate in TMEM. One CTA = one M tile of 128 rows x a contiguous range of
-// 256-entry vocabulary tiles:
+// fp32 accumulate in TMEM. One CTA = one M tile of 128 rows x one vocabulary range; the
+// ranges are whole 32-entry chunks, as equal as the chunk count allows, so every CTA of a
+// wave streams the same number of weight bytes. A range is walked in 256-entry tiles from
+// its first entry; its last tile may be narrower (then N = its width rounded up to 32).
 //   warp 4      TMA producer: 64-column panels of the row tile (128 x 64) and of the
-//               vocabulary tile (256 x 64), 128-byte swizzle, into a 4-stage ring
-//   warp 5      TMEM allocator + MMA issuer: tcgen05.mma M=128 N=256 K=16, A and B from
+//               vocabulary tile (256 x 64 in one copy, or 32-row copies for a narrow
+//               tile), 128-byte swizzle, into a 4-stage ring
+//   warp 5      TMEM allocator + MMA issuer: tcgen05.mma M=128 N<=256 K=16, A and B from
 //               shared memory (K-major), four per panel, into one of two TMEM
 //               accumulators (256 columns each) so the next tile's MMAs overlap the
 //               epilogue of this one
-//   warps 0-3   epilogue; thread = row = TMEM lane: two x128 TMEM loads per tile, the
-//               first maximum of the tile's valid columns, folded into the row's running
-//               best as a 64-bit key (larger value first, then lower index)
+//   warps 0-3   epilogue; thread = row = TMEM lane: x128 TMEM loads, the first maximum
+//               of the tile's valid columns, folded into the row's running best as a
+//               64-bit key (larger value first, then lower index)
 // Each CTA writes its best key per row; a second kernel takes the largest key of every
-// row over the vocabulary splits. Every mbarrier wait is bounded (a timeout marks the row
-// keys invalid through the abort path and the CTA drains and frees its TMEM).
+// row over the vocabulary ranges. Every mbarrier wait is bounded (a timeout marks the
+// row keys invalid through the abort path and the CTA drains and frees its TMEM).
 #include <cuda.h>
 
 #include <algorithm>
@@ -235,22 +238,29 @@ lm_head_argmax_kernel(const __grid_constant__ CUtensorMap tm_a,
   }
 }
 
-// The largest key of every row over the vocabulary splits -> argmax (and its logit). A key
-// of 0 (a split whose bounded wait gave up) gives -1.
-__global__ void __launch_bounds__(256)
+// The largest key of every row over the vocabulary ranges -> argmax (and its logit); one
+// warp per row, the lanes striding over the ranges (the loads of a row are independent,
+// so they overlap). A key of 0 (a range whose bounded wait gave up) gives -1.
+constexpr int FIN_THREADS = 256;
+__global__ void __launch_bounds__(FIN_THREADS)
 lm_head_finalize_kernel(const unsigned long long* __restrict__ keys, int rows, int splits,
                         int32_t* __restrict__ argmax, float* __restrict__ max_logit) {
   griddep_wait();
   griddep_launch();
-  const int r = blockIdx.x * 256 + threadIdx.x;
-  if (r >= rows) return;
+  const int r = (int)((blockIdx.x * (unsigned)FIN_THREADS + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;  // whole warps leave together
   unsigned long long k = 0ull;
   bool bad = false;
-  for (int s = 0; s < splits; ++s) {
+  for (int s = lane; s < splits; s += 32) {
     const unsigned long long x = keys[(size_t)s * rows + r];
     bad |= x == 0ull;
     k = max(k, x);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) k = max(k, __shfl_xor_sync(FULL, k, o));
+  bad = __any_sync(FULL, bad);
+  if (lane != 0) return;
   if (bad) {
     argmax[r] = -1;
     if (max_logit) max_logit[r] = __int_as_float(0x7fc00000);
@@ -319,7 +329,8 @@ int launch_lm_head_argmax(const LmPlan& plan, const void* hidden, const void* we
   int st = launch_pdl(lm_head_argmax_kernel, dim3(plan.m_tiles, plan.splits), dim3(LM_THREADS),
                       LM_SMEM_BYTES, stream, ma, mb, mb32, prm);
   if (st != TSV_OK) return st;
-  return launch_pdl(lm_head_finalize_kernel, dim3((unsigned)ceil_div(rows, 256)), dim3(256), 0,
+  return launch_pdl(lm_head_finalize_kernel,
+                    dim3((unsigned)ceil_div((int64_t)rows * 32, FIN_THREADS)), dim3(FIN_THREADS), 0,
                     stream, static_cast<const unsigned long long*>(ws), rows, plan.splits,
                     argmax, max_logit);
 }

@@ -1,7 +1,8 @@
 """One hot-path step over preallocated device buffers.
 
     draft expansion (depth + 1 levels) -> final selection -> tree metadata ->
-    tree-verification attention (one layer) -> greedy acceptance + KV compaction
+    tree-verification attention (one layer) -> [target lm-head argmax per node] ->
+    greedy acceptance + KV compaction
 
 Every stage is one or two calls into libtsv.so on the current stream; no stage reads
 anything back to the host, so a whole step can be captured in a CUDA graph.
@@ -29,6 +30,7 @@ class TreeShape:
     total_tokens: int = 0     # draft nodes kept; the tree has total_tokens + 1 nodes
     fixed_nodes: int = 0      # > 0: trees are given directly (no expansion)
     fixed_max_depth: int = 0
+    target_vocab: int = 0     # > 0: the target's lm_head runs in the step (its vocabulary)
 
     @property
     def max_nodes(self) -> int:
@@ -85,6 +87,10 @@ class HotPath:
         self.bonus = torch.zeros(b, **i32)
         self.slot_map = torch.zeros(b, shape.max_depth + 1, 2, **i32)
         self.new_prefix_len = torch.zeros(b, **i32)
+        if shape.target_vocab:
+            self.target = torch.zeros(b, t, **i32)
+            ws = _lib.lm_head_argmax_workspace_size(b * t, shape.target_vocab)
+            self.lm_ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
 
     # -- stages ------------------------------------------------------------------------
     def expand(self, level_logits: Sequence[torch.Tensor], root_token: torch.Tensor,
@@ -127,6 +133,21 @@ class HotPath:
                               self.position_ids, self.mask, rope_theta, softmax_scale, self.out,
                               self.attn_ws, self.s.max_prefix, self.attn_err)
 
+    def greedy_targets(self, hidden: torch.Tensor, lm_weight: torch.Tensor):
+        """The target's greedy token at every node: hidden [B, max_nodes, H] bf16 (the
+        final-normed hidden state of each node), lm_weight [target_vocab, H] bf16 ->
+        self.target [B, max_nodes] int32 (rows past a tree's num_nodes are computed too
+        and never read by the walk)."""
+        if not self.s.target_vocab:
+            raise ValueError("TreeShape.target_vocab is 0: no lm_head stage")
+        b, t = self.s.batch, self.s.max_nodes
+        if hidden.dim() != 3 or hidden.shape[:2] != (b, t):
+            raise ValueError(f"hidden must be [{b}, {t}, H]")
+        if lm_weight.shape[0] != self.s.target_vocab:
+            raise ValueError(f"lm_weight must have {self.s.target_vocab} rows")
+        _lib.lm_head_argmax(hidden.view(b * t, hidden.shape[2]), lm_weight,
+                            self.target.view(b * t), self.lm_ws)
+
     def accept(self, target_argmax, prefix_len, compact: bool = True, tree_valid=None):
         _lib.accept_and_compact(self.tokens, self.next_token, self.next_sibling, target_argmax,
                                 self.num_nodes, prefix_len, self.s.max_depth,
@@ -137,24 +158,33 @@ class HotPath:
     def step(self, level_logits, root_token, q, k_new, v_new, prefix_len, target_argmax,
              rope_theta: float, softmax_scale: float,
              level_ready: Optional[Sequence[torch.cuda.Event]] = None,
-             inputs_ready: Optional[torch.cuda.Event] = None):
+             inputs_ready: Optional[torch.cuda.Event] = None,
+             hidden: Optional[torch.Tensor] = None, lm_weight: Optional[torch.Tensor] = None):
         """One hot-path step. level_ready (see expand) and inputs_ready (q, k_new, v_new,
-        prefix_len and target_argmax in place before the tree metadata) let the inputs
-        arrive on another stream while the expansion runs."""
+        prefix_len and target_argmax or hidden in place before the tree metadata) let the
+        inputs arrive on another stream while the expansion runs. With hidden and
+        lm_weight (and target_argmax None) the target's greedy tokens come from the
+        lm_head stage (greedy_targets) instead of being given."""
         if not self.s.fixed_nodes:
             self.expand(level_logits, root_token, level_ready)
         if inputs_ready is not None:
             torch.cuda.current_stream().wait_event(inputs_ready)
         self.build_meta(prefix_len)
         self.verify(q, k_new, v_new, prefix_len, rope_theta, softmax_scale)
+        if hidden is not None:
+            if target_argmax is not None:
+                raise ValueError("give target_argmax or hidden + lm_weight, not both")
+            self.greedy_targets(hidden, lm_weight)
+            target_argmax = self.target
         self.accept(target_argmax, prefix_len)
 
     # launches of libtsv kernels per step (for the bench's launch count)
-    def kernels_per_step(self) -> int:
+    def kernels_per_step(self, lm_head: bool = False) -> int:
         """libtsv kernels one step launches: one per expansion level, the final
-        selection, the metadata, the attention call and the acceptance."""
+        selection, the metadata, the attention call, the lm_head stage (GEMM + finalize)
+        when it runs, and the acceptance."""
         n = 0 if self.s.fixed_nodes else (self.s.depth + 1) + 1
-        return n + 1 + self.attn_kernels() + 1
+        return n + 1 + self.attn_kernels() + (2 if lm_head else 0) + 1
 
     def attn_kernels(self) -> int:
         """Kernels of one tree_verify_attn call: prep, the attention kernel (tensor-core
