@@ -24,6 +24,7 @@ Modules:
   attention  RoPE and tree-masked attention over the materialised T x (P+T) mask
   accept     greedy walk (handbook form), evaluate_posterior (EAGLE-2 form), KV compaction
   lm_head    the target's greedy token at every node (argmax of the lm_head logits)
+  sampling   non-greedy acceptance: filtered target probabilities, tree rejection walk
   step       one whole hot-path pass for one request (used for the CPU baseline)
 """
-from . import tree, draft, attention, accept, lm_head, step  # noqa: F401
+from . import tree, draft, attention, accept, lm_head, sampling, step  # noqa: F401

@@ -137,3 +137,62 @@ def test_lm_head_mistakes_are_caught(monkeypatch, mistake):
         except AssertionError:
             failed += 1
     assert failed >= 1
+
+
+def _mutant(module, name, old, new):
+    """module.name with one planted change (a textual substitution of its source)."""
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(getattr(module, name)))
+    assert old in src, old
+    ns = dict(vars(module))
+    exec(compile(src.replace(old, new, 1), f"<mutant {name}>", "exec"), ns)
+    return ns[name]
+
+
+SAMPLING_MISTAKES = [
+    # (function, planted change, the pin that must fail)
+    ("rejection_walk", "p = resid / s", "p = resid",
+     "test_first_emitted_token_follows_the_target"),
+    ("rejection_walk", "resid[x] = 0.0", "pass",
+     "test_first_emitted_token_follows_the_target"),
+    ("rejection_walk", "if u_node[c] < min(1.0, ratio):", "if u_node[c] >= min(1.0, ratio):",
+     "test_zero_temperature_is_the_greedy_walk"),
+    ("filter_probs", "if not first and before >= top_p * total:",
+     "if not first and before + e[t] > top_p * total:",
+     "test_top_p_keeps_the_token_that_crosses"),
+    ("filter_probs", "total = e[keep].sum()", "total = e.sum()",
+     "test_top_p_applies_to_the_renormalised_top_k"),
+    ("filter_probs", "keep &= e >= min_p * e[keep].max()", "keep &= e >= min_p * e.sum()",
+     "test_min_p_is_relative_to_the_largest"),
+    ("filter_probs", "order = np.lexsort((np.arange(v), -lg))",
+     "order = np.lexsort((-np.arange(v), -lg))", "test_top_k_keeps_the_lower_id_on_a_tie"),
+    ("sample_inverse_cdf", 'side="right"', 'side="left"', "test_inverse_cdf_skips_zero_mass"),
+]
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("fn,old,new,pin", SAMPLING_MISTAKES)
+def test_sampling_mistakes_are_caught(monkeypatch, fn, old, new, pin):
+    import inspect
+
+    from oracle import sampling
+    from tests import test_oracle_sampling as ts
+    monkeypatch.setattr(sampling, fn, _mutant(sampling, fn, old, new))
+    test = getattr(ts, pin)
+    marks = getattr(test, "pytestmark", [])
+    cases = []
+    for m in marks:
+        if m.name == "parametrize":
+            names = [a.strip() for a in m.args[0].split(",")]
+            for vals in m.args[1]:
+                cases.append(dict(zip(names, vals if len(names) > 1 else (vals,))))
+    cases = cases or [{}]
+    failed = 0
+    for case in cases:
+        try:
+            test(**case)
+        except AssertionError:
+            failed += 1
+    assert failed >= 1, f"{fn}: {new!r} passed every case of {pin}"
+    assert inspect.isfunction(test)
