@@ -26,8 +26,10 @@ Readings (the pages leave these open; the plainest reading that the rest support
     logits (ties to the lower token id); top-p keeps, in that order, every token whose
     preceding mass is below top_p of the total (so the token that crosses is kept and
     at least one token always is); min-p keeps tokens whose probability is at least
-    min_p times the largest one. temperature 0 is greedy: all mass on the first
-    maximum.
+    min(min_p, 1) times the largest one (the most likely token always stays).
+    temperature 0 (or below, or NaN) is greedy: all mass on the first maximum; so are
+    top_k = 1, top_p <= 0 and a row whose largest logit is not finite. NaN logits read
+    as -inf.
   * An accepted child's node becomes the current node; when a node has no children,
     or all of them are rejected, one token is sampled from the current distribution
     (the residual after the rejections made at that node) and the walk ends. The
@@ -49,8 +51,9 @@ def filter_probs(logits, temperature: float, top_k: int = 0, top_p: float = 1.0,
     top_k <= 0 or >= V, top_p >= 1 and min_p <= 0 switch the filter off.
     """
     lg = np.asarray(logits, np.float64)
+    lg = np.where(np.isnan(lg), -np.inf, lg)  # a NaN logit never wins
     v = lg.shape[0]
-    if temperature <= 0.0:
+    if not temperature > 0.0 or top_k == 1 or top_p <= 0.0 or not np.isfinite(lg.max()):
         p = np.zeros(v)
         p[int(np.argmax(lg))] = 1.0  # the first maximum
         return p
@@ -71,7 +74,7 @@ def filter_probs(logits, temperature: float, top_k: int = 0, top_p: float = 1.0,
             before += e[t]
             first = False
     if min_p > 0.0:
-        keep &= e >= min_p * e[keep].max()
+        keep &= e >= min(min_p, 1.0) * e[keep].max()
     p = np.where(keep, e, 0.0)
     return p / p.sum()
 

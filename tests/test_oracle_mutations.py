@@ -163,7 +163,8 @@ SAMPLING_MISTAKES = [
      "test_top_p_keeps_the_token_that_crosses"),
     ("filter_probs", "total = e[keep].sum()", "total = e.sum()",
      "test_top_p_applies_to_the_renormalised_top_k"),
-    ("filter_probs", "keep &= e >= min_p * e[keep].max()", "keep &= e >= min_p * e.sum()",
+    ("filter_probs", "keep &= e >= min(min_p, 1.0) * e[keep].max()",
+     "keep &= e >= min(min_p, 1.0) * e.sum()",
      "test_min_p_is_relative_to_the_largest"),
     ("filter_probs", "order = np.lexsort((np.arange(v), -lg))",
      "order = np.lexsort((-np.arange(v), -lg))", "test_top_k_keeps_the_lower_id_on_a_tie"),

@@ -134,3 +134,16 @@ def test_rejected_tokens_are_never_the_correction():
         path, tok = sampling.rejection_walk(tokens, parents, [p, p, p], u, rng.random())
         if path == [0]:
             assert tok not in (0, 1)
+
+
+def test_degenerate_parameters():
+    """min_p above 1 keeps the largest; a non-finite maximum or top_p <= 0 is greedy; NaN
+    never wins."""
+    assert sampling.filter_probs(L4, 1.0, min_p=3.0).tolist() == [1.0, 0.0, 0.0, 0.0]
+    assert sampling.filter_probs(L4, 1.0, top_p=-0.5).tolist() == [1.0, 0.0, 0.0, 0.0]
+    lg = np.array([0.0, np.inf, np.inf, 1.0])
+    assert sampling.filter_probs(lg, 1.0).tolist() == [0.0, 1.0, 0.0, 0.0]
+    lg = np.array([np.nan, -1.0, 2.0])
+    assert sampling.filter_probs(lg, 0.0).tolist() == [0.0, 0.0, 1.0]
+    assert np.isfinite(sampling.filter_probs(lg, 1.0)).all()
+    assert sampling.filter_probs(np.full(3, -np.inf), 1.0).tolist() == [1.0, 0.0, 0.0]
