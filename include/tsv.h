@@ -11,6 +11,9 @@
  *                           argmax epilogue; the logits are never written)
  *   tsv_accept_and_compact  greedy acceptance walk + move of the accepted KV to
  *                           consecutive slots
+ *   tsv_tree_sample_accept  non-greedy acceptance: filtered target probabilities per node,
+ *                           tree rejection walk, correction sample, KV move
+ *   tsv_target_probs        the filtered target probabilities themselves
  *
  * Pages cited (by title):
  *   [TRT]    "TensorRT-LLM 源码完全拆解(二十二): EAGLE-3 一体式草稿——三层隐状态、草稿循环
@@ -335,6 +338,75 @@ size_t tsv_lm_head_argmax_workspace_size(int rows, int vocab);
 int tsv_lm_head_argmax(const void* hidden, const void* weight, int rows, int hidden_size,
                        int vocab, int32_t* argmax, float* max_logit, void* workspace,
                        size_t workspace_bytes, tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_tree_sample_accept — non-greedy acceptance on the tree (rejection sampling).
+ *
+ * [TRT] section 非贪心:只靠目标分布的拒绝采样: the target's logits at every node are
+ * filtered into probabilities with the request's sampling parameters (temperature,
+ * top-k, top-p, min-p); the walk follows next_token / next_sibling, makes a probability
+ * test for each candidate and, where it stops, samples a correction token from the
+ * target's distribution ("target-only": no draft probabilities needed).
+ * [HB] section 练习, exercise 2 (采样时的树): accept candidate x with probability
+ * min(1, p(x)/q(x)); on a rejection p <- norm(max(0, p - q)) and try the next candidate;
+ * all rejected: sample one token from the last residual.
+ *
+ * Per node, the filtered distribution (in this order):
+ *   temperature  <= 0 or NaN: greedy (all mass on the first maximum);
+ *   top_k        keep the top_k largest logits, ties to the lower token id (<= 0 or
+ *                >= vocab: off; 1: greedy);
+ *   top_p        on the renormalised result, in that order, keep every token whose
+ *                preceding mass is below top_p of the total (the crossing token is kept;
+ *                >= 1 or NaN: off; <= 0: only the first token);
+ *   min_p        keep tokens whose mass is at least min(min_p, 1) times the largest
+ *                (<= 0 or NaN: off);
+ * then p(v) = exp((l_v - max l) / temperature) over the kept tokens, normalised. Masses
+ * are fp32 (2^((l - m) log2(e) / T)) summed as 2^-40 fixed point.
+ * The walk: at the current node take its children in ascending node order; child c
+ * with token x is accepted when u_node[c] < min(1, p(x) / q(x)), q(x) = 1 for
+ * target-only (draft_probs NULL), else q = draft_probs[b][node] (the distribution the
+ * node's children were drawn from). A rejection replaces p by the residual (target-only:
+ * p without x; draft-aware: max(0, p - q)), renormalised; a residual of zero mass leaves
+ * p as it was. An accepted child becomes the current node. Where no child is accepted
+ * (or there are none) the walk stops and bonus_token is sampled from the current
+ * residual by inverse CDF in token-id order: the smallest t whose running sum exceeds
+ * u_final[b] times the total.
+ *
+ * target_logits    [batch, max_nodes, vocab] fp32 in (NaN reads as -inf).
+ * draft_probs      [batch, max_nodes, vocab] fp32 in, or NULL (target-only).
+ * temperature, top_p, min_p  [batch] fp32 in; top_k [batch] int32 in.
+ * u_node           [batch, max_nodes] fp32 in: uniforms in [0, 1), one per node (the
+ *                  test of node c as a candidate of its parent).
+ * u_final          [batch] fp32 in: uniform in [0, 1) of the final sample.
+ * tokens, next_token, next_sibling, num_nodes, prefix_len, tree_valid, max_depth,
+ * cache, accept_path, accept_len, slot_map, new_prefix_len, err: as for
+ *                  tsv_accept_and_compact (a request without a tree, or with an error,
+ *                  accepts the root alone and its token is sampled at the root; with
+ *                  TSV_REQ_BAD_SIZE bonus_token is -1).
+ * bonus_token      [batch] out: the sampled token where the walk stopped.
+ * workspace        tsv_tree_sample_accept_workspace_size(batch, max_nodes) bytes,
+ *                  256-byte aligned; nothing in it has to start at zero.
+ * Returns TSV_ERR_INVALID_ARG for a null pointer, vocab < 1, or sizes out of range.
+ * ------------------------------------------------------------------------------ */
+size_t tsv_tree_sample_accept_workspace_size(int batch, int max_nodes);
+int tsv_tree_sample_accept(const float* target_logits, const float* draft_probs, int vocab,
+                           const float* temperature, const int32_t* top_k, const float* top_p,
+                           const float* min_p, const float* u_node, const float* u_final,
+                           const int32_t* tokens, const int32_t* next_token,
+                           const int32_t* next_sibling, const int32_t* num_nodes,
+                           const int32_t* prefix_len, const int32_t* tree_valid, int batch,
+                           int max_nodes, int max_depth, const tsv_kv_cache* cache,
+                           int32_t* accept_path, int32_t* accept_len, int32_t* bonus_token,
+                           int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,
+                           void* workspace, size_t workspace_bytes, tsv_stream_t stream);
+
+/* tsv_target_probs — the filtered target probabilities of tsv_tree_sample_accept,
+ * written out: probs [batch, max_nodes, vocab] fp32 (rows of nodes at or past
+ * num_nodes[b] are not written). Same arguments and workspace. */
+int tsv_target_probs(const float* target_logits, int vocab, const float* temperature,
+                     const int32_t* top_k, const float* top_p, const float* min_p,
+                     const int32_t* num_nodes, int batch, int max_nodes, float* probs,
+                     void* workspace, size_t workspace_bytes, tsv_stream_t stream);
 
 /* --------------------------------------------------------------------------------
  * tsv_accept_and_compact — greedy acceptance walk and KV compaction.

@@ -79,29 +79,35 @@ def filter_probs(logits, temperature: float, top_k: int = 0, top_p: float = 1.0,
     return p / p.sum()
 
 
-def sample_inverse_cdf(p, u: float) -> int:
-    """The smallest token id t with sum(p[:t+1]) > u * sum(p)."""
+def sample_inverse_cdf(p, u: float, trace=None) -> int:
+    """The smallest token id t with sum(p[:t+1]) > u * sum(p). With a trace list, appends
+    ("final", u, p): the distribution the token was drawn from."""
     c = np.cumsum(np.asarray(p, np.float64))
-    t = int(np.searchsorted(c, u * c[-1], side="right"))
-    return min(t, len(c) - 1)
+    t = min(int(np.searchsorted(c, u * c[-1], side="right")), len(c) - 1)
+    if trace is not None:
+        trace.append(("final", float(u), np.asarray(p, np.float64)))
+    return t
 
 
 def children(parents, node):
     return [c for c in range(len(parents)) if parents[c] == node]
 
 
-def rejection_walk(tokens, parents, probs, u_node, u_final, q=None, tree_valid=True):
+def rejection_walk(tokens, parents, probs, u_node, u_final, q=None, tree_valid=True,
+                   trace=None):
     """Tree rejection sampling for one request.
 
     tokens, parents: the tree (node 0 the root). probs[i]: the filtered target
     distribution at node i (filter_probs). q: None for target-only, else q[i] is the
     draft distribution the children of node i were drawn from. Returns (path, token):
     the accepted nodes from the root, and the token sampled where the walk stopped
-    (the correction or bonus token).
+    (the correction or bonus token). With a trace list, every test appends ("test", u,
+    its acceptance probability) and the final sample ("final", u, the distribution), so
+    a caller can see how far each decision was from flipping.
     """
     path, node = [0], 0
     if not tree_valid:
-        return path, sample_inverse_cdf(probs[0], u_final)
+        return path, sample_inverse_cdf(probs[0], u_final, trace)
     while True:
         p = np.array(probs[node], np.float64)
         nxt = None
@@ -109,6 +115,8 @@ def rejection_walk(tokens, parents, probs, u_node, u_final, q=None, tree_valid=T
             x = int(tokens[c])
             qx = 1.0 if q is None else float(q[node][x])
             ratio = np.inf if qx == 0.0 and p[x] > 0.0 else (0.0 if qx == 0.0 else p[x] / qx)
+            if trace is not None:
+                trace.append(("test", float(u_node[c]), min(1.0, ratio)))
             if u_node[c] < min(1.0, ratio):
                 nxt = c
                 break
@@ -121,6 +129,6 @@ def rejection_walk(tokens, parents, probs, u_node, u_final, q=None, tree_valid=T
             if s > 0.0:
                 p = resid / s
         if nxt is None:
-            return path, sample_inverse_cdf(p, u_final)
+            return path, sample_inverse_cdf(p, u_final, trace)
         path.append(nxt)
         node = nxt

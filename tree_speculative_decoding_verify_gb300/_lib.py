@@ -73,6 +73,13 @@ _SIGNATURES = {
     "tsv_lm_head_argmax_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 2),
     "tsv_lm_head_argmax": (ctypes.c_int, [ctypes.c_void_p] * 2 + [ctypes.c_int] * 3 +
                            [ctypes.c_void_p] * 3 + [ctypes.c_size_t, ctypes.c_void_p]),
+    "tsv_tree_sample_accept_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 2),
+    "tsv_tree_sample_accept": (ctypes.c_int, [ctypes.c_void_p] * 2 + [ctypes.c_int] +
+                               [ctypes.c_void_p] * 12 + [ctypes.c_int] * 3 +
+                               [ctypes.c_void_p] * 8 + [ctypes.c_size_t, ctypes.c_void_p]),
+    "tsv_target_probs": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5 +
+                         [ctypes.c_int] * 2 + [ctypes.c_void_p] * 2 +
+                         [ctypes.c_size_t, ctypes.c_void_p]),
     "tsv_tree_verify_attn_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 9 +
                                      [ctypes.c_float] * 2 + [ctypes.c_void_p] * 3),
 }
@@ -347,6 +354,71 @@ def lm_head_argmax(hidden, weight, argmax, workspace, max_logit=None):
                                     _ptr(max_logit), _ptr(workspace), workspace.numel(),
                                     _stream()),
            "tsv_lm_head_argmax")
+
+
+def tree_sample_accept_workspace_size(batch: int, max_nodes: int) -> int:
+    return int(lib().tsv_tree_sample_accept_workspace_size(batch, max_nodes))
+
+
+def _sampling_params(b, temperature, top_k, top_p, min_p):
+    _need(temperature, torch.float32, "temperature", (b,))
+    _need(top_k, torch.int32, "top_k", (b,))
+    _need(top_p, torch.float32, "top_p", (b,))
+    _need(min_p, torch.float32, "min_p", (b,))
+
+
+def tree_sample_accept(target_logits, temperature, top_k, top_p, min_p, u_node, u_final,
+                       tokens, next_token, next_sibling, num_nodes, prefix_len, max_depth,
+                       cache: Optional[KVCache], accept_path, accept_len, bonus_token, slot_map,
+                       new_prefix_len, workspace, err=None, tree_valid=None, draft_probs=None):
+    """Non-greedy acceptance (include/tsv.h): target_logits [B, T, V] fp32; per-request
+    temperature, top_p, min_p fp32 and top_k int32 [B]; u_node [B, T] and u_final [B]
+    uniforms in [0, 1); draft_probs [B, T, V] fp32 or None (target-only)."""
+    b, t, v = target_logits.shape
+    _need(target_logits, torch.float32, "target_logits")
+    if draft_probs is not None:
+        _need(draft_probs, torch.float32, "draft_probs", (b, t, v))
+    _sampling_params(b, temperature, top_k, top_p, min_p)
+    _need(u_node, torch.float32, "u_node", (b, t))
+    _need(u_final, torch.float32, "u_final", (b,))
+    for name, x in (("tokens", tokens), ("next_token", next_token),
+                    ("next_sibling", next_sibling)):
+        _need(x, torch.int32, name, (b, t))
+    _need(num_nodes, torch.int32, "num_nodes", (b,))
+    _need(prefix_len, torch.int32, "prefix_len", (b,))
+    _need(accept_path, torch.int32, "accept_path", (b, max_depth + 1))
+    _need(accept_len, torch.int32, "accept_len", (b,))
+    _need(bonus_token, torch.int32, "bonus_token", (b,))
+    _need(slot_map, torch.int32, "slot_map", (b, max_depth + 1, 2))
+    _need(new_prefix_len, torch.int32, "new_prefix_len", (b,))
+    _need(workspace, torch.uint8, "workspace")
+    if err is not None:
+        _need(err, torch.int32, "err", (b,))
+    if tree_valid is not None:
+        _need(tree_valid, torch.int32, "tree_valid", (b,))
+    desc = ctypes.byref(cache.desc) if cache is not None else None
+    _check(lib().tsv_tree_sample_accept(
+        _ptr(target_logits), _ptr(draft_probs), v, _ptr(temperature), _ptr(top_k), _ptr(top_p),
+        _ptr(min_p), _ptr(u_node), _ptr(u_final), _ptr(tokens), _ptr(next_token),
+        _ptr(next_sibling), _ptr(num_nodes), _ptr(prefix_len), _ptr(tree_valid), b, t,
+        max_depth, desc, _ptr(accept_path), _ptr(accept_len), _ptr(bonus_token), _ptr(slot_map),
+        _ptr(new_prefix_len), _ptr(err), _ptr(workspace), workspace.numel(), _stream()),
+        "tsv_tree_sample_accept")
+
+
+def target_probs(target_logits, temperature, top_k, top_p, min_p, num_nodes, probs, workspace):
+    """The filtered target probabilities [B, T, V] of tree_sample_accept (rows of nodes
+    at or past num_nodes are left as they were)."""
+    b, t, v = target_logits.shape
+    _need(target_logits, torch.float32, "target_logits")
+    _need(probs, torch.float32, "probs", (b, t, v))
+    _sampling_params(b, temperature, top_k, top_p, min_p)
+    _need(num_nodes, torch.int32, "num_nodes", (b,))
+    _need(workspace, torch.uint8, "workspace")
+    _check(lib().tsv_target_probs(_ptr(target_logits), v, _ptr(temperature), _ptr(top_k),
+                                  _ptr(top_p), _ptr(min_p), _ptr(num_nodes), b, t, _ptr(probs),
+                                  _ptr(workspace), workspace.numel(), _stream()),
+           "tsv_target_probs")
 
 
 def accept_and_compact(tokens, next_token, next_sibling, target_argmax, num_nodes, prefix_len,

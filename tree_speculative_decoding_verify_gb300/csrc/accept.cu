@@ -10,9 +10,12 @@
 //
 // One CTA per (request, copy unit); a copy unit is one (layer, kv head,
 // keys-or-values) plane. Every CTA of a request repeats the (tiny) walk from shared
-// memory, so no CTA waits for another.
+// memory, so no CTA waits for another. With `given` the walk has been made already (the
+// non-greedy acceptance writes the path, its length and a per-request code first) and
+// the kernel only moves the rows.
 #include "common.cuh"
 #include "kernels.h"
+#include "kv_view.cuh"
 
 namespace tsv {
 namespace {
@@ -21,30 +24,12 @@ constexpr int THREADS = 128;
 constexpr int UNITS_PER_CTA = 1;  // copy units per CTA: each CTA pays one load round trip
 constexpr int MAX_ROW_BYTES = 128 * 4;  // head_dim 128 in f32
 
-struct CacheView {
-  char* k;
-  char* v;
-  const int32_t* block_table;
-  int64_t capacity, layer_stride_bytes;
-  int hkv, row_bytes, layout, max_blocks, num_blocks, num_layers;
-};
-
-__device__ __forceinline__ int64_t slot_offset(const CacheView& c, int b, int h, int slot,
-                                               bool* ok) {
-  if (c.layout == TSV_KV_CONTIGUOUS) {
-    return (((int64_t)b * c.hkv + h) * c.capacity + slot) * c.row_bytes;
-  }
-  const int blk = c.block_table[(int64_t)b * c.max_blocks + slot / TSV_KV_BLOCK];
-  if (blk < 0 || blk >= c.num_blocks) { *ok = false; return 0; }
-  return (((int64_t)blk * c.hkv + h) * TSV_KV_BLOCK + slot % TSV_KV_BLOCK) * c.row_bytes;
-}
-
 __global__ void __launch_bounds__(THREADS)
 accept_compact_kernel(const int32_t* __restrict__ tokens, const int32_t* __restrict__ next_token,
                       const int32_t* __restrict__ next_sibling, const int32_t* __restrict__ target,
                       const int32_t* __restrict__ num_nodes, const int32_t* __restrict__ prefix_len,
                       const int32_t* __restrict__ tree_valid, int max_nodes, int max_depth,
-                      CacheView cache, bool has_cache,
+                      CacheView cache, bool has_cache, const int32_t* __restrict__ given,
                       int32_t* __restrict__ accept_path, int32_t* __restrict__ accept_len,
                       int32_t* __restrict__ bonus, int32_t* __restrict__ slot_map,
                       int32_t* __restrict__ new_prefix_len, int32_t* __restrict__ err) {
@@ -61,6 +46,17 @@ accept_compact_kernel(const int32_t* __restrict__ tokens, const int32_t* __restr
   const int T = num_nodes[b];
   const int P = prefix_len[b];
   const bool size_ok = T >= 1 && T <= max_nodes && P >= 0;
+  if (given) {
+    // the path, its length and the request's code come from the walk already made
+    if (threadIdx.x == 0) {
+      const int cols = max_depth + 1;
+      const int len = min(max(accept_len[b], 1), cols);
+      for (int i = 0; i < len; ++i) s_path[i] = accept_path[(int64_t)b * cols + i];
+      s_len = len;
+      s_code = given[b];
+    }
+    __syncthreads();
+  } else {
   for (int i = threadIdx.x; i < max_nodes; i += THREADS) {
     const bool in = size_ok && i < T;
     s_tok[i] = in ? tokens[row0 + i] : -1;
@@ -97,10 +93,7 @@ accept_compact_kernel(const int32_t* __restrict__ tokens, const int32_t* __restr
       }
     }
     if (code == TSV_REQ_OK && has_cache) {
-      const int64_t cap = cache.layout == TSV_KV_CONTIGUOUS
-                              ? cache.capacity
-                              : (int64_t)cache.max_blocks * TSV_KV_BLOCK;
-      if ((int64_t)P + T > cap) code = TSV_REQ_CAPACITY;
+      if ((int64_t)P + T > cache_slots(cache)) code = TSV_REQ_CAPACITY;
       for (int i = 0; code == TSV_REQ_OK && i < len; ++i) {
         bool ok = true;
         slot_offset(cache, b, 0, P + s_path[i], &ok);
@@ -113,10 +106,11 @@ accept_compact_kernel(const int32_t* __restrict__ tokens, const int32_t* __restr
     s_code = code;
   }
   __syncthreads();
+  }
   const int len = s_len;
   const int code = s_code;
 
-  if (blockIdx.y == 0) {
+  if (blockIdx.y == 0 && !given) {
     const int cols = max_depth + 1;
     for (int i = threadIdx.x; i < cols; i += THREADS) {
       const bool in = i < len;
@@ -172,29 +166,36 @@ int launch_accept_compact(const int32_t* tokens, const int32_t* next_token,
                           int32_t* accept_path, int32_t* accept_len, int32_t* bonus,
                           int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,
                           cudaStream_t stream) {
-  CacheView cv{};
+  const CacheView cv = make_cache_view(cache);
   int ctas_y = 1;
-  if (cache) {
-    const int esize = cache->dtype == TSV_DTYPE_BF16 ? 2 : 4;
-    cv.k = static_cast<char*>(cache->k);
-    cv.v = static_cast<char*>(cache->v);
-    cv.block_table = cache->block_table;
-    cv.capacity = cache->capacity;
-    cv.layer_stride_bytes = cache->layer_stride * esize;
-    cv.hkv = cache->num_kv_heads;
-    cv.row_bytes = cache->head_dim * esize;
-    cv.layout = cache->layout;
-    cv.max_blocks = cache->max_blocks;
-    cv.num_blocks = cache->num_blocks;
-    cv.num_layers = cache->num_layers;
+  if (cache)
     ctas_y = (int)ceil_div((int64_t)cache->num_layers * cache->num_kv_heads * 2, UNITS_PER_CTA);
-  }
   dim3 grid(batch, ctas_y);
   return launch_pdl(accept_compact_kernel, grid, dim3(THREADS), 0, stream, tokens, next_token,
                     next_sibling, target, num_nodes, prefix_len, tree_valid, max_nodes,
                     max_depth, cv,
-                    cache != nullptr, accept_path, accept_len, bonus, slot_map, new_prefix_len,
+                    cache != nullptr, static_cast<const int32_t*>(nullptr), accept_path, accept_len, bonus, slot_map, new_prefix_len,
                     err);
+}
+
+}  // namespace tsv
+
+namespace tsv {
+
+int launch_compact_given(const int32_t* num_nodes, const int32_t* prefix_len, int batch,
+                         int max_nodes, int max_depth, const tsv_kv_cache* cache,
+                         const int32_t* code, int32_t* accept_path, int32_t* accept_len,
+                         cudaStream_t stream) {
+  const CacheView cv = make_cache_view(cache);
+  const int ctas_y =
+      (int)ceil_div((int64_t)cache->num_layers * cache->num_kv_heads * 2, UNITS_PER_CTA);
+  return launch_pdl(accept_compact_kernel, dim3(batch, ctas_y), dim3(THREADS), 0, stream,
+                    static_cast<const int32_t*>(nullptr), static_cast<const int32_t*>(nullptr),
+                    static_cast<const int32_t*>(nullptr), static_cast<const int32_t*>(nullptr),
+                    num_nodes, prefix_len, static_cast<const int32_t*>(nullptr), max_nodes,
+                    max_depth, cv, true, code, accept_path, accept_len,
+                    static_cast<int32_t*>(nullptr), static_cast<int32_t*>(nullptr),
+                    static_cast<int32_t*>(nullptr), static_cast<int32_t*>(nullptr));
 }
 
 }  // namespace tsv

@@ -236,6 +236,61 @@ int tsv_lm_head_argmax(const void* hidden, const void* weight, int rows, int hid
                                workspace, (cudaStream_t)stream);
 }
 
+size_t tsv_tree_sample_accept_workspace_size(int batch, int max_nodes) {
+  if (batch < 0 || max_nodes < 1 || max_nodes > TSV_MAX_NODES) return 0;
+  return sample_ws_bytes(batch, max_nodes);
+}
+
+static bool sample_sizes_ok(int batch, int max_nodes, int vocab) {
+  return batch >= 0 && batch <= 65535 && max_nodes >= 1 && max_nodes <= TSV_MAX_NODES &&
+         vocab >= 1;
+}
+
+int tsv_tree_sample_accept(const float* target_logits, const float* draft_probs, int vocab,
+                           const float* temperature, const int32_t* top_k, const float* top_p,
+                           const float* min_p, const float* u_node, const float* u_final,
+                           const int32_t* tokens, const int32_t* next_token,
+                           const int32_t* next_sibling, const int32_t* num_nodes,
+                           const int32_t* prefix_len, const int32_t* tree_valid, int batch,
+                           int max_nodes, int max_depth, const tsv_kv_cache* cache,
+                           int32_t* accept_path, int32_t* accept_len, int32_t* bonus_token,
+                           int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,
+                           void* workspace, size_t workspace_bytes, tsv_stream_t stream) {
+  if (!sample_sizes_ok(batch, max_nodes, vocab) || max_depth < 0 || max_depth > TSV_MAX_DEPTH)
+    return TSV_ERR_INVALID_ARG;
+  if (cache && !cache_ok(cache, true)) return TSV_ERR_INVALID_ARG;
+  if (batch == 0) return TSV_OK;
+  if (!target_logits || !temperature || !top_k || !top_p || !min_p || !u_node || !u_final ||
+      !tokens || !next_token || !next_sibling || !num_nodes || !prefix_len || !accept_path ||
+      !accept_len || !bonus_token || !slot_map || !new_prefix_len)
+    return TSV_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < sample_ws_bytes(batch, max_nodes) ||
+      ((uintptr_t)workspace & 255u))
+    return TSV_ERR_WORKSPACE;
+  const SampleArgs a{target_logits, draft_probs, vocab, temperature, top_k, top_p, min_p,
+                     u_node, u_final, tokens, next_token, next_sibling, num_nodes, prefix_len,
+                     tree_valid, batch, max_nodes, max_depth};
+  return launch_sample_accept(a, cache, accept_path, accept_len, bonus_token, slot_map,
+                              new_prefix_len, err, workspace, (cudaStream_t)stream);
+}
+
+int tsv_target_probs(const float* target_logits, int vocab, const float* temperature,
+                     const int32_t* top_k, const float* top_p, const float* min_p,
+                     const int32_t* num_nodes, int batch, int max_nodes, float* probs,
+                     void* workspace, size_t workspace_bytes, tsv_stream_t stream) {
+  if (!sample_sizes_ok(batch, max_nodes, vocab)) return TSV_ERR_INVALID_ARG;
+  if (batch == 0) return TSV_OK;
+  if (!target_logits || !temperature || !top_k || !top_p || !min_p || !num_nodes || !probs)
+    return TSV_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < sample_ws_bytes(batch, max_nodes) ||
+      ((uintptr_t)workspace & 255u))
+    return TSV_ERR_WORKSPACE;
+  const SampleArgs a{target_logits, nullptr, vocab, temperature, top_k, top_p, min_p,
+                     nullptr, nullptr, nullptr, nullptr, nullptr, num_nodes, nullptr,
+                     nullptr, batch, max_nodes, 0};
+  return launch_target_probs(a, probs, workspace, (cudaStream_t)stream);
+}
+
 int tsv_accept_and_compact(const int32_t* tokens, const int32_t* next_token,
                            const int32_t* next_sibling, const int32_t* target_argmax,
                            const int32_t* num_nodes, const int32_t* prefix_len,

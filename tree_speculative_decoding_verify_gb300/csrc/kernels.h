@@ -24,6 +24,38 @@ int launch_accept_compact(const int32_t* tokens, const int32_t* next_token,
                           int32_t* slot_map, int32_t* new_prefix_len, int32_t* err,
                           cudaStream_t stream);
 
+// KV compaction of a path chosen by another kernel: accept_path / accept_len as written,
+// code[b] = that request's status (only TSV_REQ_OK requests move rows).
+int launch_compact_given(const int32_t* num_nodes, const int32_t* prefix_len, int batch,
+                         int max_nodes, int max_depth, const tsv_kv_cache* cache,
+                         const int32_t* code, int32_t* accept_path, int32_t* accept_len,
+                         cudaStream_t stream);
+
+// Non-greedy acceptance.
+struct SampleArgs {
+  const float* logits;       // [batch, max_nodes, vocab]
+  const float* draft_probs;  // [batch, max_nodes, vocab] or null (target-only)
+  int vocab;
+  const float* temperature;  // [batch] each
+  const int32_t* top_k;
+  const float* top_p;
+  const float* min_p;
+  const float* u_node;       // [batch, max_nodes]
+  const float* u_final;      // [batch]
+  const int32_t* tokens;
+  const int32_t* next_token;
+  const int32_t* next_sibling;
+  const int32_t* num_nodes;
+  const int32_t* prefix_len;
+  const int32_t* tree_valid;
+  int batch, max_nodes, max_depth;
+};
+size_t sample_ws_bytes(int batch, int max_nodes);
+int launch_target_probs(const SampleArgs& a, float* probs, void* ws, cudaStream_t stream);
+int launch_sample_accept(const SampleArgs& a, const tsv_kv_cache* cache, int32_t* accept_path,
+                         int32_t* accept_len, int32_t* bonus, int32_t* slot_map,
+                         int32_t* new_prefix_len, int32_t* err, void* ws, cudaStream_t stream);
+
 // Draft expansion.
 struct TopkPlan {
   int chunks;         // CTAs per row in the streaming stage

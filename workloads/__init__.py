@@ -45,7 +45,7 @@ KV_BLOCK = 64  # tokens per paged KV block
 _STREAMS = {
     "logits": 1, "q": 2, "k_new": 3, "v_new": 4, "k_cache": 5, "v_cache": 6,
     "prefix": 7, "blocks": 8, "root": 9, "target": 10, "tokens": 11, "pad": 12,
-    "lm_hidden": 13, "lm_weight": 14,
+    "lm_hidden": 13, "lm_weight": 14, "t_logits": 15, "uniform": 16, "d_logits": 17,
 }
 
 # (hidden size, vocabulary) of the target model whose lm_head gives the greedy token at
@@ -242,3 +242,32 @@ def lm_head_weight_blocks(w: Workload, vocab: int, hidden: int, key: int = 0):
         n = min(LM_WEIGHT_BLOCK, vocab - v0)
         g = rng(w, "lm_weight", key, j)
         yield v0, (g.standard_normal((n, hidden), dtype=np.float32) * scale).astype(np.float32)
+
+
+def target_logits(w: Workload, b: int, tokens, parents, vocab: int, t_max: int,
+                  sigma: float = 2.0, boost: Optional[float] = None,
+                  stream: str = "t_logits"):
+    """[t_max, vocab] fp32 logits at every node of request b ~ N(0, sigma). Along a random
+    root-down walk that continues with probability accept_p, the logit of the next node's
+    token at its parent is raised by `boost` (default ln(vocab) + 4, which gives that
+    token most of the mass at temperature 1, so probability tests pass often enough to
+    walk the tree). Rows past the tree are drawn too."""
+    if boost is None:
+        boost = math.log(vocab) + 4.0
+    g = rng(w, stream, b)
+    x = (g.standard_normal((t_max, vocab), dtype=np.float32) * np.float32(sigma))
+    n = len(parents)
+    node = 0
+    while True:
+        kids = [c for c in range(n) if parents[c] == node]
+        if not kids or g.random() >= w.accept_p:
+            break
+        c = kids[int(g.integers(0, len(kids)))]
+        x[node, int(tokens[c])] += np.float32(boost)
+        node = c
+    return x.astype(np.float32)
+
+
+def uniforms(w: Workload, b: int, n: int) -> np.ndarray:
+    """n + 1 fp32 uniforms in [0, 1) of request b: one per node, then the final one."""
+    return rng(w, "uniform", b).random(n + 1, dtype=np.float32)
