@@ -269,6 +269,33 @@ def native(args):
     def lm_head():
         T.lm_head_argmax(lm_hidden, lm_weight, lm_argmax, lm_ws)
 
+    # non-greedy acceptance over the same trees: nucleus sampling (temperature 0.8,
+    # top-p 0.9) on the target's logits at every node, the rejection walk, compaction
+    hp.build_meta(prefix_t)
+    torch.cuda.synchronize()
+    sa_v = lm_v
+    nodes = hp.num_nodes.cpu().numpy()
+    sa_logits = torch.from_numpy(np.stack([
+        W.target_logits(w, i, toks[i][:nodes[i]], pars[i][:nodes[i]], sa_v, t_max)
+        for i in range(b)])).to(dev)
+    uni = np.stack([W.uniforms(w, i, t_max) for i in range(b)])
+    sa_u = torch.from_numpy(np.ascontiguousarray(uni[:, :t_max])).to(dev)
+    sa_uf = torch.from_numpy(np.ascontiguousarray(uni[:, t_max])).to(dev)
+    sa_prm = (torch.full((b,), 0.8, device=dev), torch.zeros(b, dtype=torch.int32, device=dev),
+              torch.full((b,), 0.9, device=dev), torch.zeros(b, device=dev))
+    sa_out = [torch.zeros(b, shape.max_depth + 1, dtype=torch.int32, device=dev),
+              torch.zeros(b, dtype=torch.int32, device=dev),
+              torch.zeros(b, dtype=torch.int32, device=dev),
+              torch.zeros(b, shape.max_depth + 1, 2, dtype=torch.int32, device=dev),
+              torch.zeros(b, dtype=torch.int32, device=dev)]
+    sa_ws = torch.empty(T.tree_sample_accept_workspace_size(b, t_max), dtype=torch.uint8,
+                        device=dev)
+
+    def sample_accept():
+        T.tree_sample_accept(sa_logits, *sa_prm, sa_u, sa_uf, hp.tokens, hp.next_token,
+                             hp.next_sibling, hp.num_nodes, prefix_t, shape.max_depth, cache,
+                             *sa_out, sa_ws)
+
     def topk_level():  # one expansion level (level 2: [B, K, V] rows)
         T.draft_topk_expand(levels[1], k, 2, hp.front[0][1], hp.front[0][2], hp.store_token,
                             hp.store_score, hp.store_parent, *lvl_out, lvl_ws)
@@ -278,10 +305,10 @@ def native(args):
     graphs = {}
     with torch.cuda.stream(stream):
         for _ in range(2):  # warm the allocator and the kernels before capture
-            step(); attn(); topk_level(); lm_head()
+            step(); attn(); topk_level(); lm_head(); sample_accept()
         stream.synchronize()
         for name, fn in (("step", step), ("attn", attn), ("topk", topk_level),
-                         ("lm_head", lm_head)):
+                         ("lm_head", lm_head), ("sample", sample_accept)):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 fn()
@@ -293,7 +320,7 @@ def native(args):
                      for _ in range(n)] for name in graphs}
         with torch.cuda.stream(stream):
             for i in range(n):
-                for name in ("step", "attn", "topk", "lm_head"):
+                for name in ("step", "attn", "topk", "lm_head", "sample"):
                     flush_buf.zero_()
                     ev[name][i][0].record(stream)
                     graphs[name].replay()
@@ -441,6 +468,16 @@ def native(args):
                "traffic_source": traffic("lm_head", w.name)[1],
                "algorithmic_bytes": lm_bytes, "algorithmic_flops": lm_flops,
                "us_per_launch": ms["lm_head"] * 1e3}
+    sa_s = ms["sample"] / 1e3
+    sa_bytes = int(nodes.sum()) * sa_v * 4
+    sa_gbps = sa_bytes / sa_s / 1e9
+    sa_roof = {"kernel": f"tree_sample_accept (filter + rejection walk + compaction; "
+                         f"{int(nodes.sum())} nodes x {sa_v} fp32 logits, T 0.8, top-p 0.9)",
+               "bound": "hbm", "achieved": sa_gbps, "peak": hbm, "unit": "GB/s",
+               "frac": sa_gbps / hbm, "peak_source": src,
+               "traffic": traffic("sample", w.name)[0],
+               "traffic_source": traffic("sample", w.name)[1],
+               "algorithmic_bytes": sa_bytes, "us_per_launch": ms["sample"] * 1e3}
     # the dominant kernel of the step: the attention call or the depth + 1 top-k levels
     dominant = "topk" if ms["topk"] * (w.depth + 1) > ms["attn"] else "attn"
     kernels_step = hp.kernels_per_step()
@@ -466,11 +503,14 @@ def native(args):
         "roofline_topk": topk_roof,
         "lm_head_us": ms["lm_head"] * 1e3,
         "roofline_lm_head": lm_roof,
+        "sample_accept_us": ms["sample"] * 1e3,
+        "roofline_sample_accept": sa_roof,
         "e2e": {"value": world * 1e3 / e2e_step_ms, "unit": UNIT, "ms_per_step": e2e_step_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         # timed region per iteration: the step graph, the attention call, one top-k level,
-        # the lm-head argmax (GEMM + finalize)
-        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1 + 2),
+        # the lm-head argmax (GEMM + finalize), the non-greedy acceptance (filter, walk,
+        # compaction)
+        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1 + 2 + 3),
         "wall_s_timed_region": t_wall,
     }
     ck = clocks.summary()

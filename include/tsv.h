@@ -81,6 +81,7 @@ enum tsv_request_error {
 #define TSV_MAX_TOPK 16   /* top_k of the expansion */
 #define TSV_MAX_DEPTH 64  /* max_depth (edges from the root to the deepest node) */
 #define TSV_KV_BLOCK 64   /* tokens per paged KV block */
+#define TSV_MAX_SAMPLE_VOCAB (1 << 20) /* vocabulary of tsv_tree_sample_accept */
 
 /* ---- element types ---- */
 enum tsv_dtype { TSV_DTYPE_F32 = 0, TSV_DTYPE_BF16 = 1 };
@@ -361,7 +362,8 @@ int tsv_lm_head_argmax(const void* hidden, const void* weight, int rows, int hid
  *   min_p        keep tokens whose mass is at least min(min_p, 1) times the largest
  *                (<= 0 or NaN: off);
  * then p(v) = exp((l_v - max l) / temperature) over the kept tokens, normalised. Masses
- * are fp32 (2^((l - m) log2(e) / T)) summed as 2^-40 fixed point.
+ * are fp32 (2^((l - m) log2(e) / T)); the sums that decide are compensated fp32 sums
+ * in a fixed order, so a call gives the same result on every run.
  * The walk: at the current node take its children in ascending node order; child c
  * with token x is accepted when u_node[c] < min(1, p(x) / q(x)), q(x) = 1 for
  * target-only (draft_probs NULL), else q = draft_probs[b][node] (the distribution the
@@ -386,7 +388,8 @@ int tsv_lm_head_argmax(const void* hidden, const void* weight, int rows, int hid
  * bonus_token      [batch] out: the sampled token where the walk stopped.
  * workspace        tsv_tree_sample_accept_workspace_size(batch, max_nodes) bytes,
  *                  256-byte aligned; nothing in it has to start at zero.
- * Returns TSV_ERR_INVALID_ARG for a null pointer, vocab < 1, or sizes out of range.
+ * Returns TSV_ERR_INVALID_ARG for a null pointer, vocab outside [1,
+ * TSV_MAX_SAMPLE_VOCAB], or sizes out of range.
  * ------------------------------------------------------------------------------ */
 size_t tsv_tree_sample_accept_workspace_size(int batch, int max_nodes);
 int tsv_tree_sample_accept(const float* target_logits, const float* draft_probs, int vocab,

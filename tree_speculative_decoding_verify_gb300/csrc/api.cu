@@ -243,7 +243,7 @@ size_t tsv_tree_sample_accept_workspace_size(int batch, int max_nodes) {
 
 static bool sample_sizes_ok(int batch, int max_nodes, int vocab) {
   return batch >= 0 && batch <= 65535 && max_nodes >= 1 && max_nodes <= TSV_MAX_NODES &&
-         vocab >= 1;
+         vocab >= 1 && vocab <= TSV_MAX_SAMPLE_VOCAB;
 }
 
 int tsv_tree_sample_accept(const float* target_logits, const float* draft_probs, int vocab,

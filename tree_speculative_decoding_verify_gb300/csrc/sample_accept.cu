@@ -16,21 +16,24 @@
 // distribution q per node from the caller.
 //
 // Kernels:
-//   filter_stats_kernel   one 1024-thread CTA per (node, request). A node's filtered
-//       distribution is described by the largest logit m, c = log2(e)/temperature, a
-//       64-bit key threshold, a min-p bound and the normaliser Z: token v is kept when
-//       its key (logit order, then the lower token id) is at least the threshold and its
-//       mass e_v = 2^((l_v - m) c) at least the min-p bound, and p(v) = e_v / Z. Masses
-//       are summed as 40-bit fixed point, so every sum is exact and independent of the
-//       order of the additions. The top-k and top-p thresholds come from a histogram of
-//       d = (m - l_v) c over 4096 linear bins of [0, 32) (the last bin also takes
-//       everything beyond), then an exact ordering of the one bin where the criterion is
-//       met: its tokens sorted in shared memory, or, when the bin holds more than 4096
-//       tokens or is the open last bin, a 64-bit radix select over its keys.
+//   filter_stats_kernel   one 1024-thread CTA per (node, request), 58 KB of shared memory.
+//       A node's filtered distribution is described by the largest
+//       logit m, c = log2(e)/temperature, a 64-bit key threshold, a min-p bound and the
+//       normaliser Z: token v is kept when its key (logit order, then the lower token id)
+//       is at least the threshold and its mass e_v = 2^((l_v - m) c) at least the min-p
+//       bound; p(v) = e_v / Z. Every pass keeps four 16-byte loads in flight per thread.
+//       Thresholds: a histogram of d = (m - l_v) c over 4096 linear bins of [0, 32) (the
+//       last bin also takes everything beyond) with exact 32-bit counts and fp32 masses
+//       locates the bins where the top-k count or the top-p mass is reached; those bins'
+//       tokens are then gathered, with the compensated mass of everything before them,
+//       sorted by key in shared memory and scanned. The fp32 sums that decide use a fixed
+//       order, so the result is the same on every run; the atomic fp32 bin masses only
+//       choose which bins to gather (with a margin, and a check that widens it). A bin
+//       range of more than 2048 tokens goes to a 64-bit radix select instead.
 //   sample_walk_kernel    one 512-thread CTA per request: the walk (the logits of a
 //       node's candidates are gathered in one round of loads), the residual passes of the
-//       draft-aware rule, and the final inverse-CDF sample over the vocabulary (one
-//       contiguous slice per thread, an exact integer scan for target-only).
+//       draft-aware rule, and the final inverse-CDF sample: per-warp sums of 2048-token
+//       tiles, the crossing tile, then a block scan inside it.
 //   accept_compact_kernel (accept.cu), given-path mode: the accepted KV rows move.
 #include <math.h>
 
@@ -43,21 +46,22 @@ namespace {
 
 typedef unsigned long long u64;
 
-constexpr int FT = 1024;                 // threads of the filter kernel
-constexpr int NB = 4096;                 // histogram bins (4 per filter thread)
-constexpr float DR = 32.f;               // bins cover d in [0, 32): masses down to 2^-32
-constexpr int CAP = 4096;                // tokens of one bin sorted in shared memory
-constexpr float FIXS = 1099511627776.0f;  // 2^40: masses as fixed point
-constexpr int WT = 512;                  // threads of the walk kernel
-static_assert(NB == 4 * FT, "cross_index takes four entries per thread");
+constexpr int FT = 1024;    // threads of the filter kernel
+constexpr int NB = 4096;    // histogram bins (4 per filter thread)
+constexpr float DR = 32.f;  // bins cover d in [0, 32)
+constexpr int CAP = 2048;   // tokens gathered and sorted in shared memory
+constexpr int WT = 512;     // threads of the walk kernel
+constexpr int TILE = 4 * WT;  // tokens per tile of the final sample
+constexpr int MAX_TILES = TSV_MAX_SAMPLE_VOCAB / TILE;
+static_assert(NB == 4 * FT, "bin scans take four bins per thread");
+static_assert(CAP == 2 * FT, "list scans take two entries per thread");
 
 struct RowStats {
   u64 thr;     // kept: key >= thr
-  u64 z;       // sum of the kept masses (fixed point)
+  float z;     // sum of the kept masses
   float m;     // largest logit
   float c;     // log2(e) / temperature; 0 = greedy (only the first maximum is kept)
   float minp;  // kept: mass >= minp
-  int valid;   // 1 once written
 };
 
 __device__ __forceinline__ float clean(float l) { return l != l ? -INFINITY : l; }
@@ -75,23 +79,50 @@ __device__ __forceinline__ float key_value(u64 k) {
 __device__ __forceinline__ float emass(float l, float m, float c) {
   return c == 0.f ? 1.f : exp2f((l - m) * c);
 }
-__device__ __forceinline__ u64 fixp(float e) { return (u64)(e * FIXS); }
 __device__ __forceinline__ int bin_of(float l, float m, float c) {
   const float d = (m - l) * c;  // >= 0, non-decreasing as l decreases; NaN/inf -> last bin
   return d < DR ? min(NB - 1, (int)(d * (NB / DR))) : NB - 1;
 }
-__device__ __forceinline__ u64 kept_mass(const RowStats& st, float l, int v) {
-  if (vkey(l, v) < st.thr) return 0ull;
+__device__ __forceinline__ float kept_mass(const RowStats& st, float l, int v) {
+  if (vkey(l, v) < st.thr) return 0.f;
   const float e = emass(l, st.m, st.c);
-  return e >= st.minp ? fixp(e) : 0ull;
+  return e >= st.minp ? e : 0.f;
 }
 
-// Visit every token of a row: f(v, logit) with NaN read as -inf.
+// Compensated fp32 sum (the additions of one thread in a fixed order).
+struct Kahan {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+  __device__ __forceinline__ float value() const { return s - c; }
+};
+
+// Visit every token of a row: f(v, logit), NaN read as -inf; four loads in flight.
 template <class F>
 __device__ __forceinline__ void for_row(const float* __restrict__ row, int V, bool vec, F&& f) {
+  const int bd = blockDim.x;
   if (vec) {
     const float4* r4 = reinterpret_cast<const float4*>(row);
-    for (int j = threadIdx.x; j < (V >> 2); j += blockDim.x) {
+    const int n4 = V >> 2;
+    int j = threadIdx.x;
+    for (; j + 3 * bd < n4; j += 4 * bd) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = __ldg(r4 + j + u * bd);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = 4 * (j + u * bd);
+        f(v, clean(x[u].x));
+        f(v + 1, clean(x[u].y));
+        f(v + 2, clean(x[u].z));
+        f(v + 3, clean(x[u].w));
+      }
+    }
+    for (; j < n4; j += bd) {
       const float4 x = __ldg(r4 + j);
       f(4 * j, clean(x.x));
       f(4 * j + 1, clean(x.y));
@@ -99,11 +130,34 @@ __device__ __forceinline__ void for_row(const float* __restrict__ row, int V, bo
       f(4 * j + 3, clean(x.w));
     }
   } else {
-    for (int v = threadIdx.x; v < V; v += blockDim.x) f(v, clean(__ldg(row + v)));
+    int v = threadIdx.x;
+    for (; v + 3 * bd < V; v += 4 * bd) {
+      float x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = __ldg(row + v + u * bd);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) f(v + u * bd, clean(x[u]));
+    }
+    for (; v < V; v += bd) f(v, clean(__ldg(row + v)));
   }
 }
 
-// ---- block-wide helpers (any multiple of 32 threads up to 1024) -----------------------
+// ---- block-wide helpers (any multiple of 32 threads up to 1024); fixed order ---------
+template <typename Tv>
+__device__ Tv warp_sum(Tv x) {
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(FULL, x, o);
+  return x;
+}
+template <typename Tv>
+__device__ Tv block_sum(Tv x, Tv* sb) {
+  x = warp_sum(x);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (l == 0) sb[w] = x;
+  __syncthreads();
+  x = l < nw ? sb[l] : (Tv)0;
+  return warp_sum(x);
+}
 __device__ u64 block_max_u64(u64 x, u64* sb) {
   for (int o = 16; o; o >>= 1) x = max(x, __shfl_xor_sync(FULL, x, o));
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -112,27 +166,6 @@ __device__ u64 block_max_u64(u64 x, u64* sb) {
   __syncthreads();
   x = l < nw ? sb[l] : 0ull;
   for (int o = 16; o; o >>= 1) x = max(x, __shfl_xor_sync(FULL, x, o));
-  return x;
-}
-__device__ u64 block_sum_u64(u64 x, u64* sb) {
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(FULL, x, o);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
-  __syncthreads();
-  if (l == 0) sb[w] = x;
-  __syncthreads();
-  x = l < nw ? sb[l] : 0ull;
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(FULL, x, o);
-  return x;
-}
-// fixed order of additions: the result is the same on every run
-__device__ double block_sum_f64(double x, double* sd) {
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(FULL, x, o);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
-  __syncthreads();
-  if (l == 0) sd[w] = x;
-  __syncthreads();
-  x = l < nw ? sd[l] : 0.0;
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(FULL, x, o);
   return x;
 }
 // Inclusive scan across the block; *total = the block's sum.
@@ -158,46 +191,21 @@ __device__ Tv block_scan(Tv x, Tv* sb, Tv* total) {
 
 // ---- filter kernel ------------------------------------------------------------------
 struct FilterSmem {
-  u64 cnt[NB];
-  u64 mass[NB];
-  u64 ckey[CAP];
-  u64 cmass[CAP];
+  unsigned cnt[NB];
+  float mass[NB];
+  u64 lkey[CAP];
+  float lmass[CAP];
+  u64 tkey[CAP / 2];  // unsorted copy for the ranking sort
+  float tmass[CAP / 2];
   u64 sb[32];
-  u64 s_before, s_prefix, s_want;
-  int s_res, s_n;
+  float sf[32];
+  unsigned su[32];
+  u64 s_prefix;
+  float s_f;
+  int s_lo, s_hi, s_n, s_j;
 };
 
-// Smallest j < n with vals[0] + ... + vals[j] >= target (target >= 1), or -1; *before =
-// the sum of the entries before j. n <= 4 * blockDim.x.
-__device__ int cross_index(const u64* vals, int n, u64 target, FilterSmem& S, u64* before) {
-  const int j0 = threadIdx.x * 4;
-  u64 loc = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    if (j0 + i < n) loc += vals[j0 + i];
-  u64 tot;
-  const u64 incl = block_scan<u64>(loc, S.sb, &tot);
-  if (threadIdx.x == 0) S.s_res = -1;
-  __syncthreads();
-  u64 acc = incl - loc;
-  if (acc < target && target <= incl) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const u64 x = j0 + i < n ? vals[j0 + i] : 0ull;
-      if (acc + x >= target) {
-        S.s_res = j0 + i;
-        S.s_before = acc;
-        break;
-      }
-      acc += x;
-    }
-  }
-  __syncthreads();
-  *before = S.s_before;
-  return S.s_res;
-}
-
-__device__ void sort_desc(u64* key, u64* val, int n) {  // n a power of two
+__device__ void sort_desc(u64* key, float* val, int n) {  // n a power of two
   for (int k = 2; k <= n; k <<= 1)
     for (int j = k >> 1; j > 0; j >>= 1) {
       for (int i = threadIdx.x; i < n; i += blockDim.x) {
@@ -208,7 +216,7 @@ __device__ void sort_desc(u64* key, u64* val, int n) {  // n a power of two
           if ((a < b) == desc) {
             key[i] = b;
             key[p] = a;
-            const u64 t = val[i];
+            const float t = val[i];
             val[i] = val[p];
             val[p] = t;
           }
@@ -218,85 +226,204 @@ __device__ void sort_desc(u64* key, u64* val, int n) {  // n a power of two
     }
 }
 
-// The tokens of bin `bsel` with key >= lo, sorted by key (descending) into S.ckey /
-// S.cmass; returns how many (the caller has checked that they fit).
-__device__ int collect_sorted(FilterSmem& S, const float* row, int V, bool vec, float m, float c,
-                              int bsel, u64 lo) {
+// Tokens with bin in [lo, hi] and key >= kmin gathered into S.lkey / S.lmass (sorted by
+// key, descending); returns the compensated mass of the tokens with bin < lo (and key >=
+// kmin), and in *n the number gathered (more than CAP: not gathered).
+__device__ float gather_bins(FilterSmem& S, const float* row, int V, bool vec, float m, float c,
+                             int lo, int hi, u64 kmin, int* n) {
   if (threadIdx.x == 0) S.s_n = 0;
   __syncthreads();
+  Kahan pre;
   for_row(row, V, vec, [&](int v, float l) {
-    if (bin_of(l, m, c) != bsel) return;
+    const int bn = bin_of(l, m, c);
+    if (bn > hi) return;
     const u64 k = vkey(l, v);
-    if (k < lo) return;
+    if (k < kmin) return;
+    const float e = emass(l, m, c);
+    if (bn < lo) {
+      pre.add(e);
+      return;
+    }
     const int pos = atomicAdd(&S.s_n, 1);
     if (pos < CAP) {
-      S.ckey[pos] = k;
-      S.cmass[pos] = fixp(emass(l, m, c));
+      S.lkey[pos] = k;
+      S.lmass[pos] = e;
     }
   });
-  __syncthreads();
-  const int n = min(S.s_n, CAP);
-  int np = 2;
-  while (np < n) np <<= 1;
-  for (int j = n + threadIdx.x; j < np; j += blockDim.x) {
-    S.ckey[j] = 0ull;
-    S.cmass[j] = 0ull;
+  const float before = block_sum<float>(pre.value(), S.sf);  // synchronises
+  *n = S.s_n;
+  if (*n <= CAP / 2) {
+    // rank by counting (keys are distinct): two barriers instead of a sorting network
+    const int nn = *n;
+    for (int j = threadIdx.x; j < nn; j += blockDim.x) {
+      S.tkey[j] = S.lkey[j];
+      S.tmass[j] = S.lmass[j];
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < nn; j += blockDim.x) {
+      const u64 kj = S.tkey[j];
+      int r = 0;
+      for (int q = 0; q < nn; ++q) r += S.tkey[q] > kj;
+      S.lkey[r] = kj;
+      S.lmass[r] = S.tmass[j];
+    }
+  } else if (*n <= CAP) {
+    int np = 2;
+    while (np < *n) np <<= 1;
+    for (int j = *n + threadIdx.x; j < np; j += blockDim.x) {
+      S.lkey[j] = 0ull;
+      S.lmass[j] = 0.f;
+    }
+    __syncthreads();
+    sort_desc(S.lkey, S.lmass, np);
   }
   __syncthreads();
-  sort_desc(S.ckey, S.cmass, np);
-  return n;
+  return before;
 }
 
-// Exact selection among the tokens of bin `bsel` with key >= lo, in descending key order:
-// mode 0 -> the token of rank `want` (0-based); mode 1 -> the token at which the running
-// mass first reaches `want` (>= 1; the last token when the bin's mass is smaller). A
-// radix select over the 64-bit keys, eight digits of 8 bits, most significant first.
+// First entry j of the sorted list whose running mass (after `before`) reaches target;
+// n - 1 when none does. *incl = before + the list's mass up to and including j.
+__device__ int list_cross(FilterSmem& S, int n, float before, float target, float* incl) {
+  if (n <= 0) {
+    *incl = before;
+    return -1;
+  }
+  const int j0 = threadIdx.x * 2;
+  const float a = j0 < n ? S.lmass[j0] : 0.f;
+  const float b = j0 + 1 < n ? S.lmass[j0 + 1] : 0.f;
+  float tot;
+  const float inc = block_scan<float>(a + b, S.sf, &tot);
+  if (threadIdx.x == 0) S.s_j = n - 1;
+  __syncthreads();
+  const float ex = before + (inc - a - b);
+  // the first crossing: the lowest j with before + prefix >= target
+  if (j0 < n && ex + a >= target) atomicMin(&S.s_j, j0);
+  else if (j0 + 1 < n && ex + a + b >= target) atomicMin(&S.s_j, j0 + 1);
+  __syncthreads();
+  const int j = S.s_j;
+  if (threadIdx.x == (j >> 1)) S.s_f = ex + a + ((j & 1) ? b : 0.f);
+  __syncthreads();
+  *incl = S.s_f;
+  return j;
+}
+
+// Fixed-order sum of the sorted list's masses 0 .. upto.
+__device__ float list_prefix(FilterSmem& S, int upto) {
+  const int j0 = threadIdx.x * 2;
+  float x = 0.f;
+  if (j0 <= upto) x += S.lmass[j0];
+  if (j0 + 1 <= upto) x += S.lmass[j0 + 1];
+  return block_sum<float>(x, S.sf);
+}
+
+// Bins [lo, hi] (contiguous) whose approximate running mass interval, widened by eps,
+// contains target: the bins the exact crossing can be in. Bins past `last` are empty.
+__device__ void candidate_bins(FilterSmem& S, float target, float eps, int last) {
+  const int j0 = threadIdx.x * 4;
+  float loc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) loc += j0 + i <= last ? S.mass[j0 + i] : 0.f;
+  float tot;
+  const float inc = block_scan<float>(loc, S.sf, &tot);
+  if (threadIdx.x == 0) {
+    S.s_lo = NB;
+    S.s_hi = -1;
+  }
+  __syncthreads();
+  float ex = inc - loc;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int bn = j0 + i;
+    if (bn > last) break;
+    const float in = ex + S.mass[bn];
+    if (ex - eps <= target && target <= in + eps) {
+      atomicMin(&S.s_lo, bn);
+      atomicMax(&S.s_hi, bn);
+    }
+    ex = in;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && S.s_hi < 0) {  // rounding left no bin: take them all
+    S.s_lo = 0;
+    S.s_hi = last;
+  }
+  __syncthreads();
+}
+
+// Exact selection among the tokens with bin in [lo, hi] and key >= kmin, in descending key
+// order: mode 0 -> the token of rank `want` (0-based); mode 1 -> the first token at which
+// `before` + the running mass reaches `target` (the last token when none does). A radix
+// select over the 64-bit keys, eight digits of 8 bits, most significant first. Used only
+// when the candidate tokens do not fit the sorted list (mode 1 sums its digit masses with
+// fp32 atomics, so on that path the result may depend on their order).
 __device__ u64 radix_select(FilterSmem& S, const float* row, int V, bool vec, float m, float c,
-                            int bsel, u64 lo, int mode, u64 want) {
-  u64* hc = S.ckey;   // 256-entry histograms (the sorted list is not in use here)
-  u64* hm = S.cmass;
+                            int lo, int hi, u64 kmin, int mode, unsigned want, float target) {
+  unsigned* hc = reinterpret_cast<unsigned*>(S.lkey);  // 256-entry histograms
+  float* hm = S.lmass;
   if (threadIdx.x == 0) {
     S.s_prefix = 0ull;
-    S.s_want = want;
+    S.s_n = (int)want;
+    S.s_f = target;
   }
   for (int d = 7; d >= 0; --d) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-      hc[i] = 0ull;
-      hm[i] = 0ull;
+      hc[i] = 0u;
+      hm[i] = 0.f;
     }
     __syncthreads();
     const u64 prefix = S.s_prefix;
     const int sh = 8 * d;
     for_row(row, V, vec, [&](int v, float l) {
+      const int bn = bin_of(l, m, c);
+      if (bn < lo || bn > hi) return;
       const u64 k = vkey(l, v);
-      if (k < lo || bin_of(l, m, c) != bsel) return;
+      if (k < kmin) return;
       if (d < 7 && (k >> (sh + 8)) != prefix) return;
       const int bk = (int)((k >> sh) & 255ull);
-      atomicAdd(&hc[bk], 1ull);
-      if (mode == 1) atomicAdd(&hm[bk], fixp(emass(l, m, c)));
+      atomicAdd(&hc[bk], 1u);
+      if (mode == 1) atomicAdd(&hm[bk], emass(l, m, c));
     });
     __syncthreads();
     if (threadIdx.x == 0) {
-      const u64 w = S.s_want;
-      u64 acc = 0;
+      unsigned w = (unsigned)S.s_n;
+      float t = S.s_f;
+      unsigned acc = 0;
+      float macc = 0.f;
       int pick = -1, last = 0;
       for (int bk = 255; bk >= 0; --bk) {
-        if (hc[bk] == 0ull) continue;
+        if (hc[bk] == 0u) continue;
         last = bk;
-        const u64 x = mode == 0 ? hc[bk] : hm[bk];
-        if (mode == 0 ? (acc + x > w) : (acc + x >= w)) {
+        if (mode == 0 ? (acc + hc[bk] > w) : (macc + hm[bk] >= t)) {
           pick = bk;
           break;
         }
-        acc += x;
+        acc += hc[bk];
+        macc += hm[bk];
       }
-      // not reached inside this bin: the last token (every later digit takes its last)
-      S.s_want = pick >= 0 ? w - acc : ~0ull;
+      if (pick >= 0) {
+        S.s_n = (int)(w - acc);
+        S.s_f = t - macc;
+      } else {  // not reached: the last token (every later digit takes its last)
+        S.s_n = 0x7fffffff;
+        S.s_f = INFINITY;
+      }
       S.s_prefix = (prefix << 8) | (u64)(pick >= 0 ? pick : last);
     }
     __syncthreads();
   }
   return S.s_prefix;
+}
+
+// Compensated mass of the tokens with key >= kmin (and mass >= minp).
+__device__ float kept_total(FilterSmem& S, const float* row, int V, bool vec, float m, float c,
+                            u64 kmin, float minp) {
+  Kahan acc;
+  for_row(row, V, vec, [&](int v, float l) {
+    if (vkey(l, v) < kmin) return;
+    const float e = emass(l, m, c);
+    if (e >= minp) acc.add(e);
+  });
+  return block_sum<float>(acc.value(), S.sf);
 }
 
 __global__ void __launch_bounds__(FT, 1)
@@ -322,11 +449,10 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
   const float mp = a.min_p[b];
   RowStats st;
   st.m = m;
-  st.valid = 1;
   const bool greedy = !(tau > 0.f) || k == 1 || pp <= 0.f || isinf(m);
   if (greedy) {
     st.thr = maxkey;
-    st.z = fixp(1.f);
+    st.z = 1.f;
     st.c = 0.f;
     st.minp = 0.f;
   } else {
@@ -336,94 +462,133 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
     st.c = c;
     st.minp = mp > 0.f ? fminf(mp, 1.f) : 0.f;
     u64 thr = 0ull;
+    float z = -1.f;  // the kept mass when a scan below has it already
     if (topk_on || topp_on) {
       for (int j = threadIdx.x; j < NB; j += FT) {
-        S.cnt[j] = 0ull;
-        S.mass[j] = 0ull;
+        S.cnt[j] = 0u;
+        S.mass[j] = 0.f;
       }
       __syncthreads();
+      // The open last bin takes no atomics (with a peaked row most tokens land there, all
+      // on one address); its count and mass follow from the totals below.
+      Kahan all;
       for_row(row, V, vec, [&](int v, float l) {
         const int bn = bin_of(l, m, c);
-        atomicAdd(&S.cnt[bn], 1ull);
-        const u64 w = fixp(emass(l, m, c));
-        if (w) atomicAdd(&S.mass[bn], w);
+        const float e = emass(l, m, c);
+        all.add(e);
+        if (bn == NB - 1) return;
+        if (topk_on) atomicAdd(&S.cnt[bn], 1u);
+        if (topp_on) atomicAdd(&S.mass[bn], e);
       });
-      __syncthreads();
-      int bk = NB;          // bins from bk on are outside the top-k set
-      bool listed = false;  // S.ckey / S.cmass hold the top-k part of bin bk, sorted
-      int nlist = 0;
-      u64 thr_k = 0ull;
-      if (topk_on) {
-        u64 before;
-        bk = cross_index(S.cnt, NB, (u64)k, S, &before);  // k < V: always found
-        const int r = k - 1 - (int)before;                // rank inside bin bk
-        u64 part = 0ull;
-        if (bk < NB - 1 && S.cnt[bk] <= (u64)CAP) {
-          collect_sorted(S, row, V, vec, m, c, bk, 0ull);
-          thr_k = S.ckey[r];
-          listed = true;
-          nlist = r + 1;
-          for (int j = threadIdx.x; j <= r; j += FT) part += S.cmass[j];
-        } else {
-          thr_k = radix_select(S, row, V, vec, m, c, bk, 0ull, 0, (u64)r);
-          for_row(row, V, vec, [&](int v, float l) {
-            if (bin_of(l, m, c) == bk && vkey(l, v) >= thr_k) part += fixp(emass(l, m, c));
-          });
+      float z1 = block_sum<float>(all.value(), S.sf);  // synchronises
+      {
+        unsigned cl = 0;
+        float ml = 0.f;
+        for (int j = threadIdx.x; j < NB - 1; j += FT) {
+          cl += S.cnt[j];
+          ml += S.mass[j];
         }
-        const u64 mass_in = block_sum_u64(part, S.sb);
-        // the histogram now describes the top-k set only
-        for (int j = threadIdx.x; j < NB; j += FT) {
-          if (j > bk) {
-            S.cnt[j] = 0ull;
-            S.mass[j] = 0ull;
-          } else if (j == bk) {
-            S.cnt[j] = (u64)(r + 1);
-            S.mass[j] = mass_in;
-          }
+        const unsigned ca = block_sum<unsigned>(cl, S.su);
+        const float ma = block_sum<float>(ml, S.sf);
+        if (threadIdx.x == 0) {
+          S.cnt[NB - 1] = (unsigned)V - ca;
+          S.mass[NB - 1] = fmaxf(0.f, z1 - ma);
         }
         __syncthreads();
       }
-      thr = thr_k;
-      if (topp_on) {
-        u64 loc = 0ull;
-        for (int j = threadIdx.x; j < NB; j += FT) loc += S.mass[j];
-        const u64 z1 = block_sum_u64(loc, S.sb);
-        const u64 target = (u64)((double)pp * (double)z1);
-        u64 thr_p;
-        if (target == 0ull) {
-          thr_p = maxkey;  // only the first token is kept
-        } else {
-          u64 before;
-          const int bp = cross_index(S.mass, NB, target, S, &before);
-          const u64 want = target - before;
-          if (listed && bp == bk) {
-            u64 b2;
-            const int j = cross_index(S.cmass, nlist, want, S, &b2);
-            thr_p = S.ckey[j < 0 ? nlist - 1 : j];
-          } else if (bp < NB - 1 && S.cnt[bp] <= (u64)CAP) {
-            const int nc = collect_sorted(S, row, V, vec, m, c, bp, thr_k);
-            u64 b2;
-            const int j = cross_index(S.cmass, nc, want, S, &b2);
-            thr_p = S.ckey[j < 0 ? nc - 1 : j];
-          } else {
-            thr_p = radix_select(S, row, V, vec, m, c, bp, thr_k, 1, want);
+      int bk = NB - 1;  // last bin of the top-k set
+      u64 thr_k = 0ull;
+      if (topk_on) {
+        // the bin holding the k-th token: exact counts
+        const int j0 = threadIdx.x * 4;
+        unsigned loc = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) loc += S.cnt[j0 + q];
+        unsigned tot;
+        const unsigned inc = block_scan<unsigned>(loc, S.su, &tot);
+        unsigned ex = inc - loc;
+        if (ex < (unsigned)k && (unsigned)k <= inc) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (ex + S.cnt[j0 + q] >= (unsigned)k) {
+              S.s_lo = j0 + q;
+              S.s_j = (int)((unsigned)k - 1u - ex);  // rank inside the bin
+              break;
+            }
+            ex += S.cnt[j0 + q];
           }
         }
+        __syncthreads();
+        bk = S.s_lo;
+        const int r = S.s_j;
+        int ng;
+        const float before = gather_bins(S, row, V, vec, m, c, bk, bk, 0ull, &ng);
+        if (ng <= CAP) {
+          thr_k = S.lkey[r];
+          // the top-k mass: everything before bin bk, then the list up to rank r
+          z1 = before + list_prefix(S, r);
+        } else {
+          thr_k = radix_select(S, row, V, vec, m, c, bk, bk, 0ull, 0, (unsigned)r, 0.f);
+          z1 = kept_total(S, row, V, vec, m, c, thr_k, 0.f);
+        }
+        z = z1;
+      }
+      thr = thr_k;
+      if (topp_on) {
+        const float target = pp * z1;
+        // the bins the crossing can be in (the top-k set ends inside bin bk; its part of
+        // bin bk replaces the bin's mass)
+        if (topk_on) {
+          // mass of bin bk inside the set = z1 - the bins before it (approximate)
+          float loc = 0.f;
+          for (int j = threadIdx.x; j < bk; j += FT) loc += S.mass[j];
+          const float pre = block_sum<float>(loc, S.sf);
+          if (threadIdx.x == 0) S.mass[bk] = fmaxf(0.f, z1 - pre);
+          __syncthreads();
+        }
+        candidate_bins(S, target, 1e-4f * z1 + 1e-30f, bk);
+        int lo = S.s_lo, hi = S.s_hi;
+        u64 thr_p = maxkey;
+        float zp = -1.f;
+        for (int tries = 0; tries < 3; ++tries) {
+          int ng;
+          const float before = gather_bins(S, row, V, vec, m, c, lo, hi, thr_k, &ng);
+          if (ng > CAP) {
+            thr_p = radix_select(S, row, V, vec, m, c, lo, hi, thr_k, 1, 0u, target - before);
+            zp = -1.f;
+            break;
+          }
+          if (before >= target && lo > 0) {  // the crossing is earlier: widen down
+            hi = lo - 1;
+            lo = 0;
+            continue;
+          }
+          float incl;
+          const int j = list_cross(S, ng, before, target, &incl);
+          if (incl < target && hi < bk) {  // the crossing is later: widen up
+            lo = hi + 1;
+            hi = bk;
+            continue;
+          }
+          if (ng > 0) {
+            thr_p = S.lkey[j];
+            zp = incl;
+          }
+          break;
+        }
         thr = max(thr_k, thr_p);
+        z = thr_p >= thr_k ? zp : z;
       }
     }
     st.thr = thr;
-    u64 z = 0ull;
-    for_row(row, V, vec, [&](int v, float l) { z += kept_mass(st, l, v); });
-    st.z = block_sum_u64(z, S.sb);
+    if (z < 0.f || st.minp > 0.f) z = kept_total(S, row, V, vec, m, c, thr, st.minp);
+    st.z = z;
   }
   if (threadIdx.x == 0) stats[(int64_t)b * T + i] = st;
   if (probs) {
     float* out = probs + ((int64_t)b * T + i) * V;
-    const double inv = 1.0 / (double)st.z;
-    for_row(row, V, false, [&](int v, float l) {
-      out[v] = (float)((double)kept_mass(st, l, v) * inv);
-    });
+    const float inv = 1.f / st.z;
+    for_row(row, V, false, [&](int v, float l) { out[v] = kept_mass(st, l, v) * inv; });
   }
 }
 
@@ -433,23 +598,32 @@ struct WalkSmem {
   int kids[TSV_MAX_NODES];
   float kl[TSV_MAX_NODES], kq[TSV_MAX_NODES];
   int removed[TSV_MAX_NODES];
-  u64 rmass[TSV_MAX_NODES];
+  float rmass[TSV_MAX_NODES];
   float zr[TSV_MAX_NODES];  // draft-aware: normalisers of the residuals at this node
   int path[TSV_MAX_DEPTH + 1];
-  u64 seg[WT];
-  double segd[WT];
-  u64 sb[32];
-  double sd[32];
+  float tile[MAX_TILES];
+  float sf[32];
   RowStats st;
-  u64 zcur;  // target-only: the current node's normaliser after its removals
-  int node, len, code, nk, acc, nrem, nz, pick;
+  float zcur;  // target-only: the current node's normaliser after its removals
+  float target;
+  int node, len, code, nk, acc, nrem, nz, pick, ptile;
 };
 
 // Draft-aware residual probability of token v after `nz` rejections at this node.
 __device__ __forceinline__ float resid_p(const WalkSmem& W, float l, int v, float q) {
-  float r = (float)((double)kept_mass(W.st, l, v) / (double)W.st.z);
+  float r = kept_mass(W.st, l, v) / W.st.z;
   for (int j = 0; j < W.nz; ++j) r = fmaxf(0.f, r - q) / W.zr[j];
   return r;
+}
+// Weight of token v (logit l, draft probability q) in the final sample, before the
+// target-only removals.
+__device__ __forceinline__ float final_w(const WalkSmem& W, bool draft, float l, int v, float q) {
+  return draft ? resid_p(W, l, v, q) : kept_mass(W.st, l, v);
+}
+__device__ __forceinline__ bool removed_tok(const WalkSmem& W, int v) {
+  for (int r = 0; r < W.nrem; ++r)
+    if (W.removed[r] == v) return true;
+  return false;
 }
 
 __global__ void __launch_bounds__(WT)
@@ -528,12 +702,12 @@ sample_walk_kernel(const SampleArgs a, const RowStats* __restrict__ stats, Cache
           const int c = W.kids[j];
           const int x = W.tok[c];
           const bool in = x >= 0 && x < V;
-          const u64 km = in ? kept_mass(W.st, W.kl[j], x) : 0ull;
+          const float km = in ? kept_mass(W.st, W.kl[j], x) : 0.f;
           float p, q = W.kq[j];
           if (!draft) {
             bool gone = false;
             for (int r = 0; r < W.nrem; ++r) gone |= W.removed[r] == x;
-            p = gone ? 0.f : (float)((double)km / (double)W.zcur);
+            p = gone ? 0.f : km / W.zcur;
             q = 1.f;
           } else {
             p = in ? resid_p(W, W.kl[j], x, q) : 0.f;
@@ -542,7 +716,7 @@ sample_walk_kernel(const SampleArgs a, const RowStats* __restrict__ stats, Cache
           const float u = a.u_node[row0 + c];
           if (u < fminf(1.f, ratio)) {
             W.acc = j;
-          } else if (!draft && p > 0.f && W.zcur > km) {
+          } else if (!draft && p > 0.f && W.zcur - km > 0.f) {
             // the residual without x (a residual of zero mass keeps p as it was)
             W.zcur -= km;
             W.removed[W.nrem] = x;
@@ -554,13 +728,13 @@ sample_walk_kernel(const SampleArgs a, const RowStats* __restrict__ stats, Cache
         if (W.acc >= 0) break;
         if (draft) {
           // residual normaliser: sum over v of max(0, p_j(v) - q(v))
-          double part = 0.0;
+          Kahan part;
           for (int v = threadIdx.x; v < V; v += WT) {
             const float q = qrow[v];
-            part += (double)fmaxf(0.f, resid_p(W, clean(lrow[v]), v, q) - q);
+            part.add(fmaxf(0.f, resid_p(W, clean(lrow[v]), v, q) - q));
           }
-          const double zn = block_sum_f64(part, W.sd);
-          if (threadIdx.x == 0 && zn > 0.0) W.zr[W.nz++] = (float)zn;
+          const float zn = block_sum<float>(part.value(), W.sf);
+          if (threadIdx.x == 0 && zn > 0.f) W.zr[W.nz++] = zn;
           __syncthreads();
         }
       }
@@ -599,78 +773,103 @@ sample_walk_kernel(const SampleArgs a, const RowStats* __restrict__ stats, Cache
   }
   __syncthreads();
 
-  // ---- the sample where the walk stopped: smallest t with prefix(t) > u * total -----
+  // ---- the sample where the walk stopped: the smallest t whose running weight exceeds
+  // u * total. Tiles of TILE tokens: warp w sums tiles w, w + 16, ...; the crossing tile
+  // is found from the tile sums in order; a block scan inside it finds the token.
   int token = -1;
   if (size_ok) {
     const int node = W.node;
     const float* lrow = a.logits + (row0 + node) * V;
     const float* qrow = draft ? a.draft_probs + (row0 + node) * V : nullptr;
-    const int L = (V + WT - 1) / WT;
-    const int v0 = min(V, threadIdx.x * L), v1 = min(V, v0 + L);
-    const float u = a.u_final[b];
-    if (!draft) {
-      u64 s = 0ull;
-      for (int v = v0; v < v1; ++v) s += kept_mass(W.st, clean(lrow[v]), v);
-      W.seg[threadIdx.x] = s;
-      __syncthreads();
-      if (threadIdx.x == 0)
-        for (int r = 0; r < W.nrem; ++r) W.seg[min(WT - 1, W.removed[r] / L)] -= W.rmass[r];
-      __syncthreads();
-      const u64 mine = W.seg[threadIdx.x];
-      u64 total;
-      const u64 incl = block_scan<u64>(mine, W.sb, &total);
-      const u64 target = (u64)((double)u * (double)total);
-      if (threadIdx.x == 0) W.pick = -1;
-      __syncthreads();
-      u64 acc = incl - mine;
-      if (acc <= target && target < incl) {
-        for (int v = v0; v < v1; ++v) {
-          bool gone = false;
-          for (int r = 0; r < W.nrem; ++r) gone |= W.removed[r] == v;
-          const u64 w = gone ? 0ull : kept_mass(W.st, clean(lrow[v]), v);
-          if (acc + w > target) {
-            W.pick = v;
-            break;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = (V + TILE - 1) / TILE;
+    for (int t = warp; t < ntiles; t += WT / 32) {
+      // lane l takes tokens t*TILE + 4*(l + 32 q) .. +3, q = 0..15, eight loads in flight
+      const int base = t * TILE + 4 * lane;
+      float s = 0.f;
+      for (int h = 0; h < 2; ++h) {
+        float lv[32], qv[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int v = base + 128 * (8 * h + q) + e;
+            lv[4 * q + e] = v < V ? __ldg(lrow + v) : -INFINITY;
+            qv[4 * q + e] = draft && v < V ? __ldg(qrow + v) : 0.f;
           }
-          acc += w;
-        }
-      }
-      __syncthreads();
-      token = W.pick;
-    } else {
-      double s = 0.0;
-      for (int v = v0; v < v1; ++v) s += (double)resid_p(W, clean(lrow[v]), v, qrow[v]);
-      double total;
-      const double incl = block_scan<double>(s, W.segd, &total);
-      const double target = (double)u * total;
-      if (threadIdx.x == 0) W.pick = -1;
-      __syncthreads();
-      double acc = incl - s;
-      if (acc <= target && target < incl) {
-        for (int v = v0; v < v1; ++v) {
-          const double w = (double)resid_p(W, clean(lrow[v]), v, qrow[v]);
-          if (acc + w > target) {
-            W.pick = v;
-            break;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int v = base + 128 * (8 * h + q) + e;
+            if (v < V) s += final_w(W, draft, clean(lv[4 * q + e]), v, qv[4 * q + e]);
           }
-          acc += w;
-        }
       }
-      __syncthreads();
-      token = W.pick;
-      if (token < 0) {
-        // rounding put the target past the last positive entry: the last kept token
-        if (threadIdx.x == 0) {
-          for (int v = V - 1; v >= 0; --v)
-            if (resid_p(W, clean(lrow[v]), v, qrow[v]) > 0.f) {
-              W.pick = v;
-              break;
-            }
-        }
-        __syncthreads();
-        token = W.pick;
-      }
+      const float ts = warp_sum(s);
+      if (lane == 0) W.tile[t] = ts;
     }
+    __syncthreads();
+    if (threadIdx.x == 0 && !draft)  // the target-only removals
+      for (int r = 0; r < W.nrem; ++r) W.tile[W.removed[r] / TILE] -= W.rmass[r];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      Kahan tot;
+      int lastpos = -1;
+      for (int t = 0; t < ntiles; ++t) {
+        tot.add(W.tile[t]);
+        if (W.tile[t] > 0.f) lastpos = t;
+      }
+      const float target = a.u_final[b] * tot.value();
+      Kahan run;
+      int pt = -1;
+      for (int t = 0; t < ntiles; ++t) {
+        if (W.tile[t] > 0.f && run.value() + W.tile[t] > target) {
+          pt = t;
+          break;
+        }
+        run.add(W.tile[t]);
+      }
+      // rounding put the target past the last positive tile: its last token
+      W.target = pt >= 0 ? target - run.value() : INFINITY;
+      W.ptile = pt >= 0 ? pt : max(lastpos, 0);
+      W.pick = 0x7fffffff;
+    }
+    __syncthreads();
+    const int t = W.ptile;
+    const int v0 = t * TILE + threadIdx.x * 4;
+    float w4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int v = v0 + q;
+      w4[q] = v < V && !(!draft && removed_tok(W, v))
+                  ? final_w(W, draft, clean(lrow[v]), v, draft ? qrow[v] : 0.f)
+                  : 0.f;
+    }
+    const float mine = w4[0] + w4[1] + w4[2] + w4[3];
+    float tot;
+    const float incl = block_scan<float>(mine, W.sf, &tot);
+    float acc = incl - mine;
+    const float target = W.target;
+    int found = -1, lastpos = -1;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (w4[q] > 0.f) {
+        lastpos = v0 + q;
+        if (found < 0 && acc + w4[q] > target) found = v0 + q;
+      }
+      acc += w4[q];
+    }
+    if (found >= 0) atomicMin(&W.pick, found);
+    __syncthreads();
+    if (W.pick == 0x7fffffff) {
+      // rounding put the target past the tile's last positive weight: take that token
+      __syncthreads();
+      if (threadIdx.x == 0) W.pick = -1;
+      __syncthreads();
+      if (lastpos >= 0) atomicMax(&W.pick, lastpos);
+      __syncthreads();
+    }
+    token = W.pick;
   }
 
   const int cols = a.max_depth + 1;
