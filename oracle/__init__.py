@@ -12,6 +12,7 @@ Pages cited in this package (by title):
   [HB]    "推理系统手册 · 投机解码进阶：树形草稿与 EAGLE"
   [EAGLE2] the EAGLE v2 dynamic-tree walkthrough ("动态树解码 … initialize_tree /
           topK_generate / tree_decoding / evaluate_posterior"), sections 3-5.
+  [MO]    "EAGLE头结构深潜: Model Optimizer 投机解码草稿模型的内部设计"
 
 Precision: fp64 everywhere, except where a floating-point value decides an integer
 (the joint top-k and the final selection): there the scores are held in fp32, the

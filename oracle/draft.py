@@ -79,17 +79,23 @@ class Level:
         self.selected = selected        # list of K flat indices, best first
 
 
-def expand_level(logits, k: int, parent_scores=None, parent_store=None) -> Level:
+def expand_level(logits, k: int, parent_scores=None, parent_store=None,
+                 product: bool = False) -> Level:
     """One topK_generate level ([EAGLE2] section 3).
 
     logits: [R, V] fp32, row s belongs to frontier node s (R = 1 at the base layer).
-    parent_scores: fp32 [R] cumulative scores of the frontier (None: the root, 0).
+    parent_scores: fp32 [R] cumulative scores of the frontier (None: the root, 0; with
+    product, 1).
     parent_store: int32 [R] store index of each frontier node (None: the root, -1).
+    product: [TRT] section 树的三套账 (_select_topk_draft_tokens): the cumulative score is
+    the parent's score times the child's probability (all_scores = new_scores *
+    previous_scores), in probability form; the child's probability is exp of its fp32
+    log-probability, rounded to fp32, and the product is an fp32 product.
     """
     logits = np.asarray(logits, dtype=F32)
     r = logits.shape[0]
     if parent_scores is None:
-        parent_scores = np.zeros(r, dtype=F32)
+        parent_scores = (np.ones if product else np.zeros)(r, dtype=F32)
         parent_store = np.full(r, -1, dtype=np.int32)
     tokens = np.zeros(r * k, dtype=np.int32)
     logp = np.zeros(r * k, dtype=F32)
@@ -102,7 +108,10 @@ def expand_level(logits, k: int, parent_scores=None, parent_store=None) -> Level
             flat = s * k + c
             tokens[flat] = top[c]
             logp[flat] = F32(float(logits[s, top[c]]) - lse)
-            cu[flat] = F32(parent_scores[s]) + logp[flat]  # fp32 sum
+            if product:
+                cu[flat] = F32(parent_scores[s]) * F32(math.exp(float(logp[flat])))
+            else:
+                cu[flat] = F32(parent_scores[s]) + logp[flat]  # fp32 sum
             pstore[flat] = parent_store[s]
     selected = topk_by_score(cu, k)
     return Level(tokens, logp, cu, pstore, selected)
@@ -127,8 +136,9 @@ class Expansion:
         self.levels = levels
 
 
-def topk_generate(level_logits, k: int) -> Expansion:
-    """All levels of one request: level_logits[0] is [1, V], the rest [K, V]."""
+def topk_generate(level_logits, k: int, product: bool = False) -> Expansion:
+    """All levels of one request: level_logits[0] is [1, V], the rest [K, V]. product:
+    the probability-product scores of expand_level."""
     depth = len(level_logits) - 1
     c = num_candidates(k, depth)
     store_token = np.zeros(c, dtype=np.int32)
@@ -139,7 +149,7 @@ def topk_generate(level_logits, k: int) -> Expansion:
     front_store = None
     for li, lg in enumerate(level_logits):
         level = li + 1
-        lv = expand_level(lg, k, front_scores, front_store)
+        lv = expand_level(lg, k, front_scores, front_store, product)
         off = level_store_offset(level, k)
         n = lv.tokens.size
         store_token[off:off + n] = lv.tokens
@@ -185,3 +195,35 @@ def margins(exp: Expansion, total_tokens: int) -> float:
     if total_tokens < len(s):
         m = min(m, s[total_tokens - 1] - s[total_tokens])
     return m
+
+
+def map_draft_to_target(tokens, num_nodes: int, d2t):
+    """Draft-vocabulary ids to target-vocabulary ids ([MO] section 独立小lm_head草稿词表压缩:
+    the drafter predicts over a smaller vocabulary and a d2t buffer maps each draft id
+    back, draft_token = d2t[draft_token]). Node 0 (the root, a token the target already
+    committed) is left as it is; a draft id outside the table maps to -1, which no
+    target token equals."""
+    out = np.array(tokens, dtype=np.int32).copy()
+    for i in range(1, num_nodes):
+        t = int(out[i])
+        out[i] = int(d2t[t]) if 0 <= t < len(d2t) else -1
+    return out
+
+
+def fixed_tree(level_logits, branching, root_token: int):
+    """The fixed-shape draft tree of [HB] section 实现 (build_draft_tree): level l gives
+    every frontier node its top-branching[l] tokens (larger logit first, lower id on
+    ties), appended frontier node by frontier node. level_logits[l] is [F_l, V], row f
+    the draft's logits at the l-th level's f-th frontier node. Returns (tokens, parents)."""
+    tokens, parents, frontier = [int(root_token)], [-1], [0]
+    for width, lg in zip(branching, level_logits):
+        lg = np.asarray(lg, dtype=F32)
+        assert lg.shape[0] == len(frontier)
+        nxt = []
+        for f, node in enumerate(frontier):
+            for t in row_topk(lg[f], width):
+                tokens.append(int(t))
+                parents.append(node)
+                nxt.append(len(tokens) - 1)
+        frontier = nxt
+    return np.array(tokens, dtype=np.int32), np.array(parents, dtype=np.int32)

@@ -153,3 +153,66 @@ def test_total_tokens_equal_to_store_keeps_everything():
     tokens, parents = draft.select_final(exp.store_token, exp.store_score, exp.store_parent, c, 5)
     assert tokens[1:].tolist() == exp.store_token.tolist()
     assert parents[1:k + 1].tolist() == [0] * k
+
+
+# ---- expansion variants ------------------------------------------------------------
+def test_product_scores_are_the_exponentials_of_the_log_sums():
+    """[TRT]'s parent-times-child probability scores: each equals exp of the log-domain
+    cumulative score (within fp32 rounding), so both modes rank alike wherever the log
+    scores are apart."""
+    from oracle import draft as D
+    rng = np.random.default_rng(4)
+    k, depth, v = 4, 3, 60
+    levels = [rng.normal(0, 2, (1, v)).astype(np.float32)] + \
+        [rng.normal(0, 2, (k, v)).astype(np.float32) for _ in range(depth)]
+    lg = D.topk_generate(levels, k)
+    pr = D.topk_generate(levels, k, product=True)
+    np.testing.assert_allclose(pr.store_score, np.exp(lg.store_score.astype(np.float64)),
+                               rtol=1e-5)
+    if D.margins(lg, 8) > 1e-4:
+        for a, b in zip(lg.levels, pr.levels):
+            assert a.selected == b.selected
+    assert lg.store_token.tolist() == pr.store_token.tolist()
+    assert lg.store_parent.tolist() == pr.store_parent.tolist()
+    # the base layer's product scores are the top-k probabilities themselves
+    p = np.exp(levels[0][0].astype(np.float64) - np.log(np.exp(levels[0][0].astype(np.float64)).sum()))
+    np.testing.assert_allclose(pr.store_score[:k], np.sort(p)[::-1][:k], rtol=1e-6)
+
+
+def test_draft_to_target_map():
+    from oracle import draft as D
+    toks = np.array([77, 0, 3, 5, 9, 2], np.int32)
+    ident = np.arange(8)
+    assert D.map_draft_to_target(toks, 6, ident).tolist() == [77, 0, 3, 5, -1, 2]
+    perm = np.array([10, 11, 12, 13, 14, 15, 16, 17]) * 3
+    assert D.map_draft_to_target(toks, 4, perm).tolist() == [77, 30, 39, 45, 9, 2]
+
+
+def test_fixed_tree_by_hand_and_by_property():
+    from oracle import draft as D
+    from oracle import tree as Tr
+    root_row = np.array([[0.1, 0.9, 0.5, 0.9, -1.0]], np.float32)  # tie: id 1 before 3
+    lvl2 = np.array([[5, 0, 0, 0, 0], [0, 0, 0, 0, 2]], np.float32)
+    tokens, parents = D.fixed_tree([root_row, lvl2], [2, 1], 42)
+    assert tokens.tolist() == [42, 1, 3, 0, 4]
+    assert parents.tolist() == [-1, 0, 0, 1, 2]
+    rng = np.random.default_rng(9)
+    branching = [3, 2, 2]
+    frontier, rows = 1, []
+    for wdt in branching:
+        rows.append(rng.normal(size=(frontier, 40)).astype(np.float32))
+        frontier *= wdt
+    tokens, parents = D.fixed_tree(rows, branching, 7)
+    assert parents.tolist() == Tr.fixed_branching_parents(branching)
+    # every node's children carry its row's top tokens, best first
+    depth = Tr.depths(parents.tolist())
+    level_nodes = {}
+    for i, d in enumerate(depth):
+        level_nodes.setdefault(d, []).append(i)
+    for d, nodes in level_nodes.items():
+        if d >= len(branching):
+            continue
+        for f, node in enumerate(nodes):
+            kids = [c for c in range(len(parents)) if parents[c] == node]
+            row = rows[d][f]
+            assert tokens[kids].tolist() == np.argsort(-row, kind="stable")[:branching[d]].tolist()

@@ -197,3 +197,23 @@ def test_sampling_mistakes_are_caught(monkeypatch, fn, old, new, pin):
             failed += 1
     assert failed >= 1, f"{fn}: {new!r} passed every case of {pin}"
     assert inspect.isfunction(test)
+
+
+VARIANT_MISTAKES = [
+    ("expand_level", "cu[flat] = F32(parent_scores[s]) * F32(math.exp(float(logp[flat])))",
+     "cu[flat] = F32(parent_scores[s]) + F32(math.exp(float(logp[flat])))",
+     "test_product_scores_are_the_exponentials_of_the_log_sums"),
+    ("map_draft_to_target", "for i in range(1, num_nodes):", "for i in range(0, num_nodes):",
+     "test_draft_to_target_map"),
+    ("fixed_tree", "for t in row_topk(lg[f], width):",
+     "for t in np.argsort(-lg[f])[:width][::-1]:", "test_fixed_tree_by_hand_and_by_property"),
+]
+
+
+@pytest.mark.parametrize("fn,old,new,pin", VARIANT_MISTAKES)
+def test_expansion_variant_mistakes_are_caught(monkeypatch, fn, old, new, pin):
+    from oracle import draft
+    from tests import test_oracle_draft as td
+    monkeypatch.setattr(draft, fn, _mutant(draft, fn, old, new))
+    with pytest.raises(AssertionError):
+        getattr(td, pin)()
