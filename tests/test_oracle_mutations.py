@@ -55,8 +55,8 @@ def test_unmasked_tree_part_is_caught(monkeypatch):
 def test_score_product_instead_of_sum_is_caught(monkeypatch):
     orig = draft.expand_level
 
-    def wrong(logits, k, parent_scores=None, parent_store=None):
-        lv = orig(logits, k, parent_scores, parent_store)
+    def wrong(logits, k, parent_scores=None, parent_store=None, product=False):
+        lv = orig(logits, k, parent_scores, parent_store, product)
         if parent_scores is not None:
             r = np.asarray(logits).shape[0]
             for s in range(r):
