@@ -5,6 +5,9 @@
  *   tsv_draft_topk_expand   one level of the draft tree expansion (per-row log-softmax +
  *                           top-k, cumulative scores, joint top-k pruning)
  *   tsv_draft_select_final  the total_tokens best candidates laid out as a tree
+ *   tsv_draft_topk_expand_product, tsv_draft_to_target, tsv_draft_fixed_level
+ *                           expansion variants: probability-product scores, the d2t id
+ *                           map, fixed-branching trees
  *   tsv_tree_build_meta     ancestor bitmask, positions, retrieve_indices, child/sibling links
  *   tsv_tree_verify_attn    RoPE + KV append + tree-masked split-KV attention of every node
  *   tsv_lm_head_argmax      the target's greedy token at every node (lm_head GEMM with an
@@ -21,6 +24,7 @@
  *   [HB]     "推理系统手册 · 投机解码进阶：树形草稿与 EAGLE"
  *   [EAGLE2] the EAGLE v2 dynamic-tree walkthrough (initialize_tree / topK_generate /
  *            tree_decoding / evaluate_posterior), sections 3-5
+ *   [MO]     "EAGLE头结构深潜: Model Optimizer 投机解码草稿模型的内部设计"
  *
  * Conventions for every call:
  *   - Every array pointer is a DEVICE pointer owned by the caller, unless stated. The
@@ -72,8 +76,9 @@ enum tsv_request_error {
   TSV_REQ_CAPACITY = 5,     /* prefix_len[b] + num_nodes[b] does not fit the KV cache */
   TSV_REQ_BAD_BLOCK = 6,    /* a block-table entry outside [0, num_blocks) */
   TSV_REQ_BAD_LINKS = 7,    /* child/sibling links leave the tree */
-  TSV_REQ_TIMEOUT = 8       /* a bounded device-side wait gave up (the request's outputs
+  TSV_REQ_TIMEOUT = 8,      /* a bounded device-side wait gave up (the request's outputs
                                are not valid; the GPU context stays usable) */
+  TSV_REQ_BAD_TOKEN = 9     /* a draft token outside the d2t table (tsv_draft_to_target) */
 };
 
 /* ---- limits ---- */
@@ -182,6 +187,58 @@ int tsv_draft_select_final(const int32_t* store_token, const float* store_score,
                            int store_cap, int total_tokens, const int32_t* root_token,
                            int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
                            tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_draft_topk_expand_product — tsv_draft_topk_expand with the probability-product
+ * scores of [TRT] section 树的三套账 (_select_topk_draft_tokens: a candidate's score is
+ * its parent's score times its own probability, new_scores * previous_scores, ranked
+ * as they are; base layer: the probabilities). The child's probability is expf of its
+ * fp32 log-probability; the product is an fp32 product. Same arguments, layout, ranking
+ * rule (larger score, then the lower flat index) and workspace; front_score_in / out
+ * and store_score hold the products. tsv_draft_select_final ranks them unchanged.
+ * ------------------------------------------------------------------------------ */
+int tsv_draft_topk_expand_product(const float* logits, int batch, int rows, int64_t row_stride,
+                                  int vocab, int top_k, int level, const float* front_score_in,
+                                  const int32_t* front_store_in, int store_cap,
+                                  int32_t* store_token, float* store_score,
+                                  int32_t* store_parent, int32_t* front_token_out,
+                                  float* front_score_out, int32_t* front_store_out,
+                                  void* workspace, size_t workspace_bytes, tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_draft_to_target — draft-vocabulary ids to target ids, in place.
+ *
+ * [MO] section 独立小lm_head草稿词表压缩: a drafter with a smaller vocabulary; the d2t
+ * buffer maps each draft id back (draft_token = d2t[draft_token]).
+ * tokens      [batch, max_nodes] in/out: nodes 1 .. num_nodes[b]-1 become d2t[token];
+ *             node 0 (the root, already a target token) is not touched. An id outside
+ *             [0, draft_vocab) becomes -1 (it matches no target token).
+ * num_nodes   [batch] in; d2t [draft_vocab] int32 in (device).
+ * err         [batch] out (may be NULL): TSV_REQ_BAD_TOKEN where an id was outside the
+ *             table, else TSV_REQ_OK.
+ * ------------------------------------------------------------------------------ */
+int tsv_draft_to_target(int32_t* tokens, const int32_t* num_nodes, int batch, int max_nodes,
+                        const int32_t* d2t, int draft_vocab, int32_t* err, tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_draft_fixed_level — one level of a fixed-branching draft tree.
+ *
+ * [HB] section 实现 (build_draft_tree): level l gives every frontier node its
+ * top-branching[l] tokens, appended frontier node by frontier node.
+ * logits      [batch, frontier, vocab] fp32, rows row_stride floats apart: row f is the
+ *             draft's logits at the level's f-th frontier node (NaN never wins).
+ * width       tokens per frontier node, 1 .. TSV_MAX_TOPK, <= vocab.
+ * first_node  node index of the level's first new node; first_parent that of the first
+ *             frontier node (the frontier is first_parent .. first_parent+frontier-1).
+ * tokens, parents [batch, max_nodes] out: for f < frontier, r < width, node
+ *             first_node + f*width + r gets the f-th row's r-th best token (larger logit,
+ *             then the lower id) and parent first_parent + f. Other entries untouched;
+ *             the caller writes the root (node 0, parent -1) and num_nodes.
+ * Returns TSV_ERR_INVALID_ARG for sizes out of range or nodes past max_nodes.
+ * ------------------------------------------------------------------------------ */
+int tsv_draft_fixed_level(const float* logits, int batch, int frontier, int64_t row_stride,
+                          int vocab, int width, int first_node, int first_parent, int max_nodes,
+                          int32_t* tokens, int32_t* parents, tsv_stream_t stream);
 
 /* --------------------------------------------------------------------------------
  * tsv_tree_build_meta — tree metadata, one warp per tree.

@@ -18,7 +18,7 @@ def built():
     assert torch.cuda.is_available()
 
 
-def run_levels(levels_per_req, k, store_cap=None, stride_pad=0):
+def run_levels(levels_per_req, k, store_cap=None, stride_pad=0, product=False):
     """Run every level on the GPU; levels_per_req[b][l] is [rows, V] fp32 numpy."""
     import tree_speculative_decoding_verify_gb300 as T
     b = len(levels_per_req)
@@ -44,7 +44,8 @@ def run_levels(levels_per_req, k, store_cap=None, stride_pad=0):
         lg = torch.from_numpy(host).to(d)[:, :, :v]
         nxt = fronts[li % 2]
         T.draft_topk_expand(lg, k, li + 1, None if cur is None else cur[1],
-                            None if cur is None else cur[2], st, ss, sp, *nxt, ws)
+                            None if cur is None else cur[2], st, ss, sp, *nxt, ws,
+                            product=product)
         torch.cuda.synchronize()
         history.append(tuple(t.cpu().numpy().copy() for t in nxt))
         # the per-request counters at the start of the workspace are back at zero

@@ -61,6 +61,16 @@ _SIGNATURES = {
                                              ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                              ctypes.c_int] + [ctypes.c_void_p] * 7 +
                               [ctypes.c_size_t, ctypes.c_void_p]),
+    "tsv_draft_topk_expand_product": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_void_p,
+                                                     ctypes.c_void_p, ctypes.c_int] +
+                                      [ctypes.c_void_p] * 7 + [ctypes.c_size_t, ctypes.c_void_p]),
+    "tsv_draft_to_target": (ctypes.c_int, [ctypes.c_void_p] * 2 + [ctypes.c_int] * 2 +
+                            [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 2),
+    "tsv_draft_fixed_level": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int64] + [ctypes.c_int] * 5 +
+                              [ctypes.c_void_p] * 3),
     "tsv_draft_select_final": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 +
                                [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 4),
     "tsv_tree_verify_attn_workspace_size": (ctypes.c_size_t, [ctypes.c_void_p] * 2),
@@ -216,8 +226,9 @@ def draft_topk_expand_workspace_size(batch, rows, vocab, top_k) -> int:
 
 def draft_topk_expand(logits, top_k, level, front_score_in, front_store_in, store_token,
                       store_score, store_parent, front_token_out, front_score_out,
-                      front_store_out, workspace):
-    """logits: fp32 [B, rows, V] (last dim may be strided: row stride = logits.stride(1))."""
+                      front_store_out, workspace, product: bool = False):
+    """logits: fp32 [B, rows, V] (last dim may be strided: row stride = logits.stride(1)).
+    product: probability-product scores (tsv_draft_topk_expand_product)."""
     if logits.dtype != torch.float32 or not logits.is_cuda or logits.dim() != 3:
         raise TypeError("logits must be a CUDA fp32 tensor [B, rows, V]")
     b, rows, v = logits.shape
@@ -239,12 +250,43 @@ def draft_topk_expand(logits, top_k, level, front_score_in, front_store_in, stor
         _need(front_score_in, torch.float32, "front_score_in", (b, rows))
         _need(front_store_in, torch.int32, "front_store_in", (b, rows))
     _need(workspace, torch.uint8, "workspace")
-    _check(lib().tsv_draft_topk_expand(
+    fn = lib().tsv_draft_topk_expand_product if product else lib().tsv_draft_topk_expand
+    _check(fn(
         _ptr(logits), b, rows, rs, v, top_k, level,
         _ptr(front_score_in if level > 1 else None), _ptr(front_store_in if level > 1 else None),
         cap, _ptr(store_token), _ptr(store_score), _ptr(store_parent), _ptr(front_token_out),
         _ptr(front_score_out), _ptr(front_store_out), _ptr(workspace), workspace.numel(),
         _stream()), "tsv_draft_topk_expand")
+
+
+def draft_to_target(tokens, num_nodes, d2t, err=None):
+    """tokens [B, max_nodes] int32 in place: nodes 1 .. num_nodes-1 through the d2t table
+    (int32 [draft_vocab])."""
+    b, t = tokens.shape
+    _need(tokens, torch.int32, "tokens")
+    _need(num_nodes, torch.int32, "num_nodes", (b,))
+    _need(d2t, torch.int32, "d2t")
+    if err is not None:
+        _need(err, torch.int32, "err", (b,))
+    _check(lib().tsv_draft_to_target(_ptr(tokens), _ptr(num_nodes), b, t, _ptr(d2t), d2t.numel(),
+                                     _ptr(err), _stream()), "tsv_draft_to_target")
+
+
+def draft_fixed_level(logits, width, first_node, first_parent, tokens, parents):
+    """One fixed-branching level: logits fp32 [B, frontier, V] (rows evenly strided);
+    writes nodes first_node .. first_node + frontier*width - 1 of tokens / parents."""
+    if logits.dtype != torch.float32 or not logits.is_cuda or logits.dim() != 3:
+        raise TypeError("logits must be a CUDA fp32 tensor [B, frontier, V]")
+    b, f, v = logits.shape
+    rs = logits.stride(1) if f > 1 else (logits.stride(0) if b > 1 else v)
+    if (v > 1 and logits.stride(2) != 1) or rs < v or (b > 1 and logits.stride(0) != f * rs):
+        raise ValueError("logits rows must be evenly strided with unit element stride")
+    t = tokens.shape[1]
+    _need(tokens, torch.int32, "tokens", (b, t))
+    _need(parents, torch.int32, "parents", (b, t))
+    _check(lib().tsv_draft_fixed_level(_ptr(logits), b, f, rs, v, width, first_node, first_parent,
+                                       t, _ptr(tokens), _ptr(parents), _stream()),
+           "tsv_draft_fixed_level")
 
 
 def draft_select_final(store_token, store_score, store_parent, num_candidates, total_tokens,

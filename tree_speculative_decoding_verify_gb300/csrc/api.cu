@@ -130,12 +130,12 @@ size_t tsv_draft_topk_expand_workspace_size(int batch, int rows, int vocab, int 
   return plan_topk(batch, rows, vocab, top_k).ws_bytes;
 }
 
-int tsv_draft_topk_expand(const float* logits, int batch, int rows, int64_t row_stride,
-                          int vocab, int top_k, int level, const float* front_score_in,
-                          const int32_t* front_store_in, int store_cap, int32_t* store_token,
-                          float* store_score, int32_t* store_parent, int32_t* front_token_out,
-                          float* front_score_out, int32_t* front_store_out, void* workspace,
-                          size_t workspace_bytes, tsv_stream_t stream) {
+static int topk_expand(const float* logits, int batch, int rows, int64_t row_stride, int vocab,
+                       int top_k, int level, const float* front_score_in,
+                       const int32_t* front_store_in, int store_cap, int32_t* store_token,
+                       float* store_score, int32_t* store_parent, int32_t* front_token_out,
+                       float* front_score_out, int32_t* front_store_out, void* workspace,
+                       size_t workspace_bytes, bool product, cudaStream_t stream) {
   if (batch < 0 || top_k < 1 || top_k > TSV_MAX_TOPK || vocab < top_k || row_stride < vocab ||
       level < 1 || rows < 1 || rows > TSV_MAX_TOPK)
     return TSV_ERR_INVALID_ARG;
@@ -153,7 +153,57 @@ int tsv_draft_topk_expand(const float* logits, int batch, int rows, int64_t row_
   return launch_topk_expand(logits, batch, rows, row_stride, vocab, top_k, level, front_score_in,
                             front_store_in, store_cap, store_token, store_score, store_parent,
                             front_token_out, front_score_out, front_store_out, workspace, plan,
-                            (cudaStream_t)stream);
+                            product, stream);
+}
+
+int tsv_draft_topk_expand(const float* logits, int batch, int rows, int64_t row_stride,
+                          int vocab, int top_k, int level, const float* front_score_in,
+                          const int32_t* front_store_in, int store_cap, int32_t* store_token,
+                          float* store_score, int32_t* store_parent, int32_t* front_token_out,
+                          float* front_score_out, int32_t* front_store_out, void* workspace,
+                          size_t workspace_bytes, tsv_stream_t stream) {
+  return topk_expand(logits, batch, rows, row_stride, vocab, top_k, level, front_score_in,
+                     front_store_in, store_cap, store_token, store_score, store_parent,
+                     front_token_out, front_score_out, front_store_out, workspace,
+                     workspace_bytes, false, (cudaStream_t)stream);
+}
+
+int tsv_draft_topk_expand_product(const float* logits, int batch, int rows, int64_t row_stride,
+                                  int vocab, int top_k, int level, const float* front_score_in,
+                                  const int32_t* front_store_in, int store_cap,
+                                  int32_t* store_token, float* store_score,
+                                  int32_t* store_parent, int32_t* front_token_out,
+                                  float* front_score_out, int32_t* front_store_out,
+                                  void* workspace, size_t workspace_bytes, tsv_stream_t stream) {
+  return topk_expand(logits, batch, rows, row_stride, vocab, top_k, level, front_score_in,
+                     front_store_in, store_cap, store_token, store_score, store_parent,
+                     front_token_out, front_score_out, front_store_out, workspace,
+                     workspace_bytes, true, (cudaStream_t)stream);
+}
+
+int tsv_draft_to_target(int32_t* tokens, const int32_t* num_nodes, int batch, int max_nodes,
+                        const int32_t* d2t, int draft_vocab, int32_t* err, tsv_stream_t stream) {
+  if (batch < 0 || max_nodes < 1 || max_nodes > TSV_MAX_NODES || draft_vocab < 1)
+    return TSV_ERR_INVALID_ARG;
+  if (batch == 0) return TSV_OK;
+  if (!tokens || !num_nodes || !d2t) return TSV_ERR_INVALID_ARG;
+  return launch_draft_to_target(tokens, num_nodes, batch, max_nodes, d2t, draft_vocab, err,
+                                (cudaStream_t)stream);
+}
+
+int tsv_draft_fixed_level(const float* logits, int batch, int frontier, int64_t row_stride,
+                          int vocab, int width, int first_node, int first_parent, int max_nodes,
+                          int32_t* tokens, int32_t* parents, tsv_stream_t stream) {
+  if (batch < 0 || frontier < 1 || width < 1 || width > TSV_MAX_TOPK || vocab < width ||
+      row_stride < vocab || max_nodes < 1 || max_nodes > TSV_MAX_NODES || first_parent < 0 ||
+      first_parent + frontier > first_node ||
+      (int64_t)first_node + (int64_t)frontier * width > max_nodes ||
+      (int64_t)batch * frontier > 65535)
+    return TSV_ERR_INVALID_ARG;
+  if (batch == 0) return TSV_OK;
+  if (!logits || !tokens || !parents) return TSV_ERR_INVALID_ARG;
+  return launch_fixed_level(logits, batch, frontier, row_stride, vocab, width, first_node,
+                            first_parent, max_nodes, tokens, parents, (cudaStream_t)stream);
 }
 
 int tsv_draft_select_final(const int32_t* store_token, const float* store_score,

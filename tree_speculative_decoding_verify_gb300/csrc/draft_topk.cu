@@ -351,6 +351,7 @@ struct LevelArgs {
   const float* logits;
   int64_t row_stride;
   int vocab, rows, k, chunks, chunk_len, level;
+  bool product;  // scores: parent score x child probability, else parent + log-probability
   TopkWs ws;
   const float* front_score_in;
   const int32_t* front_store_in;
@@ -413,7 +414,7 @@ __device__ __noinline__ void request_merge(const LevelArgs& p, int b) {
   __syncthreads();
   if (warp < rows) {
     // warp s merges row s: lane c walks chunk c's sorted list
-    const float pscore = p.level == 1 ? 0.0f : p.front_score_in[r0];
+    const float pscore = p.level == 1 ? (p.product ? 1.0f : 0.0f) : p.front_score_in[r0];
     const int pstore = p.level == 1 ? -1 : p.front_store_in[r0];
     float Rr = cs.x, sh = cs.y, sl = cs.z;
     warp_combine(Rr, sh, sl);
@@ -440,7 +441,7 @@ __device__ __noinline__ void request_merge(const LevelArgs& p, int b) {
     }
     if (lane < k) {
       const float logp = ((v - lse_hi) - lse_mid) - lse_lo;
-      const float cu = pscore + logp;
+      const float cu = p.product ? pscore * expf(logp) : pscore + logp;
       const int flat = s * k + lane;
       p.store_token[srow + off + flat] = i;
       p.store_score[srow + off + flat] = cu;
@@ -834,7 +835,7 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
                        const int32_t* front_store_in, int store_cap, int32_t* store_token,
                        float* store_score, int32_t* store_parent, int32_t* front_token_out,
                        float* front_score_out, int32_t* front_store_out, void* ws,
-                       const TopkPlan& plan, cudaStream_t stream) {
+                       const TopkPlan& plan, bool product, cudaStream_t stream) {
   const int rows_total = batch * rows;
   LevelArgs p;
   p.logits = logits;
@@ -845,6 +846,7 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
   p.chunks = plan.chunks;
   p.chunk_len = plan.chunk_len;
   p.level = level;
+  p.product = product;
   p.ws = carve(ws, batch, rows_total, plan.chunks, top_k);
   p.front_score_in = front_score_in;
   p.front_store_in = front_store_in;

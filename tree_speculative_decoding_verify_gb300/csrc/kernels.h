@@ -68,12 +68,20 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
                        const int32_t* front_store_in, int store_cap, int32_t* store_token,
                        float* store_score, int32_t* store_parent, int32_t* front_token_out,
                        float* front_score_out, int32_t* front_store_out, void* ws,
-                       const TopkPlan& plan, cudaStream_t stream);
+                       const TopkPlan& plan, bool product, cudaStream_t stream);
 int launch_select_final(const int32_t* store_token, const float* store_score,
                         const int32_t* store_parent, int batch, int num_candidates,
                         int store_cap, int total_tokens, const int32_t* root_token,
                         int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
                         cudaStream_t stream);
+
+// Expansion variants.
+int launch_draft_to_target(int32_t* tokens, const int32_t* num_nodes, int batch, int max_nodes,
+                           const int32_t* d2t, int draft_vocab, int32_t* err,
+                           cudaStream_t stream);
+int launch_fixed_level(const float* logits, int batch, int frontier, int64_t row_stride,
+                       int vocab, int width, int first_node, int first_parent, int max_nodes,
+                       int32_t* tokens, int32_t* parents, cudaStream_t stream);
 
 // Tree-verification attention.
 struct AttnPlan {

@@ -31,6 +31,7 @@ class TreeShape:
     fixed_nodes: int = 0      # > 0: trees are given directly (no expansion)
     fixed_max_depth: int = 0
     target_vocab: int = 0     # > 0: the target's lm_head runs in the step (its vocabulary)
+    score_product: bool = False  # expansion scores as probability products, not log sums
 
     @property
     def max_nodes(self) -> int:
@@ -111,11 +112,36 @@ class HotPath:
                                    None if cur is None else cur[1],
                                    None if cur is None else cur[2],
                                    self.store_token, self.store_score, self.store_parent,
-                                   nxt[0], nxt[1], nxt[2], self.topk_ws)
+                                   nxt[0], nxt[1], nxt[2], self.topk_ws,
+                                   product=s.score_product)
             cur = nxt
         _lib.draft_select_final(self.store_token, self.store_score, self.store_parent,
                                 s.num_candidates, s.total_tokens, root_token, self.tokens,
                                 self.parents, self.num_nodes)
+
+    def expand_fixed(self, level_logits: Sequence[torch.Tensor], root_token: torch.Tensor,
+                     branching: Sequence[int]):
+        """A fixed-branching tree instead of the dynamic expansion: level_logits[l] is
+        [B, F_l, V] fp32 (F_l frontier nodes, the product of the earlier widths); the
+        tree has 1 + sum over levels of F_l * branching[l] nodes (fixed_nodes)."""
+        s = self.s
+        n = 1
+        frontier, first_parent = 1, 0
+        self.tokens[:, 0].copy_(root_token)
+        self.parents[:, 0] = -1
+        for width, lg in zip(branching, level_logits):
+            _lib.draft_fixed_level(lg, width, n, first_parent, self.tokens, self.parents)
+            first_parent = n
+            n += frontier * width
+            frontier *= width
+        if n != s.max_nodes:
+            raise ValueError(f"branching {list(branching)} gives {n} nodes, max_nodes is "
+                             f"{s.max_nodes}")
+        self.num_nodes.fill_(n)
+
+    def map_to_target(self, d2t: torch.Tensor, err: Optional[torch.Tensor] = None):
+        """Draft-vocabulary ids of the tree's nodes (all but the root) to target ids."""
+        _lib.draft_to_target(self.tokens, self.num_nodes, d2t, err)
 
     def set_tree(self, tokens: torch.Tensor, parents: torch.Tensor, num_nodes: torch.Tensor):
         """Use given trees instead of the expansion (fixed-shape drafts)."""
