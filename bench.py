@@ -97,6 +97,7 @@ TRAFFIC = {
     ("topk", "llama8b"): (1354240 + 0, "profiles/topk_level_kernel_llama8b.md"),
     ("topk", "sweep"): (328446464 + 2847488, "profiles/topk_level_kernel_sweep.md"),
     ("lm_head", "llama8b"): (1052517376 + 3688704, "profiles/lm_head_argmax_kernel_llama8b.md"),
+    ("sample", "llama8b"): (31397120 + 0, "profiles/filter_stats_kernel_llama8b.md"),
 }
 
 
@@ -291,6 +292,23 @@ def native(args):
     sa_ws = torch.empty(T.tree_sample_accept_workspace_size(b, t_max), dtype=torch.uint8,
                         device=dev)
 
+    # expansion variants: one level with probability-product scores, the d2t id map over
+    # the tree, one fixed-branching level (every frontier row of the level's logits,
+    # width 2)
+    d2t = torch.from_numpy(np.random.default_rng(5).permutation(lm_v)[:v].astype(np.int32)).to(dev)
+    fx_tok = torch.zeros(b, 1 + k * 2 + k, dtype=torch.int32, device=dev)
+    fx_par = torch.zeros_like(fx_tok)
+    map_tok = hp.tokens.clone()
+
+    def topk_product():
+        T.draft_topk_expand(levels[1], k, 2, hp.front[0][1], hp.front[0][2], hp.store_token,
+                            hp.store_score, hp.store_parent, *lvl_out, lvl_ws, product=True)
+
+    def variants():
+        map_tok.copy_(hp.tokens)
+        T.draft_to_target(map_tok, hp.num_nodes, d2t)
+        T.draft_fixed_level(levels[1], 2, 1 + k, 1, fx_tok, fx_par)
+
     def sample_accept():
         T.tree_sample_accept(sa_logits, *sa_prm, sa_u, sa_uf, hp.tokens, hp.next_token,
                              hp.next_sibling, hp.num_nodes, prefix_t, shape.max_depth, cache,
@@ -305,10 +323,11 @@ def native(args):
     graphs = {}
     with torch.cuda.stream(stream):
         for _ in range(2):  # warm the allocator and the kernels before capture
-            step(); attn(); topk_level(); lm_head(); sample_accept()
+            step(); attn(); topk_level(); lm_head(); sample_accept(); topk_product(); variants()
         stream.synchronize()
         for name, fn in (("step", step), ("attn", attn), ("topk", topk_level),
-                         ("lm_head", lm_head), ("sample", sample_accept)):
+                         ("lm_head", lm_head), ("sample", sample_accept),
+                         ("topk_product", topk_product), ("variants", variants)):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 fn()
@@ -320,7 +339,8 @@ def native(args):
                      for _ in range(n)] for name in graphs}
         with torch.cuda.stream(stream):
             for i in range(n):
-                for name in ("step", "attn", "topk", "lm_head", "sample"):
+                for name in ("step", "attn", "topk", "lm_head", "sample", "topk_product",
+                             "variants"):
                     flush_buf.zero_()
                     ev[name][i][0].record(stream)
                     graphs[name].replay()
@@ -503,14 +523,17 @@ def native(args):
         "roofline_topk": topk_roof,
         "lm_head_us": ms["lm_head"] * 1e3,
         "roofline_lm_head": lm_roof,
+        "topk_product_us": ms["topk_product"] * 1e3,
+        "topk_product_hbm_frac": topk_bytes / (ms["topk_product"] / 1e3) / 1e9 / hbm,
+        "d2t_map_plus_fixed_level_us": ms["variants"] * 1e3,
         "sample_accept_us": ms["sample"] * 1e3,
         "roofline_sample_accept": sa_roof,
         "e2e": {"value": world * 1e3 / e2e_step_ms, "unit": UNIT, "ms_per_step": e2e_step_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         # timed region per iteration: the step graph, the attention call, one top-k level,
         # the lm-head argmax (GEMM + finalize), the non-greedy acceptance (filter, walk,
-        # compaction)
-        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1 + 2 + 3),
+        # compaction), a product-score level, the d2t map and a fixed level
+        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1 + 2 + 3 + 1 + 2),
         "wall_s_timed_region": t_wall,
     }
     ck = clocks.summary()
