@@ -139,3 +139,23 @@ def kary_parents(n: int, k: int) -> list:
     """Regular k-ary tree of n nodes: parent(i) = (i - 1) // k ([TRT] section
     dummy 槽为什么要造一棵 K 叉树; k = 1 gives the default linear chain)."""
     return [-1] + [(i - 1) // k for i in range(1, n)]
+
+
+def grow_level_mask(prev_mask, prev_pos, new_parents):
+    """The drafter's mask and positions after one more draft level, built as the block
+    matrix of [TRT] section 首步变长、后续定长 (_build_mask_and_position): the old nodes keep
+    their rows and see none of the new nodes (the upper-right block is zero); a new node's
+    row is its parent's row (gathered from the old mask) followed by tree_mask_init, the
+    new nodes' visibility among themselves (each sees itself only). A new node's position
+    is its parent's plus one.
+
+    prev_mask [N, N] bool, prev_pos [N], new_parents [K] (indices of old nodes).
+    Returns ([N + K, N + K] bool, [N + K] positions)."""
+    prev_mask = np.asarray(prev_mask, dtype=bool)
+    n, k = prev_mask.shape[0], len(new_parents)
+    parent_rows = prev_mask[np.asarray(new_parents, dtype=np.int64)]     # [K, N]
+    top = np.concatenate([prev_mask, np.zeros((n, k), dtype=bool)], axis=1)
+    bottom = np.concatenate([parent_rows, np.eye(k, dtype=bool)], axis=1)
+    pos = np.concatenate([np.asarray(prev_pos, dtype=np.int64),
+                          np.asarray(prev_pos, dtype=np.int64)[list(new_parents)] + 1])
+    return np.concatenate([top, bottom], axis=0), pos

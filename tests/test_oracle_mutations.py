@@ -217,3 +217,13 @@ def test_expansion_variant_mistakes_are_caught(monkeypatch, fn, old, new, pin):
     monkeypatch.setattr(draft, fn, _mutant(draft, fn, old, new))
     with pytest.raises(AssertionError):
         getattr(td, pin)()
+
+
+def test_grown_mask_without_the_parent_rows_is_caught(monkeypatch):
+    from oracle import tree as Tr
+    from tests import test_oracle_tree as tt2
+    monkeypatch.setattr(Tr, "grow_level_mask", _mutant(
+        Tr, "grow_level_mask", "bottom = np.concatenate([parent_rows, np.eye(k, dtype=bool)], axis=1)",
+        "bottom = np.concatenate([np.zeros_like(parent_rows), np.eye(k, dtype=bool)], axis=1)"))
+    with pytest.raises(AssertionError):
+        tt2.test_grown_level_masks_equal_the_ancestor_mask()

@@ -108,3 +108,24 @@ def test_root_only_tree():
 def test_invalid_parents_rejected(bad):
     with pytest.raises(ValueError):
         tree.validate_parents(bad)
+
+
+def test_grown_level_masks_equal_the_ancestor_mask():
+    """Growing the drafter's mask level by level (the block construction) gives the
+    ancestor mask and positions of the whole tree at every level; old rows never see new
+    nodes."""
+    from oracle import tree as Tr
+    rng = np.random.default_rng(2)
+    k, levels, prefix = 4, 5, 37
+    parents = [-1]
+    mask, pos = np.ones((1, 1), dtype=bool), np.array([prefix])
+    frontier = [0]
+    for _ in range(levels):
+        new_par = [frontier[int(rng.integers(0, len(frontier)))] for _ in range(k)]
+        n0 = len(parents)
+        mask, pos = Tr.grow_level_mask(mask, pos, new_par)
+        parents += new_par
+        assert (mask == Tr.tree_mask(parents)).all()
+        assert pos.tolist() == Tr.position_ids(parents, prefix).tolist()
+        assert not mask[:n0, n0:].any()
+        frontier = list(range(n0, n0 + k))
