@@ -9,6 +9,7 @@
  *                           expansion variants: probability-product scores, the d2t id
  *                           map, fixed-branching trees
  *   tsv_tree_build_meta     ancestor bitmask, positions, retrieve_indices, child/sibling links
+ *   tsv_draft_grow_mask     the drafter's mask and positions grown by one level
  *   tsv_tree_verify_attn    RoPE + KV append + tree-masked split-KV attention of every node
  *   tsv_lm_head_argmax      the target's greedy token at every node (lm_head GEMM with an
  *                           argmax epilogue; the logits are never written)
@@ -276,6 +277,30 @@ int tsv_tree_build_meta(const int32_t* parents, const int32_t* num_nodes,
                         uint32_t* mask, int32_t* position_ids, int32_t* retrieve_indices,
                         int32_t* num_leaves, int32_t* next_token, int32_t* next_sibling,
                         int32_t* err, tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_draft_grow_mask — the drafter's ancestor mask, grown by one level.
+ *
+ * [TRT] section 首步变长、后续定长 (_build_mask_and_position): per draft level the mask is
+ * the block matrix [[old mask, 0], [the new nodes' parents' rows, tree_mask_init]] (old
+ * nodes see no new node; a new node sees its parent's ancestors, its parent and itself),
+ * and a new node's position is its parent's plus one. The attention of the drafter's
+ * nodes is then tsv_tree_verify_attn with this mask and these positions.
+ * mask          [batch, max_nodes, ceil(max_nodes/32)] uint32 in/out, the layout of
+ *               tsv_tree_build_meta. Rows first_new .. first_new+count-1 are written;
+ *               rows below first_new are read (their parents' rows) and not changed.
+ *               With first_new == 1 the root's row (bit 0) is written first.
+ * position_ids  [batch, max_nodes] in/out: new nodes get their parent's position + 1
+ *               (with first_new == 1 the root gets prefix_len[b]).
+ * new_parents   [batch, count] in: node index of each new node's parent, in
+ *               [0, first_new).
+ * prefix_len    [batch] in (read when first_new == 1).
+ * err           [batch] out (may be NULL): TSV_REQ_BAD_PARENT where a parent was out of
+ *               range (that node's row holds only its own bit, its position is -1).
+ * ------------------------------------------------------------------------------ */
+int tsv_draft_grow_mask(uint32_t* mask, int32_t* position_ids, const int32_t* new_parents,
+                        const int32_t* prefix_len, int batch, int first_new, int count,
+                        int max_nodes, int32_t* err, tsv_stream_t stream);
 
 /* --------------------------------------------------------------------------------
  * tsv_tree_verify_attn — tree verification attention of one layer.

@@ -6,7 +6,7 @@ hot-path step over preallocated device buffers.
 """
 from ._lib import (  # noqa: F401
     KV_BLOCK, MAX_NODES, MAX_TOPK, REQ_CODES, KVCache, TsvError, accept_and_compact,
-    draft_fixed_level, draft_select_final, draft_to_target, draft_topk_expand,
+    draft_fixed_level, draft_grow_mask, draft_select_final, draft_to_target, draft_topk_expand,
     draft_topk_expand_workspace_size, exported_symbols,
     lib, lm_head_argmax, lm_head_argmax_workspace_size, target_probs, tree_build_meta,
     tree_sample_accept, tree_sample_accept_workspace_size, tree_verify_attn,

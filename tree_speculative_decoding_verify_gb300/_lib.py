@@ -55,6 +55,8 @@ _SIGNATURES = {
     "tsv_last_cuda_error": (ctypes.c_int, []),
     "tsv_tree_build_meta": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3 +
                             [ctypes.c_void_p] * 7 + [ctypes.c_void_p]),
+    "tsv_draft_grow_mask": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
+                            [ctypes.c_void_p] * 2),
     "tsv_draft_topk_expand_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 4),
     "tsv_draft_topk_expand": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int64, ctypes.c_int, ctypes.c_int,
@@ -218,6 +220,23 @@ def tree_build_meta(parents, num_nodes, prefix_len, max_depth, mask, position_id
                                      _ptr(retrieve_indices), _ptr(num_leaves), _ptr(next_token),
                                      _ptr(next_sibling), _ptr(err), _stream()),
            "tsv_tree_build_meta")
+
+
+def draft_grow_mask(mask, position_ids, new_parents, prefix_len, first_new, err=None):
+    """Grow the drafter's mask [B, T, W] (int32 view of the uint32 words) and positions
+    [B, T] by one level: new_parents [B, K] int32 (parents of nodes first_new ..
+    first_new + K - 1)."""
+    b, t = position_ids.shape
+    k = new_parents.shape[1]
+    _need(mask, torch.int32, "mask", (b, t, (t + 31) // 32))
+    _need(position_ids, torch.int32, "position_ids", (b, t))
+    _need(new_parents, torch.int32, "new_parents", (b, k))
+    _need(prefix_len, torch.int32, "prefix_len", (b,))
+    if err is not None:
+        _need(err, torch.int32, "err", (b,))
+    _check(lib().tsv_draft_grow_mask(_ptr(mask), _ptr(position_ids), _ptr(new_parents),
+                                     _ptr(prefix_len), b, first_new, k, t, _ptr(err), _stream()),
+           "tsv_draft_grow_mask")
 
 
 def draft_topk_expand_workspace_size(batch, rows, vocab, top_k) -> int:

@@ -125,6 +125,18 @@ int tsv_tree_build_meta(const int32_t* parents, const int32_t* num_nodes,
                            err, (cudaStream_t)stream);
 }
 
+int tsv_draft_grow_mask(uint32_t* mask, int32_t* position_ids, const int32_t* new_parents,
+                        const int32_t* prefix_len, int batch, int first_new, int count,
+                        int max_nodes, int32_t* err, tsv_stream_t stream) {
+  if (batch < 0 || max_nodes < 2 || max_nodes > TSV_MAX_NODES || first_new < 1 || count < 1 ||
+      (int64_t)first_new + count > max_nodes)
+    return TSV_ERR_INVALID_ARG;
+  if (batch == 0) return TSV_OK;
+  if (!mask || !position_ids || !new_parents || !prefix_len) return TSV_ERR_INVALID_ARG;
+  return launch_grow_mask(mask, position_ids, new_parents, prefix_len, batch, first_new, count,
+                          max_nodes, err, (cudaStream_t)stream);
+}
+
 size_t tsv_draft_topk_expand_workspace_size(int batch, int rows, int vocab, int top_k) {
   if (batch < 1 || rows < 1 || vocab < 1 || top_k < 1 || top_k > TSV_MAX_TOPK) return 0;
   return plan_topk(batch, rows, vocab, top_k).ws_bytes;

@@ -15,6 +15,10 @@ int launch_build_meta(const int32_t* parents, const int32_t* num_nodes, const in
                       int32_t* next_token, int32_t* next_sibling, int32_t* err,
                       cudaStream_t stream);
 
+int launch_grow_mask(uint32_t* mask, int32_t* position_ids, const int32_t* new_parents,
+                     const int32_t* prefix_len, int batch, int first_new, int count,
+                     int max_nodes, int32_t* err, cudaStream_t stream);
+
 int launch_accept_compact(const int32_t* tokens, const int32_t* next_token,
                           const int32_t* next_sibling, const int32_t* target,
                           const int32_t* num_nodes, const int32_t* prefix_len,

@@ -168,6 +168,45 @@ build_meta_kernel(const int32_t* __restrict__ parents, const int32_t* __restrict
   }
 }
 
+constexpr int GT = 128;
+
+__global__ void __launch_bounds__(GT)
+grow_mask_kernel(uint32_t* __restrict__ mask, int32_t* __restrict__ position_ids,
+                 const int32_t* __restrict__ new_parents, const int32_t* __restrict__ prefix_len,
+                 int first_new, int count, int max_nodes, int32_t* __restrict__ err) {
+  __shared__ int s_bad;
+  griddep_wait();
+  griddep_launch();
+  const int b = blockIdx.x;
+  const int W = (max_nodes + 31) / 32;
+  uint32_t* m = mask + (int64_t)b * max_nodes * W;
+  int32_t* pos = position_ids + (int64_t)b * max_nodes;
+  if (threadIdx.x == 0) {
+    s_bad = 0;
+    if (first_new == 1) {  // the first level also writes the root's row
+      for (int w = 0; w < W; ++w) m[w] = w == 0 ? 1u : 0u;
+      pos[0] = prefix_len[b];
+    }
+  }
+  __syncthreads();
+  // new node n = first_new + j: words of its parent's row (bits of old nodes only) and
+  // its own bit
+  for (int e = threadIdx.x; e < count * W; e += GT) {
+    const int j = e / W, w = e % W, n = first_new + j;
+    const int p = new_parents[(int64_t)b * count + j];
+    const bool ok = p >= 0 && p < first_new;
+    uint32_t word = ok && w * 32 < first_new ? m[(int64_t)p * W + w] : 0u;
+    if (w == (n >> 5)) word |= 1u << (n & 31);
+    m[(int64_t)n * W + w] = word;
+    if (w == 0) {
+      pos[n] = ok ? pos[p] + 1 : -1;
+      if (!ok) s_bad = 1;
+    }
+  }
+  __syncthreads();
+  if (err && threadIdx.x == 0) err[b] = s_bad ? TSV_REQ_BAD_PARENT : TSV_REQ_OK;
+}
+
 }  // namespace
 
 int launch_build_meta(const int32_t* parents, const int32_t* num_nodes, const int32_t* prefix_len,
@@ -179,6 +218,13 @@ int launch_build_meta(const int32_t* parents, const int32_t* num_nodes, const in
   return launch_pdl(build_meta_kernel, grid, dim3(WARPS * 32), 0, stream, parents, num_nodes,
                     prefix_len, batch, max_nodes, max_depth, mask, position_ids, retrieve,
                     num_leaves, next_token, next_sibling, err);
+}
+
+int launch_grow_mask(uint32_t* mask, int32_t* position_ids, const int32_t* new_parents,
+                     const int32_t* prefix_len, int batch, int first_new, int count,
+                     int max_nodes, int32_t* err, cudaStream_t stream) {
+  return launch_pdl(grow_mask_kernel, dim3(batch), dim3(GT), 0, stream, mask, position_ids,
+                    new_parents, prefix_len, first_new, count, max_nodes, err);
 }
 
 }  // namespace tsv
