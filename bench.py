@@ -309,6 +309,37 @@ def native(args):
         T.draft_to_target(map_tok, hp.num_nodes, d2t)
         T.draft_fixed_level(levels[1], 2, 1 + k, 1, fx_tok, fx_par)
 
+    # drafter-side tree attention: the drafter's mask grown to its last level (1 + K
+    # (depth + 1) nodes, each level's parents in the level before), then the tree
+    # attention of all its nodes over it (the drafter's layer has the target's head shape)
+    dn = 1 + k * (w.depth + 1)
+    dmask = torch.zeros(b, dn, (dn + 31) // 32, dtype=torch.int32, device=dev)
+    dpos = torch.zeros(b, dn, dtype=torch.int32, device=dev)
+    dparents = [-1]
+    n0, last = 1, None
+    for lvl in range(w.depth + 1):
+        front = [0] if lvl == 0 else list(range(n0 - k, n0))
+        par = [front[j % len(front)] for j in range(k)]
+        dparents += par
+        last = (n0, torch.tensor([par] * b, dtype=torch.int32, device=dev))
+        T.draft_grow_mask(dmask, dpos, last[1], prefix_t, n0)
+        n0 += k
+    d_depth = [0]
+    for pp in dparents[1:]:
+        d_depth.append(d_depth[pp] + 1)
+    dq = (torch.randn(b, dn, w.num_q_heads, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
+    dk = (torch.randn(b, dn, w.num_kv_heads, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
+    dv = (torch.randn(b, dn, w.num_kv_heads, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
+    dnn = torch.full((b,), dn, dtype=torch.int32, device=dev)
+    dout = torch.zeros(b, dn, w.num_q_heads, w.head_dim, dtype=torch.bfloat16, device=dev)
+    dws = torch.empty(T.tree_verify_attn_workspace_size((b, dn, w.num_q_heads, w.head_dim), cache,
+                                                        p_max), dtype=torch.uint8, device=dev)
+
+    def drafter_level():
+        T.draft_grow_mask(dmask, dpos, last[1], prefix_t, last[0])
+        T.tree_verify_attn(dq, dk, dv, cache, prefix_t, dnn, dpos, dmask, w.theta, sm_scale,
+                           dout, dws, p_max)
+
     def sample_accept():
         T.tree_sample_accept(sa_logits, *sa_prm, sa_u, sa_uf, hp.tokens, hp.next_token,
                              hp.next_sibling, hp.num_nodes, prefix_t, shape.max_depth, cache,
@@ -324,10 +355,12 @@ def native(args):
     with torch.cuda.stream(stream):
         for _ in range(2):  # warm the allocator and the kernels before capture
             step(); attn(); topk_level(); lm_head(); sample_accept(); topk_product(); variants()
+            drafter_level()
         stream.synchronize()
         for name, fn in (("step", step), ("attn", attn), ("topk", topk_level),
                          ("lm_head", lm_head), ("sample", sample_accept),
-                         ("topk_product", topk_product), ("variants", variants)):
+                         ("topk_product", topk_product), ("variants", variants),
+                         ("drafter", drafter_level)):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 fn()
@@ -340,7 +373,7 @@ def native(args):
         with torch.cuda.stream(stream):
             for i in range(n):
                 for name in ("step", "attn", "topk", "lm_head", "sample", "topk_product",
-                             "variants"):
+                             "variants", "drafter"):
                     flush_buf.zero_()
                     ev[name][i][0].record(stream)
                     graphs[name].replay()
@@ -526,14 +559,20 @@ def native(args):
         "topk_product_us": ms["topk_product"] * 1e3,
         "topk_product_hbm_frac": topk_bytes / (ms["topk_product"] / 1e3) / 1e9 / hbm,
         "d2t_map_plus_fixed_level_us": ms["variants"] * 1e3,
+        "drafter_level_us": ms["drafter"] * 1e3,
+        "drafter_nodes": dn,
+        "drafter_attn_hbm_frac": algorithmic(w, prefix, [d_depth] * b)[0] / (ms["drafter"] / 1e3) / 1e9 / hbm,
         "sample_accept_us": ms["sample"] * 1e3,
         "roofline_sample_accept": sa_roof,
         "e2e": {"value": world * 1e3 / e2e_step_ms, "unit": UNIT, "ms_per_step": e2e_step_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         # timed region per iteration: the step graph, the attention call, one top-k level,
         # the lm-head argmax (GEMM + finalize), the non-greedy acceptance (filter, walk,
-        # compaction), a product-score level, the d2t map and a fixed level
-        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1 + 2 + 3 + 1 + 2),
+        # compaction), a product-score level, the d2t map and a fixed level, the drafter's
+        # grown mask and its attention
+        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1 + 2 + 3 + 1 + 2 + 1 +
+                                      T.tree_verify_attn_launches(
+                                          (b, dn, w.num_q_heads, w.head_dim), cache, p_max)),
         "wall_s_timed_region": t_wall,
     }
     ck = clocks.summary()
