@@ -62,6 +62,20 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(values, world: int):
+    """The element-wise maximum of `values` over all ranks (every rank gets it): the
+    replicas agree on a step count and report the slowest rank's times. A plain list at
+    world size 1; a CUDA tensor for NCCL, a CPU one for gloo."""
+    if world <= 1:
+        return [float(x) for x in values]
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def workload(args):
     w = W.WORKLOADS[args.workload]
     if args.total_tokens:
@@ -389,10 +403,8 @@ def native(args):
         torch.cuda.synchronize()
         per = (time.perf_counter() - t) / 5
         args.steps = int(max(50, min(20000, 2.0 / max(per, 1e-6))))
-        if world > 1:  # every rank times the same number of steps
-            n = torch.tensor([args.steps], device=dev)
-            dist.all_reduce(n, op=dist.ReduceOp.MAX)
-            args.steps = int(n.item())
+        # every rank times the same number of steps
+        args.steps = int(max_over_ranks([args.steps], world)[0])
     if world > 1:
         dist.barrier()
     clocks = Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
@@ -472,11 +484,7 @@ def native(args):
     print("bench: end-to-end leg done", file=sys.stderr, flush=True)
 
     # ---- max over ranks ---------------------------------------------------------------
-    step_ms = ms["step"]
-    if world > 1:
-        t = torch.tensor([step_ms, e2e_step_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_step_ms = t.tolist()
+    step_ms, e2e_step_ms = max_over_ranks([ms["step"], e2e_step_ms], world)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
