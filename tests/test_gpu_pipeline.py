@@ -139,3 +139,58 @@ def test_step_with_the_lm_head_stage():
     assert hp.accept_path.cpu().numpy()[0, :n].tolist() == list(path)
     assert hp.bonus.item() == bonus
     assert hp.kernels_per_step(lm_head=True) == hp.kernels_per_step() + 2
+
+
+def test_step_with_non_greedy_acceptance():
+    """The step with the non-greedy acceptance: at temperature 0 it is the greedy step
+    (the same path, bonus and compacted cache) for any uniforms; at temperature 1 its path
+    and token match the oracle's rejection walk on the step's tree."""
+    import math
+
+    import tree_speculative_decoding_verify_gb300 as T
+    from oracle import sampling
+
+    w = W.WORKLOADS["llama8b"].with_(vocab=2048, top_k=4, depth=2, total_tokens=8,
+                                     prefix=("fixed", 200), num_q_heads=8, num_kv_heads=2)
+    d = gc.dev()
+    tokens, parents, _ = gc.oracle_tree(w, 0)
+    t_max = w.num_nodes
+    logits = W.target_logits(w, 0, tokens, parents, w.vocab, t_max)
+    u = W.uniforms(w, 0, t_max)
+    q, k_new, v_new = W.new_qkv(w)
+    bf = lambda x: gc.to_dev(x, torch.bfloat16)
+    levels = [torch.from_numpy(x[None]).to(d) for x in gc.level_logits(w, 0)]
+    results = {}
+    for mode in ("greedy", "t0", "t1"):
+        kc = torch.zeros(1, 2, 256, 128, dtype=torch.bfloat16, device=d)
+        kc[0, :, :200] = 1.0
+        vc = kc.clone()
+        shape = T.TreeShape(1, 8, 2, 128, 200, vocab=w.vocab, top_k=w.top_k, depth=w.depth,
+                            total_tokens=w.total_tokens)
+        hp = T.HotPath(shape, T.KVCache(kc, vc))
+        args = (levels, gc.i32(W.root_tokens(w)[:1]), bf(q), bf(k_new), bf(v_new), gc.i32([200]))
+        if mode == "greedy":
+            target = np.argmax(logits, axis=1).astype(np.int32)
+            hp.step(*args, gc.i32([target]), w.theta, 1 / math.sqrt(128))
+        else:
+            temp = 0.0 if mode == "t0" else 1.0
+            smp = dict(target_logits=torch.from_numpy(logits[None]).to(d),
+                       temperature=torch.tensor([temp], device=d),
+                       top_k=torch.zeros(1, dtype=torch.int32, device=d),
+                       top_p=torch.ones(1, device=d), min_p=torch.zeros(1, device=d),
+                       u_node=torch.from_numpy(u[None, :t_max].copy()).to(d),
+                       u_final=torch.from_numpy(u[t_max:].copy()).to(d))
+            hp.step(*args, None, w.theta, 1 / math.sqrt(128), sampling=smp)
+        torch.cuda.synchronize()
+        n = hp.accept_len.item()
+        results[mode] = (hp.accept_path.cpu().numpy()[0, :n].tolist(), hp.bonus.item(),
+                         kc.cpu().clone())
+    assert results["t0"][0] == results["greedy"][0] and results["t0"][1] == results["greedy"][1]
+    assert torch.equal(results["t0"][2], results["greedy"][2])
+    probs = [sampling.filter_probs(logits[i], 1.0) for i in range(len(tokens))]
+    trace = []
+    path, tok = sampling.rejection_walk(list(tokens), list(parents), probs, u[:t_max],
+                                        float(u[t_max]), trace=trace)
+    margin = min([abs(x - a) for kind, x, a in trace if kind == "test"], default=1.0)
+    if margin > 1e-5:
+        assert results["t1"][0] == path

@@ -88,6 +88,8 @@ class HotPath:
         self.bonus = torch.zeros(b, **i32)
         self.slot_map = torch.zeros(b, shape.max_depth + 1, 2, **i32)
         self.new_prefix_len = torch.zeros(b, **i32)
+        self.sample_ws = torch.empty(max(_lib.tree_sample_accept_workspace_size(b, t), 256),
+                                     dtype=torch.uint8, device=dev)
         if shape.target_vocab:
             self.target = torch.zeros(b, t, **i32)
             ws = _lib.lm_head_argmax_workspace_size(b * t, shape.target_vocab)
@@ -181,22 +183,43 @@ class HotPath:
                                 self.accept_len, self.bonus, self.slot_map, self.new_prefix_len,
                                 self.acc_err, tree_valid)
 
+    def sample_accept(self, target_logits, temperature, top_k, top_p, min_p, u_node, u_final,
+                      prefix_len, draft_probs=None, tree_valid=None, compact: bool = True):
+        """Non-greedy acceptance of the current trees (tsv_tree_sample_accept): target
+        logits [B, max_nodes, V] fp32, per-request sampling parameters [B], uniforms
+        u_node [B, max_nodes] and u_final [B]; draft_probs [B, max_nodes, V] for the
+        draft-aware rule (None: target-only). Writes the same outputs as accept()."""
+        _lib.tree_sample_accept(target_logits, temperature, top_k, top_p, min_p, u_node, u_final,
+                                self.tokens, self.next_token, self.next_sibling, self.num_nodes,
+                                prefix_len, self.s.max_depth, self.cache if compact else None,
+                                self.accept_path, self.accept_len, self.bonus, self.slot_map,
+                                self.new_prefix_len, self.sample_ws, err=self.acc_err,
+                                tree_valid=tree_valid, draft_probs=draft_probs)
+
     def step(self, level_logits, root_token, q, k_new, v_new, prefix_len, target_argmax,
              rope_theta: float, softmax_scale: float,
              level_ready: Optional[Sequence[torch.cuda.Event]] = None,
              inputs_ready: Optional[torch.cuda.Event] = None,
-             hidden: Optional[torch.Tensor] = None, lm_weight: Optional[torch.Tensor] = None):
+             hidden: Optional[torch.Tensor] = None, lm_weight: Optional[torch.Tensor] = None,
+             sampling: Optional[dict] = None):
         """One hot-path step. level_ready (see expand) and inputs_ready (q, k_new, v_new,
         prefix_len and target_argmax or hidden in place before the tree metadata) let the
         inputs arrive on another stream while the expansion runs. With hidden and
         lm_weight (and target_argmax None) the target's greedy tokens come from the
-        lm_head stage (greedy_targets) instead of being given."""
+        lm_head stage (greedy_targets) instead of being given. With `sampling` (the keyword
+        arguments of sample_accept but prefix_len; target_argmax None) the acceptance is
+        the non-greedy one."""
         if not self.s.fixed_nodes:
             self.expand(level_logits, root_token, level_ready)
         if inputs_ready is not None:
             torch.cuda.current_stream().wait_event(inputs_ready)
         self.build_meta(prefix_len)
         self.verify(q, k_new, v_new, prefix_len, rope_theta, softmax_scale)
+        if sampling is not None:
+            if target_argmax is not None or hidden is not None:
+                raise ValueError("sampling replaces target_argmax / hidden")
+            self.sample_accept(prefix_len=prefix_len, **sampling)
+            return
         if hidden is not None:
             if target_argmax is not None:
                 raise ValueError("give target_argmax or hidden + lm_weight, not both")
