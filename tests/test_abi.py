@@ -92,7 +92,40 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert ws > 0 and ws % 256 == 0 and ws >= 61 * 8
 
 
+def test_host_validation_of_the_wider_calls(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: the checks fail first
+    a256 = ctypes.c_void_p(4096)
+    # non-greedy acceptance: vocab out of range, max_nodes out of range, small workspace
+    args = lambda vocab, t, ws_bytes: ([p, None, vocab] + [p] * 12 + [1, t, 7, None] +
+                                       [p] * 5 + [None, a256, ws_bytes, None])
+    assert lib.tsv_tree_sample_accept(*args(0, 61, 1 << 20)) == 1
+    assert lib.tsv_tree_sample_accept(*args((1 << 20) + 1, 61, 1 << 20)) == 1
+    assert lib.tsv_tree_sample_accept(*args(1000, 257, 1 << 20)) == 1
+    assert lib.tsv_tree_sample_accept(*args(1000, 61, 8)) == 3
+    assert lib.tsv_tree_sample_accept_workspace_size(2, 61) >= 2 * 61 * 24
+    assert lib.tsv_tree_sample_accept_workspace_size(2, 0) == 0
+    assert lib.tsv_target_probs(p, 1000, p, p, p, p, p, 1, 61, p, a256, 8, None) == 3
+    # fixed level: width above the limit, nodes past max_nodes, frontier overlapping
+    assert lib.tsv_draft_fixed_level(p, 1, 2, 100, 100, 17, 3, 1, 64, p, p, None) == 1
+    assert lib.tsv_draft_fixed_level(p, 1, 2, 100, 100, 4, 3, 1, 10, p, p, None) == 1
+    assert lib.tsv_draft_fixed_level(p, 1, 3, 100, 100, 2, 3, 1, 64, p, p, None) == 1
+    assert lib.tsv_draft_fixed_level(p, 1, 2, 50, 100, 2, 3, 1, 64, p, p, None) == 1
+    # grown mask: new nodes past max_nodes, first_new 0
+    assert lib.tsv_draft_grow_mask(p, p, p, p, 1, 60, 8, 64, None, None) == 1
+    assert lib.tsv_draft_grow_mask(p, p, p, p, 1, 0, 4, 64, None, None) == 1
+    # d2t: empty table
+    assert lib.tsv_draft_to_target(p, p, 1, 61, p, 0, None, None) == 1
+    # product expansion: the same checks as the log-score one
+    assert lib.tsv_draft_topk_expand_product(p, 1, 1, 100, 100, 17, 1, None, None, 100,
+                                             p, p, p, p, p, p, p, 1 << 20, None) == 1
+
+
 def test_empty_batch_is_a_no_op(lib):
+    assert lib.tsv_tree_sample_accept(*([None] * 2 + [1000] + [None] * 12 + [0, 61, 7, None] +
+                                        [None] * 6 + [None, 0, None])) == 0
+    assert lib.tsv_draft_fixed_level(None, 0, 2, 100, 100, 2, 3, 1, 64, None, None, None) == 0
+    assert lib.tsv_draft_grow_mask(None, None, None, None, 0, 1, 4, 64, None, None) == 0
+    assert lib.tsv_draft_to_target(None, None, 0, 61, None, 10, None, None) == 0
     assert lib.tsv_lm_head_argmax(None, None, 0, 64, 10, None, None, None, 0, None) == 0
     assert lib.tsv_tree_build_meta(None, None, None, 0, 8, 3, None, None, None, None, None,
                                    None, None, None) == 0
