@@ -499,7 +499,7 @@ def native(args):
         achieved, peak, unit = nbytes / attn_s / 1e9, hbm, "GB/s"
     else:
         achieved, peak, unit = flops / attn_s / 1e12, tf, "TFLOP/s"
-    attn_roof = {"kernel": "tree_verify_attn (prep + tcgen05 split-KV attention with in-kernel merge)",
+    attn_roof = {"kernel": "tree_verify_attn (prep + tcgen05 split-KV attention + split merge)",
                  "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                  "frac": achieved / peak, "peak_source": src,
                  "traffic": traffic("attn", w.name)[0], "traffic_source": traffic("attn", w.name)[1],
