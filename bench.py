@@ -112,6 +112,7 @@ TRAFFIC = {
     ("topk", "sweep"): (328446464 + 2847488, "profiles/topk_level_kernel_sweep.md"),
     ("lm_head", "llama8b"): (1052517376 + 3688704, "profiles/lm_head_argmax_kernel_llama8b.md"),
     ("sample", "llama8b"): (31397120 + 0, "profiles/filter_stats_kernel_llama8b.md"),
+    ("lm_head", "serving"): (1060635136 + 3217920, "profiles/lm_head_argmax_kernel_serving.md"),
 }
 
 
