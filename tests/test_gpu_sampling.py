@@ -141,7 +141,8 @@ def make_case(w, nreq, vocab, t_max, params, seed, draft=False, max_depth=None):
     return trees, md, logits, u, q, prm
 
 
-def run_walk(trees, md, logits, u, q, prm, t_max, cache=None, prefix=None, valid=None):
+def run_walk(trees, md, logits, u, q, prm, t_max, cache=None, prefix=None, valid=None,
+             nn=None):
     import tree_speculative_decoding_verify_gb300 as T
     d = gc.dev()
     b = len(trees)
@@ -162,7 +163,8 @@ def run_walk(trees, md, logits, u, q, prm, t_max, cache=None, prefix=None, valid
         torch.from_numpy(logits).to(d), *params_t(prm),
         torch.from_numpy(np.ascontiguousarray(u[:, :t_max])).to(d),
         torch.from_numpy(np.ascontiguousarray(u[:, t_max])).to(d),
-        gc.i32(tok), gc.i32(nxt), gc.i32(sib), gc.i32([len(tk) for tk, _ in trees]),
+        gc.i32(tok), gc.i32(nxt), gc.i32(sib),
+        gc.i32(nn if nn is not None else [len(tk) for tk, _ in trees]),
         gc.i32(prefix if prefix is not None else [0] * b), md, cache, out["accept_path"],
         out["accept_len"], out["bonus_token"], out["slot_map"], out["new_prefix_len"], ws,
         err=out["err"], tree_valid=None if valid is None else gc.i32(valid),
@@ -254,6 +256,12 @@ def test_invalid_tree_and_bad_size():
     want = oracle_walk(trees, logits, u, q, prm, t_max, valid=[1, 0, 1, 0])
     compare(got, want, max_close=0.5)
     assert got["accept_len"][1] == 1 and got["accept_len"][3] == 1
+    # a request whose node count is out of range: root only, no token, TSV_REQ_BAD_SIZE
+    nn = [len(tk) for tk, _ in trees]
+    nn[2] = 0
+    bad = run_walk(trees, md, logits, u, q, prm, t_max, nn=nn)
+    assert bad["err"][2] == 4 and bad["accept_len"][2] == 1 and bad["bonus_token"][2] == -1
+    assert bad["accept_path"][2].tolist() == [0] + [-1] * md
 
 
 def test_llama8b_and_serving_shapes():
