@@ -408,8 +408,9 @@ def native(args):
         args.steps = int(max_over_ranks([args.steps], world)[0])
     if world > 1:
         dist.barrier()
-    clocks = Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-                    if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/tsv_clocks_{rank}.csv")
+    import tempfile
+    clocks = Clocks(os.path.join(os.environ.get("TSV_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"tsv_clocks_rank{rank}.csv"))
     with clocks:
         torch.cuda.synchronize()
         clocks.start()
