@@ -129,3 +129,22 @@ def test_empty_batch_is_a_no_op(lib):
     assert lib.tsv_lm_head_argmax(None, None, 0, 64, 10, None, None, None, 0, None) == 0
     assert lib.tsv_tree_build_meta(None, None, None, 0, 8, 3, None, None, None, None, None,
                                    None, None, None) == 0
+
+
+def test_lm_head_vocabulary_split_planner(lib):
+    """The host planner of the lm-head kernel (no GPU here: the SM count reads as 148):
+    one 64-bit key per (vocabulary range, row); the ranges are whole 32-entry chunks and
+    their count minimises waves x (chunks per range + 1), the largest count on ties."""
+    def model(rows, vocab, sms=148):
+        m = -(-rows // 128)
+        c = -(-vocab // 32)
+        best = None
+        for s in range(1, min(c, 8 * sms) + 1):
+            cost = -(-(m * s) // sms) * (-(-c // s) + 1)
+            if best is None or cost <= best[0]:
+                best = (cost, s)
+        return best[1]
+    for rows, vocab in [(61, 128256), (976, 128256), (4160, 128256), (1, 1), (300, 30001)]:
+        splits = model(rows, vocab)
+        want = (splits * rows * 8 + 255) // 256 * 256
+        assert lib.tsv_lm_head_argmax_workspace_size(rows, vocab) == want, (rows, vocab)
