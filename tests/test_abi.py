@@ -148,3 +148,19 @@ def test_lm_head_vocabulary_split_planner(lib):
         splits = model(rows, vocab)
         want = (splits * rows * 8 + 255) // 256 * 256
         assert lib.tsv_lm_head_argmax_workspace_size(rows, vocab) == want, (rows, vocab)
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++11")])
+def test_header_is_plain_c(tmp_path, lang, std):
+    """include/tsv.h is a C header (no torch or CUDA types in the signatures): it compiles
+    alone as C99 and as C++11 with warnings as errors."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc" if lang == "c" else "g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    src = tmp_path / ("t.c" if lang == "c" else "t.cc")
+    src.write_text('#include "tsv.h"\nint main(void) { return TSV_OK; }\n')
+    r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
