@@ -96,11 +96,15 @@ def test_filtered_probabilities(vocab):
     logits[3, 0, ::3] = -np.inf                        # masked entries
     logits[5, 2, :] = np.round(logits[5, 2, :], 1)     # many exact ties
     logits[9, 1, 10] = logits[9, 1].max()              # a tie for the maximum
+    logits[7, 2, :] = 1.0  # one tie group of the whole row: top-p 0.5 keeps the lower half
+                           # by id, more tokens than the sorted list holds (radix select)
     nn = [t] * b
     nn[2] = 1  # rows of absent nodes are left alone
     got = run_probs(logits, PARAMS, nn)
     check_probs(got, logits, PARAMS, nn)
     assert (got[2, 1:] == -1.0).all()
+    kept = np.flatnonzero(got[7, 2] > 0)
+    assert kept.tolist() == list(range((vocab + 1) // 2))
 
 
 def _links(parents, t_max):

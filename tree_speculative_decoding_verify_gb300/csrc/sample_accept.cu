@@ -553,8 +553,10 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
         for (int tries = 0; tries < 3; ++tries) {
           int ng;
           const float before = gather_bins(S, row, V, vec, m, c, lo, hi, thr_k, &ng);
-          if (ng > CAP) {
-            thr_p = radix_select(S, row, V, vec, m, c, lo, hi, thr_k, 1, 0u, target - before);
+          if (ng > CAP || tries == 2) {  // too many, or the last try: the exact select
+            const bool all = tries == 2;  // (then over every bin the crossing can be in)
+            thr_p = radix_select(S, row, V, vec, m, c, all ? 0 : lo, all ? bk : hi, thr_k, 1,
+                                 0u, all ? target : target - before);
             zp = -1.f;
             break;
           }
