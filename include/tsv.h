@@ -448,10 +448,15 @@ int tsv_lm_head_argmax(const void* hidden, const void* weight, int rows, int hid
  * in a fixed order, so a call gives the same result on every run.
  * The walk: at the current node take its children in ascending node order; child c
  * with token x is accepted when u_node[c] < min(1, p(x) / q(x)), q(x) = 1 for
- * target-only (draft_probs NULL), else q = draft_probs[b][node] (the distribution the
- * node's children were drawn from). A rejection replaces p by the residual (target-only:
- * p without x; draft-aware: max(0, p - q)), renormalised; a residual of zero mass leaves
- * p as it was. An accepted child becomes the current node. Where no child is accepted
+ * target-only (draft_probs NULL). Draft-aware: draft_probs[b][node] is the distribution
+ * q the node's children were drawn from, one after another without replacement (they
+ * are distinct tokens), so the j-th child is tested against q_j = q with the tokens of
+ * the children rejected before it set to 0, renormalised (q_0 = q as given). A
+ * rejection replaces p by the residual (target-only: p without x; draft-aware:
+ * max(0, p - q_j)), renormalised; a residual of zero mass leaves p as it was; if q_j has
+ * no mass left the later children are tested against 0 (accepted where p > 0). The
+ * output then follows the target distribution exactly when the children were drawn
+ * that way. An accepted child becomes the current node. Where no child is accepted
  * (or there are none) the walk stops and bonus_token is sampled from the current
  * residual by inverse CDF in token-id order: the smallest t whose running sum exceeds
  * u_final[b] times the total.

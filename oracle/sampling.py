@@ -19,8 +19,14 @@ Readings (the pages leave these open; the plainest reading that the rest support
   * Target-only is the same rule with q = the point mass on the candidate being tested
     (the draft's token is treated as fixed): accept x with probability p(x); on a
     rejection p <- p with x removed, renormalised.
-  * Draft-aware: q is one distribution per node (the one its children were drawn
-    from), given by the caller, the same for every candidate of that node.
+  * Draft-aware: q is one distribution per node, the one its children were drawn from,
+    given by the caller. The siblings of a tree are distinct tokens, so they were drawn
+    from q without replacement: the j-th candidate comes from q with the j - 1 tokens
+    drawn before it removed and the rest renormalised. That is the q of each test and
+    of each residual ("q as the candidates were drawn"): after a rejection of x the
+    target side becomes norm(max(0, p - q)) with the q that x was tested against, and
+    the draft side norm(q with q(x) = 0). If q has no mass left, the later candidates
+    are tested against q = 0 (accepted wherever p > 0).
   * The filters apply in the order the page lists them: temperature, then top-k, then
     top-p on the renormalised result, then min-p on that. top-k keeps the k best
     logits (ties to the lower token id); top-p keeps, in that order, every token whose
@@ -99,7 +105,8 @@ def rejection_walk(tokens, parents, probs, u_node, u_final, q=None, tree_valid=T
 
     tokens, parents: the tree (node 0 the root). probs[i]: the filtered target
     distribution at node i (filter_probs). q: None for target-only, else q[i] is the
-    draft distribution the children of node i were drawn from. Returns (path, token):
+    draft distribution the children of node i were drawn from, without replacement, in
+    ascending node order. Returns (path, token):
     the accepted nodes from the root, and the token sampled where the walk stopped
     (the correction or bonus token). With a trace list, every test appends ("test", u,
     its acceptance probability) and the final sample ("final", u, the distribution), so
@@ -110,10 +117,11 @@ def rejection_walk(tokens, parents, probs, u_node, u_final, q=None, tree_valid=T
         return path, sample_inverse_cdf(probs[0], u_final, trace)
     while True:
         p = np.array(probs[node], np.float64)
+        qc = None if q is None else np.array(q[node], np.float64)  # q of the next draw
         nxt = None
         for c in children(parents, node):
             x = int(tokens[c])
-            qx = 1.0 if q is None else float(q[node][x])
+            qx = 1.0 if q is None else float(qc[x])
             ratio = np.inf if qx == 0.0 and p[x] > 0.0 else (0.0 if qx == 0.0 else p[x] / qx)
             if trace is not None:
                 trace.append(("test", float(u_node[c]), min(1.0, ratio)))
@@ -124,7 +132,12 @@ def rejection_walk(tokens, parents, probs, u_node, u_final, q=None, tree_valid=T
                 resid = p.copy()
                 resid[x] = 0.0
             else:
-                resid = np.maximum(0.0, p - np.asarray(q[node], np.float64))
+                resid = np.maximum(0.0, p - qc)
+                # the next sibling was drawn from q without the tokens drawn before it
+                qc[x] = 0.0
+                sq = qc.sum()
+                if sq > 0.0:
+                    qc = qc / sq
             s = resid.sum()
             if s > 0.0:
                 p = resid / s

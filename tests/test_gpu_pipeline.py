@@ -8,6 +8,7 @@ import workloads as W
 from oracle import step as ostep
 from oracle import tree
 from tests import gpu_cases as gc
+from tests.test_gpu_sampling import valid_sample
 
 pytestmark = pytest.mark.gpu
 
@@ -192,5 +193,10 @@ def test_step_with_non_greedy_acceptance():
     path, tok = sampling.rejection_walk(list(tokens), list(parents), probs, u[:t_max],
                                         float(u[t_max]), trace=trace)
     margin = min([abs(x - a) for kind, x, a in trace if kind == "test"], default=1.0)
+    final = [(x, p) for kind, x, p in trace if kind == "final"][-1]
     if margin > 1e-5:
         assert results["t1"][0] == path
+        # the sampled token: the oracle's, or (a near-tie of the inverse CDF) a token the
+        # oracle's final distribution gives for a uniform within 1e-6 of this one
+        assert results["t1"][1] == tok or valid_sample(results["t1"][1], final), (
+            results["t1"][1], tok)

@@ -156,6 +156,22 @@ SAMPLING_MISTAKES = [
      "test_first_emitted_token_follows_the_target"),
     ("rejection_walk", "resid[x] = 0.0", "pass",
      "test_first_emitted_token_follows_the_target"),
+    # the draft side kept fixed: right only for siblings drawn with replacement
+    ("rejection_walk", "qc[x] = 0.0", "pass",
+     "test_first_token_distribution_is_exact_for_draws_without_replacement"),
+    ("rejection_walk", "qc[x] = 0.0", "pass", "test_first_emitted_token_follows_the_target"),
+    # the residual formed with the q of the next draw instead of the one x was tested with
+    ("rejection_walk", """resid = np.maximum(0.0, p - qc)
+                # the next sibling was drawn from q without the tokens drawn before it
+                qc[x] = 0.0
+                sq = qc.sum()
+                if sq > 0.0:
+                    qc = qc / sq""", """qc[x] = 0.0
+                sq = qc.sum()
+                if sq > 0.0:
+                    qc = qc / sq
+                resid = np.maximum(0.0, p - qc)""",
+     "test_first_token_distribution_is_exact_for_draws_without_replacement"),
     ("rejection_walk", "if u_node[c] < min(1.0, ratio):", "if u_node[c] >= min(1.0, ratio):",
      "test_zero_temperature_is_the_greedy_walk"),
     ("filter_probs", "if not first and before >= top_p * total:",

@@ -99,12 +99,23 @@ def _first_token(tokens, parents, probs, u_node, u_final, q=None):
     return tokens[path[1]] if len(path) > 1 else tok
 
 
+def _draw_without_replacement(rng, q, k):
+    """k distinct tokens drawn one after another from q, each from what is left of q
+    renormalised (successive sampling)."""
+    rem, out = np.array(q, np.float64), []
+    for _ in range(k):
+        x = int(rng.choice(len(rem), p=rem / rem.sum()))
+        out.append(x)
+        rem[x] = 0.0
+    return out
+
+
 @pytest.mark.parametrize("mode", ["target_only", "draft_aware"])
 def test_first_emitted_token_follows_the_target(mode):
     """The guarantee of rejection sampling: the first token the step emits (an accepted
     child's token, else the sample at the root) is distributed as the filtered target
     distribution at the root. Target-only holds for any fixed candidates; the
-    draft-aware rule needs candidates drawn from q (here i.i.d. per trial)."""
+    draft-aware rule for distinct siblings drawn from q without replacement."""
     rng = np.random.default_rng(7)
     p_root = np.array([0.05, 0.4, 0.1, 0.3, 0.15])
     q_root = np.array([0.3, 0.1, 0.25, 0.05, 0.3])
@@ -117,12 +128,61 @@ def test_first_emitted_token_follows_the_target(mode):
         if mode == "target_only":
             tokens, q = [0, 3, 0, 4, 1, 2], None
         else:
-            tokens = [0] + [int(x) for x in rng.choice(5, 3, p=q_root)] + [1, 2]
+            tokens = [0] + _draw_without_replacement(rng, q_root, 3) + [1, 2]
             q = [q_root] + [other] * 5
         counts[_first_token(tokens, parents, probs, rng.random(6), rng.random(), q)] += 1
     freq = counts / n
     sigma = np.sqrt(p_root * (1 - p_root) / n)
     assert (np.abs(freq - p_root) < 4.5 * sigma).all(), (freq, p_root)
+
+
+def _exact_first_token(p_root, cand, q_root=None):
+    """The distribution of the first emitted token of a root with candidate children
+    `cand`, integrated exactly over the uniforms: every accept/reject pattern is forced
+    through the walk (u = 0 accepts, u just below 1 rejects) and weighted by the
+    acceptance probabilities the walk's trace reports."""
+    k = len(cand)
+    tokens, parents = [0] + list(cand), [-1] + [0] * k
+    probs = [p_root] * (k + 1)
+    q = None if q_root is None else [q_root] * (k + 1)
+    out = np.zeros(len(p_root))
+    below_one = np.nextafter(1.0, 0.0)
+    for stop in range(k + 1):  # accept candidate `stop`, or (stop == k) reject them all
+        u = [below_one] * (k + 1)
+        if stop < k:
+            u[stop + 1] = 0.0
+        trace = []
+        path, _ = sampling.rejection_walk(tokens, parents, probs, u, 0.0, q, True, trace)
+        tests = [a for kind, _, a in trace if kind == "test"]
+        if len(tests) != min(stop + 1, k) or (len(path) > 1) != (stop < k):
+            continue  # this pattern has probability zero (an acceptance of 0 or 1)
+        w = np.prod([1.0 - a for a in tests[:stop]])
+        if stop < k:
+            out[tokens[path[1]]] += w * tests[stop]
+        else:
+            final = [d for kind, _, d in trace if kind == "final"][0]
+            out += w * final / final.sum()
+    return out
+
+
+def test_first_token_distribution_is_exact_for_draws_without_replacement():
+    """Integrated over every ordered draw of three distinct candidates from q (each
+    draw's probability by successive sampling) and over the uniforms, the first emitted
+    token is distributed exactly as p. The same holds for target-only on any fixed
+    candidate list."""
+    import itertools
+    p_root = np.array([0.05, 0.4, 0.1, 0.3, 0.15])
+    q_root = np.array([0.3, 0.1, 0.25, 0.05, 0.3])
+    total = np.zeros(5)
+    for seq in itertools.permutations(range(5), 3):
+        pr, rem = 1.0, q_root.copy()
+        for x in seq:
+            pr *= rem[x] / rem.sum()
+            rem[x] = 0.0
+        total += pr * _exact_first_token(p_root, seq, q_root)
+    np.testing.assert_allclose(total, p_root, atol=1e-12)
+    for cand in ([3, 0, 4], [1], [4, 3, 2, 1, 0]):
+        np.testing.assert_allclose(_exact_first_token(p_root, cand), p_root, atol=1e-12)
 
 
 def test_rejected_tokens_are_never_the_correction():

@@ -13,10 +13,14 @@
 //
 // Target-only is the rule with q = the point mass on the candidate (accept x with
 // probability p(x); a rejection removes x from p); draft-aware takes one draft
-// distribution q per node from the caller.
+// distribution q per node from the caller, from which the node's children (distinct
+// tokens) were drawn without replacement: the j-th candidate is tested against q with
+// the j - 1 tokens drawn before it removed and renormalised, q_j = q / D_j off those
+// tokens (D_0 = 1, D_j = sum(q) - the q of the rejected tokens), and the residual after
+// its rejection is norm(max(0, p_j - q_j)).
 //
 // Kernels:
-//   filter_stats_kernel   one 1024-thread CTA per (node, request), 58 KB of shared memory.
+//   filter_stats_kernel   one 1024-thread CTA per (node, request), 68 KB of shared memory.
 //       A node's filtered distribution is described by the largest
 //       logit m, c = log2(e)/temperature, a 64-bit key threshold, a min-p bound and the
 //       normaliser Z: token v is kept when its key (logit order, then the lower token id)
@@ -601,7 +605,11 @@ struct WalkSmem {
   float kl[TSV_MAX_NODES], kq[TSV_MAX_NODES];
   int removed[TSV_MAX_NODES];
   float rmass[TSV_MAX_NODES];
-  float zr[TSV_MAX_NODES];  // draft-aware: normalisers of the residuals at this node
+  // draft-aware, per rejection j at this node: the residual's normaliser (0: p kept as
+  // it was) and 1 / D_j, the normaliser of the q that candidate was tested against
+  float zr[TSV_MAX_NODES];
+  float qi[TSV_MAX_NODES + 1];
+  float qrem;  // D of the next candidate: sum(q) less the q of the rejected tokens
   int path[TSV_MAX_DEPTH + 1];
   float tile[MAX_TILES];
   float sf[32];
@@ -611,10 +619,14 @@ struct WalkSmem {
   int node, len, code, nk, acc, nrem, nz, pick, ptile;
 };
 
-// Draft-aware residual probability of token v after `nz` rejections at this node.
+// Draft-aware residual probability of token v (draft probability q) after `nz`
+// rejections at this node. A rejected token already has residual 0 after its own
+// rejection (it was rejected only if p_j < q_j there), so removing it from the later
+// q_j changes nothing here.
 __device__ __forceinline__ float resid_p(const WalkSmem& W, float l, int v, float q) {
   float r = kept_mass(W.st, l, v) / W.st.z;
-  for (int j = 0; j < W.nz; ++j) r = fmaxf(0.f, r - q) / W.zr[j];
+  for (int j = 0; j < W.nz; ++j)
+    if (W.zr[j] > 0.f) r = fmaxf(0.f, r - q * W.qi[j]) / W.zr[j];
   return r;
 }
 // Weight of token v (logit l, draft probability q) in the final sample, before the
@@ -675,6 +687,7 @@ sample_walk_kernel(const SampleArgs a, const RowStats* __restrict__ stats, Cache
         W.zcur = W.st.z;
         W.nrem = 0;
         W.nz = 0;
+        W.qi[0] = 1.f;
         W.acc = -1;
         // children in ascending node order: the chain strictly increases within [0, n)
         int nk = 0, c = W.nxt[node], prev = node;
@@ -713,6 +726,7 @@ sample_walk_kernel(const SampleArgs a, const RowStats* __restrict__ stats, Cache
             q = 1.f;
           } else {
             p = in ? resid_p(W, W.kl[j], x, q) : 0.f;
+            q *= W.qi[W.nz];
           }
           const float ratio = q > 0.f ? p / q : (p > 0.f ? INFINITY : 0.f);
           const float u = a.u_node[row0 + c];
@@ -729,14 +743,25 @@ sample_walk_kernel(const SampleArgs a, const RowStats* __restrict__ stats, Cache
         __syncthreads();
         if (W.acc >= 0) break;
         if (draft) {
-          // residual normaliser: sum over v of max(0, p_j(v) - q(v))
-          Kahan part;
+          // residual normaliser: sum over v of max(0, p_j(v) - q_j(v)); the first pass
+          // at a node also sums q
+          const int nz = W.nz;
+          const float qs = W.qi[nz];
+          Kahan part, qtot;
           for (int v = threadIdx.x; v < V; v += WT) {
             const float q = qrow[v];
-            part.add(fmaxf(0.f, resid_p(W, clean(lrow[v]), v, q) - q));
+            part.add(fmaxf(0.f, resid_p(W, clean(lrow[v]), v, q) - q * qs));
+            if (nz == 0) qtot.add(q);
           }
           const float zn = block_sum<float>(part.value(), W.sf);
-          if (threadIdx.x == 0 && zn > 0.f) W.zr[W.nz++] = zn;
+          const float qsum = nz == 0 ? block_sum<float>(qtot.value(), W.sf) : 0.f;
+          if (threadIdx.x == 0) {
+            // the next sibling was drawn from q without the tokens drawn before it
+            W.qrem = (nz == 0 ? qsum : W.qrem) - W.kq[j];
+            W.qi[nz + 1] = W.qrem > 0.f ? 1.f / W.qrem : 0.f;
+            W.zr[nz] = zn > 0.f ? zn : 0.f;
+            W.nz = nz + 1;
+          }
           __syncthreads();
         }
       }
