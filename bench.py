@@ -11,6 +11,13 @@ in HBM before the timed region; the step is replayed from a CUDA graph; L2 is fl
 the per-call times, the roofline of the attention call against MEASURED_PEAKS.json,
 an end-to-end number through host buffers, and the CPU oracle as a baseline.
 
+The default workload is long70b (batch 4, prefix 32768, 70B-shaped heads: the largest
+single-GPU shape, a long-prefix one). In the same timed loop the attention call of the
+serving mix and of the large-batch sweep (65-node trees) and the sweep's top-k level
+([640, 128256] fp32 logits) are replayed, each after its own L2 flush, and reported as
+roofline_attn_serving, roofline_attn_sweep and roofline_topk_sweep (--no-side leaves
+them out).
+
 --impl reference times the CPU oracle (the reference arm: a deliberately slow,
 obviously correct restatement of the method) on the same workload.
 """
@@ -54,10 +61,12 @@ def parse():
     ap.add_argument("--steps", type=int, default=None,
                     help="timed steps (default: enough for about 2 s of timed work, at least 50)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="llama8b", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="long70b", choices=sorted(W.WORKLOADS))
     ap.add_argument("--total-tokens", type=int, default=0)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side", action="store_true",
+                    help="time only the chosen workload (no serving / sweep side legs)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     return ap.parse_args()
 
@@ -101,24 +110,34 @@ def algorithmic(w, prefix, depths_per_req, esize=2):
     return nbytes, flops
 
 
-# DRAM bytes (read + write) per launch of the dominant kernels, from one ncu capture of
-# the same workload each (profiles/<kernel>_<workload>.md, which give the command). The
-# attention figure is the tcgen05 kernel alone (the call's roofline also counts the prep
-# and the split merge). Absent: no capture of the current kernel for that workload.
-TRAFFIC = {
-    ("attn", "serving"): (332767232 + 35483648, "profiles/attn_tc_kernel_serving.md"),
-    ("attn", "long70b"): (606232320 + 41901824, "profiles/attn_tc_kernel_long70b.md"),
-    ("topk", "llama8b"): (1354240 + 0, "profiles/topk_level_kernel_llama8b.md"),
-    ("topk", "sweep"): (328446464 + 2847488, "profiles/topk_level_kernel_sweep.md"),
-    ("lm_head", "llama8b"): (1052517376 + 3688704, "profiles/lm_head_argmax_kernel_llama8b.md"),
-    ("sample", "llama8b"): (31397120 + 0, "profiles/filter_stats_kernel_llama8b.md"),
-    ("lm_head", "serving"): (1060635136 + 3217920, "profiles/lm_head_argmax_kernel_serving.md"),
-}
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def source_digest(paths):
+    """sha256 over the named source files (repository-relative), in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def traffic(kernel, workload):
-    t = TRAFFIC.get((kernel, workload))
-    return (t[0], t[1]) if t else (None, None)
+    """DRAM bytes (read + write) of one launch of `kernel` on `workload` from the ncu
+    capture recorded in profiles/traffic.json, with the summary that holds it; (None,
+    reason) when there is no capture, or the kernel's sources have changed since."""
+    path = os.path.join(PROFILES, "traffic.json")
+    if not os.path.exists(path):
+        return None, "no capture"
+    with open(path) as f:
+        entries = json.load(f)["entries"]
+    for e in entries:
+        if e["kernel"] == kernel and e["workload"] == workload:
+            if source_digest(e["sources"]) != e["sources_sha256"]:
+                return None, f"kernel changed since the capture in {e['summary']}"
+            return int(e["dram_read"] + e["dram_write"]), e["summary"]
+    return None, "no capture"
 
 
 def peaks():
@@ -203,6 +222,110 @@ class Clocks:
 
 
 # --------------------------------------------------------------------------------------
+# Side legs: the attention call of other workloads (and the sweep's top-k level), timed
+# in the same loop as the main workload so one run reports every long-prefix roofline.
+SIDE_LEGS = (("serving", ("attn",)), ("sweep", ("attn", "topk")))
+
+
+def kv_cache(w, dev, gen, T, cap):
+    """Random (already rotated) KV cache of the workload: contiguous [B, Hkv, cap, D] or
+    paged [pool, Hkv, 64, D] behind the workload's block table."""
+    import torch
+    if w.paged:
+        table, pool = W.block_table(w, cap)
+        shp = (pool, w.num_kv_heads, 64, w.head_dim)
+        kc = (torch.randn(*shp, device=dev, generator=gen) * w.scale).to(torch.bfloat16)
+        vc = (torch.randn(*shp, device=dev, generator=gen) * w.scale).to(torch.bfloat16)
+        return T.KVCache(kc, vc, torch.from_numpy(table).to(dev))
+    shp = (w.batch, w.num_kv_heads, cap, w.head_dim)
+    kc = (torch.randn(*shp, device=dev, generator=gen) * w.scale).to(torch.bfloat16)
+    vc = (torch.randn(*shp, device=dev, generator=gen) * w.scale).to(torch.bfloat16)
+    return T.KVCache(kc, vc)
+
+
+def tree_depths(parents_rows):
+    out = []
+    for pars in parents_rows:
+        d = []
+        for p in pars:
+            d.append(0 if p < 0 else d[p] + 1)
+        out.append(d)
+    return out
+
+
+def side_state(name, legs, dev, gen, T):
+    """Inputs in HBM for one side workload: its trees from the expansion of its own
+    seeded draft logits, their metadata, q/k/v and a KV cache; returns the legs as
+    callables with what their rooflines need."""
+    import torch
+    w = W.WORKLOADS[name]
+    b, k = w.batch, w.top_k
+    prefix = W.prefix_lengths(w)
+    t_max = w.num_nodes
+    cap = int(math.ceil((w.max_prefix + t_max + 16) / 64) * 64)
+    cache = kv_cache(w, dev, gen, T, cap)
+    shape = T.TreeShape(b, w.num_q_heads, w.num_kv_heads, w.head_dim, w.max_prefix,
+                        vocab=w.vocab, top_k=k, depth=w.depth, total_tokens=w.total_tokens)
+    hp = T.HotPath(shape, cache)
+    levels = [torch.from_numpy(W.draft_logits_batch(w, lvl)).to(dev)
+              for lvl in range(1, w.depth + 2)]
+    root = torch.from_numpy(W.root_tokens(w)).to(dev)
+    prefix_t = torch.from_numpy(prefix).to(dev)
+    hp.expand(levels, root)
+    hp.build_meta(prefix_t)
+    torch.cuda.synchronize()
+    depths = tree_depths(hp.parents.cpu().numpy())
+    q, k_new, v_new = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in W.new_qkv(w))
+    sm_scale = 1.0 / math.sqrt(w.head_dim)
+    fns = {}
+    if "attn" in legs:
+        fns["attn_" + name] = lambda: hp.verify(q, k_new, v_new, prefix_t, w.theta, sm_scale)
+    if "topk" in legs:
+        lvl_out = hp.front[1]
+        fns["topk_" + name] = lambda: T.draft_topk_expand(
+            levels[1], k, 2, hp.front[0][1], hp.front[0][2], hp.store_token, hp.store_score,
+            hp.store_parent, *lvl_out, hp.topk_ws)
+    # keep the inputs alive with the callables
+    return {"w": w, "prefix": prefix, "depths": depths, "fns": fns, "hp": hp,
+            "keep": (levels, root, q, k_new, v_new, prefix_t, cache),
+            "attn_launches": hp.attn_kernels()}
+
+
+def attn_roofline(w, prefix, depths, us, hbm, tf, src):
+    """Roofline of one tree_verify_attn call (SURVEY-style algorithmic bytes / FLOPs)."""
+    nbytes, flops = algorithmic(w, prefix, depths)
+    s = us / 1e6
+    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tf * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = nbytes / s / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = flops / s / 1e12, tf, "TFLOP/s"
+    tr, tr_src = traffic("attn", w.name)
+    return {"kernel": f"tree_verify_attn on {w.name} (prep + tcgen05 split-KV attention + "
+                      "split merge)",
+            "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "peak_source": src, "traffic": tr, "traffic_source": tr_src,
+            "algorithmic_bytes": nbytes, "algorithmic_flops": flops, "us_per_launch": us,
+            "roofline_us": max(t_hbm, t_tc) * 1e6, "hbm_GBps": nbytes / s / 1e9,
+            "nodes_kv_tokens_per_s": sum(len(d) * (int(p) + len(d))
+                                         for p, d in zip(prefix, depths)) / s}
+
+
+def topk_roofline(w, us, hbm, src):
+    """Roofline of one expansion level: every frontier row's fp32 logits read once."""
+    rows = w.batch * w.top_k
+    nbytes = rows * w.vocab * 4
+    gbps = nbytes / (us / 1e6) / 1e9
+    tr, tr_src = traffic("topk", w.name)
+    return {"kernel": f"draft_topk_expand level on {w.name} ({rows} rows x {w.vocab} fp32)",
+            "bound": "hbm", "achieved": gbps, "peak": hbm, "unit": "GB/s", "frac": gbps / hbm,
+            "peak_source": src, "traffic": tr, "traffic_source": tr_src,
+            "algorithmic_bytes": nbytes, "us_per_launch": us,
+            "rows_per_s": rows / (us / 1e6)}
+
+
+# --------------------------------------------------------------------------------------
 def native(args):
     import torch
     import torch.distributed as dist
@@ -233,15 +356,7 @@ def native(args):
     t_max = w.num_nodes
     cap = int(math.ceil((p_max + t_max + 16) / 64) * 64)
     scale = w.scale
-    if paged:
-        table, pool = W.block_table(w, cap)
-        kc = (torch.randn(pool, w.num_kv_heads, 64, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
-        vc = (torch.randn(pool, w.num_kv_heads, 64, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
-        cache = T.KVCache(kc, vc, torch.from_numpy(table).to(dev))
-    else:
-        kc = (torch.randn(b, w.num_kv_heads, cap, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
-        vc = (torch.randn(b, w.num_kv_heads, cap, w.head_dim, device=dev, generator=gen) * scale).to(torch.bfloat16)
-        cache = T.KVCache(kc, vc)
+    cache = kv_cache(w, dev, gen, T, cap)
     shape = T.TreeShape(b, w.num_q_heads, w.num_kv_heads, w.head_dim, p_max, vocab=v, top_k=k,
                         depth=w.depth, total_tokens=w.total_tokens)
     hp = T.HotPath(shape, cache)
@@ -255,12 +370,7 @@ def native(args):
     pars = hp.parents.cpu().numpy()
     target = np.stack([W.plant_target(w, i, toks[i], pars[i]) for i in range(b)])
     target_t = torch.from_numpy(target).to(dev)
-    depths = []
-    for i in range(b):
-        d = []
-        for p in pars[i]:
-            d.append(0 if p < 0 else d[p] + 1)
-        depths.append(d)
+    depths = tree_depths(pars)
 
     def step():
         hp.step(levels, root, q, k_new, v_new, prefix_t, target_t, w.theta, sm_scale)
@@ -364,18 +474,26 @@ def native(args):
         T.draft_topk_expand(levels[1], k, 2, hp.front[0][1], hp.front[0][2], hp.store_token,
                             hp.store_score, hp.store_parent, *lvl_out, lvl_ws)
 
+    legs = {"step": step, "attn": attn, "topk": topk_level, "lm_head": lm_head,
+            "sample": sample_accept, "topk_product": topk_product, "variants": variants,
+            "drafter": drafter_level}
+    sides = {}
+    if not args.no_side:
+        for name, want in SIDE_LEGS:
+            if name != w.name:
+                sides[name] = side_state(name, want, dev, gen, T)
+                legs.update(sides[name]["fns"])
+                print(f"bench: side legs of {name} ready", file=sys.stderr, flush=True)
+
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     graphs = {}
     with torch.cuda.stream(stream):
         for _ in range(2):  # warm the allocator and the kernels before capture
-            step(); attn(); topk_level(); lm_head(); sample_accept(); topk_product(); variants()
-            drafter_level()
+            for fn in legs.values():
+                fn()
         stream.synchronize()
-        for name, fn in (("step", step), ("attn", attn), ("topk", topk_level),
-                         ("lm_head", lm_head), ("sample", sample_accept),
-                         ("topk_product", topk_product), ("variants", variants),
-                         ("drafter", drafter_level)):
+        for name, fn in legs.items():
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 fn()
@@ -387,8 +505,7 @@ def native(args):
                      for _ in range(n)] for name in graphs}
         with torch.cuda.stream(stream):
             for i in range(n):
-                for name in ("step", "attn", "topk", "lm_head", "sample", "topk_product",
-                             "variants", "drafter"):
+                for name in graphs:
                     flush_buf.zero_()
                     ev[name][i][0].record(stream)
                     graphs[name].replay()
@@ -493,28 +610,9 @@ def native(args):
         return
 
     hbm, tf, src = peaks()
-    nbytes, flops = algorithmic(w, prefix, depths)
+    attn_roof = attn_roofline(w, prefix, depths, ms["attn"] * 1e3, hbm, tf, src)
+    topk_roof = topk_roofline(w, ms["topk"] * 1e3, hbm, src)
     attn_s = ms["attn"] / 1e3
-    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tf * 1e12)
-    bound = "hbm" if t_hbm >= t_tc else "tensor"
-    if bound == "hbm":
-        achieved, peak, unit = nbytes / attn_s / 1e9, hbm, "GB/s"
-    else:
-        achieved, peak, unit = flops / attn_s / 1e12, tf, "TFLOP/s"
-    attn_roof = {"kernel": "tree_verify_attn (prep + tcgen05 split-KV attention + split merge)",
-                 "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                 "frac": achieved / peak, "peak_source": src,
-                 "traffic": traffic("attn", w.name)[0], "traffic_source": traffic("attn", w.name)[1],
-                 "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
-                 "us_per_launch": ms["attn"] * 1e3}
-    topk_rows = b * k / (ms["topk"] / 1e3)
-    topk_bytes = b * k * v * 4
-    topk_gbps = topk_bytes / (ms["topk"] / 1e3) / 1e9
-    topk_roof = {"kernel": "draft_topk_expand level (rows x vocab fp32 logits)", "bound": "hbm",
-                 "achieved": topk_gbps, "peak": hbm, "unit": "GB/s", "frac": topk_gbps / hbm,
-                 "peak_source": src, "traffic": traffic("topk", w.name)[0],
-                 "traffic_source": traffic("topk", w.name)[1], "algorithmic_bytes": topk_bytes,
-                 "us_per_launch": ms["topk"] * 1e3}
     lm_s = ms["lm_head"] / 1e3
     lm_bytes = lm_v * lm_h * 2 + lm_rows * lm_h * 2 + lm_rows * 4
     lm_flops = 2 * lm_rows * lm_v * lm_h
@@ -556,18 +654,18 @@ def native(args):
                    "paged": paged, "l2": "flushed (256 MiB write) before every timed launch",
                    "parallelism": f"replicas x{world}", "graph": "CUDA graph per step"},
         "attn_us_per_layer": ms["attn"] * 1e3,
-        "attn_hbm_GBps": nbytes / attn_s / 1e9,
-        "attn_roofline_us": max(t_hbm, t_tc) * 1e6,
-        "topk_rows_per_s": topk_rows,
-        "topk_hbm_GBps": topk_bytes / (ms["topk"] / 1e3) / 1e9,
-        "nodes_kv_tokens_per_s": sum(len(d) * (p + len(d)) for p, d in zip(prefix, depths)) / attn_s,
+        "attn_hbm_GBps": attn_roof["hbm_GBps"],
+        "attn_roofline_us": attn_roof["roofline_us"],
+        "topk_rows_per_s": topk_roof["rows_per_s"],
+        "topk_hbm_GBps": topk_roof["achieved"],
+        "nodes_kv_tokens_per_s": attn_roof["nodes_kv_tokens_per_s"],
         "roofline": topk_roof if dominant == "topk" else attn_roof,
         "roofline_attn": attn_roof,
         "roofline_topk": topk_roof,
         "lm_head_us": ms["lm_head"] * 1e3,
         "roofline_lm_head": lm_roof,
         "topk_product_us": ms["topk_product"] * 1e3,
-        "topk_product_hbm_frac": topk_bytes / (ms["topk_product"] / 1e3) / 1e9 / hbm,
+        "topk_product_hbm_frac": topk_roof["algorithmic_bytes"] / (ms["topk_product"] / 1e3) / 1e9 / hbm,
         "d2t_map_plus_fixed_level_us": ms["variants"] * 1e3,
         "drafter_level_us": ms["drafter"] * 1e3,
         "drafter_nodes": dn,
@@ -582,9 +680,20 @@ def native(args):
         # grown mask and its attention
         "gpu_launches": args.steps * (kernels_step + attn_kernels + 1 + 2 + 3 + 1 + 2 + 1 +
                                       T.tree_verify_attn_launches(
-                                          (b, dn, w.num_q_heads, w.head_dim), cache, p_max)),
+                                          (b, dn, w.num_q_heads, w.head_dim), cache, p_max) +
+                                      sum(sd["attn_launches"] * any(n.startswith("attn_") for n in sd["fns"]) +
+                                          sum(n.startswith("topk_") for n in sd["fns"])
+                                          for sd in sides.values())),
         "wall_s_timed_region": t_wall,
     }
+    for name, sd in sides.items():
+        for leg in sd["fns"]:
+            kind = leg.split("_")[0]
+            if kind == "attn":
+                line["roofline_attn_" + name] = attn_roofline(sd["w"], sd["prefix"], sd["depths"],
+                                                              ms[leg] * 1e3, hbm, tf, src)
+            else:
+                line["roofline_topk_" + name] = topk_roofline(sd["w"], ms[leg] * 1e3, hbm, src)
     ck = clocks.summary()
     if ck:
         line["clocks"] = ck
@@ -623,22 +732,96 @@ def cpu_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(w, seconds):
-    """The oracle timed on this host: whole oracle steps for one request at a time
-    (cycling through the batch) until `seconds` have passed; steps/s scaled to the
-    workload's batch (a step processes all B requests)."""
-    inputs = [oracle_step_inputs(w, b) for b in range(min(w.batch, 4))]
-    n = 0
-    t0 = time.perf_counter()
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+BLAS_ENV = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS",
+            "BLIS_NUM_THREADS", "NUMEXPR_NUM_THREADS")
+
+
+def _oracle_worker(job):
+    """One process of a CPU leg (spawned with the BLAS thread variables at 1, so numpy
+    runs on one thread): whole oracle steps of request `b` for `seconds`; returns
+    (steps, seconds taken)."""
+    name, b, seconds = job
+    w = W.WORKLOADS[name]
+    inputs = oracle_step_inputs(w, b)
+    n, t0 = 0, time.perf_counter()
     while time.perf_counter() - t0 < seconds or n == 0:
-        run_oracle_step(w, n % len(inputs), inputs[n % len(inputs)])
+        run_oracle_step(w, b, inputs)
         n += 1
-    dt = time.perf_counter() - t0
-    per_request = dt / n
-    return {"value": 1.0 / (per_request * w.batch), "unit": UNIT, "cores": cpu_threads(),
-            "kind": "oracle",
-            "sample": f"{n} oracle steps of single requests of the {w.name} workload "
-                      f"({dt:.1f} s), scaled to a batch of {w.batch}"}
+    return n, time.perf_counter() - t0
+
+
+def _run_workers(name, seconds, workers, batch):
+    """`workers` spawned processes, each on one BLAS thread, running oracle steps of
+    independent requests at the same time; returns the per-worker (steps, seconds)."""
+    import multiprocessing as mp
+    saved = {k: os.environ.get(k) for k in BLAS_ENV}
+    for k in BLAS_ENV:
+        os.environ[k] = "1"  # read by numpy's BLAS when the spawned child imports it
+    try:
+        with mp.get_context("spawn").Pool(workers) as pool:
+            return pool.map(_oracle_worker, [(name, i % batch, seconds) for i in range(workers)])
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+def _mem_available_bytes():
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+def cpu_baseline(w, seconds):
+    """The oracle timed on this host, in two legs of whole single-request oracle steps,
+    each about `seconds` long: one thread (one spawned process on one BLAS thread), and
+    all cores (one spawned process per core, each on one BLAS thread, independent
+    requests). steps/s scaled to the workload's batch (a step processes all B
+    requests). The all-core figure is `value`."""
+    nproc = os.cpu_count() or 1
+    # one thread: one spawned process
+    (n, dt1), = _run_workers(w.name, seconds, 1, w.batch)
+    one = 1.0 / (dt1 / n * w.batch)
+    # all cores: as many workers as cores, fewer if host memory would not hold them
+    per_worker = 3 << 30 if w.max_prefix > 8192 else 1 << 30
+    avail = _mem_available_bytes()
+    workers = nproc if avail is None else max(1, min(nproc, avail // per_worker))
+    res = _run_workers(w.name, seconds, workers, w.batch)
+    rate = sum(k / t for k, t in res)  # requests per second over all workers
+    allc = rate / w.batch
+    return {"value": allc, "unit": UNIT, "cores": int(workers), "kind": "oracle",
+            "sample": f"{sum(k for k, _ in res)} single-request oracle steps of the {w.name} "
+                      f"workload on {workers} processes (one BLAS thread each, about "
+                      f"{seconds:.0f} s), scaled to a batch of {w.batch}",
+            "one_thread": {"value": one, "unit": UNIT, "cores": 1,
+                           "sample": f"{n} single-request oracle steps ({dt1:.1f} s) on one "
+                                     f"thread, scaled to a batch of {w.batch}"},
+            "nproc": nproc, "cpu_model": cpu_model()}
 
 
 def reference(args):
@@ -667,7 +850,8 @@ def reference(args):
         "config": {"workload": w.name, "batch": w.batch, "nodes": w.num_nodes,
                    "sample": "each timed step is one request's oracle step, scaled by batch"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                         "sample": f"{args.steps} single-request oracle steps of {w.name}"},
+                         "sample": f"{args.steps} single-request oracle steps of {w.name}",
+                         "nproc": os.cpu_count() or 1, "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(plain(line)))
