@@ -374,7 +374,12 @@ int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void*
  * - Returns TSV_ERR_WORKSPACE when the call would need more scratch than that
  *   (tsv_tree_verify_attn_workspace_size tells how much a shape needs).
  * - The first call on a device looks up the array's device address on that device
- *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   (cudaGetSymbolAddress); make that first call before any stream capture. The address
+ *   is kept per device together with the CUDA context it was found in: after a device
+ *   reset (cudaDeviceReset), or from another context on that device, the next call looks
+ *   it up again, so that call too should come before any capture.
+ * - Its host checks are those of tsv_tree_verify_attn (the same function runs them), so
+ *   both calls return the same status for the same invalid arguments.
  * - Every call on a device shares the one array, and a call leaves its contents behind.
  *   Nothing in it has to start at zero. Calls whose GPU work overlaps (on different
  *   streams, without ordering between them) race on the array and give wrong results.

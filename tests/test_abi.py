@@ -164,3 +164,39 @@ def test_header_is_plain_c(tmp_path, lang, std):
     r = subprocess.run([cc, std, "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
                         "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_attention_entry_points_share_host_checks(lib):
+    """tsv_tree_verify_attn and tsv_tree_verify_attn_noalloc run one host validator: the
+    same invalid arguments give the same status from both (every case below returns
+    before any CUDA work)."""
+    p = ctypes.c_void_p(16)
+    k = ctypes.c_void_p(256)
+
+    def both(shape, cache, q=p, mask=p, theta=1e4, scale=0.1):
+        a = lib.tsv_tree_verify_attn(ctypes.byref(shape), q, p, p, ctypes.byref(cache), p, p, p,
+                                     mask, theta, scale, p, p, 1 << 30, None, None)
+        b = lib.tsv_tree_verify_attn_noalloc(ctypes.byref(shape), q, p, p, ctypes.byref(cache),
+                                             p, p, p, mask, theta, scale, p, None, None)
+        return a, b
+
+    def fresh():
+        return (_lib.AttnShape(2, 61, 32, 2048),
+                _lib.KVCacheDesc(k, k, 1, 8, 128, 0, 2176, None, 0, 0, 1, 0))
+
+    cases = []
+    s, c = fresh(); c.head_dim = 96; cases.append(both(s, c))            # head_dim
+    s, c = fresh(); s.num_q_heads = 30; cases.append(both(s, c))         # GQA mismatch
+    s, c = fresh(); s.max_nodes = 257; cases.append(both(s, c))          # too many nodes
+    s, c = fresh(); s.batch = 70000; cases.append(both(s, c))            # grid limit
+    s, c = fresh(); c.capacity = 100; cases.append(both(s, c))           # capacity % 64
+    s, c = fresh(); c.layout = 5; cases.append(both(s, c))               # unknown layout
+    s, c = fresh(); c.layout = 1; cases.append(both(s, c))               # paged, no table
+    s, c = fresh(); cases.append(both(s, c, theta=0.0))                  # RoPE theta
+    s, c = fresh(); cases.append(both(s, c, scale=float("nan")))         # softmax scale
+    s, c = fresh(); cases.append(both(s, c, q=ctypes.c_void_p(24)))      # misaligned q
+    s, c = fresh(); cases.append(both(s, c, mask=None))                  # missing mask
+    for a, b in cases:
+        assert a == b == 1, cases
+    s, c = fresh(); s.batch = 0
+    assert both(s, c) == (0, 0)  # an empty batch is a no-op for both

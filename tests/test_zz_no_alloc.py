@@ -2,15 +2,15 @@
 memory (their memory is owned by their own pool, or their loop must not call cudaMalloc,
 which can synchronize the device). It runs on a fixed scratch array inside the library
 instead of a caller workspace; these tests check that two calls in a row give the same
-results as tsv_tree_verify_attn on the same inputs, and that a shape needing more scratch
-than the array holds is refused."""
+results as tsv_tree_verify_attn on the same inputs and as the fp64 oracle, and that a
+shape needing more scratch than the array holds is refused."""
 import math
 
 import numpy as np
 import pytest
 import torch
 
-from oracle import tree
+from oracle import attention, tree
 from tests import gpu_cases as gc
 
 pytestmark = pytest.mark.gpu
@@ -41,7 +41,17 @@ def inputs(seed, b=2, hq=32, hkv=8, d=128, p_len=1500, n=61, cap=1664):
                 k_new=f(b, n, hkv, d).to(torch.bfloat16).to(dev),
                 v_new=f(b, n, hkv, d).to(torch.bfloat16).to(dev),
                 k=k, v=v, prefix=gc.i32([p_len] * b), nodes=gc.i32([n] * b), pos=gc.i32(pos),
-                mask=torch.from_numpy(mask.view(np.int32)).to(dev), p_len=p_len)
+                mask=torch.from_numpy(mask.view(np.int32)).to(dev), p_len=p_len, parents=parents)
+
+
+def oracle_out(x, b):
+    """The fp64 oracle's attention output of request b (from the bf16 values the call got)."""
+    f64 = lambda t: t.double().cpu().numpy()
+    p_len = x["p_len"]
+    out, _, _ = attention.tree_verify_attention(
+        f64(x["q"][b]), f64(x["k_new"][b]), f64(x["v_new"][b]), f64(x["k"][b, :, :p_len]),
+        f64(x["v"][b, :, :p_len]), list(x["parents"][b]), 1e4, 1 / math.sqrt(x["q"].shape[-1]))
+    return out
 
 
 def run(x, noalloc):
@@ -73,6 +83,11 @@ def test_two_calls_in_a_row_match_the_workspace_call():
         assert diff.max().item() <= gc.BF16_ATOL_MAX
         assert diff.mean().item() <= gc.BF16_ATOL_MEAN
         assert torch.equal(k, ref_k) and torch.equal(v, ref_v)
+        # and directly against the fp64 oracle, every output of every request
+        for b in range(x["q"].shape[0]):
+            want = oracle_out(x, b)
+            d = np.abs(out[b].float().cpu().numpy().astype(np.float64) - want)
+            assert d.max() <= gc.BF16_ATOL_MAX and d.mean() <= gc.BF16_ATOL_MEAN, (d.max(), d.mean())
 
 
 def test_shape_beyond_the_scratch_is_refused():

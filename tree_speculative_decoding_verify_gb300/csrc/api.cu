@@ -91,6 +91,37 @@ namespace {
 inline bool aligned16(const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 }  // namespace
 
+static bool attn_shape_ok(const tsv_attn_shape* s, const tsv_kv_cache* c) {
+  if (!s || !cache_ok(c, false)) return false;
+  if (s->batch < 0 || s->max_nodes < 1 || s->max_nodes > TSV_MAX_NODES || s->max_prefix < 0)
+    return false;
+  if (s->num_q_heads < 1 || s->num_q_heads % c->num_kv_heads) return false;
+  if ((int64_t)s->batch * c->num_kv_heads > 65535) return false;  // grid.y/z limit
+  if ((int64_t)s->max_nodes * (s->num_q_heads / c->num_kv_heads) > 1024) return false;
+  return true;
+}
+
+namespace tsv {
+int attn_call_check(const tsv_attn_shape* shape, const tsv_kv_cache* cache, const void* q,
+                    const void* k_new, const void* v_new, const int32_t* prefix_len,
+                    const int32_t* num_nodes, const int32_t* position_ids, const uint32_t* mask,
+                    float rope_theta, float softmax_scale, const void* out, bool* empty) {
+  *empty = false;
+  if (!attn_shape_ok(shape, cache)) return TSV_ERR_INVALID_ARG;
+  if (!(rope_theta > 0.f) || !(softmax_scale > 0.f)) return TSV_ERR_INVALID_ARG;
+  if (shape->batch == 0) {
+    *empty = true;
+    return TSV_OK;
+  }
+  if (!q || !k_new || !v_new || !prefix_len || !num_nodes || !position_ids || !mask || !out)
+    return TSV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
+    return TSV_ERR_INVALID_ARG;
+  return TSV_OK;
+}
+}  // namespace tsv
+
+
 extern "C" {
 
 const char* tsv_version(void) { return "tsv 0.1.0 (sm_103a)"; }
@@ -234,16 +265,6 @@ int tsv_draft_select_final(const int32_t* store_token, const float* store_score,
                              num_nodes, (cudaStream_t)stream);
 }
 
-static bool attn_shape_ok(const tsv_attn_shape* s, const tsv_kv_cache* c) {
-  if (!s || !cache_ok(c, false)) return false;
-  if (s->batch < 0 || s->max_nodes < 1 || s->max_nodes > TSV_MAX_NODES || s->max_prefix < 0)
-    return false;
-  if (s->num_q_heads < 1 || s->num_q_heads % c->num_kv_heads) return false;
-  if ((int64_t)s->batch * c->num_kv_heads > 65535) return false;  // grid.y/z limit
-  if ((int64_t)s->max_nodes * (s->num_q_heads / c->num_kv_heads) > 1024) return false;
-  return true;
-}
-
 size_t tsv_tree_verify_attn_workspace_size(const tsv_attn_shape* shape,
                                            const tsv_kv_cache* cache) {
   if (!attn_shape_ok(shape, cache)) return 0;
@@ -262,13 +283,10 @@ int tsv_tree_verify_attn(const tsv_attn_shape* shape, const void* q, const void*
                          const int32_t* position_ids, const uint32_t* mask, float rope_theta,
                          float softmax_scale, void* out, void* workspace,
                          size_t workspace_bytes, int32_t* err, tsv_stream_t stream) {
-  if (!attn_shape_ok(shape, cache)) return TSV_ERR_INVALID_ARG;
-  if (!(rope_theta > 0.f) || !(softmax_scale > 0.f)) return TSV_ERR_INVALID_ARG;
-  if (shape->batch == 0) return TSV_OK;
-  if (!q || !k_new || !v_new || !prefix_len || !num_nodes || !position_ids || !mask || !out)
-    return TSV_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out))
-    return TSV_ERR_INVALID_ARG;
+  bool empty = false;
+  const int st = attn_call_check(shape, cache, q, k_new, v_new, prefix_len, num_nodes,
+                                 position_ids, mask, rope_theta, softmax_scale, out, &empty);
+  if (st != TSV_OK || empty) return st;
   const AttnPlan plan = plan_attn(shape, cache);
   if (!workspace || workspace_bytes < plan.ws_bytes ||
       reinterpret_cast<uintptr_t>(workspace) % 256)

@@ -100,6 +100,13 @@ struct AttnPlan {
   size_t off_qrot, off_opart, off_ml, off_valid, ws_bytes;
 };
 AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache);
+// Host checks of every tree-verification attention entry point (shape, cache, pointers,
+// alignment, scalars): TSV_OK or TSV_ERR_INVALID_ARG; *empty is set for a batch of 0
+// (nothing to launch). The workspace is each entry point's own check.
+int attn_call_check(const tsv_attn_shape* shape, const tsv_kv_cache* cache, const void* q,
+                    const void* k_new, const void* v_new, const int32_t* prefix_len,
+                    const int32_t* num_nodes, const int32_t* position_ids, const uint32_t* mask,
+                    float rope_theta, float softmax_scale, const void* out, bool* empty);
 int launch_attn(const AttnPlan& plan, const void* q, const void* k_new, const void* v_new,
                 const tsv_kv_cache* cache, const int32_t* prefix_len, const int32_t* num_nodes,
                 const int32_t* position_ids, const uint32_t* mask, float rope_theta,

@@ -7,6 +7,8 @@
 // latency-critical loop that must not call cudaMalloc (which can synchronize the device)
 // and that cannot size and keep a workspace itself. The array costs every GPU that loads
 // the library TSV_NOALLOC_SCRATCH_BYTES of memory until the process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "attn_common.cuh"
@@ -21,11 +23,42 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[TSV_NOALLOC_SCRATCH_BYTES];
 
 constexpr int MAX_DEVICES = 64;
-void* g_scratch_addr[MAX_DEVICES];
+// Device address of the scratch per device, with the CUDA context it was looked up in: a
+// device reset (or any new context on the device) loads the module again at another
+// address, so a lookup from another context is not reused.
+struct ScratchAddr {
+  CUcontext ctx;
+  void* addr;
+};
+ScratchAddr g_scratch[MAX_DEVICES];
 std::mutex g_scratch_mu;
 
-// Device address of the scratch on the current device (looked up once per device, with
-// that device current). nullptr if the lookup failed.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    cudaGetLastError();
+  }
+  return fn;
+}
+
+CUcontext current_context() {
+  CUcontext c = nullptr;
+  const CtxGetCurrentFn fn = ctx_get_current();
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of the scratch on the current device, looked up with that device current
+// the first time a context uses it. nullptr if the lookup failed.
 void* scratch_address() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
@@ -33,37 +66,19 @@ void* scratch_address() {
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) {
-      record_cuda_error(e);
-      cudaGetLastError();
-      return nullptr;
-    }
-    g_scratch_addr[dev] = p;
+  CUcontext ctx = current_context();
+  if (ctx && g_scratch[dev].addr && g_scratch[dev].ctx == ctx) return g_scratch[dev].addr;
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) {
+    record_cuda_error(e);
+    cudaGetLastError();
+    return nullptr;
   }
-  return g_scratch_addr[dev];
-}
-
-bool shape_ok(const tsv_attn_shape* s, const tsv_kv_cache* c) {
-  if (!s || !c || !c->k || !c->v) return false;
-  if (c->dtype != TSV_DTYPE_F32 && c->dtype != TSV_DTYPE_BF16) return false;
-  if (c->num_kv_heads < 1 || (c->head_dim != 64 && c->head_dim != 128)) return false;
-  if (c->layout == TSV_KV_CONTIGUOUS) {
-    if (c->capacity < TSV_KV_BLOCK || c->capacity % TSV_KV_BLOCK) return false;
-  } else if (c->layout == TSV_KV_PAGED) {
-    if (!c->block_table || c->max_blocks < 1 || c->num_blocks < 1) return false;
-  } else {
-    return false;
-  }
-  if ((reinterpret_cast<uintptr_t>(c->k) | reinterpret_cast<uintptr_t>(c->v)) % 16) return false;
-  if (s->batch < 0 || s->max_nodes < 1 || s->max_nodes > TSV_MAX_NODES || s->max_prefix < 0)
-    return false;
-  if (s->num_q_heads < 1 || s->num_q_heads % c->num_kv_heads) return false;
-  if ((int64_t)s->batch * c->num_kv_heads > 65535) return false;
-  if ((int64_t)s->max_nodes * (s->num_q_heads / c->num_kv_heads) > 1024) return false;
-  return true;
+  // the lookup made the device's primary context current if none was
+  g_scratch[dev].ctx = ctx ? ctx : current_context();
+  g_scratch[dev].addr = p;
+  return p;
 }
 
 }  // namespace
@@ -78,14 +93,11 @@ extern "C" int tsv_tree_verify_attn_noalloc(const tsv_attn_shape* shape, const v
                                             const uint32_t* mask, float rope_theta,
                                             float softmax_scale, void* out, int32_t* err,
                                             tsv_stream_t stream) {
-  if (!shape_ok(shape, cache)) return TSV_ERR_INVALID_ARG;
-  if (!(rope_theta > 0.f) || !(softmax_scale > 0.f)) return TSV_ERR_INVALID_ARG;
-  if (shape->batch == 0) return TSV_OK;
-  if (!q || !k_new || !v_new || !prefix_len || !num_nodes || !position_ids || !mask || !out)
-    return TSV_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_new) |
-       reinterpret_cast<uintptr_t>(v_new) | reinterpret_cast<uintptr_t>(out)) % 16)
-    return TSV_ERR_INVALID_ARG;
+  // the same host checks as tsv_tree_verify_attn
+  bool empty = false;
+  const int st = attn_call_check(shape, cache, q, k_new, v_new, prefix_len, num_nodes,
+                                 position_ids, mask, rope_theta, softmax_scale, out, &empty);
+  if (st != TSV_OK || empty) return st;
   const AttnPlan plan = plan_attn(shape, cache);
   if (plan.ws_bytes > (size_t)TSV_NOALLOC_SCRATCH_BYTES) return TSV_ERR_WORKSPACE;
   void* ws = scratch_address();
