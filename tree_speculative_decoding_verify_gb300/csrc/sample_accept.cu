@@ -555,12 +555,16 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
         u64 thr_p = maxkey;
         float zp = -1.f;
         for (int tries = 0; tries < 3; ++tries) {
+          if (tries == 2) {  // the last try: the exact select over every bin the crossing
+                             // can be in (no gather pass first: its list would be unused)
+            thr_p = radix_select(S, row, V, vec, m, c, 0, bk, thr_k, 1, 0u, target);
+            zp = -1.f;
+            break;
+          }
           int ng;
           const float before = gather_bins(S, row, V, vec, m, c, lo, hi, thr_k, &ng);
-          if (ng > CAP || tries == 2) {  // too many, or the last try: the exact select
-            const bool all = tries == 2;  // (then over every bin the crossing can be in)
-            thr_p = radix_select(S, row, V, vec, m, c, all ? 0 : lo, all ? bk : hi, thr_k, 1,
-                                 0u, all ? target : target - before);
+          if (ng > CAP) {  // too many for the sorted list: the exact select over these bins
+            thr_p = radix_select(S, row, V, vec, m, c, lo, hi, thr_k, 1, 0u, target - before);
             zp = -1.f;
             break;
           }
