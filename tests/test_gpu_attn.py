@@ -209,7 +209,8 @@ def test_long70b_sampled():
     _, parents, _ = gc.oracle_tree(w, 0)
     c = Case([parents] * w.batch, [w.max_prefix] * w.batch, w.num_q_heads, w.num_kv_heads,
              w.head_dim, torch.bfloat16, seed=13)
-    check(c, samples=[(0, 0), (3, 7), (1, 4)])
+    # eight (request, KV head) pairs: every request twice, every KV head once
+    check(c, samples=[(0, 0), (0, 7), (1, 2), (1, 5), (2, 1), (2, 6), (3, 3), (3, 4)])
 
 
 @pytest.mark.parametrize("total", W.SWEEP_TOTAL_TOKENS)
@@ -219,7 +220,8 @@ def test_sweep_sampled(total):
     trees = [gc.random_tree(rng, total + 1, w.depth + 1) for _ in range(w.batch)]
     c = Case(trees, [w.max_prefix] * w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim,
              torch.bfloat16, seed=14)
-    check(c, samples=[(0, 0), (31, 3), (63, 7)])
+    # eight (request, KV head) pairs spread over the batch, every KV head once
+    check(c, samples=[(9 * i, i) for i in range(8)])
 
 
 def test_request_that_does_not_fit_is_rejected_on_device():

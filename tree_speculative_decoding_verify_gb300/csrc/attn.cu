@@ -437,7 +437,8 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
   if (st != TSV_OK) return st;
 
   if (p.tensor_core) {
-    // the split partials are merged inside the kernel (last split of each row block)
+    // tensor-core attention plus, when the plan splits the keys, the separate
+    // warp-per-row split merge kernel
     return launch_attn_tc(p, a, scale_log2, out, stream);
   } else {
     dim3 gs((unsigned)ceil_div(p.rows, SIMT_WARPS), p.nsplit, p.batch * p.hkv);

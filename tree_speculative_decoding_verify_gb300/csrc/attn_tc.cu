@@ -26,10 +26,9 @@
 //   warp 6      relay: arrives on GO for step j once V_j and K_{j+2} have landed (a step
 //               ahead of the softmax: GO alternates between two barriers by step
 //               parity); the four softmax warps arrive on it once P_j is written. The
-//               MMA warp tests that one barrier per step: every test it makes is an issue
-//               gap in which the shallow MMA queue drains, and every mbarrier operation
-//               waits behind the operand traffic of the shared-memory port (a few hundred
-//               cycles), so the critical path softmax -> MMA crosses a single barrier.
+//               MMA warp tests that one barrier per step, between steps: a test's round
+//               trip behind the shared-memory operand traffic (a few hundred cycles)
+//               stalls the warp's issue, so none sits between the MMAs of a step.
 //   warps 0-3   softmax warpgroup; thread = query row = TMEM lane. Each thread first
 //               copies its rotated query row into TMEM. Per tile: one x128 TMEM load of
 //               S_j, the row max over 8 chains, P = exp2(s * scale * log2e - m) rounded to
@@ -256,26 +255,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       __syncwarp();
     };
     // O += P_j V_j over ksteps of 16 keys (V rows 16 ks .. 16 ks + 15: MN-major, 16
-    // rows of 128 bytes per k-step)
-    // Also tests (without waiting) the barrier of the next step before the last k-step
-    // is issued: the test's round trip overlaps the queued MMAs instead of leaving the
-    // tensor pipe idle after them. Returns whether that phase had completed.
-    auto pv = [&](int j, int ksteps, uint32_t next_bar, uint32_t next_parity) {
+    // rows of 128 bytes per k-step). (Testing the next step's barrier between these
+    // MMAs was measured to slow their issue: its shared-memory round trip stalls the
+    // warp.)
+    auto pv = [&](int j, int ksteps) {
       const uint64_t vd = dv + (uint64_t)((j % VST) * TILE_D);
       const uint32_t pa = tmem + TMEM_S + (j & 1) * 128;  // P_j over S_j's buffer
       const uint32_t acc0 = j > 0 ? 1u : 0u;
-      bool next_ready = false;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        if (ks == 7 && next_bar) next_ready = mbar_test(next_bar, next_parity);
+      for (int ks = 0; ks < 8; ++ks)
         if (ks < ksteps && elect_one())
           mma_ts(tmem + TMEM_O, pa + ks * 8, vd + (uint64_t)(ks * 128), ID_PV, ks > 0 ? 1u : acc0);
-      }
       if (elect_one()) {
         mma_commit(bar(BAR_V_EMPTY + j % VST));
         mma_commit(bar(BAR_PV_DONE + (j & 1)));
       }
-      return __all_sync(FULL, next_ready);
+      __syncwarp();
     };
     // S_0 and S_1 first; then step j issues P_j V_j and S_{j+2} = Q K_{j+2}^T, so the
     // softmax always finds the next S computed while it works on the current one
@@ -288,13 +283,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
         qk(1);
       }
     }
-    bool ready = false;  // GO phase j already seen complete
     for (int j = 0; ok && j < n; ++j) {
       // GO phase j: P_j written by the softmax, V_j and K_{j+2} landed
-      if (!ready && !(ok = warp_wait(bar(BAR_GO + (j & 1)), (j >> 1) & 1, abort, true))) break;
+      if (!(ok = warp_wait(bar(BAR_GO + (j & 1)), (j >> 1) & 1, abort, true))) break;
       tc_fence_after();
-      ready = pv(j, (min(KEYS, keys - (t0 + j) * KEYS) + 15) >> 4,
-                 j + 1 < n ? bar(BAR_GO + ((j + 1) & 1)) : 0u, ((j + 1) >> 1) & 1);
+      pv(j, (min(KEYS, keys - (t0 + j) * KEYS) + 15) >> 4);
       if (j + 2 < n) qk(j + 2);
     }
     const bool issuer = lane == 0;
