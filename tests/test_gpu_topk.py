@@ -181,3 +181,28 @@ def test_two_step_units_in_registers(v):
     reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
              for l in range(2)] for _ in range(b)]
     compare(reqs, k)
+
+
+@pytest.mark.parametrize("v,k,b,pad,product", [
+    (40000, 10, 64, 0, False),   # 640 rows: shares of 4.2 rows, rows split between CTAs
+    (40000, 10, 64, 4, True),    # padded (still 16-byte aligned) rows, product scores
+    (32000, 16, 24, 0, False),   # the largest top_k: 384 rows, shares just over a row
+    (40000, 10, 64, 1, False),   # unaligned stride: the per-unit kernel, same layout
+])
+def test_large_batch_shares(v, k, b, pad, product):
+    """Large batches take the persistent kernel (one CTA per SM over an equal share of all
+    rows' entries, so a row may be split between two CTAs); every level is compared with
+    the oracle: tokens, parents and frontier exactly, scores within 1e-5."""
+    rng = np.random.default_rng(v + k + pad)
+    reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
+             for l in range(2)] for _ in range(b)]
+    if product:
+        st, ss, sp, hist = run_levels(reqs, k, stride_pad=pad, product=True)
+        for bi, levels in enumerate(reqs):
+            exp = draft.topk_generate(levels, k, product=True)
+            c = exp.store_token.size
+            np.testing.assert_array_equal(st[bi, :c], exp.store_token)
+            np.testing.assert_array_equal(sp[bi, :c], exp.store_parent)
+            np.testing.assert_allclose(ss[bi, :c], exp.store_score, rtol=gc.SCORE_RTOL, atol=0)
+    else:
+        compare(reqs, k, stride_pad=pad)

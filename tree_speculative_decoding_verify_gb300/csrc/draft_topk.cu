@@ -53,6 +53,19 @@ constexpr int MERGE_SMEM_MAX = TSV_MAX_TOPK * (MAX_CHUNKS + 1) * TSV_MAX_TOPK * 
 // survivors of a unit's finish (value, index): at most 8 register entries per thread
 constexpr int SURV_MAX = 8 * A_THREADS;
 constexpr float L2E = 1.4426950408889634f;
+// Ring of a long unit: thread 0 copies the row chunk into shared memory in stages of four
+// steps (8192 entries, 32 KB) with bulk copies, RING_STAGES ahead; the CTA consumes from
+// shared memory. Units of at least RING_MIN entries on 16-byte aligned rows take it.
+constexpr int RING_STAGES = 3;
+constexpr int STAGE_F4 = 4 * A_THREADS;  // float4 groups per stage
+constexpr int STAGE_ENTRIES = 4 * STAGE_F4;
+constexpr int RING_BYTES = RING_STAGES * STAGE_ENTRIES * 4;
+constexpr int RING_MIN = 2 * STAGE_ENTRIES;
+// Ring of the persistent kernel (large batches): two CTAs per SM, so one CTA's piece
+// finish overlaps the other's streaming.
+constexpr int P_STAGES = 2;
+constexpr int P_CTAS_PER_SM = 2;
+constexpr int MAX_STAGES = P_STAGES > RING_STAGES ? P_STAGES : RING_STAGES;
 
 struct ChunkStat {
   float ref;     // reference (a running maximum)
@@ -203,7 +216,10 @@ struct TopkSmem {
   unsigned long long gkey[A_THREADS / 8];      // best entry of each eight-lane group
   unsigned long long gthr;                     // key() of the best warp threshold
   unsigned long long tau;                      // bound of the unit's top k
+  unsigned long long full[MAX_STAGES];         // ring: stage landed (bulk copy bytes)
+  unsigned long long empty[MAX_STAGES];        // ring: every warp has read the stage
   int ns;                                      // survivors collected
+  int fail;                                    // a ring wait gave up (never expected)
   bool last;
 };
 
@@ -317,21 +333,65 @@ __device__ __forceinline__ void step4(TopkSmem& sm, UnitState& u, int warp, int 
   }
 }
 
-// Seed of the CTA-wide bound: the k-th best of the 64 eight-lane group maxima of the unit's
-// first step (in sm.gkey, as keys with index INT_MAX: a group maximum is an entry of the
-// unit, so k entries are at or above the seed). Run by warp 0; sm.gthr is read after the
-// next barrier.
-__device__ __forceinline__ void seed_threshold(TopkSmem& sm, int lane, int k) {
-  const unsigned long long a0 = sm.gkey[lane], a1 = sm.gkey[lane + 32];
-  int r0 = 0, r1 = 0;
-#pragma unroll 8
-  for (int t = 0; t < A_THREADS / 8; ++t) {
-    const unsigned long long o = sm.gkey[t];
-    r0 += (o > a0 || (o == a0 && t < lane)) ? 1 : 0;
-    r1 += (o > a1 || (o == a1 && t < lane + 32)) ? 1 : 0;
+// The filter half of step4 for a group whose largest entry m4 is known (its exp-sum
+// terms are added by the caller). Warp-uniform call.
+__device__ __forceinline__ void filter4(TopkSmem& sm, UnitState& u, int warp, int lane, int k,
+                                        float4 a, float m4, int e, int end) {
+  const bool q = m4 >= u.thr;
+  const unsigned bal = __ballot_sync(FULL, q);
+  if (bal) {
+    const int n = __popc(bal);
+    if (u.cnt + n > GROUPS) fold(sm, u, warp, lane, k, end);
+    if (q) {
+      const int pos = u.cnt + __popc(bal & ((1u << lane) - 1u));
+      sm.gv[warp][pos] = a;
+      sm.gi[warp][pos] = e;
+    }
+    u.cnt += n;
   }
-  if (r0 == k - 1) sm.gthr = a0;
-  if (r1 == k - 1) sm.gthr = a1;
+}
+
+// Four consecutive steps of a thread (entries e, e + 4 A_THREADS, ...; every entry in
+// range): one raise check and one filter vote for all sixteen entries, the exp-sum terms
+// in the order of four step4 calls, then the group flush. The per-group filter runs only
+// when some lane's sixteen entries reach the filter (rare once the list is full).
+__device__ __forceinline__ void step16(TopkSmem& sm, UnitState& u, int warp, int lane, int k,
+                                       const float4 (&a)[4], int e, int end) {
+  float m[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) m[q] = max4(a[q]);
+  const float m16 = fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+  if (m16 > u.lse.ref + RAISE) u.lse.raise(m16);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    u.lse.g += (u.lse.term(a[q].x) + u.lse.term(a[q].y)) + (u.lse.term(a[q].z) + u.lse.term(a[q].w));
+  u.lse.flush();
+  if (__any_sync(FULL, m16 >= u.thr)) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) filter4(sm, u, warp, lane, k, a[q], m[q], e + 4 * q * A_THREADS, end);
+  }
+}
+
+// The k-th best of 64 keys (ties by position), written to *out by the thread that finds
+// it; the whole CTA takes part: eight threads per key, each comparing it with eight of the
+// 64, their counts added by shuffles. Block-uniform call; *out is read after the next
+// barrier.
+__device__ __forceinline__ void kth_of_64(const unsigned long long* keys, int k,
+                                          unsigned long long* out) {
+  static_assert(A_THREADS == 64 * 8, "eight threads per key");
+  const int t = threadIdx.x >> 3, part = threadIdx.x & 7;
+  const unsigned long long a = keys[t];
+  int r = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int o = part * 8 + u;
+    const unsigned long long b = keys[o];
+    r += (b > a || (b == a && o < t)) ? 1 : 0;
+  }
+  r += __shfl_xor_sync(FULL, r, 1);
+  r += __shfl_xor_sync(FULL, r, 2);
+  r += __shfl_xor_sync(FULL, r, 4);
+  if (part == 0 && r == k - 1) *out = a;
 }
 
 // Starts a unit's per-thread state (sm.gthr was set before the CTA's last barrier).
@@ -352,6 +412,8 @@ struct LevelArgs {
   int64_t row_stride;
   int vocab, rows, k, chunks, chunk_len, level;
   bool product;  // scores: parent score x child probability, else parent + log-probability
+  bool ring;     // the launch has RING_BYTES of dynamic shared memory for long units
+  int rows_total;  // batch * rows
   TopkWs ws;
   const float* front_score_in;
   const int32_t* front_store_in;
@@ -371,15 +433,14 @@ struct LevelArgs {
 // rounds of a warp tournament over list heads, the winning lane stepping its pointer, so
 // no list is held in registers. Out of line: it is rare, and inlined its registers would
 // crowd the streaming loop.
-__device__ __noinline__ void request_merge(const LevelArgs& p, int b) {
-  extern __shared__ float4 dyn_smem[];
+__device__ __noinline__ void request_merge(const LevelArgs& p, int b, float4* stage) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = p.k, rows = p.rows, chunks = p.chunks;
   const int off = p.level == 1 ? 0 : k + (p.level - 2) * k * k;
   const int64_t srow = (int64_t)b * p.store_cap;
   // lists of the request: entry j of (row s, chunk c) at (s * chunks + c) * k + j
   const int n = rows * chunks * k;
-  float* mv = reinterpret_cast<float*>(dyn_smem);
+  float* mv = reinterpret_cast<float*>(stage);
   int* mi = reinterpret_cast<int*>(mv + n);
   // the rows' cumulative scores and tokens (flat = row * k + j); through the declared
   // shared array the compiler emits shared-memory accesses (a generic pointer to the
@@ -485,11 +546,14 @@ __device__ __noinline__ void request_merge(const LevelArgs& p, int b) {
 // of the request to finish (an atomic ticket) then merges the request's rows. Called by
 // the whole CTA; ng is the number of register groups per lane of a short unit (0 when
 // streaming).
+// surv: room for surv_cap survivors; merge_stage: the request merge's staging area.
+// With also_empty the unit also stands for chunk + 1 of its row, which holds no entry
+// (its list is placeholders and its exp-sum zero) and counts on the request's ticket.
 __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int row, int chunk,
-                            int end, int ng, float4 g0, float4 g1, int e0, int e1) {
-  extern __shared__ float4 dyn_smem[];
-  float* sv = reinterpret_cast<float*>(dyn_smem);
-  int* si = reinterpret_cast<int*>(sv + SURV_MAX);
+                            int end, int ng, float4 g0, float4 g1, int e0, int e1, float4* surv,
+                            int surv_cap, float4* merge_stage, bool also_empty = false) {
+  float* sv = reinterpret_cast<float*>(surv);
+  int* si = reinterpret_cast<int*>(sv + surv_cap);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int k = p.k, rows = p.rows, chunks = p.chunks;
   u.lse.flush();
@@ -517,22 +581,8 @@ __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int 
   }
   if (tid == 0) sm.ns = 0;
   __syncthreads();
-  {
-    if (warp == 0) {
-      // rank of each group maximum among the 64 (ties by position); rank k - 1 is tau
-      const unsigned long long a0 = sm.gkey[lane], a1 = sm.gkey[lane + 32];
-      int r0 = 0, r1 = 0;
-#pragma unroll 8
-      for (int t = 0; t < A_THREADS / 8; ++t) {
-        const unsigned long long o = sm.gkey[t];
-        r0 += (o > a0 || (o == a0 && t < lane)) ? 1 : 0;
-        r1 += (o > a1 || (o == a1 && t < lane + 32)) ? 1 : 0;
-      }
-      if (r0 == k - 1) sm.tau = a0;
-      if (r1 == k - 1) sm.tau = a1;
-    }
-    __syncthreads();
-  }
+  kth_of_64(sm.gkey, k, &sm.tau);  // the 64 candidates' k-th best is tau
+  __syncthreads();
   const unsigned long long tau = ng > 0 ? sm.tau : max(sm.tau, sm.gthr);
 
   // survivors, appended with one shared-memory atomic per warp and entry slot
@@ -582,6 +632,20 @@ __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int 
     p.ws.val[base + t] = -INFINITY;
     p.ws.idx[base + t] = INT_MAX;
   }
+  if (also_empty) {
+    for (int t = tid; t < k; t += A_THREADS) {
+      p.ws.val[base + k + t] = -INFINITY;
+      p.ws.idx[base + k + t] = INT_MAX;
+    }
+    if (tid == 0) {
+      ChunkStat cs;
+      cs.ref = -INFINITY;
+      cs.hi = 0.f;
+      cs.lo = 0.f;
+      cs.pad = 0.f;
+      p.ws.stat[(size_t)row * chunks + chunk + 1] = cs;
+    }
+  }
   if (warp == A_WARPS - 1) {  // the block's exp-sum
     float rr = lane < A_WARPS ? sm.red[lane] : -INFINITY;
     float hh = lane < A_WARPS ? sm.shi[lane] : 0.f, ll = lane < A_WARPS ? sm.slo[lane] : 0.f;
@@ -601,19 +665,276 @@ __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int 
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    const unsigned t = atomicAdd(&p.ws.tickets[b], 1u);
-    sm.last = (t == (unsigned)(rows * chunks - 1));
+    const unsigned inc = also_empty ? 2u : 1u;
+    const unsigned t = atomicAdd(&p.ws.tickets[b], inc);
+    sm.last = (t + inc == (unsigned)(rows * chunks));
   }
   __syncthreads();
   if (!sm.last) return;
   __threadfence();
-  griddep_launch();  // the other CTAs have exited: the next kernel may be scheduled
-  request_merge(p, b);
+  griddep_launch();  // the next kernel may be scheduled (it waits for this grid to finish)
+  request_merge(p, b, merge_stage);
+}
+
+// ---- ring of bulk copies ---------------------------------------------------------------
+__device__ __forceinline__ uint32_t sa(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ bool bar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for a ring barrier phase: after about a second (never expected: a bulk
+// copy of this GPU's own memory always lands) the CTA is marked failed and its waits
+// return at once, so the call finishes instead of hanging (the unit's result is then
+// incomplete).
+__device__ bool ring_wait(TopkSmem& sm, uint32_t bar, uint32_t parity) {
+  if (bar_test(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t i = 0;; ++i) {
+    if (bar_test(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&sm.fail)) return false;
+    if ((i & 255u) == 255u) {
+      uint64_t t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > 1000000000ull) {
+        sm.fail = 1;
+        return false;
+      }
+    }
+  }
+}
+// Stage i of the unit's chunk [start, end4) into ring slot i % RING_STAGES (thread 0).
+__device__ __forceinline__ void ring_issue(TopkSmem& sm, uint32_t ring0, const float* x,
+                                           int start, int end4, int i) {
+  const int s = i % RING_STAGES;
+  const int e0 = start + i * STAGE_ENTRIES;
+  const uint32_t bytes = (uint32_t)min(STAGE_ENTRIES, end4 - e0) * 4u;  // a multiple of 16
+  const uint32_t full = sa(&sm.full[s]);
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          ring0 + (uint32_t)s * (STAGE_ENTRIES * 4)),
+      "l"(x + e0), "r"(bytes), "r"(full)
+      : "memory");
+}
+
+// A long unit through the ring: the same per-thread entries, exp-sum grouping and filter
+// as the streaming loop, sixteen entries (four steps) per stage read from shared memory,
+// so the loads hold no registers and never stall the arithmetic.
+__device__ __forceinline__ void stream_ring(TopkSmem& sm, const LevelArgs& p, int row, int chunk,
+                                            int start, int end, const float* x) {
+  extern __shared__ float4 dyn_smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int end4 = start + ((end - start) & ~3);  // entries the bulk copies bring
+  const int nst = (end4 - start + STAGE_ENTRIES - 1) / STAGE_ENTRIES;
+  const uint32_t ring0 = sa(dyn_smem);
+  const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  if (tid == 0) {
+    for (int st = 0; st < RING_STAGES; ++st) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa(&sm.full[st])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.empty[st])),
+                   "r"(A_WARPS)
+                   : "memory");
+    }
+    sm.fail = 0;
+    sm.gthr = 0ull;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int i = 0; i < min(RING_STAGES, nst); ++i) ring_issue(sm, ring0, x, start, end4, i);
+  }
+  __syncthreads();
+  // The first stage: the common starting reference (its largest entry) and the seed of the
+  // CTA-wide bound, the k-th best of the maxima of 64 disjoint groups of 128 entries
+  // (eight threads' sixteen entries each; a group maximum is an entry of the unit, so k
+  // entries are at or above the seed).
+  ring_wait(sm, sa(&sm.full[0]), 0);
+  float first = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (start + 4 * (tid + q * A_THREADS) < end4) first = fmaxf(first, max4(dyn_smem[tid + q * A_THREADS]));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
+  if ((lane & 7) == 0) sm.gkey[tid >> 3] = key(first, INT_MAX);
+#pragma unroll
+  for (int o = 8; o < 32; o <<= 1) first = fmaxf(first, __shfl_xor_sync(FULL, first, o));
+  if (lane == 0) sm.red[warp] = first;
+  __syncthreads();
+  kth_of_64(sm.gkey, p.k, &sm.gthr);
+  first = sm.red[0];
+#pragma unroll
+  for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, sm.red[w]);
+  __syncthreads();  // sm.red is reused by finish_unit; sm.gthr is seeded
+  UnitState u;
+  unit_begin(u, first, sm.gthr);
+  const unsigned long long* gthr = &sm.gthr;
+  for (int i = 0; i < nst; ++i) {
+    const int st = i % RING_STAGES;
+    const uint32_t par = (uint32_t)(i / RING_STAGES) & 1u;
+    const bool ok = i == 0 || ring_wait(sm, sa(&sm.full[st]), par);
+    const float4* stage = dyn_smem + st * STAGE_F4;
+    const int eb = start + i * STAGE_ENTRIES + 4 * tid;  // entry of this thread's first group
+    float4 cur[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) cur[q] = ok && eb + 4 * q * A_THREADS < end4 ? stage[tid + q * A_THREADS] : none;
+    __syncwarp();
+    if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(&sm.empty[st])) : "memory");
+    step16(sm, u, warp, lane, p.k, cur, eb, end);
+    u.thr = fmaxf(u.thr, unord((unsigned)(*reinterpret_cast<const volatile unsigned long long*>(gthr) >> 32)));
+    if (tid == 0 && i + RING_STAGES < nst) {
+      // every warp has read this stage: it takes stage i + RING_STAGES
+      if (ring_wait(sm, sa(&sm.empty[st]), par)) ring_issue(sm, ring0, x, start, end4, i + RING_STAGES);
+    }
+  }
+  // entries past the last group of four (at most three), by warp 0
+  if (warp == 0) {
+    float4 t = none;
+    int e = end;
+    if (lane == 0 && end4 < end) {
+      e = end4;
+      t.x = x[end4];
+      if (end4 + 1 < end) t.y = x[end4 + 1];
+      if (end4 + 2 < end) t.z = x[end4 + 2];
+    }
+    step4(sm, u, warp, lane, p.k, t, e, end);
+  }
+  finish_unit(sm, u, p, row, chunk, end, 0, none, none, end, end, dyn_smem, SURV_MAX, dyn_smem);
+}
+
+
+// ---- large batches: persistent CTAs (two per SM), each over an equal share of all entries
+// The rows' entries, laid end to end (row r at r * V), are cut into one contiguous share
+// per CTA (multiples of four entries; each share at least a row long, so a row lies in at
+// most two shares: its first piece is chunk 0 of the workspace, a second piece chunk 1).
+// A CTA streams its pieces in order through one ring of P_STAGES bulk-copy stages
+// (thread 0 issues them), so the copies of the next piece keep flowing while a piece is
+// finished; every piece is a unit like those of topk_level_kernel (same entry order per
+// thread, exp-sum grouping, filter, finish and request merge). A row that lies wholly in
+// one share also accounts for its empty chunk 1.
+constexpr int P_SURV = A_WARPS * KMAX;  // survivors of a streamed unit: the warp lists
+constexpr int P_RING_BYTES = P_STAGES * STAGE_ENTRIES * 4;
+
+// Share [lo, hi) of CTA c among g (flat entry indices, multiples of four).
+__host__ __device__ inline void share_of(int64_t total, int g, int c, int64_t* lo, int64_t* hi) {
+  *lo = ((int64_t)c * total / g) & ~(int64_t)3;
+  *hi = c + 1 == g ? total : (((int64_t)(c + 1) * total / g) & ~(int64_t)3);
+}
+
+__global__ void __launch_bounds__(A_THREADS, 2) topk_stream_kernel(const LevelArgs p) {
+  extern __shared__ float4 dyn_smem[];
+  __shared__ TopkSmem sm;
+  griddep_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = p.vocab;
+  int64_t lo, hi;
+  share_of((int64_t)p.rows_total * V, gridDim.x, blockIdx.x, &lo, &hi);
+  float4* ring = dyn_smem;
+  float4* surv = dyn_smem + P_RING_BYTES / 16;
+  float4* mstage = surv + P_SURV * 8 / 16;
+  const uint32_t ring0 = sa(ring);
+  const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  const int r_first = (int)(lo / V), r_last = hi > lo ? (int)((hi - 1) / V) : r_first - 1;
+  // piece of row r inside the share: entries [e0, e1) of the row
+  auto piece = [&](int r, int* e0, int* e1) {
+    const int64_t a = lo - (int64_t)r * V, z = hi - (int64_t)r * V;
+    *e0 = a > 0 ? (int)a : 0;
+    *e1 = z < V ? (int)z : V;
+  };
+  // producer cursor (thread 0): the next stage to copy starts at entry pe of row pr
+  int pr = r_first, pe = 0, pe1 = 0;
+  if (pr <= r_last) piece(pr, &pe, &pe1);
+  int64_t issued = 0;  // stages copied so far (global sequence)
+  auto issue_next = [&]() {  // thread 0: copy the stage at the cursor, advance it
+    if (pr > r_last) return;
+    const int st = (int)(issued % P_STAGES);
+    const uint32_t bytes = (uint32_t)min(STAGE_ENTRIES, pe1 - pe) * 4u;  // a multiple of 16
+    const uint32_t fb = sa(&sm.full[st]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            ring0 + (uint32_t)st * (STAGE_ENTRIES * 4)),
+        "l"(p.logits + (int64_t)pr * p.row_stride + pe), "r"(bytes), "r"(fb)
+        : "memory");
+    ++issued;
+    pe += STAGE_ENTRIES;
+    if (pe >= pe1 && ++pr <= r_last) piece(pr, &pe, &pe1);
+  };
+  if (tid == 0) {
+    for (int st = 0; st < P_STAGES; ++st) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa(&sm.full[st])) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(&sm.empty[st])),
+                   "r"(A_WARPS)
+                   : "memory");
+    }
+    sm.fail = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int i = 0; i < P_STAGES; ++i) issue_next();
+  }
+  __syncthreads();
+  int64_t g = 0;  // global index of the next stage to consume
+  for (int r = r_first; r <= r_last; ++r) {
+    int e0, e1;
+    piece(r, &e0, &e1);
+    const int nst = (e1 - e0 + STAGE_ENTRIES - 1) / STAGE_ENTRIES;
+    // the piece's first stage: starting reference and seed of the CTA-wide bound
+    {
+      const int st = (int)(g % P_STAGES);
+      ring_wait(sm, sa(&sm.full[st]), (uint32_t)(g / P_STAGES) & 1u);
+      const float4* stage = ring + st * STAGE_F4;
+      float m = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (e0 + 4 * (tid + q * A_THREADS) < e1) m = fmaxf(m, max4(stage[tid + q * A_THREADS]));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+      if ((lane & 7) == 0) sm.gkey[tid >> 3] = key(m, INT_MAX);
+#pragma unroll
+      for (int o = 8; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+      if (lane == 0) sm.red[warp] = m;
+      if (tid == 0) sm.gthr = 0ull;
+      __syncthreads();
+      kth_of_64(sm.gkey, p.k, &sm.gthr);
+    }
+    float first = sm.red[0];
+#pragma unroll
+    for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, sm.red[w]);
+    __syncthreads();  // sm.red is reused by the finish; sm.gthr is seeded
+    UnitState u;
+    unit_begin(u, first, sm.gthr);
+    const unsigned long long* gthr = &sm.gthr;
+    for (int i = 0; i < nst; ++i, ++g) {
+      const int st = (int)(g % P_STAGES);
+      const uint32_t par = (uint32_t)(g / P_STAGES) & 1u;
+      const bool ok = i == 0 || ring_wait(sm, sa(&sm.full[st]), par);
+      const float4* stage = ring + st * STAGE_F4;
+      const int eb = e0 + i * STAGE_ENTRIES + 4 * tid;
+      float4 cur[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cur[q] = ok && eb + 4 * q * A_THREADS < e1 ? stage[tid + q * A_THREADS] : none;
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(&sm.empty[st])) : "memory");
+      step16(sm, u, warp, lane, p.k, cur, eb, e1);
+      u.thr = fmaxf(u.thr, unord((unsigned)(*reinterpret_cast<const volatile unsigned long long*>(gthr) >> 32)));
+      if (tid == 0 && pr <= r_last) {
+        // every warp has read stage g: its slot takes the next stage at the cursor
+        if (ring_wait(sm, sa(&sm.empty[st]), par)) issue_next();
+      }
+    }
+    finish_unit(sm, u, p, r, e0 == 0 ? 0 : 1, e1, 0, none, none, e1, e1, surv, P_SURV, mstage,
+                e0 == 0 && e1 == V);
+  }
 }
 
 // ---- streaming: one (row, chunk) unit per CTA -----------------------------------------
 __global__ void __launch_bounds__(A_THREADS, CTAS_PER_SM)
 topk_level_kernel(const LevelArgs p, bool vec) {
+  extern __shared__ float4 dyn_smem[];
   __shared__ TopkSmem sm;
   griddep_wait();
   const int row = blockIdx.y, chunk = blockIdx.x;
@@ -621,6 +942,10 @@ topk_level_kernel(const LevelArgs p, bool vec) {
   const float* x = p.logits + (int64_t)row * p.row_stride;
   const int start = chunk * p.chunk_len;
   const int end = min(p.vocab, start + p.chunk_len);
+  if (p.ring && vec && end - start >= RING_MIN) {
+    stream_ring(sm, p, row, chunk, start, end, x);
+    return;
+  }
 
   // Every thread takes 4 consecutive entries per step (one 128-bit load when the row is
   // 16-byte aligned), up to three steps prefetched ahead.
@@ -651,7 +976,7 @@ topk_level_kernel(const LevelArgs p, bool vec) {
   if (lane == 0) sm.red[warp] = first;
   if (tid == 0) sm.gthr = 0ull;
   __syncthreads();
-  if (warp == 0 && steps > 2) seed_threshold(sm, lane, p.k);
+  if (steps > 2) kth_of_64(sm.gkey, p.k, &sm.gthr);
   first = sm.red[0];
 #pragma unroll
   for (int w = 1; w < A_WARPS; ++w) first = fmaxf(first, sm.red[w]);
@@ -664,14 +989,15 @@ topk_level_kernel(const LevelArgs p, bool vec) {
     // short unit (one or two steps): every entry stays in registers for the finish
     lse4(u, a, max4(a));
     if (steps == 2) lse4(u, bnext, max4(bnext));
-    finish_unit(sm, u, p, row, chunk, end, steps, a, bnext, e0, e0 + 4 * A_THREADS);
+    finish_unit(sm, u, p, row, chunk, end, steps, a, bnext, e0, e0 + 4 * A_THREADS, dyn_smem,
+                SURV_MAX, dyn_smem);
     return;
   }
-  // Two steps in flight (32 KB per SM with two resident CTAs; a third did not raise the
-  // rate: the loop is bound by instructions, not by latency). Every fourth step the
-  // exp-sum group (16 terms) is flushed and the filter takes up the CTA-wide bound.
   const unsigned long long* gthr = &sm.gthr;
-  for (int it = 0; it < steps; ++it) {
+  int it = 0;
+  // Two steps in flight. Every fourth step the exp-sum group (16 terms) is flushed and
+  // the filter takes up the CTA-wide bound.
+  for (; it < steps; ++it) {
     const float4 c = it + 2 < steps ? load4(it + 2) : none;
     step4(sm, u, warp, lane, p.k, a, e0 + 4 * it * A_THREADS, end);
     a = bnext;
@@ -681,7 +1007,7 @@ topk_level_kernel(const LevelArgs p, bool vec) {
       u.thr = fmaxf(u.thr, unord((unsigned)(*reinterpret_cast<const volatile unsigned long long*>(gthr) >> 32)));
     }
   }
-  finish_unit(sm, u, p, row, chunk, end, 0, none, none, end, end);
+  finish_unit(sm, u, p, row, chunk, end, 0, none, none, end, end, dyn_smem, SURV_MAX, dyn_smem);
 }
 
 // ---- final selection --------------------------------------------------------------
@@ -806,6 +1132,22 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
 TopkPlan plan_topk(int batch, int rows, int vocab, int top_k) {
   TopkPlan p{};
   const int64_t rows_total = (int64_t)batch * rows;
+  // Large batches: the persistent kernel, one CTA per SM, when every share is at least a
+  // row long (with room for the rounding to four entries) and rows are whole groups of
+  // four entries; chunks = 2 gives each row two workspace slots (its at most two pieces),
+  // and chunk_len lets the per-unit kernel use the same layout should the logits turn
+  // out not to be 16-byte aligned.
+  const int64_t shares = (int64_t)P_CTAS_PER_SM * device_sm_count();
+  if (vocab % 4 == 0 && vocab >= RING_MIN && shares > 0 &&
+      rows_total * vocab / shares - 8 >= vocab) {
+    p.persistent = true;
+    p.chunks = 2;
+    p.chunk_len = (int)round_up(ceil_div(vocab, 2), 4);
+    const size_t n = (size_t)rows_total * p.chunks;
+    p.ws_bytes = align256((size_t)batch * sizeof(unsigned)) + align256(n * sizeof(ChunkStat)) +
+                 align256(n * top_k * sizeof(float)) + align256(n * top_k * sizeof(int32_t));
+    return p;
+  }
   // Chunks per row: the count with the shortest estimated makespan, waves of resident CTAs
   // x (chunk length + a fixed cost per unit of about FIX_ENTRIES entries' streaming time:
   // start, finish and merge).
@@ -858,15 +1200,35 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
   p.front_score_out = front_score_out;
   p.front_store_out = front_store_out;
   const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (row_stride % 4 == 0);
-  dim3 grid(plan.chunks, rows_total);
-  const size_t smem = std::max<size_t>((size_t)SURV_MAX * 8,
-                                       (size_t)rows * (plan.chunks + 1) * top_k * 8);
-  static bool attr_set[64] = {};
+  p.ring = vec && plan.chunk_len >= RING_MIN;
+  p.rows_total = rows_total;
   int dev = 0;
   cudaGetDevice(&dev);
+  if (plan.persistent && vec) {
+    // ring, survivors, and the request merge's staging for two slots per row
+    constexpr size_t P_MERGE_MAX = (size_t)TSV_MAX_TOPK * 3 * TSV_MAX_TOPK * 8;
+    constexpr size_t P_SMEM_MAX = (size_t)P_RING_BYTES + (size_t)P_SURV * 8 + P_MERGE_MAX;
+    const size_t psmem = (size_t)P_RING_BYTES + (size_t)P_SURV * 8 +
+                         (size_t)rows * (plan.chunks + 1) * top_k * 8;
+    static bool pattr_set[64] = {};
+    if (dev < 0 || dev >= 64) return TSV_ERR_UNSUPPORTED;
+    if (!pattr_set[dev]) {
+      if (cudaFuncSetAttribute(topk_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)P_SMEM_MAX) != cudaSuccess)
+        return launch_status();
+      pattr_set[dev] = true;
+    }
+    return launch_pdl(topk_stream_kernel, dim3(P_CTAS_PER_SM * device_sm_count()), dim3(A_THREADS),
+                      psmem, stream, p);
+  }
+  dim3 grid(plan.chunks, rows_total);
+  const size_t smem = std::max<size_t>({(size_t)SURV_MAX * 8,
+                                        (size_t)rows * (plan.chunks + 1) * top_k * 8,
+                                        p.ring ? (size_t)RING_BYTES : (size_t)0});
+  static bool attr_set[64] = {};
   if (smem > 48 * 1024 && dev >= 0 && dev < 64 && !attr_set[dev]) {
     if (cudaFuncSetAttribute(topk_level_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             std::max(MERGE_SMEM_MAX, SURV_MAX * 8)) != cudaSuccess)
+                             std::max({MERGE_SMEM_MAX, SURV_MAX * 8, RING_BYTES})) != cudaSuccess)
       return launch_status();
     attr_set[dev] = true;
   }

@@ -62,8 +62,9 @@ int launch_sample_accept(const SampleArgs& a, const tsv_kv_cache* cache, int32_t
 
 // Draft expansion.
 struct TopkPlan {
-  int chunks;         // CTAs per row in the streaming stage
+  int chunks;         // CTAs per row in the streaming stage (workspace slots per row)
   int chunk_len;      // vocab entries per chunk (multiple of 4)
+  bool persistent;    // large batch: one CTA per SM over equal shares of all entries
   size_t ws_bytes;
 };
 TopkPlan plan_topk(int batch, int rows, int vocab, int top_k);
