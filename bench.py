@@ -642,6 +642,18 @@ def native(args):
     # the dominant kernel of the step: the attention call or the depth + 1 top-k levels
     dominant = "topk" if ms["topk"] * (w.depth + 1) > ms["attn"] else "attn"
     kernels_step = hp.kernels_per_step()
+    # one expansion level ([B, K, V] rows): one kernel, or two for a large batch
+    lvl_launches = T.draft_topk_expand_launches(b, k, v, k)
+
+    def side_launches(sd):
+        sw = sd["w"]
+        n = 0
+        for leg in sd["fns"]:
+            if leg.startswith("attn_"):
+                n += sd["attn_launches"]
+            else:
+                n += T.draft_topk_expand_launches(sw.batch, sw.top_k, sw.vocab, sw.top_k)
+        return n
     attn_kernels = hp.attn_kernels()
     line = {
         "metric": METRIC, "value": world * 1e3 / step_ms, "unit": UNIT, "n_gpus": world,
@@ -677,13 +689,11 @@ def native(args):
         # timed region per iteration: the step graph, the attention call, one top-k level,
         # the lm-head argmax (GEMM + finalize), the non-greedy acceptance (filter, walk,
         # compaction), a product-score level, the d2t map and a fixed level, the drafter's
-        # grown mask and its attention
-        "gpu_launches": args.steps * (kernels_step + attn_kernels + 1 + 2 + 3 + 1 + 2 + 1 +
+        # grown mask and its attention, and the side legs
+        "gpu_launches": args.steps * (kernels_step + attn_kernels + 2 * lvl_launches + 2 + 3 + 2 + 1 +
                                       T.tree_verify_attn_launches(
                                           (b, dn, w.num_q_heads, w.head_dim), cache, p_max) +
-                                      sum(sd["attn_launches"] * any(n.startswith("attn_") for n in sd["fns"]) +
-                                          sum(n.startswith("topk_") for n in sd["fns"])
-                                          for sd in sides.values())),
+                                      sum(side_launches(sd) for sd in sides.values())),
         "wall_s_timed_region": t_wall,
     }
     for name, sd in sides.items():

@@ -159,6 +159,11 @@ int tsv_last_cuda_error(void);
  * this level, or rows inconsistent with level.
  * ------------------------------------------------------------------------------ */
 size_t tsv_draft_topk_expand_workspace_size(int batch, int rows, int vocab, int top_k);
+/* Kernels one tsv_draft_topk_expand (or _product) call of this shape launches on its stream
+ * when the logits rows are 16-byte aligned: 1, or 2 for a large batch (the streaming
+ * kernel over equal shares of all rows, then one merge per request). 0 for a shape the
+ * call rejects. Host only, no device work. */
+int tsv_draft_topk_expand_launches(int batch, int rows, int vocab, int top_k);
 int tsv_draft_topk_expand(const float* logits, int batch, int rows, int64_t row_stride,
                           int vocab, int top_k, int level, const float* front_score_in,
                           const int32_t* front_store_in, int store_cap, int32_t* store_token,

@@ -58,6 +58,7 @@ _SIGNATURES = {
     "tsv_draft_grow_mask": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 +
                             [ctypes.c_void_p] * 2),
     "tsv_draft_topk_expand_workspace_size": (ctypes.c_size_t, [ctypes.c_int] * 4),
+    "tsv_draft_topk_expand_launches": (ctypes.c_int, [ctypes.c_int] * 4),
     "tsv_draft_topk_expand": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
@@ -241,6 +242,11 @@ def draft_grow_mask(mask, position_ids, new_parents, prefix_len, first_new, err=
 
 def draft_topk_expand_workspace_size(batch, rows, vocab, top_k) -> int:
     return int(lib().tsv_draft_topk_expand_workspace_size(batch, rows, vocab, top_k))
+
+
+def draft_topk_expand_launches(batch, rows, vocab, top_k) -> int:
+    """Kernels one expansion level of this shape launches (16-byte aligned rows)."""
+    return int(lib().tsv_draft_topk_expand_launches(batch, rows, vocab, top_k))
 
 
 def draft_topk_expand(logits, top_k, level, front_score_in, front_store_in, store_token,

@@ -173,6 +173,11 @@ size_t tsv_draft_topk_expand_workspace_size(int batch, int rows, int vocab, int 
   return plan_topk(batch, rows, vocab, top_k).ws_bytes;
 }
 
+int tsv_draft_topk_expand_launches(int batch, int rows, int vocab, int top_k) {
+  if (batch < 1 || rows < 1 || vocab < 1 || top_k < 1 || top_k > TSV_MAX_TOPK) return 0;
+  return plan_topk(batch, rows, vocab, top_k).persistent ? 2 : 1;
+}
+
 static int topk_expand(const float* logits, int batch, int rows, int64_t row_stride, int vocab,
                        int top_k, int level, const float* front_score_in,
                        const int32_t* front_store_in, int store_cap, int32_t* store_token,

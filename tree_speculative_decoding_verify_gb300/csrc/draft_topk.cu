@@ -63,7 +63,7 @@ constexpr int RING_BYTES = RING_STAGES * STAGE_ENTRIES * 4;
 constexpr int RING_MIN = 2 * STAGE_ENTRIES;
 // Ring of the persistent kernel (large batches): two CTAs per SM, so one CTA's piece
 // finish overlaps the other's streaming.
-constexpr int P_STAGES = 2;
+constexpr int P_STAGES = 3;
 constexpr int P_CTAS_PER_SM = 2;
 constexpr int MAX_STAGES = P_STAGES > RING_STAGES ? P_STAGES : RING_STAGES;
 
@@ -549,9 +549,11 @@ __device__ __noinline__ void request_merge(const LevelArgs& p, int b, float4* st
 // surv: room for surv_cap survivors; merge_stage: the request merge's staging area.
 // With also_empty the unit also stands for chunk + 1 of its row, which holds no entry
 // (its list is placeholders and its exp-sum zero) and counts on the request's ticket.
+// Without merge_here the request merge is left to topk_merge_kernel (no ticket).
 __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int row, int chunk,
                             int end, int ng, float4 g0, float4 g1, int e0, int e1, float4* surv,
-                            int surv_cap, float4* merge_stage, bool also_empty = false) {
+                            int surv_cap, float4* merge_stage, bool also_empty = false,
+                            bool merge_here = true) {
   float* sv = reinterpret_cast<float*>(surv);
   int* si = reinterpret_cast<int*>(sv + surv_cap);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -663,6 +665,7 @@ __device__ void finish_unit(TopkSmem& sm, UnitState& u, const LevelArgs& p, int 
   // The last unit of this request to finish merges its rows and runs the joint top-K.
   const int b = row / rows;
   __syncthreads();
+  if (!merge_here) return;  // every thread: the list and stat buffers are free again
   if (tid == 0) {
     __threadfence();
     const unsigned inc = also_empty ? 2u : 1u;
@@ -927,8 +930,16 @@ __global__ void __launch_bounds__(A_THREADS, 2) topk_stream_kernel(const LevelAr
       }
     }
     finish_unit(sm, u, p, r, e0 == 0 ? 0 : 1, e1, 0, none, none, e1, e1, surv, P_SURV, mstage,
-                e0 == 0 && e1 == V);
+                e0 == 0 && e1 == V, false);
   }
+  griddep_launch();  // the merge kernel may be scheduled (it waits for this grid)
+}
+
+// The request merges of the persistent kernel's level, one CTA per request, after it.
+__global__ void __launch_bounds__(A_THREADS) topk_merge_kernel(const LevelArgs p) {
+  extern __shared__ float4 dyn_smem[];
+  griddep_wait();
+  request_merge(p, blockIdx.x, dyn_smem);
 }
 
 // ---- streaming: one (row, chunk) unit per CTA -----------------------------------------
@@ -1208,8 +1219,7 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
     // ring, survivors, and the request merge's staging for two slots per row
     constexpr size_t P_MERGE_MAX = (size_t)TSV_MAX_TOPK * 3 * TSV_MAX_TOPK * 8;
     constexpr size_t P_SMEM_MAX = (size_t)P_RING_BYTES + (size_t)P_SURV * 8 + P_MERGE_MAX;
-    const size_t psmem = (size_t)P_RING_BYTES + (size_t)P_SURV * 8 +
-                         (size_t)rows * (plan.chunks + 1) * top_k * 8;
+    const size_t psmem = (size_t)P_RING_BYTES + (size_t)P_SURV * 8;
     static bool pattr_set[64] = {};
     if (dev < 0 || dev >= 64) return TSV_ERR_UNSUPPORTED;
     if (!pattr_set[dev]) {
@@ -1218,8 +1228,11 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
         return launch_status();
       pattr_set[dev] = true;
     }
-    return launch_pdl(topk_stream_kernel, dim3(P_CTAS_PER_SM * device_sm_count()), dim3(A_THREADS),
-                      psmem, stream, p);
+    const int st = launch_pdl(topk_stream_kernel, dim3(P_CTAS_PER_SM * device_sm_count()),
+                              dim3(A_THREADS), psmem, stream, p);
+    if (st != TSV_OK) return st;
+    return launch_pdl(topk_merge_kernel, dim3(batch), dim3(A_THREADS),
+                      (size_t)rows * (plan.chunks + 1) * top_k * 8, stream, p);
   }
   dim3 grid(plan.chunks, rows_total);
   const size_t smem = std::max<size_t>({(size_t)SURV_MAX * 8,

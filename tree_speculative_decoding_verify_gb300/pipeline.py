@@ -229,10 +229,14 @@ class HotPath:
 
     # launches of libtsv kernels per step (for the bench's launch count)
     def kernels_per_step(self, lm_head: bool = False) -> int:
-        """libtsv kernels one step launches: one per expansion level, the final
-        selection, the metadata, the attention call, the lm_head stage (GEMM + finalize)
-        when it runs, and the acceptance."""
-        n = 0 if self.s.fixed_nodes else (self.s.depth + 1) + 1
+        """libtsv kernels one step launches: one or two per expansion level (two for a
+        large batch: streaming + merge), the final selection, the metadata, the attention
+        call, the lm_head stage (GEMM + finalize) when it runs, and the acceptance."""
+        n = 0
+        if not self.s.fixed_nodes:
+            s = self.s
+            n = sum(_lib.draft_topk_expand_launches(s.batch, 1 if lvl == 0 else s.top_k, s.vocab,
+                                                    s.top_k) for lvl in range(s.depth + 1)) + 1
         return n + 1 + self.attn_kernels() + (2 if lm_head else 0) + 1
 
     def attn_kernels(self) -> int:
