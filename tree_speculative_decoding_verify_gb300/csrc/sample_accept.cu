@@ -364,6 +364,11 @@ __device__ u64 radix_select(FilterSmem& S, const float* row, int V, bool vec, fl
                             int lo, int hi, u64 kmin, int mode, unsigned want, float target) {
   unsigned* hc = reinterpret_cast<unsigned*>(S.lkey);  // 256-entry histograms
   float* hm = S.lmass;
+  // every thread has read the shared results of the step before (the gathered count in
+  // S.s_n, the crossing mass in S.s_f) before thread 0 overwrites them: without this
+  // barrier a late reader could see the new values and take another branch of the
+  // block-uniform control flow
+  __syncthreads();
   if (threadIdx.x == 0) {
     S.s_prefix = 0ull;
     S.s_n = (int)want;
