@@ -19,10 +19,13 @@
 //                 S_{j+2} = Q K_{j+2}^T     A = Q in TMEM, B = K (shared, K-major)
 //               once the softmax has written P_j. S is double-buffered and P_j is
 //               written over the first half of S_j's buffer, so the softmax always finds
-//               the next S computed while it works on the current tile, and the tensor
-//               pipe always has the next P V and Q K^T queued (its in-order execution
-//               keeps S_{j+2} from overwriting P_j before P_j V_j has read it). Q and P
-//               come from TMEM: the shared-memory port carries only the K and V tiles.
+//               the next S computed while it works on the current tile. Only MMAs into
+//               the same accumulator are guaranteed to execute in issue order: S_{j+2}
+//               (accumulator S) may otherwise overlap P_j V_j (accumulator O) and write
+//               over P_j while it is being read, so the warp waits for P_j V_j's
+//               completion before it issues S_{j+2} (hidden: S_{j+2} is needed a whole
+//               tile later). Q and P come from TMEM: the shared-memory port carries only
+//               the K and V tiles.
 //   warp 6      relay: arrives on GO for step j once V_j and K_{j+2} have landed (a step
 //               ahead of the softmax: GO alternates between two barriers by step
 //               parity); the four softmax warps arrive on it once P_j is written. The
@@ -240,8 +243,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
     // k-step ks of a K-major operand: 16 columns = 32 bytes inside a 64-column panel
     auto kmaj = [](int ks) -> uint64_t { return (uint64_t)((ks >> 2) * (HALF >> 4) + (ks & 3) * 2); };
     // S_j = Q K_j^T into S buffer j % 2; A = Q in TMEM (8 columns = 16 bf16 per k-step).
-    // The buffer held P_{j-2}: P_{j-2} V_{j-2} was issued before, and the tensor pipe
-    // executes in order.
+    // The buffer held P_{j-2}: the caller has seen P_{j-2} V_{j-2} complete.
     auto qk = [&](int j) {
       const uint64_t kd = dk + (uint64_t)((j % KST) * TILE_D);
       const uint32_t sd = tmem + TMEM_S + (j & 1) * 128;
@@ -288,7 +290,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__
       if (!(ok = warp_wait(bar(BAR_GO + (j & 1)), (j >> 1) & 1, abort, true))) break;
       tc_fence_after();
       pv(j, (min(KEYS, keys - (t0 + j) * KEYS) + 15) >> 4);
-      if (j + 2 < n) qk(j + 2);
+      if (j + 2 < n) {
+        // S_{j+2} goes into the buffer that holds P_j, and MMAs into different
+        // accumulators are not ordered: P_j V_j has finished reading P_j first
+        if (!(ok = warp_wait(bar(BAR_PV_DONE + (j & 1)), (j >> 1) & 1, abort, true))) break;
+        tc_fence_after();
+        qk(j + 2);
+      }
     }
     const bool issuer = lane == 0;
     if (issuer) {
