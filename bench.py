@@ -354,7 +354,9 @@ def native(args):
     root = torch.from_numpy(W.root_tokens(w)).to(dev)
     q, k_new, v_new = (torch.from_numpy(x).to(torch.bfloat16).to(dev) for x in W.new_qkv(w))
     t_max = w.num_nodes
-    cap = int(math.ceil((p_max + t_max + 16) / 64) * 64)
+    # room for the verified tree and for the drafter leg's grown tree (1 + K (depth + 1)
+    # nodes), each rounded up to 16 slots past the prefix
+    cap = int(math.ceil((p_max + max(t_max, 1 + k * (w.depth + 1)) + 16) / 64) * 64)
     scale = w.scale
     cache = kv_cache(w, dev, gen, T, cap)
     shape = T.TreeShape(b, w.num_q_heads, w.num_kv_heads, w.head_dim, p_max, vocab=v, top_k=k,
