@@ -1,6 +1,7 @@
 // Tree-verification attention: RoPE + KV append (prep), split-KV partial attention
-// (CUDA-core path here; the tcgen05 tensor-core path lives in attn_tc.cu) and the
-// log-sum-exp merge of the split partials.
+// (CUDA-core path here; the bf16 tensor-core paths live in attn_umma.cu and
+// attn_mma.cu) and the
+// log-sum-exp merges of the split partials.
 //
 // Pages: "推理系统手册 · 投机解码进阶：树形草稿与 EAGLE", section 实现 (forward_with_mask:
 // every node attends to the whole committed prefix and, among the tree nodes, to its
@@ -319,7 +320,72 @@ merge_kernel(AttnArgs a, T* __restrict__ out) {
   }
 }
 
+// ---- split merge of the bf16 tensor-core paths: one warp per query row -------------
+// Combines the key splits of the rows whose request took more than one split: lane s
+// holds split s's (m, l) (m in log2 units), the warp forms the log-sum-exp weights
+// w_s = 2^(m_s - M) / L, and lane c accumulates output columns 4c .. 4c + 3 over the splits
+// (eight partial loads in flight), written as bf16. Rows of a single-split request were
+// written by the attention kernel itself; rows past the tree were zeroed by the prep.
+constexpr int SMERGE_ROWS = 8;  // warps (query rows) per CTA
+
+__global__ void __launch_bounds__(SMERGE_ROWS * 32)
+split_merge_kernel(const AttnArgs a, __nv_bfloat16* __restrict__ out) {
+  griddep_wait();
+  griddep_launch();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = blockIdx.x * SMERGE_ROWS + warp;
+  const int b = blockIdx.y / a.hkv, h = blockIdx.y % a.hkv;
+  if (!a.valid[b]) return;
+  const int T = a.num_nodes[b], P = a.prefix_len[b];
+  if (r >= T * a.group) return;
+  const int n_tiles = (P + T + a.tile_keys - 1) / a.tile_keys;
+  const int nsp = (n_tiles + a.tiles_per_split - 1) / a.tiles_per_split;
+  if (nsp <= 1) return;
+  const int64_t pbase = ((int64_t)b * a.hkv + h) * a.nsplit;
+  float2 ml = make_float2(-INFINITY, 0.f);
+  if (lane < nsp) ml = reinterpret_cast<const float2*>(a.ml)[(pbase + lane) * a.rows_pad + r];
+  float M = ml.x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+  const float e = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+  float L = ml.y * e;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(FULL, L, o);
+  const float w = L > 0.f ? e / L : 0.f;  // this lane's split weight
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4* src = reinterpret_cast<const float4*>(a.o_part) + (pbase * a.rows_pad + r) * 32 + lane;
+  const int64_t stride = (int64_t)a.rows_pad * 32;  // float4s between splits
+  for (int s0 = 0; s0 < nsp; s0 += 8) {
+    float4 x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      x[u] = s0 + u < nsp ? __ldcg(src + (s0 + u) * stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float ws = __shfl_sync(FULL, w, (s0 + u) & 31);
+      if (s0 + u < nsp && ws != 0.f) {  // a split with no visible key holds no partial
+        acc.x += ws * x[u].x;
+        acc.y += ws * x[u].y;
+        acc.z += ws * x[u].z;
+        acc.w += ws * x[u].w;
+      }
+    }
+  }
+  const int node = r / a.group;
+  __nv_bfloat16* dst = out + (((int64_t)b * a.max_nodes + node) * a.hq + h * a.group + r % a.group) * 128;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  reinterpret_cast<uint2*>(dst)[lane] =
+      make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+}
+
 }  // namespace
+
+int launch_split_merge(const AttnPlan& p, const AttnArgs& a, void* out, cudaStream_t stream) {
+  dim3 gm((unsigned)ceil_div(p.rows, SMERGE_ROWS), p.batch * p.hkv);
+  return launch_pdl(split_merge_kernel, gm, dim3(SMERGE_ROWS * 32), 0, stream, a,
+                    static_cast<__nv_bfloat16*>(out));
+}
 
 AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache) {
   AttnPlan p{};
@@ -332,29 +398,32 @@ AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache) {
   p.dtype = cache->dtype;
   p.max_prefix = shape->max_prefix;
   p.rows = p.max_nodes * p.group;
-  p.tensor_core = tc_supported(p);
-  p.rows_pad = (int)round_up(p.rows, p.tensor_core ? TC_M_GROUP : 8);
-  p.tile_keys = 128;
+  // bf16 with head_dim 128: the tcgen05 kernel (attn_umma.cu) on sm_100+, else the
+  // warp-level tensor-core kernel (attn_mma.cu)
+  p.tensor_core = p.dtype == TSV_DTYPE_BF16 && p.head_dim == 128 && device_cc() >= 80;
+  p.umma = p.tensor_core && umma_supported(p);
+  p.rows_pad = (int)round_up(p.rows, p.tensor_core ? MMA_M_GROUP : 8);
+  p.tile_keys = p.umma ? 128 : (p.tensor_core ? MMA_TILE_KEYS : 128);
   const int64_t keys_max = (int64_t)p.max_prefix + p.max_nodes;
   const int64_t n_tiles = ceil_div(keys_max, p.tile_keys);
   const int sms = device_sm_count();
   if (p.tensor_core) {
-    // One CTA per SM. Splits: at least ~2 CTAs per SM (request lengths vary below
-    // max_prefix), and at least the count with the shortest estimated makespan for
-    // full-length requests (waves x (tiles per split + 1 tile of fixed cost)); partials
-    // stay under about half of the KV bytes.
-    const int64_t units = (int64_t)p.batch * p.hkv * ceil_div(p.rows, TC_M_GROUP);
-    const int64_t rows_g = std::min<int64_t>(p.rows, TC_M_GROUP);
+    // One CTA per SM. Splits: the count with the shortest estimated makespan for
+    // full-length requests (waves x (tiles per split + 2 tiles of fixed cost: the ring's
+    // fill and the epilogue)), at least one full wave; partials stay under about half of
+    // the KV bytes.
+    const int64_t units = (int64_t)p.batch * p.hkv * ceil_div(p.rows, MMA_M_GROUP);
+    const int64_t rows_g = std::min<int64_t>(p.rows, MMA_M_GROUP);
     const int64_t cap = std::max<int64_t>(
         1, std::min<int64_t>({n_tiles, keys_max / (2 * rows_g), (int64_t)TSV_ATTN_MAX_SPLITS}));
     int64_t best = 1, best_cost = INT64_MAX;
     for (int64_t ns = 1; ns <= cap; ++ns) {
       const int64_t tps = ceil_div(n_tiles, ns);
       const int64_t eff = ceil_div(n_tiles, tps);
-      const int64_t cost = ceil_div(units * eff, sms) * (tps + 1);
+      const int64_t cost = ceil_div(units * eff, sms) * (tps + 2);
       if (cost < best_cost) { best_cost = cost; best = ns; }
     }
-    best = std::min(cap, std::max(best, ceil_div(2LL * sms, units)));
+    best = std::min(cap, std::max(best, ceil_div((int64_t)sms, units)));
     p.tiles_per_split = (int)ceil_div(n_tiles, best);
   } else {
     const int64_t ctas = (int64_t)p.batch * p.hkv;
@@ -439,7 +508,8 @@ int launch_attn(const AttnPlan& p, const void* q, const void* k_new, const void*
   if (p.tensor_core) {
     // tensor-core attention plus, when the plan splits the keys, the separate
     // warp-per-row split merge kernel
-    return launch_attn_tc(p, a, scale_log2, out, stream);
+    return p.umma ? launch_attn_umma(p, a, scale_log2, out, stream)
+                  : launch_attn_mma(p, a, scale_log2, out, stream);
   } else {
     dim3 gs((unsigned)ceil_div(p.rows, SIMT_WARPS), p.nsplit, p.batch * p.hkv);
     const dim3 bs(SIMT_WARPS * 32);

@@ -45,5 +45,19 @@ constexpr int TC_M_GROUP = 128;
 bool tc_supported(const AttnPlan& p);
 int launch_attn_tc(const AttnPlan& p, const AttnArgs& a, float scale_log2, void* out,
                    cudaStream_t stream);
+// tcgen05 path with cp.async-fed K/V rings (attn_umma.cu): bf16, head_dim 128, sm_100+;
+// keys in tiles of 128.
+bool umma_supported(const AttnPlan& p);
+int launch_attn_umma(const AttnPlan& p, const AttnArgs& a, float scale_log2, void* out,
+                     cudaStream_t stream);
+// Warp-level tensor-core path (mma.sync, attn_mma.cu): bf16, head_dim 128, sm_80+; keys
+// in tiles of MMA_TILE_KEYS.
+constexpr int MMA_TILE_KEYS = 64;
+constexpr int MMA_M_GROUP = 128;
+int launch_attn_mma(const AttnPlan& p, const AttnArgs& a, float scale_log2, void* out,
+                    cudaStream_t stream);
+// Log-sum-exp merge of the key splits into the bf16 output (rows of requests that took
+// one split are left as the attention kernel wrote them).
+int launch_split_merge(const AttnPlan& p, const AttnArgs& a, void* out, cudaStream_t stream);
 
 }  // namespace tsv

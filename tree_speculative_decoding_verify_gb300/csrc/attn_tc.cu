@@ -1,6 +1,12 @@
 // Tree-verification attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA),
 // bf16 in, fp32 accumulate, head_dim 128.
 //
+// NOT DISPATCHED: tree_verify_attn runs attn_mma.cu. With one 128-row M tile per KV head
+// and every K/V byte streamed from HBM (B = 64, P = 1024, 9-node trees) right after a
+// large write, about one call in a hundred ended in an unspecified launch failure, one
+// CTA stopping in the middle of its key loop with K/V copies in flight; the cause is
+// not known, so this kernel is kept for reference only.
+//
 // Pages: "推理系统手册 · 投机解码进阶：树形草稿与 EAGLE", section 实现 (forward_with_mask:
 // each node attends to the whole prefix and, among the tree nodes, to its ancestors and
 // itself; GQA heads share a KV head) and "TensorRT-LLM 源码完全拆解(二十二)", section

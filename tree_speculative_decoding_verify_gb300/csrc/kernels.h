@@ -97,7 +97,8 @@ struct AttnPlan {
   int nsplit;         // splits along the keys
   int tiles_per_split;
   int max_prefix;
-  bool tensor_core;   // tcgen05 path
+  bool tensor_core;   // a bf16 tensor-core path (q_rot in bf16, M tiles of 128 rows)
+  bool umma;          // that path is the tcgen05 kernel (else the mma.sync one)
   size_t off_qrot, off_opart, off_ml, off_valid, ws_bytes;
 };
 AttnPlan plan_attn(const tsv_attn_shape* shape, const tsv_kv_cache* cache);
