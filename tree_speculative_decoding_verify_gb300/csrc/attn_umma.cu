@@ -186,7 +186,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_umma_kernel(const UmmaParams 
       if (npend > 1) mbar_arrive(pend1);
       npend = 0;
     };
-    // one K or V tile j (of this CTA's range) into ring slot dst; full = its FULL barrier
+    // one K or V tile j (of this CTA's range) into ring slot dst; full = its FULL barrier.
+    // Thread lt copies 16-byte chunk c16 of rows rr + 4 i (i < 32): its global addresses
+    // step by 1 KB and its shared ones by 512 bytes, and row (rr + 4 i) & 7 takes two
+    // values, so every copy is one instruction with constant offsets.
+    const int rr = lt >> 4, c16 = lt & 15;
+    const uint32_t sw_even = (uint32_t)((c16 & 7) ^ (rr & 7)) << 4;
+    const uint32_t sw_odd = (uint32_t)((c16 & 7) ^ ((rr + 4) & 7)) << 4;
+    const uint32_t dlane = (uint32_t)(c16 >> 3) * HALF + (uint32_t)rr * 128u;
     auto copy_tile = [&](const char* cache, uint32_t dst, uint32_t full, int j) {
       const int k0 = (t0 + j) * KEYS;
       int64_t rb0, rb1;  // cache rows of keys k0 and k0 + 64
@@ -200,15 +207,25 @@ __global__ void __launch_bounds__(THREADS, 1) attn_umma_kernel(const UmmaParams 
         rb0 = ((int64_t)blk0 * a.hkv + h) * TSV_KV_BLOCK;
         rb1 = ((int64_t)blk1 * a.hkv + h) * TSV_KV_BLOCK;
       }
+      const char* s0 = cache + (rb0 + rr) * 256 + c16 * 16;  // rows rr + 4 i, i < 16
+      const char* s1 = cache + (rb1 + rr) * 256 + c16 * 16;  // rows 64 + rr + 4 i
+      const uint32_t d0 = dst + dlane;
+      const int lim = kload - k0 - rr;  // row rr + 4 i holds data when 4 i < lim
+      if (lim >= 128) {  // every row of the tile
 #pragma unroll
-      for (int i = 0; i < CHUNKS_PER_THREAD; ++i) {
-        const int q = lt + i * LOADERS, r = q >> 4, c16 = q & 15;
-        const bool in = k0 + r < kload;
-        const int64_t row = r < 64 ? rb0 + r : rb1 + (r - 64);
-        const char* src = in ? cache + row * 256 + c16 * 16 : cache;
-        const uint32_t d = dst + (uint32_t)(c16 >> 3) * HALF + (uint32_t)r * 128u +
-                           ((uint32_t)((c16 & 7) ^ (r & 7)) << 4);
-        cp_async16(d, src, in);
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t sw = (i & 1) ? sw_odd : sw_even;
+          cp_async16(d0 + 512u * i + sw, s0 + 1024 * i, true);
+          cp_async16(d0 + 8192u + 512u * i + sw, s1 + 1024 * i, true);
+        }
+      } else {  // the tile that ends the tree: rows past it are zero-filled, never read
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t sw = (i & 1) ? sw_odd : sw_even;
+          const bool in0 = 4 * i < lim, in1 = 64 + 4 * i < lim;
+          cp_async16(d0 + 512u * i + sw, in0 ? s0 + 1024 * i : cache, in0);
+          cp_async16(d0 + 8192u + 512u * i + sw, in1 ? s1 + 1024 * i : cache, in1);
+        }
       }
       cp_commit();
       if (npend == 2) {  // three tiles in flight: the oldest has landed
@@ -229,7 +246,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_umma_kernel(const UmmaParams 
     auto slot_free = [&](uint32_t empty, uint32_t parity) {
       if (mbar_test(empty, parity)) return true;
       signal_all();  // never block while holding tiles the MMA warp may be waiting for
-      return mbar_wait(empty, parity, abort, true);
+      // the ring's slack absorbs the wake-up latency: poll with short sleeps, leaving
+      // the issue slots to the softmax warps sharing this sub-partition
+      return mbar_wait(empty, parity, abort, false);
     };
     bool ok = true;
     for (int j = 0; ok && j <= n + 1; ++j) {  // K_j, then V_{j-2}
