@@ -855,7 +855,9 @@ def reference(args):
     step_s = per_req * w.batch
     value = 1.0 / step_s
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        # n_gpus: the launch's N (the line the driver compares with); the oracle itself
+        # runs on the host cores of rank 0
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
