@@ -776,15 +776,20 @@ __device__ __forceinline__ void stream_ring(TopkSmem& sm, const LevelArgs& p, in
   UnitState u;
   unit_begin(u, first, sm.gthr);
   const unsigned long long* gthr = &sm.gthr;
+  int st = 0;  // ring slot and phase parity of stage i, advanced stage by stage
+  uint32_t par = 0u;
   for (int i = 0; i < nst; ++i) {
-    const int st = i % RING_STAGES;
-    const uint32_t par = (uint32_t)(i / RING_STAGES) & 1u;
     const bool ok = i == 0 || ring_wait(sm, sa(&sm.full[st]), par);
     const float4* stage = dyn_smem + st * STAGE_F4;
     const int eb = start + i * STAGE_ENTRIES + 4 * tid;  // entry of this thread's first group
     float4 cur[4];
+    if (i + 1 < nst) {  // a full stage: every entry is in the unit
 #pragma unroll
-    for (int q = 0; q < 4; ++q) cur[q] = ok && eb + 4 * q * A_THREADS < end4 ? stage[tid + q * A_THREADS] : none;
+      for (int q = 0; q < 4; ++q) cur[q] = ok ? stage[tid + q * A_THREADS] : none;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cur[q] = ok && eb + 4 * q * A_THREADS < end4 ? stage[tid + q * A_THREADS] : none;
+    }
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(&sm.empty[st])) : "memory");
     step16(sm, u, warp, lane, p.k, cur, eb, end);
@@ -792,6 +797,10 @@ __device__ __forceinline__ void stream_ring(TopkSmem& sm, const LevelArgs& p, in
     if (tid == 0 && i + RING_STAGES < nst) {
       // every warp has read this stage: it takes stage i + RING_STAGES
       if (ring_wait(sm, sa(&sm.empty[st]), par)) ring_issue(sm, ring0, x, start, end4, i + RING_STAGES);
+    }
+    if (++st == RING_STAGES) {
+      st = 0;
+      par ^= 1u;
     }
   }
   // entries past the last group of four (at most three), by warp 0
@@ -851,10 +860,10 @@ __global__ void __launch_bounds__(A_THREADS, 2) topk_stream_kernel(const LevelAr
   // producer cursor (thread 0): the next stage to copy starts at entry pe of row pr
   int pr = r_first, pe = 0, pe1 = 0;
   if (pr <= r_last) piece(pr, &pe, &pe1);
-  int64_t issued = 0;  // stages copied so far (global sequence)
+  int islot = 0;  // ring slot of the next stage to copy (stages go round the ring in order)
   auto issue_next = [&]() {  // thread 0: copy the stage at the cursor, advance it
     if (pr > r_last) return;
-    const int st = (int)(issued % P_STAGES);
+    const int st = islot;
     const uint32_t bytes = (uint32_t)min(STAGE_ENTRIES, pe1 - pe) * 4u;  // a multiple of 16
     const uint32_t fb = sa(&sm.full[st]);
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes)
@@ -864,7 +873,7 @@ __global__ void __launch_bounds__(A_THREADS, 2) topk_stream_kernel(const LevelAr
             ring0 + (uint32_t)st * (STAGE_ENTRIES * 4)),
         "l"(p.logits + (int64_t)pr * p.row_stride + pe), "r"(bytes), "r"(fb)
         : "memory");
-    ++issued;
+    if (++islot == P_STAGES) islot = 0;
     pe += STAGE_ENTRIES;
     if (pe >= pe1 && ++pr <= r_last) piece(pr, &pe, &pe1);
   };
@@ -880,16 +889,18 @@ __global__ void __launch_bounds__(A_THREADS, 2) topk_stream_kernel(const LevelAr
     for (int i = 0; i < P_STAGES; ++i) issue_next();
   }
   __syncthreads();
-  int64_t g = 0;  // global index of the next stage to consume
+  // ring slot and phase parity of the next stage to consume, advanced stage by stage
+  // (no division in the loop)
+  int cst = 0;
+  uint32_t cpar = 0u;
   for (int r = r_first; r <= r_last; ++r) {
     int e0, e1;
     piece(r, &e0, &e1);
     const int nst = (e1 - e0 + STAGE_ENTRIES - 1) / STAGE_ENTRIES;
     // the piece's first stage: starting reference and seed of the CTA-wide bound
     {
-      const int st = (int)(g % P_STAGES);
-      ring_wait(sm, sa(&sm.full[st]), (uint32_t)(g / P_STAGES) & 1u);
-      const float4* stage = ring + st * STAGE_F4;
+      ring_wait(sm, sa(&sm.full[cst]), cpar);
+      const float4* stage = ring + cst * STAGE_F4;
       float m = -INFINITY;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
@@ -911,15 +922,24 @@ __global__ void __launch_bounds__(A_THREADS, 2) topk_stream_kernel(const LevelAr
     UnitState u;
     unit_begin(u, first, sm.gthr);
     const unsigned long long* gthr = &sm.gthr;
-    for (int i = 0; i < nst; ++i, ++g) {
-      const int st = (int)(g % P_STAGES);
-      const uint32_t par = (uint32_t)(g / P_STAGES) & 1u;
+    for (int i = 0; i < nst; ++i) {
+      const int st = cst;
+      const uint32_t par = cpar;
+      if (++cst == P_STAGES) {
+        cst = 0;
+        cpar ^= 1u;
+      }
       const bool ok = i == 0 || ring_wait(sm, sa(&sm.full[st]), par);
       const float4* stage = ring + st * STAGE_F4;
       const int eb = e0 + i * STAGE_ENTRIES + 4 * tid;
       float4 cur[4];
+      if (i + 1 < nst) {  // a full stage: every entry is in the piece
 #pragma unroll
-      for (int q = 0; q < 4; ++q) cur[q] = ok && eb + 4 * q * A_THREADS < e1 ? stage[tid + q * A_THREADS] : none;
+        for (int q = 0; q < 4; ++q) cur[q] = ok ? stage[tid + q * A_THREADS] : none;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) cur[q] = ok && eb + 4 * q * A_THREADS < e1 ? stage[tid + q * A_THREADS] : none;
+      }
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(&sm.empty[st])) : "memory");
       step16(sm, u, warp, lane, p.k, cur, eb, e1);
