@@ -70,13 +70,55 @@ def compare(levels_per_req, k, **kw):
     return st, ss, sp
 
 
+@pytest.mark.parametrize("b", [3, 40])
 @pytest.mark.parametrize("v", [64, 1000, 4001, 32000])
-def test_levels_small_and_ragged_vocab(v):
-    rng = np.random.default_rng(v)
+def test_levels_small_and_ragged_vocab(v, b):
+    """3 requests take the row-per-CTA cluster kernel at every level; 40 requests of 4
+    rows (160 rows, more than the GPU's SMs) take the per-unit kernel from level 2 on."""
+    rng = np.random.default_rng(v + b)
     k, depth = 4, 3
     reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
-             for l in range(depth + 1)] for _ in range(3)]
+             for l in range(depth + 1)] for _ in range(b)]
     compare(reqs, k)
+
+
+@pytest.mark.parametrize("v,k,b,pad,product", [
+    (32768, 16, 4, 0, False),    # the longest row and the largest cluster (16 rows)
+    (32767, 16, 3, 1, False),    # stride 32768 but ragged: 128-bit loads, a partial group
+    (30001, 10, 6, 0, False),    # unaligned rows: scalar loads
+    (30001, 10, 6, 3, True),     # aligned ragged rows, product scores
+    (32000, 8, 4, 0, False),     # clusters of 8 (the long-prefix workload's shape)
+    (20, 16, 2, 0, False),       # fewer threads with entries than k: every entry survives
+])
+def test_row_clusters(v, k, b, pad, product):
+    """Small batches: one CTA per frontier row holds the whole row in registers and the
+    request's rows form a thread-block cluster whose rank-0 CTA runs the joint top-K over
+    distributed shared memory. Every level is compared with the oracle."""
+    rng = np.random.default_rng(v + 7 * k + b + pad)
+    reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
+             for l in range(3)] for _ in range(b)]
+    if product:
+        st, ss, sp, hist = run_levels(reqs, k, stride_pad=pad, product=True)
+        for bi, levels in enumerate(reqs):
+            exp = draft.topk_generate(levels, k, product=True)
+            c = exp.store_token.size
+            np.testing.assert_array_equal(st[bi, :c], exp.store_token)
+            np.testing.assert_array_equal(sp[bi, :c], exp.store_parent)
+            np.testing.assert_allclose(ss[bi, :c], exp.store_score, rtol=gc.SCORE_RTOL, atol=0)
+    else:
+        compare(reqs, k, stride_pad=pad)
+
+
+@pytest.mark.parametrize("v", [32768, 5000])
+def test_row_clusters_constant_rows(v):
+    """Rows whose entries are all equal: every warp's and thread's best entry ties in value,
+    so the bounds are decided by index alone and hundreds of thread maxima reach the first
+    bound; the top k must be the k lowest ids of every row."""
+    k, b = 16, 2
+    reqs = [[np.full((1 if l == 0 else k, v), 0.25 * (l + 1), dtype=np.float32)
+             for l in range(2)] for _ in range(b)]
+    st, ss, sp = compare(reqs, k)
+    assert st[0, :k].tolist() == list(range(k))
 
 
 def test_strided_rows_and_max_topk():

@@ -1041,6 +1041,264 @@ topk_level_kernel(const LevelArgs p, bool vec) {
   finish_unit(sm, u, p, row, chunk, end, 0, none, none, end, end, dyn_smem, SURV_MAX, dyn_smem);
 }
 
+// ---- small batches: one CTA per frontier row, a thread-block cluster per request -------
+// A level of a few requests has too few rows to fill the GPU with (row, chunk) units unless
+// they are short, and then the grid-wide ticket and the one-CTA request merge set its
+// latency. Here a row is one CTA that holds the whole row in registers (R_NF groups of four
+// entries per thread, all loads in flight at once), and the rows of a request form one
+// cluster: every CTA writes its row's candidates and keeps their cumulative scores in its
+// shared memory, and the rank-0 CTA reads them across the cluster for the joint top-K.
+//   - log-sum-exp: the thread's terms against its own largest entry (none above 1),
+//     summed in groups of 16 and added exactly into an unevaluated (hi, lo) pair, then
+//     combined over the CTA as in the per-unit path.
+//   - top-k: tau1 = the k-th best of the warps' best entries bounds the row's k-th entry
+//     from below; the thread maxima at or above it (a handful) are ranked for the exact
+//     k-th best thread maximum tau; only the k threads whose maximum reaches tau can hold
+//     entries at or above it, and those survivors (k or a few more) are ranked by counting.
+constexpr int R_THREADS = 512;
+constexpr int R_WARPS = R_THREADS / 32;
+constexpr int R_NF = 16;                           // groups of four entries per thread
+constexpr int R_MAX_VOCAB = 4 * R_NF * R_THREADS;  // 32768 entries per row
+constexpr int R_SURV = KMAX * 4 * R_NF;            // k threads' entries at most
+constexpr int R_MAX_ROWS = 16;                     // cluster size (non-portable above 8)
+static_assert(R_WARPS >= KMAX, "tau1 needs k warp maxima");
+
+struct RowSmem {
+  unsigned long long wkey[R_WARPS];   // each warp's best entry (key())
+  unsigned long long cand[R_THREADS]; // thread maxima at or above tau1
+  unsigned long long surv[R_SURV];    // entries at or above tau
+  float red[R_WARPS], shi[R_WARPS], slo[R_WARPS];
+  float lse[3];                       // the row's log-sum-exp as hi + mid + lo
+  unsigned long long tau;
+  int nc, ns;
+  float cu[KMAX];                     // the row's k cumulative scores, best first
+  int tok[KMAX];
+  float all_cu[R_MAX_ROWS * KMAX];    // rank 0: the request's rows * k scores (flat order)
+  int all_tok[R_MAX_ROWS * KMAX];
+};
+
+__device__ __forceinline__ float comp(const float4& a, int q) {
+  return q == 0 ? a.x : (q == 1 ? a.y : (q == 2 ? a.z : a.w));
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of this CTA's shared-memory object p in the shared memory of cluster rank r.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, int r) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(out)
+               : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(r));
+  return out;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+// grid (rows, batch), cluster (rows, 1, 1): blockIdx.x is the frontier row and the rank in
+// the request's cluster. VEC: 16-byte aligned rows (128-bit loads), else scalar loads.
+template <bool VEC>
+__global__ void __launch_bounds__(R_THREADS, 1) topk_row_kernel(const LevelArgs p) {
+  __shared__ RowSmem sm;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = blockIdx.x, b = blockIdx.y;
+  const int rows = p.rows, k = p.k, V = p.vocab;
+  const int r0 = b * rows + s;
+  if (tid == 0) {
+    sm.nc = 0;
+    sm.ns = 0;
+    sm.tau = 0ull;
+  }
+  griddep_wait();
+  griddep_launch();  // one wave of CTAs: the next kernel may be scheduled beside it
+  const float* x = p.logits + (int64_t)r0 * p.row_stride;
+
+  // entry 4 (tid + R_THREADS j) + q of the row sits in a[j], component q; entries past
+  // the row are -inf (never selected, zero exp-sum terms)
+  const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  float4 a[R_NF];
+#pragma unroll
+  for (int j = 0; j < R_NF; ++j) {
+    const int e = 4 * (tid + R_THREADS * j);
+    if (VEC) {
+      a[j] = e + 3 < V ? ld_stream(reinterpret_cast<const float4*>(x + e)) : none;
+    } else {
+      a[j].x = e < V ? x[e] : -INFINITY;
+      a[j].y = e + 1 < V ? x[e + 1] : -INFINITY;
+      a[j].z = e + 2 < V ? x[e + 2] : -INFINITY;
+      a[j].w = e + 3 < V ? x[e + 3] : -INFINITY;
+    }
+  }
+  if (VEC && (V & 3)) {  // the group that straddles the row's end
+#pragma unroll
+    for (int j = 0; j < R_NF; ++j) {
+      const int e = 4 * (tid + R_THREADS * j);
+      if (e < V && e + 3 >= V) {
+        a[j].x = x[e];
+        a[j].y = e + 1 < V ? x[e + 1] : -INFINITY;
+        a[j].z = e + 2 < V ? x[e + 2] : -INFINITY;
+      }
+    }
+  }
+
+  // the thread's best entry: the first of its largest (entries run in ascending index)
+  const bool has = 4 * tid < V;
+  float m = a[0].x;
+  int am = 0;
+#pragma unroll
+  for (int t = 1; t < 4 * R_NF; ++t) {
+    const float v = comp(a[t >> 2], t & 3);
+    if (v > m) { m = v; am = t; }
+  }
+  const int mi = 4 * tid + 4 * R_THREADS * (am >> 2) + (am & 3);
+  const unsigned long long kt = has ? key(m, mi) : 0ull;
+
+  // exp-sum against the thread's largest entry
+  {
+    const float ref = fmaxf(m, -1e30f), rl = ref * L2E;
+    float hi = 0.f, lo = 0.f;
+#pragma unroll
+    for (int g = 0; g < R_NF / 4; ++g) {
+      float gs = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 c = a[4 * g + u];
+        gs += (ex2(fmaf(c.x, L2E, -rl)) + ex2(fmaf(c.y, L2E, -rl))) +
+              (ex2(fmaf(c.z, L2E, -rl)) + ex2(fmaf(c.w, L2E, -rl)));
+      }
+      pair_add(hi, lo, gs, 0.f);
+    }
+    float R = ref;
+    warp_combine(R, hi, lo);
+    if (lane == 0) { sm.red[warp] = R; sm.shi[warp] = hi; sm.slo[warp] = lo; }
+  }
+  // the warp's best entry
+  {
+    const unsigned h = __reduce_max_sync(FULL, (unsigned)(kt >> 32));
+    const unsigned l = __reduce_max_sync(FULL, (unsigned)(kt >> 32) == h ? (unsigned)kt : 0u);
+    if (lane == 0) sm.wkey[warp] = ((unsigned long long)h << 32) | l;
+  }
+  __syncthreads();
+
+  // tau1: the k-th best warp maximum (every warp computes it; ties by warp)
+  unsigned long long tau1;
+  {
+    const unsigned long long mine = lane < R_WARPS ? sm.wkey[lane] : 0ull;
+    int rank = 0;
+#pragma unroll
+    for (int o = 0; o < R_WARPS; ++o) {
+      const unsigned long long w = sm.wkey[o];
+      rank += (w > mine || (w == mine && o < lane)) ? 1 : 0;
+    }
+    const unsigned sel = __ballot_sync(FULL, lane < R_WARPS && rank == k - 1);
+    tau1 = __shfl_sync(FULL, mine, __ffs(sel) - 1);
+  }
+  {  // candidates: thread maxima at or above tau1
+    const bool c = kt != 0ull && kt >= tau1;
+    const unsigned bal = __ballot_sync(FULL, c);
+    if (bal) {
+      const int leader = __ffs(bal) - 1;
+      int at = 0;
+      if (lane == leader) at = atomicAdd(&sm.nc, __popc(bal));
+      at = __shfl_sync(FULL, at, leader);
+      if (c) sm.cand[at + __popc(bal & ((1u << lane) - 1u))] = kt;
+    }
+  }
+  if (warp == R_WARPS - 1) {  // the row's exp-sum
+    float rr = lane < R_WARPS ? sm.red[lane] : -INFINITY;
+    float hh = lane < R_WARPS ? sm.shi[lane] : 0.f, ll = lane < R_WARPS ? sm.slo[lane] : 0.f;
+    warp_combine(rr, hh, ll);
+    // log(hi + lo) = log(hi) + log1p(lo / hi); |lo / hi| is below an ulp
+    if (lane == 0) { sm.lse[0] = rr; sm.lse[1] = logf(hh); sm.lse[2] = ll / hh; }
+  }
+  __syncthreads();
+
+  // tau: the k-th best thread maximum (0 when fewer than k threads hold entries)
+  const int nc = sm.nc;
+  for (int c = tid; c < nc; c += R_THREADS) {
+    const unsigned long long u = sm.cand[c];
+    int rank = 0;
+    for (int o = 0; o < nc; ++o) rank += sm.cand[o] > u ? 1 : 0;
+    if (rank == k - 1) sm.tau = u;
+  }
+  __syncthreads();
+
+  // survivors: entries at or above tau, from the threads whose maximum reaches it
+  const unsigned long long tau = sm.tau;
+  if (kt != 0ull && kt >= tau) {
+    const float tv = tau != 0ull ? unord((unsigned)(tau >> 32)) : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < R_NF; ++j) {
+      if (fmaxf(fmaxf(a[j].x, a[j].y), fmaxf(a[j].z, a[j].w)) >= tv) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int e = 4 * (tid + R_THREADS * j) + q;
+          const unsigned long long u = key(comp(a[j], q), e);
+          if (e < V && u >= tau) sm.surv[atomicAdd(&sm.ns, 1)] = u;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // the row's top k by rank among the survivors; log-probabilities and cumulative scores
+  const int S = sm.ns;
+  const int off = p.level == 1 ? 0 : k + (p.level - 2) * k * k;
+  const int64_t srow = (int64_t)b * p.store_cap;
+  const float pscore = p.level == 1 ? (p.product ? 1.0f : 0.0f) : p.front_score_in[r0];
+  const int pstore = p.level == 1 ? -1 : p.front_store_in[r0];
+  for (int t = tid; t < S; t += R_THREADS) {
+    const unsigned long long u = sm.surv[t];
+    int rank = 0;
+    for (int o = 0; o < S; ++o) rank += sm.surv[o] > u ? 1 : 0;
+    if (rank < k) {
+      const float v = unord((unsigned)(u >> 32));
+      const int i = (int)~(unsigned)u;
+      const float logp = ((v - sm.lse[0]) - sm.lse[1]) - sm.lse[2];
+      const float cu = p.product ? pscore * expf(logp) : pscore + logp;
+      const int flat = s * k + rank;
+      p.store_token[srow + off + flat] = i;
+      p.store_score[srow + off + flat] = cu;
+      p.store_parent[srow + off + flat] = pstore;
+      sm.cu[rank] = cu;
+      sm.tok[rank] = i;
+    }
+  }
+  cluster_sync_all();  // every row's scores are visible across the cluster
+
+  const int nf = rows * k;
+  if (s == 0 && tid < nf) {
+    const int src = tid / k, j = tid - src * k;
+    sm.all_cu[tid] = ld_cluster_f32(cluster_addr(&sm.cu[j], src));
+    sm.all_tok[tid] = ld_cluster_s32(cluster_addr(&sm.tok[j], src));
+  }
+  cluster_sync_all();  // rank 0 is done reading the others' shared memory
+  if (s != 0) return;
+  // Joint top-K over the rows * K cumulative scores (ties to the lower flat index), as in
+  // the per-unit path's request merge.
+  if (tid < nf) {
+    const float cv = sm.all_cu[tid];
+    int rank = 0;
+#pragma unroll 4
+    for (int u = 0; u < nf; ++u) {
+      const float o = sm.all_cu[u];
+      rank += (o > cv || (o == cv && u < tid)) ? 1 : 0;
+    }
+    if (rank < k) {
+      p.front_token_out[b * k + rank] = sm.all_tok[tid];
+      p.front_score_out[b * k + rank] = cv;
+      p.front_store_out[b * k + rank] = off + tid;
+    }
+  }
+}
+
 // ---- final selection --------------------------------------------------------------
 // The total_tokens-th best key (ord() of the score) by a three-pass radix select over
 // shared-memory histograms (11, 11 and 10 bits); the kept candidates are the keys above
@@ -1158,11 +1416,56 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
   }
 }
 
+// Clusters of `rows` row CTAs that can be resident at once (0 when the device or the
+// runtime cannot run them), cached per device and cluster size.
+int row_cluster_capacity(int rows) {
+  static int cache[64][R_MAX_ROWS + 1];
+  static bool known[64][R_MAX_ROWS + 1] = {};
+  int dev = 0;
+  if (rows < 1 || rows > R_MAX_ROWS || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (known[dev][rows]) return cache[dev][rows];
+  int n = 0;
+  if (device_cc() >= 90 &&
+      cudaFuncSetAttribute(topk_row_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+          cudaSuccess &&
+      cudaFuncSetAttribute(topk_row_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+          cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows, 1);
+    cfg.blockDim = dim3(R_THREADS);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = rows;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, topk_row_kernel<true>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cache[dev][rows] = n;
+  known[dev][rows] = true;
+  return n;
+}
+
 }  // namespace
 
 TopkPlan plan_topk(int batch, int rows, int vocab, int top_k) {
   TopkPlan p{};
   const int64_t rows_total = (int64_t)batch * rows;
+  // Small batches: one CTA per row and a cluster per request, when the row fits the CTA's
+  // registers and every cluster is resident at once.
+  if (vocab <= R_MAX_VOCAB && rows <= R_MAX_ROWS && rows_total <= device_sm_count() &&
+      batch <= row_cluster_capacity(rows)) {
+    p.cluster = true;
+    p.chunks = 1;
+    p.chunk_len = (int)round_up(vocab, 4);
+    p.ws_bytes = align256((size_t)batch * sizeof(unsigned));
+    return p;
+  }
   // Large batches: the persistent kernel, one CTA per SM, when every share is at least a
   // row long (with room for the rounding to four entries) and rows are whole groups of
   // four entries; chunks = 2 gives each row two workspace slots (its at most two pieces),
@@ -1235,6 +1538,29 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
   p.rows_total = rows_total;
   int dev = 0;
   cudaGetDevice(&dev);
+  if (plan.cluster) {
+    if (row_cluster_capacity(rows) < batch) return TSV_ERR_UNSUPPORTED;  // sets the cluster attribute
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows, batch);
+    cfg.blockDim = dim3(R_THREADS);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = rows;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    void (*kern)(const LevelArgs) = vec ? topk_row_kernel<true> : topk_row_kernel<false>;
+    if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
+      cudaGetLastError();  // no programmatic serialization here: a plain cluster launch
+      cfg.numAttrs = 1;
+      cudaLaunchKernelEx(&cfg, kern, p);
+    }
+    return launch_status();
+  }
   if (plan.persistent && vec) {
     // ring, survivors, and the request merge's staging for two slots per row
     constexpr size_t P_MERGE_MAX = (size_t)TSV_MAX_TOPK * 3 * TSV_MAX_TOPK * 8;

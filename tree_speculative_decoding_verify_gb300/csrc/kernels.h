@@ -65,6 +65,7 @@ struct TopkPlan {
   int chunks;         // CTAs per row in the streaming stage (workspace slots per row)
   int chunk_len;      // vocab entries per chunk (multiple of 4)
   bool persistent;    // large batch: one CTA per SM over equal shares of all entries
+  bool cluster;       // small batch: one CTA per row, a thread-block cluster per request
   size_t ws_bytes;
 };
 TopkPlan plan_topk(int batch, int rows, int vocab, int top_k);
