@@ -1046,42 +1046,52 @@ topk_level_kernel(const LevelArgs p, bool vec) {
 // they are short, and then the grid-wide ticket and the one-CTA request merge set its
 // latency. Here a row is one CTA that holds the whole row in registers (R_NF groups of four
 // entries per thread, all loads in flight at once), and the rows of a request form one
-// cluster: every CTA writes its row's candidates and keeps their cumulative scores in its
-// shared memory, and the rank-0 CTA reads them across the cluster for the joint top-K.
+// cluster: every CTA stores its row's k cumulative scores and tokens into the rank-0 CTA's
+// shared memory, which runs the joint top-K once the cluster barrier completes.
 //   - log-sum-exp: the thread's terms against its own largest entry (none above 1),
 //     summed in groups of 16 and added exactly into an unevaluated (hi, lo) pair, then
 //     combined over the CTA as in the per-unit path.
-//   - top-k: tau1 = the k-th best of the warps' best entries bounds the row's k-th entry
-//     from below; the thread maxima at or above it (a handful) are ranked for the exact
-//     k-th best thread maximum tau; only the k threads whose maximum reaches tau can hold
-//     entries at or above it, and those survivors (k or a few more) are ranked by counting.
+//   - top-k: t1 = the k-th largest of the warps' largest values is at most the row's k-th
+//     largest value, so the entries of value t1 or more hold the row's top k; a thread
+//     scans only its groups whose largest entry reaches t1, and the survivors (a handful
+//     on untied rows) are ranked by counting. When ties or ordered rows leave more
+//     survivors than the buffer holds, an exact bound on (value, index) keys -- the k-th
+//     best thread maximum, found among the thread maxima at or above the k-th best warp
+//     maximum -- leaves at most k threads' entries.
 constexpr int R_THREADS = 512;
 constexpr int R_WARPS = R_THREADS / 32;
 constexpr int R_NF = 16;                           // groups of four entries per thread
 constexpr int R_MAX_VOCAB = 4 * R_NF * R_THREADS;  // 32768 entries per row
-constexpr int R_SURV = KMAX * 4 * R_NF;            // k threads' entries at most
+constexpr int R_SURV = KMAX * 4 * R_NF;            // k threads' entries (the exact bound)
 constexpr int R_MAX_ROWS = 16;                     // cluster size (non-portable above 8)
-static_assert(R_WARPS >= KMAX, "tau1 needs k warp maxima");
+static_assert(R_WARPS >= KMAX, "the bounds need k warp maxima");
 
 struct RowSmem {
-  unsigned long long wkey[R_WARPS];   // each warp's best entry (key())
-  unsigned long long cand[R_THREADS]; // thread maxima at or above tau1
-  unsigned long long surv[R_SURV];    // entries at or above tau
+  unsigned long long wkey[R_WARPS];   // exact bound: each warp's best entry (key())
+  unsigned wmax[R_WARPS];             // ord() of each warp's largest value
+  unsigned long long cand[R_THREADS]; // exact bound: thread maxima at or above it
+  unsigned long long surv[R_SURV];    // survivors (key())
   float red[R_WARPS], shi[R_WARPS], slo[R_WARPS];
   float lse[3];                       // the row's log-sum-exp as hi + mid + lo
   unsigned long long tau;
-  int nc, ns;
-  float cu[KMAX];                     // the row's k cumulative scores, best first
-  int tok[KMAX];
-  float all_cu[R_MAX_ROWS * KMAX];    // rank 0: the request's rows * k scores (flat order)
-  int all_tok[R_MAX_ROWS * KMAX];
+  int nc, ns, ns2;                    // candidates; survivors (value bound, exact bound)
+  // rank 0: the request's rows * k candidates in flat order, as keys (ord() of the
+  // cumulative score above the complemented flat index: larger is better) and tokens
+  alignas(16) unsigned long long jkey[R_MAX_ROWS * KMAX];
+  int jtok[R_MAX_ROWS * KMAX];
 };
 
 __device__ __forceinline__ float comp(const float4& a, int q) {
   return q == 0 ? a.x : (q == 1 ? a.y : (q == 2 ? a.z : a.w));
 }
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 // Address of this CTA's shared-memory object p in the shared memory of cluster rank r.
 __device__ __forceinline__ uint32_t cluster_addr(const void* p, int r) {
@@ -1091,15 +1101,93 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, int r) {
                : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(r));
   return out;
 }
-__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
+__device__ __forceinline__ void st_cluster(uint32_t a, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
 }
-__device__ __forceinline__ int ld_cluster_s32(uint32_t a) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
-  return v;
+__device__ __forceinline__ void st_cluster(uint32_t a, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster(uint32_t a, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+
+// Appends the entries of group g (first index e) that the predicate keeps; out of line so
+// that the sixteen call sites stay small.
+__device__ __noinline__ void row_push(RowSmem& sm, int* count, float4 g, int e, int V, float tv,
+                                      unsigned long long tau) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float v = comp(g, q);
+    const unsigned long long u = key(v, e + q);
+    if (e + q < V && v >= tv && u >= tau) {
+      const int at = atomicAdd(count, 1);
+      if (at < R_SURV) sm.surv[at] = u;
+    }
+  }
+}
+
+// The exact bound (rare): every thread's best entry as a key, the k-th best warp maximum,
+// the thread maxima at or above it, their k-th best tau, and the entries at or above tau
+// (at most k threads' entries). Called by the whole CTA; leaves the sm.ns2 survivors in
+// sm.surv (sm.nc, sm.ns2 and sm.tau start at zero).
+__device__ __forceinline__ void row_exact(RowSmem& sm, const float4 (&a)[R_NF], int V, int k) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float m = a[0].x;
+  int am = 0;
+#pragma unroll
+  for (int t = 1; t < 4 * R_NF; ++t) {
+    const float v = comp(a[t >> 2], t & 3);
+    if (v > m) { m = v; am = t; }
+  }
+  const int mi = 4 * tid + 4 * R_THREADS * (am >> 2) + (am & 3);
+  const unsigned long long kt = 4 * tid < V ? key(m, mi) : 0ull;
+  {
+    const unsigned h = __reduce_max_sync(FULL, (unsigned)(kt >> 32));
+    const unsigned l = __reduce_max_sync(FULL, (unsigned)(kt >> 32) == h ? (unsigned)kt : 0u);
+    if (lane == 0) sm.wkey[warp] = ((unsigned long long)h << 32) | l;
+  }
+  __syncthreads();
+  unsigned long long tau1;
+  {
+    const unsigned long long mine = lane < R_WARPS ? sm.wkey[lane] : 0ull;
+    int rank = 0;
+#pragma unroll
+    for (int o = 0; o < R_WARPS; ++o) {
+      const unsigned long long w = sm.wkey[o];
+      rank += (w > mine || (w == mine && o < lane)) ? 1 : 0;
+    }
+    const unsigned sel = __ballot_sync(FULL, lane < R_WARPS && rank == k - 1);
+    tau1 = __shfl_sync(FULL, mine, __ffs(sel) - 1);
+  }
+  {
+    const bool c = kt != 0ull && kt >= tau1;
+    const unsigned bal = __ballot_sync(FULL, c);
+    if (bal) {
+      const int leader = __ffs(bal) - 1;
+      int at = 0;
+      if (lane == leader) at = atomicAdd(&sm.nc, __popc(bal));
+      at = __shfl_sync(FULL, at, leader);
+      if (c) sm.cand[at + __popc(bal & ((1u << lane) - 1u))] = kt;
+    }
+  }
+  __syncthreads();
+  const int nc = sm.nc;  // 0 < nc: fewer than k means every entry survives (tau stays 0)
+  for (int c = tid; c < nc; c += R_THREADS) {
+    const unsigned long long u = sm.cand[c];
+    int rank = 0;
+    for (int o = 0; o < nc; ++o) rank += sm.cand[o] > u ? 1 : 0;
+    if (rank == k - 1) sm.tau = u;
+  }
+  __syncthreads();
+  const unsigned long long tau = sm.tau;
+  if (kt != 0ull && kt >= tau) {
+    const float tv = tau != 0ull ? unord((unsigned)(tau >> 32)) : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < R_NF; ++j)
+      if (fmaxf(fmaxf(a[j].x, a[j].y), fmaxf(a[j].z, a[j].w)) >= tv)
+        row_push(sm, &sm.ns2, a[j], 4 * (tid + R_THREADS * j), V, tv, tau);
+  }
+  __syncthreads();
 }
 
 // grid (rows, batch), cluster (rows, 1, 1): blockIdx.x is the frontier row and the rank in
@@ -1111,17 +1199,22 @@ __global__ void __launch_bounds__(R_THREADS, 1) topk_row_kernel(const LevelArgs 
   const int s = blockIdx.x, b = blockIdx.y;
   const int rows = p.rows, k = p.k, V = p.vocab;
   const int r0 = b * rows + s;
+  // every CTA of the cluster has started before the first store into rank 0's memory
+  cluster_arrive_relaxed();
   if (tid == 0) {
-    sm.nc = 0;
     sm.ns = 0;
+    sm.ns2 = 0;
+    sm.nc = 0;
     sm.tau = 0ull;
   }
   griddep_wait();
   griddep_launch();  // one wave of CTAs: the next kernel may be scheduled beside it
+  const float pscore = p.level == 1 ? (p.product ? 1.0f : 0.0f) : p.front_score_in[r0];
+  const int pstore = p.level == 1 ? -1 : p.front_store_in[r0];
   const float* x = p.logits + (int64_t)r0 * p.row_stride;
 
   // entry 4 (tid + R_THREADS j) + q of the row sits in a[j], component q; entries past
-  // the row are -inf (never selected, zero exp-sum terms)
+  // the row are -inf (never kept, zero exp-sum terms)
   const float4 none = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
   float4 a[R_NF];
 #pragma unroll
@@ -1148,21 +1241,26 @@ __global__ void __launch_bounds__(R_THREADS, 1) topk_row_kernel(const LevelArgs 
     }
   }
 
-  // the thread's best entry: the first of its largest (entries run in ascending index)
-  const bool has = 4 * tid < V;
-  float m = a[0].x;
-  int am = 0;
+  // group maxima and the thread's largest value
+  float m4[R_NF];
 #pragma unroll
-  for (int t = 1; t < 4 * R_NF; ++t) {
-    const float v = comp(a[t >> 2], t & 3);
-    if (v > m) { m = v; am = t; }
+  for (int j = 0; j < R_NF; ++j) m4[j] = fmaxf(fmaxf(a[j].x, a[j].y), fmaxf(a[j].z, a[j].w));
+  float m;
+  {
+    float t8[R_NF / 2];
+#pragma unroll
+    for (int j = 0; j < R_NF / 2; ++j) t8[j] = fmaxf(m4[2 * j], m4[2 * j + 1]);
+    const float t4a = fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3]));
+    const float t4b = fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7]));
+    m = fmaxf(t4a, t4b);
   }
-  const int mi = 4 * tid + 4 * R_THREADS * (am >> 2) + (am & 3);
-  const unsigned long long kt = has ? key(m, mi) : 0ull;
-
+  {
+    const unsigned wm = __reduce_max_sync(FULL, ord(m));
+    if (lane == 0) sm.wmax[warp] = wm;
+  }
   // exp-sum against the thread's largest entry
   {
-    const float ref = fmaxf(m, -1e30f), rl = ref * L2E;
+    const float ref = fmaxf(m, -1e30f), rl = ref * L2E;  // finite: x = -inf gives 0
     float hi = 0.f, lo = 0.f;
 #pragma unroll
     for (int g = 0; g < R_NF / 4; ++g) {
@@ -1179,37 +1277,26 @@ __global__ void __launch_bounds__(R_THREADS, 1) topk_row_kernel(const LevelArgs 
     warp_combine(R, hi, lo);
     if (lane == 0) { sm.red[warp] = R; sm.shi[warp] = hi; sm.slo[warp] = lo; }
   }
-  // the warp's best entry
-  {
-    const unsigned h = __reduce_max_sync(FULL, (unsigned)(kt >> 32));
-    const unsigned l = __reduce_max_sync(FULL, (unsigned)(kt >> 32) == h ? (unsigned)kt : 0u);
-    if (lane == 0) sm.wkey[warp] = ((unsigned long long)h << 32) | l;
-  }
   __syncthreads();
 
-  // tau1: the k-th best warp maximum (every warp computes it; ties by warp)
-  unsigned long long tau1;
+  // t1: the k-th largest warp maximum (every warp computes it; ties by warp)
+  float tv;
   {
-    const unsigned long long mine = lane < R_WARPS ? sm.wkey[lane] : 0ull;
+    const unsigned mine = lane < R_WARPS ? sm.wmax[lane] : 0u;
     int rank = 0;
 #pragma unroll
     for (int o = 0; o < R_WARPS; ++o) {
-      const unsigned long long w = sm.wkey[o];
+      const unsigned w = sm.wmax[o];
       rank += (w > mine || (w == mine && o < lane)) ? 1 : 0;
     }
     const unsigned sel = __ballot_sync(FULL, lane < R_WARPS && rank == k - 1);
-    tau1 = __shfl_sync(FULL, mine, __ffs(sel) - 1);
+    tv = unord(__shfl_sync(FULL, mine, __ffs(sel) - 1));
   }
-  {  // candidates: thread maxima at or above tau1
-    const bool c = kt != 0ull && kt >= tau1;
-    const unsigned bal = __ballot_sync(FULL, c);
-    if (bal) {
-      const int leader = __ffs(bal) - 1;
-      int at = 0;
-      if (lane == leader) at = atomicAdd(&sm.nc, __popc(bal));
-      at = __shfl_sync(FULL, at, leader);
-      if (c) sm.cand[at + __popc(bal & ((1u << lane) - 1u))] = kt;
-    }
+  // survivors: entries of value tv or more
+  if (m >= tv) {
+#pragma unroll
+    for (int j = 0; j < R_NF; ++j)
+      if (m4[j] >= tv) row_push(sm, &sm.ns, a[j], 4 * (tid + R_THREADS * j), V, tv, 0ull);
   }
   if (warp == R_WARPS - 1) {  // the row's exp-sum
     float rr = lane < R_WARPS ? sm.red[lane] : -INFINITY;
@@ -1219,82 +1306,82 @@ __global__ void __launch_bounds__(R_THREADS, 1) topk_row_kernel(const LevelArgs 
     if (lane == 0) { sm.lse[0] = rr; sm.lse[1] = logf(hh); sm.lse[2] = ll / hh; }
   }
   __syncthreads();
-
-  // tau: the k-th best thread maximum (0 when fewer than k threads hold entries)
-  const int nc = sm.nc;
-  for (int c = tid; c < nc; c += R_THREADS) {
-    const unsigned long long u = sm.cand[c];
-    int rank = 0;
-    for (int o = 0; o < nc; ++o) rank += sm.cand[o] > u ? 1 : 0;
-    if (rank == k - 1) sm.tau = u;
+  int S = sm.ns;
+  if (S > R_SURV) {  // block-uniform
+    row_exact(sm, a, V, k);
+    S = sm.ns2;
   }
-  __syncthreads();
 
-  // survivors: entries at or above tau, from the threads whose maximum reaches it
-  const unsigned long long tau = sm.tau;
-  if (kt != 0ull && kt >= tau) {
-    const float tv = tau != 0ull ? unord((unsigned)(tau >> 32)) : -INFINITY;
-#pragma unroll
-    for (int j = 0; j < R_NF; ++j) {
-      if (fmaxf(fmaxf(a[j].x, a[j].y), fmaxf(a[j].z, a[j].w)) >= tv) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int e = 4 * (tid + R_THREADS * j) + q;
-          const unsigned long long u = key(comp(a[j], q), e);
-          if (e < V && u >= tau) sm.surv[atomicAdd(&sm.ns, 1)] = u;
-        }
-      }
-    }
-  }
-  __syncthreads();
-
-  // the row's top k by rank among the survivors; log-probabilities and cumulative scores
-  const int S = sm.ns;
+  // the row's top k by rank among the survivors (one warp with shuffles when they fit a
+  // warp), stored into rank 0's shared memory as joint keys
   const int off = p.level == 1 ? 0 : k + (p.level - 2) * k * k;
-  const int64_t srow = (int64_t)b * p.store_cap;
-  const float pscore = p.level == 1 ? (p.product ? 1.0f : 0.0f) : p.front_score_in[r0];
-  const int pstore = p.level == 1 ? -1 : p.front_store_in[r0];
-  for (int t = tid; t < S; t += R_THREADS) {
-    const unsigned long long u = sm.surv[t];
-    int rank = 0;
-    for (int o = 0; o < S; ++o) rank += sm.surv[o] > u ? 1 : 0;
-    if (rank < k) {
-      const float v = unord((unsigned)(u >> 32));
-      const int i = (int)~(unsigned)u;
-      const float logp = ((v - sm.lse[0]) - sm.lse[1]) - sm.lse[2];
-      const float cu = p.product ? pscore * expf(logp) : pscore + logp;
-      const int flat = s * k + rank;
-      p.store_token[srow + off + flat] = i;
-      p.store_score[srow + off + flat] = cu;
-      p.store_parent[srow + off + flat] = pstore;
-      sm.cu[rank] = cu;
-      sm.tok[rank] = i;
+  if (s == 0 && tid >= rows * k && tid < (rows * k + 7) / 8 * 8) sm.jkey[tid] = 0ull;  // padding
+  cluster_wait();  // every CTA of the cluster has started
+  float cu = 0.f;
+  int tok = -1, flat = -1;
+  auto take = [&](unsigned long long u, int rank) {
+    if (flat >= 0) {  // a second candidate of this thread (more than R_THREADS survivors)
+      const int64_t at = (int64_t)b * p.store_cap + off + flat;
+      p.store_token[at] = tok;
+      p.store_score[at] = cu;
+      p.store_parent[at] = pstore;
+    }
+    const float v = unord((unsigned)(u >> 32));
+    const float logp = ((v - sm.lse[0]) - sm.lse[1]) - sm.lse[2];
+    cu = p.product ? pscore * expf(logp) : pscore + logp;
+    tok = (int)~(unsigned)u;
+    flat = s * k + rank;
+    const float cz = cu == 0.f ? 0.f : cu;  // -0 and +0 tie, as the comparison of scores has it
+    st_cluster(cluster_addr(&sm.jkey[flat], 0), ((unsigned long long)ord(cz) << 32) | ~(unsigned)flat);
+    st_cluster(cluster_addr(&sm.jtok[flat], 0), tok);
+  };
+  if (S <= 32) {
+    if (warp == 0) {
+      const unsigned long long u = lane < S ? sm.surv[lane] : 0ull;
+      int rank = 0;
+#pragma unroll
+      for (int o = 0; o < 32; ++o) rank += __shfl_sync(FULL, u, o) > u ? 1 : 0;
+      if (lane < S && rank < k) take(u, rank);
+    }
+  } else {
+    for (int t = tid; t < S; t += R_THREADS) {
+      const unsigned long long u = sm.surv[t];
+      int rank = 0;
+      for (int o = 0; o < S; ++o) rank += sm.surv[o] > u ? 1 : 0;
+      if (rank < k) take(u, rank);
     }
   }
-  cluster_sync_all();  // every row's scores are visible across the cluster
-
-  const int nf = rows * k;
-  if (s == 0 && tid < nf) {
-    const int src = tid / k, j = tid - src * k;
-    sm.all_cu[tid] = ld_cluster_f32(cluster_addr(&sm.cu[j], src));
-    sm.all_tok[tid] = ld_cluster_s32(cluster_addr(&sm.tok[j], src));
+  cluster_arrive_release();
+  if (flat >= 0) {  // the row's candidates (after the release: it does not wait for them)
+    const int64_t at = (int64_t)b * p.store_cap + off + flat;
+    p.store_token[at] = tok;
+    p.store_score[at] = cu;
+    p.store_parent[at] = pstore;
   }
-  cluster_sync_all();  // rank 0 is done reading the others' shared memory
+  cluster_wait();  // rank 0: every row's keys have landed
   if (s != 0) return;
-  // Joint top-K over the rows * K cumulative scores (ties to the lower flat index), as in
-  // the per-unit path's request merge.
-  if (tid < nf) {
-    const float cv = sm.all_cu[tid];
+
+  // Joint top-K over the rows * K candidates: a candidate's rank is the number of larger
+  // keys (larger cumulative score, then lower flat index). Four lanes per candidate count
+  // a quarter of the keys each (two keys per 128-bit load; the padding keys are zero).
+  const int nf = rows * k, n2 = (nf + 7) / 8 * 4;  // key pairs
+  const ulonglong2* kp = reinterpret_cast<const ulonglong2*>(sm.jkey);
+  for (int f0 = 0; f0 < nf; f0 += R_THREADS / 4) {
+    if (f0 + 8 * warp >= nf) break;  // warp-uniform: the warp's eight candidates are past the end
+    const int f = f0 + (tid >> 2), part = tid & 3;
+    const unsigned long long kf = f < nf ? sm.jkey[f] : ~0ull;
     int rank = 0;
 #pragma unroll 4
-    for (int u = 0; u < nf; ++u) {
-      const float o = sm.all_cu[u];
-      rank += (o > cv || (o == cv && u < tid)) ? 1 : 0;
+    for (int u = part; u < n2; u += 4) {
+      const ulonglong2 x = kp[u];
+      rank += (x.x > kf ? 1 : 0) + (x.y > kf ? 1 : 0);
     }
-    if (rank < k) {
-      p.front_token_out[b * k + rank] = sm.all_tok[tid];
-      p.front_score_out[b * k + rank] = cv;
-      p.front_store_out[b * k + rank] = off + tid;
+    rank += __shfl_xor_sync(FULL, rank, 1);
+    rank += __shfl_xor_sync(FULL, rank, 2);
+    if (part == 0 && f < nf && rank < k) {
+      p.front_token_out[b * k + rank] = sm.jtok[f];
+      p.front_score_out[b * k + rank] = unord((unsigned)(kf >> 32));
+      p.front_store_out[b * k + rank] = off + f;
     }
   }
 }
