@@ -248,3 +248,64 @@ def test_large_batch_shares(v, k, b, pad, product):
             np.testing.assert_allclose(ss[bi, :c], exp.store_score, rtol=gc.SCORE_RTOL, atol=0)
     else:
         compare(reqs, k, stride_pad=pad)
+
+
+def _select_expected(score, parent, total):
+    """Kept store indices (the oracle's ordering: score, then lower index) and the tree
+    they form; a kept candidate whose parent was not kept hangs from the root (node 0)."""
+    best = sorted(draft.topk_by_score(score, total))
+    node_of = {c: i + 1 for i, c in enumerate(best)}
+    par = [-1] + [node_of.get(int(parent[c]), 0) if parent[c] >= 0 else 0 for c in best]
+    return best, par
+
+
+@pytest.mark.parametrize("case", ["spread", "coarse_ties", "all_equal", "narrow_bin",
+                                  "keep_all", "keep_one", "signed_zeros"])
+def test_select_final_thresholds(case):
+    """The final selection on synthetic stores: spread scores (one histogram pass and a
+    few candidates ranked in the threshold bin), scores on a coarse grid (ties inside the
+    bin), all-equal scores and a bin of about 600 candidates (the radix-select fallback),
+    every candidate kept, a single one kept, and -0 / +0 ties."""
+    import tree_speculative_decoding_verify_gb300 as T
+    rng = np.random.default_rng(sum(map(ord, case)))
+    C, total = 4096, 60
+    if case == "spread":
+        score = (rng.standard_normal(C) * 4 - 10).astype(np.float32)
+    elif case == "coarse_ties":
+        C = 610
+        score = np.round(rng.standard_normal(C) * 3 - 8).astype(np.float32)
+    elif case == "all_equal":
+        score = np.full(C, -3.5, dtype=np.float32)
+    elif case == "narrow_bin":
+        C = 3000
+        score = (-8.0 - rng.random(C) * 0.9).astype(np.float32)  # one 12-bit bin
+        total = 100
+    elif case == "keep_all":
+        C = 250  # total_tokens + 1 nodes, at most 256
+        score = (rng.standard_normal(C) - 5).astype(np.float32)
+        total = C
+    elif case == "keep_one":
+        score = (rng.standard_normal(C) - 5).astype(np.float32)
+        total = 1
+    else:
+        C = 200
+        score = np.where(rng.random(C) < 0.5, np.float32(0.0), np.float32(-0.0)).astype(np.float32)
+        score[::7] = -1.0
+        total = 50
+    parent = np.array([-1 if c < 10 else int(rng.integers(0, c)) for c in range(C)], np.int32)
+    token = (np.arange(C) + 1000).astype(np.int32)
+    d = gc.dev()
+    nodes = total + 1
+    tok = torch.zeros(1, nodes + 2, dtype=torch.int32, device=d)
+    par = torch.zeros_like(tok)
+    nn = torch.zeros(1, dtype=torch.int32, device=d)
+    T.draft_select_final(gc.i32(token[None]), torch.from_numpy(score[None]).to(d),
+                         gc.i32(parent[None]), C, total, gc.i32(np.array([7], np.int32)),
+                         tok, par, nn)
+    torch.cuda.synchronize()
+    best, exp_par = _select_expected(score, parent, total)
+    got_tok = tok.cpu().numpy()[0]
+    assert got_tok[0] == 7 and nn.item() == nodes
+    assert (got_tok[1:nodes] - 1000).tolist() == best
+    assert par.cpu().numpy()[0, :nodes].tolist() == exp_par
+    assert got_tok[nodes:].tolist() == [-1, -1]

@@ -1387,16 +1387,27 @@ __global__ void __launch_bounds__(R_THREADS, 1) topk_row_kernel(const LevelArgs 
 }
 
 // ---- final selection --------------------------------------------------------------
-// The total_tokens-th best key (ord() of the score) by a three-pass radix select over
-// shared-memory histograms (11, 11 and 10 bits); the kept candidates are the keys above
-// it plus, in ascending store index, as many of the keys equal to it as are still
-// needed. Node numbers (ascending store index) come from a block prefix sum.
+// The total_tokens best candidates by key (ord() of the score; -0 taken as +0), ties to
+// the lower store index. One 12-bit histogram pass finds the bin that holds the
+// total_tokens-th best key; the candidates of that bin (a few dozen on spread scores) are
+// ranked exactly by counting. When a bin holds more than F_BIN_MAX candidates (heavily
+// tied scores) a radix select over the remaining bits (11, 10 and 10 more bits... as three
+// passes over the full key) gives the threshold key and the number of its equal keys to
+// keep, in ascending store index. Node numbers (ascending store index) come from a block
+// prefix sum.
 constexpr int F_THREADS = 512;
-constexpr int F_MAX = 4096;   // candidates per request
-constexpr int F_BINS = 2048;  // histogram bins of the widest pass
+constexpr int F_WARPS = F_THREADS / 32;
+constexpr int F_MAX = 4096;                 // candidates per request
+constexpr int F_PER = F_MAX / F_THREADS;    // candidates per thread
+constexpr int F_TOP_BITS = 12;              // first pass: the key's top 12 bits
+constexpr int F_TOP_BINS = 1 << F_TOP_BITS;
+constexpr int F_BIN_MAX = 512;              // threshold-bin candidates ranked directly
+constexpr int F_BINS = 2048;                // histogram bins of the fallback's widest pass
 
-// Exclusive prefix sum of x over the block (thread order); s_warp holds F_THREADS / 32
-// partials. Ends with a barrier, so s_warp may be reused at once.
+__device__ __forceinline__ unsigned score_key(float x) { return ord(x == 0.f ? 0.f : x); }
+
+// Exclusive prefix sum of x over the block (thread order); s_warp holds F_WARPS
+// partials. One barrier: two calls on the same s_warp need a barrier between them.
 __device__ __forceinline__ int block_exclusive_scan(int x, int* s_warp) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = x;
@@ -1407,31 +1418,16 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int* s_warp) {
   }
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
-  int before = incl - x;
-  for (int w = 0; w < warp; ++w) before += s_warp[w];
-  __syncthreads();
-  return before;
+  const int ws = lane < F_WARPS && lane < warp ? s_warp[lane] : 0;
+  return __reduce_add_sync(FULL, ws) + incl - x;
 }
 
-__global__ void __launch_bounds__(F_THREADS)
-select_final_kernel(const int32_t* __restrict__ store_token, const float* __restrict__ store_score,
-                    const int32_t* __restrict__ store_parent, int C, int store_cap,
-                    int total, const int32_t* __restrict__ root_token, int max_nodes,
-                    int32_t* __restrict__ tokens, int32_t* __restrict__ parents,
-                    int32_t* __restrict__ num_nodes) {
-  __shared__ unsigned s_key[F_MAX];
-  __shared__ int s_node[F_MAX];
-  __shared__ unsigned s_hist[F_BINS];
-  __shared__ int s_warp[F_THREADS / 32];
-  __shared__ unsigned s_sel[2];
-  const int b = blockIdx.x, tid = threadIdx.x;
-  const int64_t srow = (int64_t)b * store_cap;
-  griddep_wait();
-  griddep_launch();
-  for (int c = tid; c < C; c += F_THREADS) s_key[c] = ord(store_score[srow + c]);
-
-  // radix select: after the passes, `prefix` is the total-th largest key and `need` the
-  // number of candidates with exactly that key that are kept (the lowest store indices)
+// Fallback radix select over the full keys: the total-th largest key and the number of
+// candidates with exactly that key that are kept (the lowest store indices).
+__device__ __noinline__ void radix_threshold(const unsigned* s_key, int C, int total,
+                                             unsigned* s_hist, int* s_warp, unsigned* s_sel,
+                                             unsigned& prefix_out, int& need_out) {
+  const int tid = threadIdx.x;
   unsigned prefix = 0;
   int need = total;
 #pragma unroll 1
@@ -1439,6 +1435,7 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
     const int bits = pass == 2 ? 10 : 11;
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int nb = 1 << bits, per = nb / F_THREADS;
+    __syncthreads();  // the previous users of s_hist, s_sel and s_warp are done
     for (int i = tid; i < nb; i += F_THREADS) s_hist[i] = 0u;
     __syncthreads();
     for (int c = tid; c < C; c += F_THREADS) {
@@ -1465,23 +1462,120 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
     __syncthreads();
     prefix = (prefix << bits) | s_sel[0];
     need -= (int)s_sel[1];
-    __syncthreads();  // s_sel and s_hist are rewritten by the next pass
   }
+  prefix_out = prefix;
+  need_out = need;
+  __syncthreads();
+}
 
-  // kept flags, then node numbers, over contiguous per-thread segments (store order)
+__global__ void __launch_bounds__(F_THREADS)
+select_final_kernel(const int32_t* __restrict__ store_token, const float* __restrict__ store_score,
+                    const int32_t* __restrict__ store_parent, int C, int store_cap,
+                    int total, const int32_t* __restrict__ root_token, int max_nodes,
+                    int32_t* __restrict__ tokens, int32_t* __restrict__ parents,
+                    int32_t* __restrict__ num_nodes) {
+  __shared__ unsigned s_key[F_MAX];
+  // the histogram until the threshold is known, then the kept flags and node numbers
+  static_assert(F_TOP_BINS == F_MAX && F_BINS <= F_TOP_BINS, "one array for both");
+  __shared__ unsigned s_hist[F_TOP_BINS];
+  int* s_node = reinterpret_cast<int*>(s_hist);
+  __shared__ unsigned long long s_bin[F_BIN_MAX];  // key above the complemented index
+  __shared__ int s_warp[2][F_WARPS];
+  __shared__ unsigned s_sel[2];
+  __shared__ int s_nbin;
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const int64_t srow = (int64_t)b * store_cap;
+  for (int i = tid; i < F_TOP_BINS; i += F_THREADS) s_hist[i] = 0u;
+  if (tid == 0) s_nbin = 0;
+  griddep_wait();
+  griddep_launch();
+  unsigned kr[F_PER];
+#pragma unroll
+  for (int i = 0; i < F_PER; ++i) {
+    const int c = tid + i * F_THREADS;
+    kr[i] = c < C ? score_key(store_score[srow + c]) : 0u;
+  }
+  __syncthreads();  // the histogram is clear
+#pragma unroll
+  for (int i = 0; i < F_PER; ++i) {
+    const int c = tid + i * F_THREADS;
+    if (c < C) {
+      s_key[c] = kr[i];
+      atomicAdd(&s_hist[kr[i] >> (32 - F_TOP_BITS)], 1u);
+    }
+  }
+  __syncthreads();
+  // the threshold bin: thread t holds bins F_TOP_BINS - 1 - 8t downwards
+  static_assert(F_TOP_BINS == 8 * F_THREADS, "eight bins per thread");
+  unsigned hv[8];
+  int local = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    hv[q] = s_hist[F_TOP_BINS - 1 - (tid * 8 + q)];
+    local += (int)hv[q];
+  }
+  int acc = block_exclusive_scan(local, s_warp[0]);  // candidates in the bins above
+  if (acc < total && total <= acc + local) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (acc < total && total <= acc + (int)hv[q]) {
+        s_sel[0] = (unsigned)(F_TOP_BINS - 1 - (tid * 8 + q));
+        s_sel[1] = (unsigned)acc;
+      }
+      acc += (int)hv[q];
+    }
+  }
+  __syncthreads();
+  const unsigned bin = s_sel[0];
+  const int need = total - (int)s_sel[1];  // candidates kept from the threshold bin
+#pragma unroll
+  for (int i = 0; i < F_PER; ++i) {
+    const int c = tid + i * F_THREADS;
+    if (c < C && (kr[i] >> (32 - F_TOP_BITS)) == bin) {
+      const int at = atomicAdd(&s_nbin, 1);
+      if (at < F_BIN_MAX) s_bin[at] = ((unsigned long long)kr[i] << 32) | ~(unsigned)c;
+    }
+  }
+  __syncthreads();
+  const int nbin = s_nbin;
+  if (nbin <= F_BIN_MAX) {  // block-uniform
+    // kept: the bins above; in the threshold bin, the `need` best by (key, lower index)
+#pragma unroll
+    for (int i = 0; i < F_PER; ++i) {
+      const int c = tid + i * F_THREADS;
+      if (c < C && (kr[i] >> (32 - F_TOP_BITS)) != bin)
+        s_node[c] = (kr[i] >> (32 - F_TOP_BITS)) > bin ? 1 : 0;
+    }
+    for (int t = tid; t < nbin; t += F_THREADS) {
+      const unsigned long long u = s_bin[t];
+      int rank = 0;
+#pragma unroll 4
+      for (int o = 0; o < nbin; ++o) rank += s_bin[o] > u ? 1 : 0;
+      s_node[~(unsigned)u] = rank < need ? 1 : 0;
+    }
+  } else {
+    unsigned prefix;
+    int need2;
+    radix_threshold(s_key, C, total, s_hist, s_warp[1], s_sel, prefix, need2);
+    // equal keys kept in ascending store index: contiguous per-thread segments
+    const int seg = (C + F_THREADS - 1) / F_THREADS;
+    const int c0 = min(C, tid * seg), c1 = min(C, c0 + seg);
+    int eq = 0;
+    for (int c = c0; c < c1; ++c) eq += s_key[c] == prefix ? 1 : 0;
+    int e = block_exclusive_scan(eq, s_warp[0]);
+    for (int c = c0; c < c1; ++c) {
+      const unsigned key = s_key[c];
+      s_node[c] = key > prefix || (key == prefix && e++ < need2) ? 1 : 0;
+    }
+  }
+  __syncthreads();
+
+  // node numbers in ascending store index, over contiguous per-thread segments
   const int seg = (C + F_THREADS - 1) / F_THREADS;
   const int c0 = min(C, tid * seg), c1 = min(C, c0 + seg);
-  int eq = 0;
-  for (int c = c0; c < c1; ++c) eq += s_key[c] == prefix ? 1 : 0;
-  int e = block_exclusive_scan(eq, s_warp);
   int mine = 0;
-  for (int c = c0; c < c1; ++c) {
-    const unsigned key = s_key[c];
-    const bool kept = key > prefix || (key == prefix && e++ < need);
-    s_node[c] = kept ? 1 : 0;
-    mine += kept ? 1 : 0;
-  }
-  int before = block_exclusive_scan(mine, s_warp);
+  for (int c = c0; c < c1; ++c) mine += s_node[c];
+  int before = block_exclusive_scan(mine, s_warp[1]);
   for (int c = c0; c < c1; ++c)
     if (s_node[c]) s_node[c] = 1 + before++;
   __syncthreads();
