@@ -5,6 +5,7 @@
  *   tsv_draft_topk_expand   one level of the draft tree expansion (per-row log-softmax +
  *                           top-k, cumulative scores, joint top-k pruning)
  *   tsv_draft_select_final  the total_tokens best candidates laid out as a tree
+ *   tsv_draft_select_tree   tsv_draft_select_final and tsv_tree_build_meta in one launch
  *   tsv_draft_topk_expand_product, tsv_draft_to_target, tsv_draft_fixed_level
  *                           expansion variants: probability-product scores, the d2t id
  *                           map, fixed-branching trees
@@ -282,6 +283,27 @@ int tsv_tree_build_meta(const int32_t* parents, const int32_t* num_nodes,
                         uint32_t* mask, int32_t* position_ids, int32_t* retrieve_indices,
                         int32_t* num_leaves, int32_t* next_token, int32_t* next_sibling,
                         int32_t* err, tsv_stream_t stream);
+
+/* --------------------------------------------------------------------------------
+ * tsv_draft_select_tree — tsv_draft_select_final followed by tsv_tree_build_meta of
+ * the selected trees, in one launch.
+ *
+ * [EAGLE2] section 3 (the total_tokens best candidates as a tree, then the tree's
+ * retrieve_indices) with the metadata of [HB] section 实现 and [TRT] section
+ * 树构建内核做了什么. The arguments up to num_nodes are those of tsv_draft_select_final
+ * (num_nodes may be NULL); prefix_len .. err are those of tsv_tree_build_meta, whose
+ * parents and num_nodes are the selected trees here (total_tokens + 1 nodes). Every
+ * output and every error state is the one of the two calls made in order; err may be
+ * NULL. Returns TSV_ERR_INVALID_ARG where either call would.
+ * ------------------------------------------------------------------------------ */
+int tsv_draft_select_tree(const int32_t* store_token, const float* store_score,
+                          const int32_t* store_parent, int batch, int num_candidates,
+                          int store_cap, int total_tokens, const int32_t* root_token,
+                          int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
+                          const int32_t* prefix_len, int max_depth, uint32_t* mask,
+                          int32_t* position_ids, int32_t* retrieve_indices, int32_t* num_leaves,
+                          int32_t* next_token, int32_t* next_sibling, int32_t* err,
+                          tsv_stream_t stream);
 
 /* --------------------------------------------------------------------------------
  * tsv_draft_grow_mask — the drafter's ancestor mask, grown by one level.

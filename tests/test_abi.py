@@ -61,6 +61,17 @@ def test_host_validation_rejects_bad_arguments(lib):
                                      p, p, p, p, p, p, p, 8, None) == 3
     # select_final: total_tokens above the candidate count
     assert lib.tsv_draft_select_final(p, p, p, 1, 10, 10, 11, p, 64, p, p, None, None) == 1
+    # select_tree: the same check, a depth past TSV_MAX_DEPTH, a missing metadata array;
+    # an empty batch is a no-op
+    meta = [p] * 6 + [None]
+    assert lib.tsv_draft_select_tree(p, p, p, 1, 10, 10, 11, p, 64, p, p, None, p, 8, *meta,
+                                     None) == 1
+    assert lib.tsv_draft_select_tree(p, p, p, 1, 10, 10, 5, p, 64, p, p, None, p, 99, *meta,
+                                     None) == 1
+    assert lib.tsv_draft_select_tree(p, p, p, 1, 10, 10, 5, p, 64, p, p, None, p, 8, None,
+                                     *meta[1:], None) == 1
+    assert lib.tsv_draft_select_tree(None, None, None, 0, 10, 10, 5, None, 64, None, None, None,
+                                     None, 8, *([None] * 7), None) == 0
     # attention: unsupported head_dim, GQA mismatch, missing workspace
     k = ctypes.c_void_p(256)
     cache = _lib.KVCacheDesc(k, k, 1, 8, 96, 0, 128, None, 0, 0, 1, 0)

@@ -309,3 +309,43 @@ def test_select_final_thresholds(case):
     assert (got_tok[1:nodes] - 1000).tolist() == best
     assert par.cpu().numpy()[0, :nodes].tolist() == exp_par
     assert got_tok[nodes:].tolist() == [-1, -1]
+
+
+def test_select_tree_matches_the_two_calls():
+    """tsv_draft_select_tree (selection and metadata in one launch) against
+    tsv_draft_select_final followed by tsv_tree_build_meta on the same stores: every
+    output identical, on three expanded requests with different prefix lengths."""
+    import tree_speculative_decoding_verify_gb300 as T
+    w = W.WORKLOADS["llama8b"]
+    k, depth, total = w.top_k, w.depth, w.total_tokens
+    reqs = [gc.level_logits(w, 0)]
+    rng = np.random.default_rng(31)
+    for _ in range(2):
+        reqs.append([(rng.standard_normal((1 if l == 0 else k, w.vocab)) * 2).astype(np.float32)
+                     for l in range(depth + 1)])
+    st, ss, sp, _ = run_levels(reqs, k)
+    d = gc.dev()
+    b, t, cols = len(reqs), w.num_nodes + 3, depth + 2
+    words = (t + 31) // 32
+    st, ss, sp = gc.i32(st), torch.from_numpy(ss).to(d), gc.i32(sp)
+    root = gc.i32(np.array([5, 6, 7], np.int32))
+    prefix = gc.i32(np.array([2048, 17, 0], np.int32))
+
+    def outs():
+        z = lambda *shape: torch.full(shape, -9, dtype=torch.int32, device=d)
+        return dict(tok=z(b, t), par=z(b, t), nn=z(b), mask=z(b, t, words), pos=z(b, t),
+                    ret=z(b, t, cols), nl=z(b), nt=z(b, t), ns=z(b, t), err=z(b))
+
+    a, c = outs(), outs()
+    T.draft_select_final(st, ss, sp, w.num_candidates, total, root, a["tok"], a["par"], a["nn"])
+    T.tree_build_meta(a["par"], a["nn"], prefix, cols - 1, a["mask"], a["pos"], a["ret"],
+                      a["nl"], a["nt"], a["ns"], a["err"])
+    T.draft_select_tree(st, ss, sp, w.num_candidates, total, root, c["tok"], c["par"], c["nn"],
+                        prefix, cols - 1, c["mask"], c["pos"], c["ret"], c["nl"], c["nt"],
+                        c["ns"], c["err"])
+    torch.cuda.synchronize()
+    for name in a:
+        assert torch.equal(a[name], c[name]), name
+    assert c["err"].cpu().tolist() == [0, 0, 0]
+    tokens, parents, _ = gc.oracle_tree(w, 0)
+    assert c["tok"].cpu().numpy()[0, :w.num_nodes].tolist() == [5] + tokens.tolist()[1:]

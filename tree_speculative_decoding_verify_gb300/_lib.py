@@ -76,6 +76,9 @@ _SIGNATURES = {
                               [ctypes.c_void_p] * 3),
     "tsv_draft_select_final": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 +
                                [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 4),
+    "tsv_draft_select_tree": (ctypes.c_int, [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4 +
+                              [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 4 +
+                              [ctypes.c_int] + [ctypes.c_void_p] * 8),
     "tsv_tree_verify_attn_workspace_size": (ctypes.c_size_t, [ctypes.c_void_p] * 2),
     "tsv_tree_verify_attn_launches": (ctypes.c_int, [ctypes.c_void_p] * 2),
     "tsv_tree_verify_attn": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_float] * 2 +
@@ -330,6 +333,41 @@ def draft_select_final(store_token, store_score, store_parent, num_candidates, t
                                         b, num_candidates, cap, total_tokens, _ptr(root_token), t,
                                         _ptr(tokens), _ptr(parents), _ptr(num_nodes), _stream()),
            "tsv_draft_select_final")
+
+
+def draft_select_tree(store_token, store_score, store_parent, num_candidates, total_tokens,
+                      root_token, tokens, parents, num_nodes, prefix_len, max_depth, mask,
+                      position_ids, retrieve_indices, num_leaves, next_token, next_sibling,
+                      err=None):
+    """draft_select_final and tree_build_meta of the selected trees in one launch."""
+    b, cap = store_token.shape
+    _need(store_token, torch.int32, "store_token")
+    _need(store_score, torch.float32, "store_score", (b, cap))
+    _need(store_parent, torch.int32, "store_parent", (b, cap))
+    _need(root_token, torch.int32, "root_token", (b,))
+    t = tokens.shape[1]
+    w = (t + 31) // 32
+    _need(tokens, torch.int32, "tokens", (b, t))
+    _need(parents, torch.int32, "parents", (b, t))
+    if num_nodes is not None:
+        _need(num_nodes, torch.int32, "num_nodes", (b,))
+    _need(prefix_len, torch.int32, "prefix_len", (b,))
+    _need(mask, torch.int32, "mask", (b, t, w))
+    _need(position_ids, torch.int32, "position_ids", (b, t))
+    _need(retrieve_indices, torch.int32, "retrieve_indices", (b, t, max_depth + 1))
+    _need(num_leaves, torch.int32, "num_leaves", (b,))
+    _need(next_token, torch.int32, "next_token", (b, t))
+    _need(next_sibling, torch.int32, "next_sibling", (b, t))
+    if err is not None:
+        _need(err, torch.int32, "err", (b,))
+    _check(lib().tsv_draft_select_tree(_ptr(store_token), _ptr(store_score), _ptr(store_parent),
+                                       b, num_candidates, cap, total_tokens, _ptr(root_token), t,
+                                       _ptr(tokens), _ptr(parents), _ptr(num_nodes),
+                                       _ptr(prefix_len), max_depth, _ptr(mask),
+                                       _ptr(position_ids), _ptr(retrieve_indices),
+                                       _ptr(num_leaves), _ptr(next_token), _ptr(next_sibling),
+                                       _ptr(err), _stream()),
+           "tsv_draft_select_tree")
 
 
 def _attn_shape(q: torch.Tensor, max_prefix: int) -> AttnShape:

@@ -267,7 +267,31 @@ int tsv_draft_select_final(const int32_t* store_token, const float* store_score,
     return TSV_ERR_INVALID_ARG;
   return launch_select_final(store_token, store_score, store_parent, batch, num_candidates,
                              store_cap, total_tokens, root_token, max_nodes, tokens, parents,
-                             num_nodes, (cudaStream_t)stream);
+                             num_nodes, nullptr, 0, nullptr, (cudaStream_t)stream);
+}
+
+int tsv_draft_select_tree(const int32_t* store_token, const float* store_score,
+                          const int32_t* store_parent, int batch, int num_candidates,
+                          int store_cap, int total_tokens, const int32_t* root_token,
+                          int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
+                          const int32_t* prefix_len, int max_depth, uint32_t* mask,
+                          int32_t* position_ids, int32_t* retrieve_indices, int32_t* num_leaves,
+                          int32_t* next_token, int32_t* next_sibling, int32_t* err,
+                          tsv_stream_t stream) {
+  if (batch < 0 || total_tokens < 1 || num_candidates < total_tokens || num_candidates > 4096 ||
+      store_cap < num_candidates || max_nodes < total_tokens + 1 || max_nodes > TSV_MAX_NODES ||
+      max_depth < 0 || max_depth > TSV_MAX_DEPTH)
+    return TSV_ERR_INVALID_ARG;
+  if (batch == 0) return TSV_OK;
+  if (!store_token || !store_score || !store_parent || !root_token || !tokens || !parents ||
+      !prefix_len || !mask || !position_ids || !retrieve_indices || !num_leaves || !next_token ||
+      !next_sibling)
+    return TSV_ERR_INVALID_ARG;
+  const MetaOut meta{mask, position_ids, retrieve_indices, num_leaves, next_token, next_sibling,
+                     err};
+  return launch_select_final(store_token, store_score, store_parent, batch, num_candidates,
+                             store_cap, total_tokens, root_token, max_nodes, tokens, parents,
+                             num_nodes, prefix_len, max_depth, &meta, (cudaStream_t)stream);
 }
 
 size_t tsv_tree_verify_attn_workspace_size(const tsv_attn_shape* shape,

@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tree_meta.cuh"
 
 namespace tsv {
 namespace {
@@ -1473,7 +1474,8 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
                     const int32_t* __restrict__ store_parent, int C, int store_cap,
                     int total, const int32_t* __restrict__ root_token, int max_nodes,
                     int32_t* __restrict__ tokens, int32_t* __restrict__ parents,
-                    int32_t* __restrict__ num_nodes) {
+                    int32_t* __restrict__ num_nodes, const int32_t* __restrict__ prefix_len,
+                    int max_depth, MetaOut meta) {
   __shared__ unsigned s_key[F_MAX];
   // the histogram until the threshold is known, then the kept flags and node numbers
   static_assert(F_TOP_BINS == F_MAX && F_BINS <= F_TOP_BINS, "one array for both");
@@ -1483,6 +1485,9 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
   __shared__ int s_warp[2][F_WARPS];
   __shared__ unsigned s_sel[2];
   __shared__ int s_nbin;
+  // the tree's metadata (meta.mask set): parents by node, the builder's scratch
+  __shared__ int32_t s_tpar[TSV_MAX_NODES], s_dep[TSV_MAX_NODES], s_first[TSV_MAX_NODES],
+      s_last[TSV_MAX_NODES];
   const int b = blockIdx.x, tid = threadIdx.x;
   const int64_t srow = (int64_t)b * store_cap;
   for (int i = tid; i < F_TOP_BINS; i += F_THREADS) s_hist[i] = 0u;
@@ -1593,7 +1598,16 @@ select_final_kernel(const int32_t* __restrict__ store_token, const float* __rest
     if (!node) continue;
     tokens[trow + node] = store_token[srow + c];
     const int p = store_parent[srow + c];
-    parents[trow + node] = (p >= 0 && p < C) ? s_node[p] : 0;
+    const int pn = (p >= 0 && p < C) ? s_node[p] : 0;
+    parents[trow + node] = pn;
+    s_tpar[node] = pn;
+  }
+  if (meta.mask) {  // the tree's metadata, from the parents in shared memory
+    if (tid == 0) s_tpar[0] = -1;
+    __syncthreads();
+    if (tid < 32)
+      build_meta_warp(b, s_tpar, total + 1, prefix_len[b], max_nodes, max_depth, meta, s_tpar,
+                      s_dep, s_first, s_last);
   }
 }
 
@@ -1779,11 +1793,14 @@ int launch_select_final(const int32_t* store_token, const float* store_score,
                         const int32_t* store_parent, int batch, int num_candidates,
                         int store_cap, int total_tokens, const int32_t* root_token,
                         int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
+                        const int32_t* prefix_len, int max_depth, const MetaOut* meta,
                         cudaStream_t stream) {
   if (num_candidates > F_MAX) return TSV_ERR_INVALID_ARG;
+  const MetaOut none{};
   return launch_pdl(select_final_kernel, dim3(batch), dim3(F_THREADS), 0, stream, store_token,
                     store_score, store_parent, num_candidates, store_cap, total_tokens,
-                    root_token, max_nodes, tokens, parents, num_nodes);
+                    root_token, max_nodes, tokens, parents, num_nodes, prefix_len, max_depth,
+                    meta ? *meta : none);
 }
 
 }  // namespace tsv

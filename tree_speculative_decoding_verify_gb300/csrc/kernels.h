@@ -75,10 +75,23 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
                        float* store_score, int32_t* store_parent, int32_t* front_token_out,
                        float* front_score_out, int32_t* front_store_out, void* ws,
                        const TopkPlan& plan, bool product, cudaStream_t stream);
+// Outputs of the tree metadata build (the arrays of tsv_tree_build_meta).
+struct MetaOut {
+  uint32_t* mask;
+  int32_t* position_ids;
+  int32_t* retrieve;
+  int32_t* num_leaves;
+  int32_t* next_token;
+  int32_t* next_sibling;
+  int32_t* err;
+};
+// meta (may be null): also build the selected trees' metadata in the same launch, with
+// prefix_len and max_depth as tsv_tree_build_meta takes them.
 int launch_select_final(const int32_t* store_token, const float* store_score,
                         const int32_t* store_parent, int batch, int num_candidates,
                         int store_cap, int total_tokens, const int32_t* root_token,
                         int max_nodes, int32_t* tokens, int32_t* parents, int32_t* num_nodes,
+                        const int32_t* prefix_len, int max_depth, const MetaOut* meta,
                         cudaStream_t stream);
 
 // Expansion variants.

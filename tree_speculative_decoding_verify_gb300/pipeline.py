@@ -97,11 +97,12 @@ class HotPath:
 
     # -- stages ------------------------------------------------------------------------
     def expand(self, level_logits: Sequence[torch.Tensor], root_token: torch.Tensor,
-               level_ready: Optional[Sequence[torch.cuda.Event]] = None):
+               level_ready: Optional[Sequence[torch.cuda.Event]] = None, select: bool = True):
         """level_logits[0]: [B, 1, V]; level_logits[l]: [B, K, V] fp32 (device).
         level_ready[l] (optional): an event after which level l's logits (and, for l = 0,
         root_token) are in place; the stream waits for it just before that level, so
-        the logits of later levels can still be arriving while earlier levels run."""
+        the logits of later levels can still be arriving while earlier levels run.
+        select=False stops after the last level (select_tree then lays out the tree)."""
         s = self.s
         if len(level_logits) != s.depth + 1:
             raise ValueError(f"expected {s.depth + 1} levels of logits")
@@ -117,9 +118,20 @@ class HotPath:
                                    nxt[0], nxt[1], nxt[2], self.topk_ws,
                                    product=s.score_product)
             cur = nxt
-        _lib.draft_select_final(self.store_token, self.store_score, self.store_parent,
-                                s.num_candidates, s.total_tokens, root_token, self.tokens,
-                                self.parents, self.num_nodes)
+        if select:
+            _lib.draft_select_final(self.store_token, self.store_score, self.store_parent,
+                                    s.num_candidates, s.total_tokens, root_token, self.tokens,
+                                    self.parents, self.num_nodes)
+
+    def select_tree(self, root_token: torch.Tensor, prefix_len: torch.Tensor):
+        """The final selection and the selected trees' metadata in one launch (after
+        expand(..., select=False)): the outputs of expand's selection and of build_meta."""
+        s = self.s
+        _lib.draft_select_tree(self.store_token, self.store_score, self.store_parent,
+                               s.num_candidates, s.total_tokens, root_token, self.tokens,
+                               self.parents, self.num_nodes, prefix_len, s.max_depth, self.mask,
+                               self.position_ids, self.retrieve, self.num_leaves,
+                               self.next_token, self.next_sibling, self.meta_err)
 
     def expand_fixed(self, level_logits: Sequence[torch.Tensor], root_token: torch.Tensor,
                      branching: Sequence[int]):
@@ -210,10 +222,13 @@ class HotPath:
         arguments of sample_accept but prefix_len; target_argmax None) the acceptance is
         the non-greedy one."""
         if not self.s.fixed_nodes:
-            self.expand(level_logits, root_token, level_ready)
+            self.expand(level_logits, root_token, level_ready, select=False)
         if inputs_ready is not None:
             torch.cuda.current_stream().wait_event(inputs_ready)
-        self.build_meta(prefix_len)
+        if self.s.fixed_nodes:
+            self.build_meta(prefix_len)
+        else:
+            self.select_tree(root_token, prefix_len)
         self.verify(q, k_new, v_new, prefix_len, rope_theta, softmax_scale)
         if sampling is not None:
             if target_argmax is not None or hidden is not None:
@@ -230,13 +245,14 @@ class HotPath:
     # launches of libtsv kernels per step (for the bench's launch count)
     def kernels_per_step(self, lm_head: bool = False) -> int:
         """libtsv kernels one step launches: one or two per expansion level (two for a
-        large batch: streaming + merge), the final selection, the metadata, the attention
-        call, the lm_head stage (GEMM + finalize) when it runs, and the acceptance."""
+        large batch: streaming + merge), the final selection with the metadata (or the
+        metadata alone for a fixed tree), the attention call, the lm_head stage (GEMM +
+        finalize) when it runs, and the acceptance."""
         n = 0
         if not self.s.fixed_nodes:
             s = self.s
             n = sum(_lib.draft_topk_expand_launches(s.batch, 1 if lvl == 0 else s.top_k, s.vocab,
-                                                    s.top_k) for lvl in range(s.depth + 1)) + 1
+                                                    s.top_k) for lvl in range(s.depth + 1))
         return n + 1 + self.attn_kernels() + (2 if lm_head else 0) + 1
 
     def attn_kernels(self) -> int:
