@@ -24,8 +24,11 @@
 //       A node's filtered distribution is described by the largest
 //       logit m, c = log2(e)/temperature, a 64-bit key threshold, a min-p bound and the
 //       normaliser Z: token v is kept when its key (logit order, then the lower token id)
-//       is at least the threshold and its mass e_v = 2^((l_v - m) c) at least the min-p
-//       bound; p(v) = e_v / Z. Every pass keeps four 16-byte loads in flight per thread.
+//       is at least the threshold and its mass e_v = 2^(l_v c - m c) (one FFMA and the
+//       hardware base-2 exponential) at least the min-p bound; p(v) = e_v / Z. Every pass
+//       keeps four 16-byte loads in flight per thread. The first pass finds m (a float
+//       maximum and its first token); the second sums Z (fp32 groups of 16 terms, each
+//       added exactly into a (hi, lo) pair) and builds the histogram.
 //       Thresholds: a histogram of d = (m - l_v) c over 4096 linear bins of [0, 32) (the
 //       last bin also takes everything beyond) with exact 32-bit counts and fp32 masses
 //       locates the bins where the top-k count or the top-p mass is reached; those bins'
@@ -65,6 +68,7 @@ struct RowStats {
   float z;     // sum of the kept masses
   float m;     // largest logit
   float c;     // log2(e) / temperature; 0 = greedy (only the first maximum is kept)
+  float mc;    // m * c rounded once: a token's mass is 2^(l c - mc)
   float minp;  // kept: mass >= minp
 };
 
@@ -79,17 +83,29 @@ __device__ __forceinline__ float key_value(u64 k) {
   const unsigned u = (unsigned)(k >> 32);
   return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
 }
-// Mass relative to the largest logit (1 there; 0 for -inf).
-__device__ __forceinline__ float emass(float l, float m, float c) {
-  return c == 0.f ? 1.f : exp2f((l - m) * c);
+// A token's mass relative to the largest logit is 2^t with t = l c - m c, the exponent
+// from one FFMA against mc = m c rounded once per row (t <= 0 up to that rounding; -inf
+// for l = -inf), and 2^t from the hardware's base-2 exponential (relative error a few
+// units in the last place; masses below 2^-126 flush to zero). Greedy rows (c = 0) keep
+// mass 1. Every pass and the walk use these two functions, so the masses agree exactly.
+__device__ __forceinline__ float ex2a(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
-__device__ __forceinline__ int bin_of(float l, float m, float c) {
-  const float d = (m - l) * c;  // >= 0, non-decreasing as l decreases; NaN/inf -> last bin
-  return d < DR ? min(NB - 1, (int)(d * (NB / DR))) : NB - 1;
+__device__ __forceinline__ float expo(float l, float c, float mc) { return fmaf(l, c, -mc); }
+__device__ __forceinline__ float emass(float l, float c, float mc) {
+  return c == 0.f ? 1.f : ex2a(expo(l, c, mc));
 }
+// Histogram bin of exponent t: d = -t in [0, DR) over NB linear bins; -t >= DR (and
+// l = -inf) -> the last bin. Non-decreasing as l decreases.
+__device__ __forceinline__ int bin_t(float t) {
+  return t > -DR ? min(NB - 1, (int)(-t * (NB / DR))) : NB - 1;
+}
+__device__ __forceinline__ int bin_of(float l, float c, float mc) { return bin_t(expo(l, c, mc)); }
 __device__ __forceinline__ float kept_mass(const RowStats& st, float l, int v) {
   if (vkey(l, v) < st.thr) return 0.f;
-  const float e = emass(l, st.m, st.c);
+  const float e = emass(l, st.c, st.mc);
   return e >= st.minp ? e : 0.f;
 }
 
@@ -146,6 +162,73 @@ __device__ __forceinline__ void for_row(const float* __restrict__ row, int V, bo
   }
 }
 
+// for_row with g() called after every batch of (up to) 16 tokens a thread visits, and
+// after its last tokens: g closes a group of fp32 terms (see Pair).
+template <class F, class G>
+__device__ __forceinline__ void for_row_batched(const float* __restrict__ row, int V, bool vec,
+                                                F&& f, G&& g) {
+  const int bd = blockDim.x;
+  if (vec) {
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const int n4 = V >> 2;
+    int j = threadIdx.x;
+    for (; j + 3 * bd < n4; j += 4 * bd) {
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = __ldg(r4 + j + u * bd);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = 4 * (j + u * bd);
+        f(v, clean(x[u].x));
+        f(v + 1, clean(x[u].y));
+        f(v + 2, clean(x[u].z));
+        f(v + 3, clean(x[u].w));
+      }
+      g();
+    }
+    for (; j < n4; j += bd) {
+      const float4 x = __ldg(r4 + j);
+      f(4 * j, clean(x.x));
+      f(4 * j + 1, clean(x.y));
+      f(4 * j + 2, clean(x.z));
+      f(4 * j + 3, clean(x.w));
+    }
+  } else {
+    int v = threadIdx.x;
+    for (; v + 3 * bd < V; v += 4 * bd) {
+      float x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = __ldg(row + v + u * bd);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) f(v + u * bd, clean(x[u]));
+      g();
+    }
+    for (; v < V; v += bd) f(v, clean(__ldg(row + v)));
+  }
+  g();
+}
+
+// Exact sum of two floats as an unevaluated pair (Knuth's TwoSum): s + e == a + b.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bp = s - a;
+  e = (a - (s - bp)) + (b - bp);
+}
+// A thread's sum of many masses: fp32 groups of at most 16 terms (each term at most a
+// few units), every group added exactly into an unevaluated (hi, lo) pair.
+struct Pair {
+  float hi = 0.f, lo = 0.f, g = 0.f;
+  __device__ __forceinline__ void close() {
+    float s, e;
+    two_sum(hi, g, s, e);
+    e += lo;
+    hi = s + e;
+    lo = e - (hi - s);
+    g = 0.f;
+  }
+  __device__ __forceinline__ float value() const { return hi + lo; }
+};
+
 // ---- block-wide helpers (any multiple of 32 threads up to 1024); fixed order ---------
 template <typename Tv>
 __device__ Tv warp_sum(Tv x) {
@@ -197,6 +280,11 @@ __device__ Tv block_scan(Tv x, Tv* sb, Tv* total) {
 struct FilterSmem {
   unsigned cnt[NB];
   float mass[NB];
+  // bin masses during the histogram pass as 32-bit fixed point: bin b's masses lie in
+  // (2^-(o+1), 2^-o] with o = b / 128 (its octave of d), so a mass times 2^o is in (1/2, 1]
+  // and is added as round(mass * 2^(o + qs)), qs = 32 - bits(V): no bin can overflow.
+  // Integer shared-memory atomics cost a fraction of fp32 ones.
+  unsigned qm[NB];
   u64 lkey[CAP];
   float lmass[CAP];
   u64 tkey[CAP / 2];  // unsorted copy for the ranking sort
@@ -233,17 +321,18 @@ __device__ void sort_desc(u64* key, float* val, int n) {  // n a power of two
 // Tokens with bin in [lo, hi] and key >= kmin gathered into S.lkey / S.lmass (sorted by
 // key, descending); returns the compensated mass of the tokens with bin < lo (and key >=
 // kmin), and in *n the number gathered (more than CAP: not gathered).
-__device__ float gather_bins(FilterSmem& S, const float* row, int V, bool vec, float m, float c,
+__device__ float gather_bins(FilterSmem& S, const float* row, int V, bool vec, float c, float mc,
                              int lo, int hi, u64 kmin, int* n) {
   if (threadIdx.x == 0) S.s_n = 0;
   __syncthreads();
   Kahan pre;
   for_row(row, V, vec, [&](int v, float l) {
-    const int bn = bin_of(l, m, c);
+    const float t = expo(l, c, mc);
+    const int bn = bin_t(t);
     if (bn > hi) return;
     const u64 k = vkey(l, v);
     if (k < kmin) return;
-    const float e = emass(l, m, c);
+    const float e = ex2a(t);  // non-greedy rows only (c > 0)
     if (bn < lo) {
       pre.add(e);
       return;
@@ -360,7 +449,7 @@ __device__ void candidate_bins(FilterSmem& S, float target, float eps, int last)
 // select over the 64-bit keys, eight digits of 8 bits, most significant first. Used only
 // when the candidate tokens do not fit the sorted list (mode 1 sums its digit masses with
 // fp32 atomics, so on that path the result may depend on their order).
-__device__ u64 radix_select(FilterSmem& S, const float* row, int V, bool vec, float m, float c,
+__device__ u64 radix_select(FilterSmem& S, const float* row, int V, bool vec, float c, float mc,
                             int lo, int hi, u64 kmin, int mode, unsigned want, float target) {
   unsigned* hc = reinterpret_cast<unsigned*>(S.lkey);  // 256-entry histograms
   float* hm = S.lmass;
@@ -383,14 +472,14 @@ __device__ u64 radix_select(FilterSmem& S, const float* row, int V, bool vec, fl
     const u64 prefix = S.s_prefix;
     const int sh = 8 * d;
     for_row(row, V, vec, [&](int v, float l) {
-      const int bn = bin_of(l, m, c);
+      const int bn = bin_of(l, c, mc);
       if (bn < lo || bn > hi) return;
       const u64 k = vkey(l, v);
       if (k < kmin) return;
       if (d < 7 && (k >> (sh + 8)) != prefix) return;
       const int bk = (int)((k >> sh) & 255ull);
       atomicAdd(&hc[bk], 1u);
-      if (mode == 1) atomicAdd(&hm[bk], emass(l, m, c));
+      if (mode == 1) atomicAdd(&hm[bk], emass(l, c, mc));
     });
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -424,12 +513,12 @@ __device__ u64 radix_select(FilterSmem& S, const float* row, int V, bool vec, fl
 }
 
 // Compensated mass of the tokens with key >= kmin (and mass >= minp).
-__device__ float kept_total(FilterSmem& S, const float* row, int V, bool vec, float m, float c,
+__device__ float kept_total(FilterSmem& S, const float* row, int V, bool vec, float c, float mc,
                             u64 kmin, float minp) {
   Kahan acc;
   for_row(row, V, vec, [&](int v, float l) {
     if (vkey(l, v) < kmin) return;
-    const float e = emass(l, m, c);
+    const float e = emass(l, c, mc);
     if (e >= minp) acc.add(e);
   });
   return block_sum<float>(acc.value(), S.sf);
@@ -448,9 +537,16 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
   const float* row = a.logits + ((int64_t)b * T + i) * V;
   const bool vec = (V & 3) == 0 && ((uintptr_t)row & 15u) == 0;
 
-  u64 best = 0ull;
-  for_row(row, V, vec, [&](int v, float l) { best = max(best, vkey(l, v)); });
-  const u64 maxkey = block_max_u64(best, S.sb);
+  // the largest logit and its first token (a thread visits its tokens in ascending id)
+  float mx = -INFINITY;
+  int mi = -1;
+  for_row(row, V, vec, [&](int v, float l) {
+    if (l > mx || mi < 0) {
+      mx = l;
+      mi = v;
+    }
+  });
+  const u64 maxkey = block_max_u64(mi >= 0 ? vkey(mx, mi) : 0ull, S.sb);
   const float m = key_value(maxkey);
   const float tau = a.temperature[b];
   const int k = a.top_k[b];
@@ -463,9 +559,12 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
     st.thr = maxkey;
     st.z = 1.f;
     st.c = 0.f;
+    st.mc = 0.f;
     st.minp = 0.f;
   } else {
     const float c = 1.4426950408889634f / tau;
+    const float mc = m * c;
+    st.mc = mc;
     const bool topk_on = k > 1 && k < V;
     const bool topp_on = pp < 1.f;
     st.c = c;
@@ -475,27 +574,33 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
     if (topk_on || topp_on) {
       for (int j = threadIdx.x; j < NB; j += FT) {
         S.cnt[j] = 0u;
-        S.mass[j] = 0.f;
+        S.qm[j] = 0u;
       }
+      const int qs = __clz(V);  // 32 - bits(V)
       __syncthreads();
       // The open last bin takes no atomics (with a peaked row most tokens land there, all
       // on one address); its count and mass follow from the totals below.
-      Kahan all;
-      for_row(row, V, vec, [&](int v, float l) {
-        const int bn = bin_of(l, m, c);
-        const float e = emass(l, m, c);
-        all.add(e);
+      Pair all;
+      for_row_batched(row, V, vec, [&](int v, float l) {
+        const float t = expo(l, c, mc);
+        const float e = ex2a(t);
+        all.g += e;
+        const int bn = bin_t(t);
         if (bn == NB - 1) return;
         if (topk_on) atomicAdd(&S.cnt[bn], 1u);
-        if (topp_on) atomicAdd(&S.mass[bn], e);
-      });
+        if (topp_on)  // e * 2^(octave + qs), rounded
+          atomicAdd(&S.qm[bn], __float2uint_rn(e * __int_as_float((127 + qs + (bn >> 7)) << 23)));
+      }, [&] { all.close(); });
       float z1 = block_sum<float>(all.value(), S.sf);  // synchronises
       {
         unsigned cl = 0;
         float ml = 0.f;
         for (int j = threadIdx.x; j < NB - 1; j += FT) {
           cl += S.cnt[j];
-          ml += S.mass[j];
+          const float mj =
+              topp_on ? (float)S.qm[j] * __int_as_float((127 - qs - (j >> 7)) << 23) : 0.f;
+          S.mass[j] = mj;
+          ml += mj;
         }
         const unsigned ca = block_sum<unsigned>(cl, S.su);
         const float ma = block_sum<float>(ml, S.sf);
@@ -531,14 +636,14 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
         bk = S.s_lo;
         const int r = S.s_j;
         int ng;
-        const float before = gather_bins(S, row, V, vec, m, c, bk, bk, 0ull, &ng);
+        const float before = gather_bins(S, row, V, vec, c, mc, bk, bk, 0ull, &ng);
         if (ng <= CAP) {
           thr_k = S.lkey[r];
           // the top-k mass: everything before bin bk, then the list up to rank r
           z1 = before + list_prefix(S, r);
         } else {
-          thr_k = radix_select(S, row, V, vec, m, c, bk, bk, 0ull, 0, (unsigned)r, 0.f);
-          z1 = kept_total(S, row, V, vec, m, c, thr_k, 0.f);
+          thr_k = radix_select(S, row, V, vec, c, mc, bk, bk, 0ull, 0, (unsigned)r, 0.f);
+          z1 = kept_total(S, row, V, vec, c, mc, thr_k, 0.f);
         }
         z = z1;
       }
@@ -562,14 +667,14 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
         for (int tries = 0; tries < 3; ++tries) {
           if (tries == 2) {  // the last try: the exact select over every bin the crossing
                              // can be in (no gather pass first: its list would be unused)
-            thr_p = radix_select(S, row, V, vec, m, c, 0, bk, thr_k, 1, 0u, target);
+            thr_p = radix_select(S, row, V, vec, c, mc, 0, bk, thr_k, 1, 0u, target);
             zp = -1.f;
             break;
           }
           int ng;
-          const float before = gather_bins(S, row, V, vec, m, c, lo, hi, thr_k, &ng);
+          const float before = gather_bins(S, row, V, vec, c, mc, lo, hi, thr_k, &ng);
           if (ng > CAP) {  // too many for the sorted list: the exact select over these bins
-            thr_p = radix_select(S, row, V, vec, m, c, lo, hi, thr_k, 1, 0u, target - before);
+            thr_p = radix_select(S, row, V, vec, c, mc, lo, hi, thr_k, 1, 0u, target - before);
             zp = -1.f;
             break;
           }
@@ -596,7 +701,7 @@ filter_stats_kernel(const SampleArgs a, RowStats* __restrict__ stats, float* __r
       }
     }
     st.thr = thr;
-    if (z < 0.f || st.minp > 0.f) z = kept_total(S, row, V, vec, m, c, thr, st.minp);
+    if (z < 0.f || st.minp > 0.f) z = kept_total(S, row, V, vec, c, mc, thr, st.minp);
     st.z = z;
   }
   if (threadIdx.x == 0) stats[(int64_t)b * T + i] = st;
