@@ -103,8 +103,16 @@ __device__ __forceinline__ int bin_t(float t) {
   return t > -DR ? min(NB - 1, (int)(-t * (NB / DR))) : NB - 1;
 }
 __device__ __forceinline__ int bin_of(float l, float c, float mc) { return bin_t(expo(l, c, mc)); }
+// key(l, v) >= k0 with the float order first: the 64-bit key only decides a tie in value
+// (float order and key order agree on unequal values; -0 and +0 compare equal as floats
+// and are then told apart by their keys). kv = key_floor(k0); k0 = 0 keeps every token
+// (every key is positive).
+__device__ __forceinline__ float key_floor(u64 k0) { return k0 ? key_value(k0) : -INFINITY; }
+__device__ __forceinline__ bool key_at_least(float l, int v, float kv, u64 k0) {
+  return l > kv || (l == kv && vkey(l, v) >= k0);
+}
 __device__ __forceinline__ float kept_mass(const RowStats& st, float l, int v) {
-  if (vkey(l, v) < st.thr) return 0.f;
+  if (!key_at_least(l, v, key_floor(st.thr), st.thr)) return 0.f;
   const float e = emass(l, st.c, st.mc);
   return e >= st.minp ? e : 0.f;
 }
@@ -325,24 +333,24 @@ __device__ float gather_bins(FilterSmem& S, const float* row, int V, bool vec, f
                              int lo, int hi, u64 kmin, int* n) {
   if (threadIdx.x == 0) S.s_n = 0;
   __syncthreads();
-  Kahan pre;
-  for_row(row, V, vec, [&](int v, float l) {
+  const float kv = key_floor(kmin);
+  Pair pre;
+  for_row_batched(row, V, vec, [&](int v, float l) {
     const float t = expo(l, c, mc);
     const int bn = bin_t(t);
     if (bn > hi) return;
-    const u64 k = vkey(l, v);
-    if (k < kmin) return;
+    if (kmin != 0ull && !key_at_least(l, v, kv, kmin)) return;
     const float e = ex2a(t);  // non-greedy rows only (c > 0)
     if (bn < lo) {
-      pre.add(e);
+      pre.g += e;
       return;
     }
     const int pos = atomicAdd(&S.s_n, 1);
     if (pos < CAP) {
-      S.lkey[pos] = k;
+      S.lkey[pos] = vkey(l, v);
       S.lmass[pos] = e;
     }
-  });
+  }, [&] { pre.close(); });
   const float before = block_sum<float>(pre.value(), S.sf);  // synchronises
   *n = S.s_n;
   if (*n <= CAP / 2) {
@@ -515,12 +523,13 @@ __device__ u64 radix_select(FilterSmem& S, const float* row, int V, bool vec, fl
 // Compensated mass of the tokens with key >= kmin (and mass >= minp).
 __device__ float kept_total(FilterSmem& S, const float* row, int V, bool vec, float c, float mc,
                             u64 kmin, float minp) {
-  Kahan acc;
-  for_row(row, V, vec, [&](int v, float l) {
-    if (vkey(l, v) < kmin) return;
+  const float kv = key_floor(kmin);
+  Pair acc;
+  for_row_batched(row, V, vec, [&](int v, float l) {
+    if (!key_at_least(l, v, kv, kmin)) return;
     const float e = emass(l, c, mc);
-    if (e >= minp) acc.add(e);
-  });
+    if (e >= minp) acc.g += e;
+  }, [&] { acc.close(); });
   return block_sum<float>(acc.value(), S.sf);
 }
 
