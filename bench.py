@@ -9,7 +9,12 @@ attention, merge) and the greedy acceptance with KV compaction. Inputs are resid
 in HBM before the timed region; the step is replayed from a CUDA graph; L2 is flushed
 (a 256 MiB write) between timed launches. The JSON line reports steps/s (whole job),
 the per-call times, the roofline of the attention call against MEASURED_PEAKS.json,
-an end-to-end number through host buffers, and the CPU oracle as a baseline.
+an end-to-end number through host buffers, and the CPU oracle as a baseline. An
+attention or top-k leg whose inputs are larger than L2 is also replayed as four calls
+back to back in one graph (each call streams its inputs from HBM, so no flush is needed
+between them); its roofline takes that per-call time (the time inside a step, without
+the launch latency of a graph of one call) and keeps the one-call figure beside it
+(us_per_launch_alone, frac_alone).
 
 The default workload is long70b (batch 4, prefix 32768, 70B-shaped heads: the largest
 single-GPU shape, a long-prefix one). In the same timed loop the attention call of the
@@ -42,6 +47,8 @@ import workloads as W  # noqa: E402
 METRIC = "tree-verify attn µs/layer, achieved HBM GB/s and % roofline; top-k rows/s"
 UNIT = "layer-verify steps/s"
 L2_FLUSH_BYTES = 256 << 20
+L2_BYTES = 129 * 10 ** 6  # GB300 L2
+CHAIN = 4  # calls per chained graph of a leg whose inputs exceed L2
 
 
 def plain(x):
@@ -487,6 +494,21 @@ def native(args):
                 legs.update(sides[name]["fns"])
                 print(f"bench: side legs of {name} ready", file=sys.stderr, flush=True)
 
+    def leg_bytes(name):
+        """Algorithmic input bytes of one call of an attention or top-k leg (0 for the
+        others, which are timed only one call at a time after a flush)."""
+        if name == "attn":
+            return algorithmic(w, prefix, depths)[0]
+        if name == "topk":
+            return b * k * v * 4
+        for sname, sd in sides.items():
+            if name == "attn_" + sname:
+                return algorithmic(sd["w"], sd["prefix"], sd["depths"])[0]
+            if name == "topk_" + sname:
+                return sd["w"].batch * sd["w"].top_k * sd["w"].vocab * 4
+        return 0
+    chain_legs = [n for n in legs if leg_bytes(n) > L2_BYTES]
+
     flush_buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     graphs = {}
@@ -500,6 +522,15 @@ def native(args):
             with torch.cuda.graph(g, stream=stream):
                 fn()
             graphs[name] = g
+        # A leg whose inputs exceed L2 is also timed as CHAIN calls back to back in one
+        # graph (no flush between them: each call streams its inputs from HBM): the
+        # per-call time inside a step, without the launch latency of a graph of one call.
+        for name in chain_legs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(CHAIN):
+                    legs[name]()
+            graphs[name + "@chain"] = g
     torch.cuda.synchronize()
 
     def timed_loop(n, record):
@@ -541,6 +572,8 @@ def native(args):
     if world > 1:
         dist.barrier()
     ms = {name: sum(a.elapsed_time(c) for a, c in ev[name]) / args.steps for name in ev}
+    for name in chain_legs:  # per call
+        ms[name + "@chain"] /= CHAIN
     print("bench: timed region done", file=sys.stderr, flush=True)
 
     # ---- end to end through host buffers --------------------------------------------
@@ -612,9 +645,25 @@ def native(args):
         return
 
     hbm, tf, src = peaks()
-    attn_roof = attn_roofline(w, prefix, depths, ms["attn"] * 1e3, hbm, tf, src)
-    topk_roof = topk_roofline(w, ms["topk"] * 1e3, hbm, src)
-    attn_s = ms["attn"] / 1e3
+
+    def us_of(name):
+        """Per-call µs of a leg: the chained figure when its inputs exceed L2."""
+        return (ms[name + "@chain"] if name in chain_legs else ms[name]) * 1e3
+
+    def timing(name, roof):
+        """How a roofline's time was taken, with the one-call figure beside a chain's."""
+        if name in chain_legs:
+            alone = ms[name] * 1e3
+            roof["timing"] = (f"{CHAIN} calls back to back in one graph, per call (inputs "
+                              f"larger than L2, no flush between them)")
+            roof["us_per_launch_alone"] = alone
+            roof["frac_alone"] = roof["frac"] * roof["us_per_launch"] / alone
+        else:
+            roof["timing"] = "one call in a graph of its own after a 256 MiB L2 flush"
+        return roof
+    attn_roof = timing("attn", attn_roofline(w, prefix, depths, us_of("attn"), hbm, tf, src))
+    topk_roof = timing("topk", topk_roofline(w, us_of("topk"), hbm, src))
+    attn_s = us_of("attn") / 1e6
     lm_s = ms["lm_head"] / 1e3
     lm_bytes = lm_v * lm_h * 2 + lm_rows * lm_h * 2 + lm_rows * 4
     lm_flops = 2 * lm_rows * lm_v * lm_h
@@ -642,7 +691,7 @@ def native(args):
                "traffic_source": traffic("sample", w.name)[1],
                "algorithmic_bytes": sa_bytes, "us_per_launch": ms["sample"] * 1e3}
     # the dominant kernel of the step: the attention call or the depth + 1 top-k levels
-    dominant = "topk" if ms["topk"] * (w.depth + 1) > ms["attn"] else "attn"
+    dominant = "topk" if us_of("topk") * (w.depth + 1) > us_of("attn") else "attn"
     kernels_step = hp.kernels_per_step()
     # one expansion level ([B, K, V] rows): one kernel, or two for a large batch
     lvl_launches = T.draft_topk_expand_launches(b, k, v, k)
@@ -657,6 +706,19 @@ def native(args):
                 n += T.draft_topk_expand_launches(sw.batch, sw.top_k, sw.vocab, sw.top_k)
         return n
     attn_kernels = hp.attn_kernels()
+
+    def leg_launches(name):
+        """Kernels of one call of an attention or top-k leg."""
+        if name == "attn":
+            return attn_kernels
+        if name == "topk":
+            return lvl_launches
+        for sd in sides.values():
+            if name in sd["fns"]:
+                sw = sd["w"]
+                return (sd["attn_launches"] if name.startswith("attn_") else
+                        T.draft_topk_expand_launches(sw.batch, sw.top_k, sw.vocab, sw.top_k))
+        return 0
     line = {
         "metric": METRIC, "value": world * 1e3 / step_ms, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -665,9 +727,10 @@ def native(args):
         "config": {"workload": w.name, "batch": b, "prefix": (int(prefix.min()), int(prefix.max())),
                    "nodes": t_max, "top_k": k, "depth": w.depth, "vocab": v,
                    "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "paged": paged, "l2": "flushed (256 MiB write) before every timed launch",
+                   "paged": paged, "l2": ("flushed (256 MiB write) before every timed launch; legs whose inputs exceed "
+                          f"L2 also timed as {CHAIN} calls in one graph"),
                    "parallelism": f"replicas x{world}", "graph": "CUDA graph per step"},
-        "attn_us_per_layer": ms["attn"] * 1e3,
+        "attn_us_per_layer": us_of("attn"),
         "attn_hbm_GBps": attn_roof["hbm_GBps"],
         "attn_roofline_us": attn_roof["roofline_us"],
         "topk_rows_per_s": topk_roof["rows_per_s"],
@@ -691,21 +754,24 @@ def native(args):
         # timed region per iteration: the step graph, the attention call, one top-k level,
         # the lm-head argmax (GEMM + finalize), the non-greedy acceptance (filter, walk,
         # compaction), a product-score level, the d2t map and a fixed level, the drafter's
-        # grown mask and its attention, and the side legs
+        # grown mask and its attention, the side legs, and the chained calls of the legs
+        # whose inputs exceed L2
         "gpu_launches": args.steps * (kernels_step + attn_kernels + 2 * lvl_launches + 2 + 3 + 2 + 1 +
                                       T.tree_verify_attn_launches(
                                           (b, dn, w.num_q_heads, w.head_dim), cache, p_max) +
-                                      sum(side_launches(sd) for sd in sides.values())),
+                                      sum(side_launches(sd) for sd in sides.values()) +
+                                      CHAIN * sum(leg_launches(n) for n in chain_legs)),
         "wall_s_timed_region": t_wall,
     }
     for name, sd in sides.items():
         for leg in sd["fns"]:
             kind = leg.split("_")[0]
             if kind == "attn":
-                line["roofline_attn_" + name] = attn_roofline(sd["w"], sd["prefix"], sd["depths"],
-                                                              ms[leg] * 1e3, hbm, tf, src)
+                line["roofline_attn_" + name] = timing(leg, attn_roofline(
+                    sd["w"], sd["prefix"], sd["depths"], us_of(leg), hbm, tf, src))
             else:
-                line["roofline_topk_" + name] = topk_roofline(sd["w"], ms[leg] * 1e3, hbm, src)
+                line["roofline_topk_" + name] = timing(leg, topk_roofline(
+                    sd["w"], us_of(leg), hbm, src))
     ck = clocks.summary()
     if ck:
         line["clocks"] = ck
