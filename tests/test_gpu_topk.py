@@ -70,11 +70,12 @@ def compare(levels_per_req, k, **kw):
     return st, ss, sp
 
 
-@pytest.mark.parametrize("b", [3, 40])
+@pytest.mark.parametrize("b", [3, 80])
 @pytest.mark.parametrize("v", [64, 1000, 4001, 32000])
 def test_levels_small_and_ragged_vocab(v, b):
-    """3 requests take the row-per-CTA cluster kernel at every level; 40 requests of 4
-    rows (160 rows, more than the GPU's SMs) take the per-unit kernel from level 2 on."""
+    """3 requests take the row-per-CTA cluster kernel at every level; 80 requests of 4
+    rows (320 rows, more than two waves of the GPU's SMs) take the per-unit kernel from
+    level 2 on."""
     rng = np.random.default_rng(v + b)
     k, depth = 4, 3
     reqs = [[(rng.standard_normal((1 if l == 0 else k, v)) * 2).astype(np.float32)
@@ -88,6 +89,7 @@ def test_levels_small_and_ragged_vocab(v, b):
     (30001, 10, 6, 0, False),    # unaligned rows: scalar loads
     (30001, 10, 6, 3, True),     # aligned ragged rows, product scores
     (32000, 8, 4, 0, False),     # clusters of 8 (the long-prefix workload's shape)
+    (32000, 10, 16, 0, False),   # 160 rows: the clusters run in two waves (serving's shape)
     (20, 16, 2, 0, False),       # fewer threads with entries than k: every entry survives
 ])
 def test_row_clusters(v, k, b, pad, product):

@@ -1652,9 +1652,9 @@ TopkPlan plan_topk(int batch, int rows, int vocab, int top_k) {
   TopkPlan p{};
   const int64_t rows_total = (int64_t)batch * rows;
   // Small batches: one CTA per row and a cluster per request, when the row fits the CTA's
-  // registers and every cluster is resident at once.
-  if (vocab <= R_MAX_VOCAB && rows <= R_MAX_ROWS && rows_total <= device_sm_count() &&
-      batch <= row_cluster_capacity(rows)) {
+  // registers and the clusters run in at most two waves.
+  if (vocab <= R_MAX_VOCAB && rows <= R_MAX_ROWS && rows_total <= 2 * device_sm_count() &&
+      batch <= 2 * row_cluster_capacity(rows)) {
     p.cluster = true;
     p.chunks = 1;
     p.chunk_len = (int)round_up(vocab, 4);
@@ -1734,7 +1734,7 @@ int launch_topk_expand(const float* logits, int batch, int rows, int64_t row_str
   int dev = 0;
   cudaGetDevice(&dev);
   if (plan.cluster) {
-    if (row_cluster_capacity(rows) < batch) return TSV_ERR_UNSUPPORTED;  // sets the cluster attribute
+    if (row_cluster_capacity(rows) < 1) return TSV_ERR_UNSUPPORTED;  // sets the cluster attribute
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(rows, batch);
     cfg.blockDim = dim3(R_THREADS);
