@@ -1102,9 +1102,6 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, int r) {
                : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(r));
   return out;
 }
-__device__ __forceinline__ void st_cluster(uint32_t a, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
-}
 __device__ __forceinline__ void st_cluster(uint32_t a, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
 }
