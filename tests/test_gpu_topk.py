@@ -351,3 +351,50 @@ def test_select_tree_matches_the_two_calls():
     assert c["err"].cpu().tolist() == [0, 0, 0]
     tokens, parents, _ = gc.oracle_tree(w, 0)
     assert c["tok"].cpu().numpy()[0, :w.num_nodes].tolist() == [5] + tokens.tolist()[1:]
+
+
+def test_row_clusters_masked_rows():
+    """Rows that are -inf except for three tokens (a masked vocabulary): two of every
+    row's five candidates are -inf tokens, taken by lower id, and the value bound leaves
+    every entry, so the exact bound runs."""
+    k = 5
+    rng = np.random.default_rng(77 + k)
+    v, b = 32000, 3
+    reqs = []
+    for _ in range(b):
+        lv = []
+        for l in range(3):
+            rows = 1 if l == 0 else k
+            x = np.full((rows, v), -np.inf, dtype=np.float32)
+            for r in range(rows):
+                idx = rng.choice(v, size=3, replace=False)
+                x[r, idx] = rng.standard_normal(3).astype(np.float32) * 2
+            lv.append(x)
+        reqs.append(lv)
+    st, ss, sp, _ = run_levels(reqs, k)
+    for bi, levels in enumerate(reqs):
+        exp = draft.topk_generate(levels, k)
+        c = exp.store_token.size
+        np.testing.assert_array_equal(st[bi, :c], exp.store_token)
+        np.testing.assert_array_equal(sp[bi, :c], exp.store_parent)
+        fin = np.isfinite(exp.store_score)
+        assert np.array_equal(np.isfinite(ss[bi, :c]), fin)
+        np.testing.assert_allclose(ss[bi, :c][fin], exp.store_score[fin], rtol=gc.SCORE_RTOL)
+
+
+def test_row_clusters_tied_maxima():
+    """Every row holds its largest value four times (at random ids) over a spread of
+    smaller ones: the ties at the top go to the lower ids."""
+    rng = np.random.default_rng(91)
+    k, v, b = 6, 30000, 3
+    reqs = []
+    for _ in range(b):
+        lv = []
+        for l in range(3):
+            rows = 1 if l == 0 else k
+            x = (rng.standard_normal((rows, v)) * 2).astype(np.float32)
+            for r in range(rows):
+                x[r, rng.choice(v, size=4, replace=False)] = np.float32(9.5)
+            lv.append(x)
+        reqs.append(lv)
+    compare(reqs, k)
