@@ -9,9 +9,16 @@
 // follows "TensorRT-LLM 源码完全拆解(二十二)", section 树的三套账 (flat = parent * K +
 // child, parent = flat / K).
 //
-// One kernel per level, one CTA per (row, vocab chunk); the chunk count per row keeps the
-// units in as few waves of resident CTAs as the makespan allows (small batches: one wave
-// of short chunks). Each unit is read once with 128-bit loads:
+// One level runs one of three designs, chosen by plan_topk:
+//   - small batches (rows of at most 32768 entries, every request's rows in one thread-
+//     block cluster, the clusters in at most two waves): topk_row_kernel, one CTA per row
+//     holding the row in registers; the rank-0 CTA of a request's cluster runs the joint
+//     top-K over distributed shared memory (see its section below);
+//   - large batches (every share of the level at least a row long): topk_stream_kernel,
+//     a persistent kernel over equal shares of all rows' entries, then topk_merge_kernel;
+//   - otherwise topk_level_kernel, one CTA per (row, vocab chunk); the chunk count per row
+//     keeps the units in as few waves of resident CTAs as the makespan allows.
+// In the last two, each unit is read once with 128-bit loads:
 //   - log-sum-exp: fp32 terms 2^(x log2 e - ref log2 e) against a running reference,
 //     summed in groups of 16 and added exactly (two-sum) into an unevaluated (hi, lo)
 //     pair; the reference is raised, and the pair rescaled, only when an entry exceeds it
@@ -24,8 +31,9 @@
 //     folds them into a register list 32 groups at a time. At the end a bound with k
 //     entries of the unit at or above it leaves a handful of survivors, ranked by
 //     counting in shared memory.
-// The last CTA of a request to finish (an atomic ticket) stages the request's chunk
-// lists in shared memory, merges each row (k rounds of a warp tournament over list
+// The request merge (in topk_level_kernel the last CTA of a request to finish, found by
+// an atomic ticket; after the persistent kernel, topk_merge_kernel) stages the request's
+// chunk lists in shared memory, merges each row (k rounds of a warp tournament over list
 // heads), writes the level's candidates to the store and ranks the rows' cumulative
 // scores for the joint top-K.
 #include <float.h>
