@@ -1397,10 +1397,10 @@ __global__ void __launch_bounds__(R_THREADS, 1) topk_row_kernel(const LevelArgs 
 // the lower store index. One 12-bit histogram pass finds the bin that holds the
 // total_tokens-th best key; the candidates of that bin (a few dozen on spread scores) are
 // ranked exactly by counting. When a bin holds more than F_BIN_MAX candidates (heavily
-// tied scores) a radix select over the remaining bits (11, 10 and 10 more bits... as three
-// passes over the full key) gives the threshold key and the number of its equal keys to
-// keep, in ascending store index. Node numbers (ascending store index) come from a block
-// prefix sum.
+// tied scores) a radix select over the full key in three passes (11, 11 and 10 bits)
+// gives the threshold key and the number of its equal keys to keep, in ascending store
+// index. Node numbers (ascending store index) come from a block prefix sum. With
+// tsv_draft_select_tree one warp then builds the selected trees' metadata.
 constexpr int F_THREADS = 512;
 constexpr int F_WARPS = F_THREADS / 32;
 constexpr int F_MAX = 4096;                 // candidates per request
